@@ -1,0 +1,412 @@
+"""Benchmark of one hybrid-batch attention step (KV append + attention).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl native|reference]
+
+A step is one pass of the hot path over one synthetic hybrid batch: the KV
+append of the batch's new tokens and the attention of every new token (decode
+rows and prefill chunks) over the paged cache, through the C ABI.  The batch
+layout (q_len, context_len, block tables) is fixed per workload, so the plan
+is built once.  The default workload is the Mistral-7B attention shape at a
+512-token budget (64 decode rows + one 448-token chunk).
+
+Printed (rank 0, one JSON line): tokens/s over the timed steps with inputs
+resident in HBM (`value`), the same through host buffers with the copies in
+the timed region (`e2e`), the dominant kernel's roofline figures, the whole
+step's fraction of its roofline, the CPU oracle timed on a bounded sample, and
+the SM clocks sampled during the timed region.
+
+`--impl reference` times the fp64 CPU oracle instead (rank 0 only).
+Under torchrun (N > 1) each rank runs an independent replica of the workload;
+timing is the max over ranks and `value` counts every rank's tokens.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from chunked_prefill_decode_gb300 import workloads  # noqa: E402
+
+METRIC = "mixed-batch paged attention tokens/s; % of roofline (HBM GB/s or TC util)"
+L2_BYTES = 129 * 1024 * 1024
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "source": "fallback"}
+
+
+def algorithmic_counts(layout):
+    """FLOPs and bytes of one step, by kernel, counted from the definition.
+
+    attention FLOPs: 4 * Hq * D * sum over new tokens of (keys it sees);
+    decode bytes: K and V of every decode row's context once per kv head,
+    plus its q row and output; chunk bytes: K and V of the chunk's context
+    once per kv head, plus q and out; append bytes: new K and V read and
+    written."""
+    sh = layout.shape
+    Hq, Hkv, D = sh.num_q_heads, sh.num_kv_heads, sh.head_dim
+    kv_tok = 2 * Hkv * D * 2               # K+V bytes per cached token
+    qo_tok = 2 * Hq * D * 2                # q read + out written per new token
+    c = {"decode_bytes": 0, "decode_flops": 0, "chunk_bytes": 0, "chunk_flops": 0}
+    for q, ctx in zip(layout.q_len.tolist(), layout.context_len.tolist()):
+        seen = sum(ctx - q + j + 1 for j in range(q))
+        flops = 4 * Hq * D * seen
+        byts = ctx * kv_tok + q * qo_tok
+        kind = "decode" if q == 1 else "chunk"
+        c[kind + "_bytes"] += byts
+        c[kind + "_flops"] += flops
+    c["append_bytes"] = 2 * layout.total_q * kv_tok
+    c["bytes"] = c["decode_bytes"] + c["chunk_bytes"] + c["append_bytes"]
+    c["flops"] = c["decode_flops"] + c["chunk_flops"]
+    return c
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index, period_ms=20):
+        self.proc = None
+        self.idx = device_index
+        self.period = period_ms
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", str(self.period)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is None:
+            return False
+        time.sleep(0.05)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        self.lines = [l for l in out.splitlines() if l.strip()]
+        return False
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in getattr(self, "lines", []):
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _dist():
+    n = int(os.environ.get("WORLD_SIZE", "1"))
+    if n > 1 and not torch.distributed.is_initialized():
+        torch.distributed.init_process_group("nccl")
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return n, rank, local
+
+
+def _barrier(n):
+    if n > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(x: float, n: int) -> float:
+    if n <= 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+def oracle_sample_rate(layout, ten_host, budget_s=12.0, rows=None):
+    """Time the fp64 oracle on the CPU on a sample of the batch's rows:
+    decode rows first (each is one token), then single chunk tokens, until
+    `budget_s` seconds have been spent.  Returns (tokens/s, description)."""
+    from oracle import paged_attention as pa
+    sh = layout.shape
+    bits = workloads.bf16_bits
+    q = bits(ten_host.q)
+    kc, vc = bits(ten_host.k_cache), bits(ten_host.v_cache)
+    kn, vn = bits(ten_host.k_new), bits(ten_host.v_new)
+    kp, vp = pa.kv_append(kc, vc, kn, vn, layout.q_len, layout.context_len,
+                          layout.block_table, sh.page_size)
+    cu = layout.cu_q_len
+    order = rows
+    if order is None:
+        dec = [int(cu[s]) for s in range(layout.num_seqs) if layout.q_len[s] == 1]
+        chk = [int(cu[s] + j) for s in range(layout.num_seqs) if layout.q_len[s] > 1
+               for j in range(0, int(layout.q_len[s]), 7)]
+        order = dec + chk
+    scale = 1.0 / math.sqrt(sh.head_dim)
+    done, t0 = 0, time.perf_counter()
+    for tok in order:
+        pa.attention(q, kp, vp, layout.q_len, layout.context_len, layout.block_table,
+                     sh.page_size, sh.num_q_heads, sh.num_kv_heads, scale, tokens=[tok])
+        done += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return done / dt, f"{done} new tokens (all {sh.num_q_heads} heads) of this batch, " \
+                      f"decode rows first, {dt:.1f} s"
+
+
+def run_reference(args):
+    """The fp64 CPU oracle as the reference arm (rank 0 only)."""
+    n, rank, _ = _dist() if int(os.environ.get("WORLD_SIZE", "1")) > 1 else (1, 0, 0)
+    if rank != 0:
+        return
+    layout = workloads.WORKLOADS[args.workload]()
+    ten = workloads.make_tensors(layout, seed=1)
+    cu = layout.cu_q_len
+    dec = [int(cu[s]) for s in range(layout.num_seqs) if layout.q_len[s] == 1]
+    from oracle import paged_attention as pa
+    sh = layout.shape
+    bits = workloads.bf16_bits
+    kp, vp = pa.kv_append(bits(ten.k_cache), bits(ten.v_cache), bits(ten.k_new),
+                          bits(ten.v_new), layout.q_len, layout.context_len,
+                          layout.block_table, sh.page_size)
+    qb = bits(ten.q)
+    scale = 1.0 / math.sqrt(sh.head_dim)
+
+    def step(i):
+        tok = dec[i % len(dec)]
+        pa.attention(qb, kp, vp, layout.q_len, layout.context_len, layout.block_table,
+                     sh.page_size, sh.num_q_heads, sh.num_kv_heads, scale, tokens=[tok])
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        step(args.warmup + i)
+    dt = time.perf_counter() - t0
+    v = args.steps / dt
+    cores = len(os.sched_getaffinity(0))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s",
+        "n_gpus": n, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * dt / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload},
+        "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": "each step: one decode row (all q heads) of the batch, "
+                                   "rows cycled, fp64 numpy oracle"},
+        "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_native(args):
+    n, rank, local = _dist()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import __graft_entry__
+    __graft_entry__.build()
+    from chunked_prefill_decode_gb300 import hb
+    from chunked_prefill_decode_gb300.device import device_batch
+
+    layout = workloads.WORKLOADS[args.workload]()
+    sh = layout.shape
+    ten = workloads.make_tensors(layout, seed=1 + rank, device=dev)
+    db = device_batch(layout.q_len, layout.context_len, layout.block_table,
+                      layout.num_pages, sh.num_q_heads, sh.num_kv_heads, sh.head_dim,
+                      sh.page_size, dev)
+    scale = 1.0 / math.sqrt(sh.head_dim)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    out = torch.empty_like(ten.q)
+    kc, vc = ten.k_cache, ten.v_cache
+    plan, ws = hb.hb_plan(db.batch, db.q_len, db.context_len, sms)
+    T = layout.total_q
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        hb.hb_kv_append(db.batch, ten.k_new, ten.v_new, kc, vc)
+        hb.hb_attention(db.batch, plan, ten.q, kc, vc, scale, out, ws)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    hb.hb_check()
+    # ---- timed region: inputs resident in HBM
+    _barrier(n)
+    torch.cuda.synchronize(dev)
+    hb.hb_timing_enable(True)
+    launches0 = hb.hb_launch_count()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        ev0.record(stream)
+        for _ in range(args.steps):
+            step()
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+    launches = hb.hb_launch_count() - launches0
+    ktimes = hb.hb_timing_read()
+    hb.hb_timing_enable(False)
+    hb.hb_check()
+    _barrier(n)
+    ms = ev0.elapsed_time(ev1)
+    ms_max = max_over_ranks(ms, n)
+    value = n * T * args.steps / (ms_max / 1e3)
+
+    # ---- end to end through the public API with host buffers
+    pin = lambda t: t.detach().cpu().pin_memory()
+    h_q, h_kn, h_vn = pin(ten.q), pin(ten.k_new), pin(ten.v_new)
+    h_cu = torch.from_numpy(layout.cu_q_len).pin_memory()
+    h_ctx = torch.from_numpy(layout.context_len).pin_memory()
+    h_bt = torch.from_numpy(np.ascontiguousarray(layout.block_table)).pin_memory()
+    h_out = torch.empty_like(h_q).pin_memory()
+    d_q, d_kn, d_vn = torch.empty_like(ten.q), torch.empty_like(ten.k_new), torch.empty_like(ten.v_new)
+    d_cu, d_ctx, d_bt = db.cu_q_len, db.context_len_d, db.block_table
+    e2e_steps = max(1, min(args.steps, 200))
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_kn, h_vn, h_cu, h_ctx, h_bt))
+    d2h = h_out.numel() * h_out.element_size()
+
+    def e2e_step():
+        d_q.copy_(h_q, non_blocking=True)
+        d_kn.copy_(h_kn, non_blocking=True)
+        d_vn.copy_(h_vn, non_blocking=True)
+        d_cu.copy_(h_cu, non_blocking=True)
+        d_ctx.copy_(h_ctx, non_blocking=True)
+        d_bt.copy_(h_bt, non_blocking=True)
+        p, _ = hb.hb_plan(db.batch, layout.q_len, layout.context_len, sms, workspace=ws,
+                          plan=plan)
+        hb.hb_kv_append(db.batch, d_kn, d_vn, kc, vc)
+        hb.hb_attention(db.batch, p, d_q, kc, vc, scale, out, ws)
+        h_out.copy_(out, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    _barrier(n)
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e2e_s = max_over_ranks(time.perf_counter() - t0, n)
+    plan_bytes = int(hb.plan_header(plan)["num_decode_items"]) * 32 + \
+        int(hb.plan_header(plan)["num_chunk_items"]) * 32
+    e2e = {"value": n * T * e2e_steps / e2e_s, "unit": "tokens/s",
+           "h2d_bytes_per_step": h2d + plan_bytes, "d2h_bytes_per_step": d2h}
+
+    if rank != 0:
+        return
+    peaks = _peaks()
+    cnt = algorithmic_counts(layout)
+    t_dec = ktimes["decode"][0] / max(1, ktimes["decode"][1])
+    t_chk = ktimes["chunk"][0] / max(1, ktimes["chunk"][1])
+    t_app = ktimes["kv_append"][0] / max(1, ktimes["kv_append"][1])
+    # dominant kernel = the one with the largest share of the step
+    shares = {"decode": ktimes["decode"][0], "chunk": ktimes["chunk"][0],
+              "kv_append": ktimes["kv_append"][0]}
+    dom = max(shares, key=shares.get)
+    if dom == "chunk":
+        achieved = cnt["chunk_flops"] / (t_chk / 1e3) / 1e12
+        roof = {"kernel": "chunk", "bound": "tensor", "achieved": achieved,
+                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": achieved / peaks["bf16_tflops"], "traffic": None}
+    else:
+        key, t = ("decode", t_dec) if dom == "decode" else ("append", t_app)
+        byts = cnt["decode_bytes"] if dom == "decode" else cnt["append_bytes"]
+        achieved = byts / (t / 1e3) / 1e9
+        roof = {"kernel": dom, "bound": "hbm", "achieved": achieved,
+                "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"], "traffic": None}
+    roof["peak_source"] = peaks["source"]
+    roof["avg_launch_ms"] = {"decode": t_dec, "chunk": t_chk, "kv_append": t_app}
+    step_roof_s = max(cnt["flops"] / (peaks["bf16_tflops"] * 1e12),
+                      cnt["bytes"] / (peaks["hbm_gbs"] * 1e9))
+    ms_step = ms_max / args.steps
+    cpu_v, cpu_desc = oracle_sample_rate(layout, workloads.make_tensors(layout, seed=1),
+                                         budget_s=args.cpu_seconds)
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": n,
+        "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": args.workload, "num_q_heads": sh.num_q_heads,
+                   "num_kv_heads": sh.num_kv_heads, "head_dim": sh.head_dim,
+                   "page_size": sh.page_size, "tokens_per_step": T,
+                   "decode_rows": int((layout.q_len == 1).sum()),
+                   "chunk_rows": int((layout.q_len > 1).sum()),
+                   "kv_bytes_per_step": cnt["bytes"],
+                   "l2": "inputs larger than L2 (KV read per step %.0f MB > 129 MB)" % (cnt["bytes"] / 1e6),
+                   "parallelism": f"replicas{n}" if n > 1 else "single"},
+        "roofline": roof,
+        "step_roofline": {"frac": (step_roof_s * 1e3) / ms_step,
+                          "roofline_ms": step_roof_s * 1e3,
+                          "flops": cnt["flops"], "bytes": cnt["bytes"],
+                          "bound": "hbm" if cnt["bytes"] / (peaks["hbm_gbs"] * 1e9) >=
+                          cnt["flops"] / (peaks["bf16_tflops"] * 1e12) else "tensor"},
+        "cpu_baseline": {"value": cpu_v, "unit": "tokens/s",
+                         "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
+                         "sample": cpu_desc},
+        "e2e": e2e,
+        "gpu_launches": int(launches),
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default="mistral_b512", choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_native(args)
+    if torch.distributed.is_initialized():
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,586 @@
+// api.cu -- the C ABI of libhb (declared in include/hb.h): argument checks,
+// the host-side plan, TMA descriptors, kernel launches, the device error word
+// and launch timing.  Every exported function catches everything: no C++
+// exception crosses the boundary.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "hb.h"
+#include "hb_internal.h"
+
+__device__ int g_hb_device_error = 0;
+
+namespace hb {
+cudaError_t launch_kv_append(const AppendParams& p, int num_sms, cudaStream_t stream);
+cudaError_t launch_decode(const DecodeParams& p, int head_dim, int grid,
+                          const CUtensorMap& kmap, const CUtensorMap& vmap,
+                          cudaStream_t stream);
+cudaError_t launch_chunk(const ChunkParams& p, int head_dim, const CUtensorMap& qmap,
+                         const CUtensorMap& kmap, const CUtensorMap& vmap,
+                         cudaStream_t stream);
+}  // namespace hb
+
+using namespace hb;
+
+namespace {
+
+thread_local std::string t_err;
+
+hb_status fail(hb_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  t_err = buf;
+  return s;
+}
+
+hb_status ok() {
+  t_err.clear();
+  return HB_OK;
+}
+
+hb_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(HB_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+std::atomic<int64_t> g_launches{0};
+
+// ---------------------------------------------------------------- per device
+struct DevState {
+  bool ready = false;
+  int* err = nullptr;
+  int num_sms = 0;
+};
+std::mutex g_dev_mu;
+DevState g_dev[64];
+
+hb_status device_state(DevState** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= 64) return fail(HB_ERR_UNSUPPORTED, "device index %d", dev);
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DevState& d = g_dev[dev];
+  if (!d.ready) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_hb_device_error);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(error word)");
+    e = cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+    d.err = static_cast<int*>(p);
+    d.ready = true;
+  }
+  *out = &d;
+  return HB_OK;
+}
+
+// ---------------------------------------------------------------- TMA maps
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+hb_status get_encoder() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  if (!g_encode) return fail(HB_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+  return HB_OK;
+}
+
+hb_status encode_map(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims,
+                     const cuuint64_t* strides_bytes, const cuuint32_t* box,
+                     const char* what) {
+  cuuint32_t elem[5] = {1, 1, 1, 1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank,
+                        const_cast<void*>(base), dims, strides_bytes, box, elem,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(HB_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed: %d", what, (int)r);
+  return HB_OK;
+}
+
+// ---------------------------------------------------------------- timing
+struct TimingRec {
+  cudaEvent_t a, b;
+  int kernel;
+};
+std::mutex g_time_mu;
+bool g_timing = false;
+std::vector<TimingRec> g_recs;
+std::vector<cudaEvent_t> g_event_pool;
+constexpr size_t kMaxTimingRecs = 1 << 14;
+
+cudaEvent_t pool_event() {
+  if (!g_event_pool.empty()) {
+    cudaEvent_t e = g_event_pool.back();
+    g_event_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+  return e;
+}
+
+// Bracket one launch with events when timing is on.
+struct LaunchTimer {
+  TimingRec rec{};
+  bool on = false;
+  cudaStream_t s;
+  LaunchTimer(int kernel, cudaStream_t stream) : s(stream) {
+    std::lock_guard<std::mutex> lk(g_time_mu);
+    if (!g_timing || g_recs.size() >= kMaxTimingRecs) return;
+    rec.a = pool_event();
+    rec.b = pool_event();
+    rec.kernel = kernel;
+    if (!rec.a || !rec.b) return;
+    on = cudaEventRecord(rec.a, s) == cudaSuccess;
+  }
+  void done() {
+    if (!on) return;
+    if (cudaEventRecord(rec.b, s) != cudaSuccess) return;
+    std::lock_guard<std::mutex> lk(g_time_mu);
+    g_recs.push_back(rec);
+  }
+};
+
+// ---------------------------------------------------------------- checks
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+hb_status check_batch(const hb_batch* b) {
+  if (!b) return fail(HB_ERR_INVALID_ARG, "batch is NULL");
+  if (b->num_seqs < 0 || b->total_q < 0)
+    return fail(HB_ERR_SHAPE, "num_seqs (%d) and total_q (%d) must be >= 0", b->num_seqs, b->total_q);
+  if (b->total_q > 0 && b->num_seqs == 0)
+    return fail(HB_ERR_SHAPE, "total_q > 0 with no sequences");
+  if (b->page_size != kPageSize)
+    return fail(HB_ERR_UNSUPPORTED, "page_size %d (only 16 is built)", b->page_size);
+  if (b->head_dim != 64 && b->head_dim != 128)
+    return fail(HB_ERR_UNSUPPORTED, "head_dim %d (64 or 128 are built)", b->head_dim);
+  if (b->num_q_heads <= 0 || b->num_kv_heads <= 0 || b->num_q_heads % b->num_kv_heads)
+    return fail(HB_ERR_SHAPE, "num_q_heads (%d) must be a positive multiple of num_kv_heads (%d)",
+                b->num_q_heads, b->num_kv_heads);
+  const int g = b->num_q_heads / b->num_kv_heads;
+  if (g > kMaxGroup) return fail(HB_ERR_UNSUPPORTED, "group size %d > %d", g, kMaxGroup);
+  if (b->num_kv_heads > kDecodeKvhBlock && b->num_kv_heads % kDecodeKvhBlock)
+    return fail(HB_ERR_UNSUPPORTED, "num_kv_heads %d: more than 8 must be a multiple of 8",
+                b->num_kv_heads);
+  if (b->max_pages_per_seq <= 0 || b->num_pages <= 0)
+    return fail(HB_ERR_SHAPE, "max_pages_per_seq and num_pages must be > 0");
+  if ((int64_t)b->num_pages * kPageSize > 0x7fffffffLL)
+    return fail(HB_ERR_UNSUPPORTED, "num_pages %d too large", b->num_pages);
+  if (b->num_seqs > 0 && (!b->cu_q_len || !b->context_len || !b->block_table))
+    return fail(HB_ERR_INVALID_ARG, "cu_q_len, context_len and block_table must be non-NULL");
+  return HB_OK;
+}
+
+hb_status check_ptr(const void* p, const char* name) {
+  if (!p) return fail(HB_ERR_INVALID_ARG, "%s is NULL", name);
+  if (!aligned16(p)) return fail(HB_ERR_INVALID_ARG, "%s is not 16-byte aligned", name);
+  return HB_OK;
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+}  // namespace
+
+// =========================================================================
+extern "C" {
+
+const char* hb_last_error(void) { return t_err.c_str(); }
+
+const char* hb_status_string(hb_status s) {
+  switch (s) {
+    case HB_OK: return "HB_OK";
+    case HB_ERR_INVALID_ARG: return "HB_ERR_INVALID_ARG";
+    case HB_ERR_SHAPE: return "HB_ERR_SHAPE";
+    case HB_ERR_UNSUPPORTED: return "HB_ERR_UNSUPPORTED";
+    case HB_ERR_WORKSPACE: return "HB_ERR_WORKSPACE";
+    case HB_ERR_CUDA: return "HB_ERR_CUDA";
+    case HB_ERR_DEVICE_INDEX: return "HB_ERR_DEVICE_INDEX";
+    case HB_ERR_TIMEOUT: return "HB_ERR_TIMEOUT";
+    case HB_ERR_OUT_OF_PAGES: return "HB_ERR_OUT_OF_PAGES";
+  }
+  return "HB_ERR_UNKNOWN";
+}
+
+hb_status hb_kv_append(const hb_batch* batch, const void* k_new, const void* v_new,
+                       void* k_cache, void* v_cache, void* stream) {
+  try {
+    hb_status s = check_batch(batch);
+    if (s != HB_OK) return s;
+    if (batch->total_q == 0) return ok();
+    if ((s = check_ptr(k_new, "k_new")) != HB_OK) return s;
+    if ((s = check_ptr(v_new, "v_new")) != HB_OK) return s;
+    if ((s = check_ptr(k_cache, "k_cache")) != HB_OK) return s;
+    if ((s = check_ptr(v_cache, "v_cache")) != HB_OK) return s;
+    DevState* dev = nullptr;
+    if ((s = device_state(&dev)) != HB_OK) return s;
+    AppendParams p{};
+    p.cu_q_len = batch->cu_q_len;
+    p.context_len = batch->context_len;
+    p.block_table = batch->block_table;
+    p.num_seqs = batch->num_seqs;
+    p.total_q = batch->total_q;
+    p.max_pages_per_seq = batch->max_pages_per_seq;
+    p.num_pages = batch->num_pages;
+    p.row_vec16 = batch->num_kv_heads * batch->head_dim * 2 / 16;
+    p.k_new = static_cast<const uint16_t*>(k_new);
+    p.v_new = static_cast<const uint16_t*>(v_new);
+    p.k_cache = static_cast<uint16_t*>(k_cache);
+    p.v_cache = static_cast<uint16_t*>(v_cache);
+    p.dev_error = dev->err;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    LaunchTimer t(0, st);
+    cudaError_t e = launch_kv_append(p, dev->num_sms, st);
+    t.done();
+    if (e != cudaSuccess) return cuda_fail(e, "kv_append launch");
+    g_launches.fetch_add(1);
+    return ok();
+  } catch (...) {
+    return fail(HB_ERR_CUDA, "unexpected exception in hb_kv_append");
+  }
+}
+
+hb_status hb_plan(const hb_batch* batch, const int32_t* h_q_len,
+                  const int32_t* h_context_len, int32_t num_sms, void* h_plan,
+                  size_t* plan_bytes, void* d_workspace, size_t* workspace_bytes,
+                  void* stream) {
+  try {
+    hb_status s = check_batch(batch);
+    if (s != HB_OK) return s;
+    if (!plan_bytes || !workspace_bytes)
+      return fail(HB_ERR_INVALID_ARG, "plan_bytes and workspace_bytes must be non-NULL");
+    if (num_sms <= 0) return fail(HB_ERR_INVALID_ARG, "num_sms must be > 0");
+    const int S = batch->num_seqs;
+    if (S > 0 && (!h_q_len || !h_context_len))
+      return fail(HB_ERR_INVALID_ARG, "h_q_len and h_context_len must be non-NULL");
+    const int Hq = batch->num_q_heads, Hkv = batch->num_kv_heads, D = batch->head_dim;
+    const int g = Hq / Hkv;
+    const int64_t max_ctx = (int64_t)batch->max_pages_per_seq * kPageSize;
+    int64_t tq = 0;
+    for (int i = 0; i < S; ++i) {
+      if (h_q_len[i] < 1 || h_q_len[i] > h_context_len[i])
+        return fail(HB_ERR_SHAPE, "row %d: q_len %d, context_len %d (need 1 <= q_len <= context_len)",
+                    i, h_q_len[i], h_context_len[i]);
+      if (h_context_len[i] > max_ctx)
+        return fail(HB_ERR_SHAPE, "row %d: context_len %d exceeds max_pages_per_seq * 16", i,
+                    h_context_len[i]);
+      tq += h_q_len[i];
+    }
+    if (tq != batch->total_q)
+      return fail(HB_ERR_SHAPE, "sum of q_len (%lld) != total_q (%d)", (long long)tq, batch->total_q);
+
+    // ---- decode items: rows with q_len == 1, split over page ranges
+    const int kvhb = std::min(Hkv, kDecodeKvhBlock);
+    const int n_blocks = Hkv / kvhb;
+    int64_t total_pages = 0;
+    for (int i = 0; i < S; ++i)
+      if (h_q_len[i] == 1) total_pages += (int64_t)((h_context_len[i] + kPageSize - 1) / kPageSize) * n_blocks;
+    const int64_t target_items = 3LL * num_sms;
+    int split_pages = (int)std::max<int64_t>(8, (total_pages + target_items - 1) / std::max<int64_t>(1, target_items));
+    std::vector<DecodeItem> dec;
+    int n_slots = 0, n_merge = 0;
+    for (int i = 0; i < S; ++i) {
+      if (h_q_len[i] != 1) continue;
+      const int np = (h_context_len[i] + kPageSize - 1) / kPageSize;
+      const int ns = (np + split_pages - 1) / split_pages;
+      const int per = (np + ns - 1) / ns;
+      for (int b = 0; b < n_blocks; ++b) {
+        int slot = 0, merge_id = 0;
+        if (ns > 1) {
+          slot = n_slots;
+          n_slots += ns;
+          merge_id = n_merge++;
+        }
+        for (int k = 0; k < ns; ++k) {
+          DecodeItem it{};
+          it.seq = i;
+          it.kvh0 = b * kvhb;
+          it.page_begin = k * per;
+          it.page_end = std::min(np, (k + 1) * per);
+          it.split = k;
+          it.n_splits = ns;
+          it.slot = slot;
+          it.merge_id = merge_id;
+          if (it.page_begin < it.page_end) dec.push_back(it);
+        }
+      }
+    }
+    // a split with an empty range can only appear when per * (ns-1) >= np,
+    // which the ceil-division above rules out; keep n_splits consistent anyway
+    std::stable_sort(dec.begin(), dec.end(), [](const DecodeItem& a, const DecodeItem& b) {
+      return (a.page_end - a.page_begin) > (b.page_end - b.page_begin);
+    });
+
+    // ---- chunk items: rows with q_len > 1, (kv head, query tile)
+    const int tpt = kChunkRows / g;
+    std::vector<ChunkItem> chk;
+    for (int i = 0; i < S; ++i) {
+      if (h_q_len[i] == 1) continue;
+      const int off = h_context_len[i] - h_q_len[i];
+      for (int kvh = 0; kvh < Hkv; ++kvh)
+        for (int t0 = 0; t0 < h_q_len[i]; t0 += tpt) {
+          ChunkItem c{};
+          c.seq = i;
+          c.kv_head = kvh;
+          c.tok0 = t0;
+          c.ntok = std::min(tpt, h_q_len[i] - t0);
+          c.kv_tiles = (off + t0 + c.ntok + kChunkKeys - 1) / kChunkKeys;
+          chk.push_back(c);
+        }
+    }
+    std::stable_sort(chk.begin(), chk.end(), [](const ChunkItem& a, const ChunkItem& b) {
+      return a.kv_tiles > b.kv_tiles;
+    });
+
+    // ---- sizes
+    const size_t items_bytes = align_up(dec.size() * sizeof(DecodeItem) + chk.size() * sizeof(ChunkItem), 256);
+    const size_t need_plan = sizeof(PlanHeader) + items_bytes;
+    const size_t ws_counters = items_bytes;
+    const size_t ws_partial_o = align_up(ws_counters + (size_t)(kCounterMerge0 + n_merge) * 4, 256);
+    const size_t ws_partial_ml = align_up(ws_partial_o + (size_t)n_slots * Hq * D * 4, 256);
+    const size_t ws_total = std::max<size_t>(256, align_up(ws_partial_ml + (size_t)n_slots * Hq * 8, 256));
+
+    const size_t have_plan = *plan_bytes, have_ws = *workspace_bytes;
+    *plan_bytes = need_plan;
+    *workspace_bytes = ws_total;
+    if (h_plan == nullptr) return ok();  // size query
+    if (have_plan < need_plan)
+      return fail(HB_ERR_WORKSPACE, "plan buffer has %zu bytes, needs %zu", have_plan, need_plan);
+    if (d_workspace != nullptr) {
+      if (have_ws < ws_total)
+        return fail(HB_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", have_ws, ws_total);
+      if ((reinterpret_cast<uintptr_t>(d_workspace) & 255u) != 0)
+        return fail(HB_ERR_INVALID_ARG, "d_workspace must be 256-byte aligned");
+    }
+
+    PlanHeader h{};
+    h.magic = kPlanMagic;
+    h.version = kPlanVersion;
+    h.num_seqs = S;
+    h.total_q = batch->total_q;
+    h.num_q_heads = Hq;
+    h.num_kv_heads = Hkv;
+    h.head_dim = D;
+    h.page_size = batch->page_size;
+    h.max_pages_per_seq = batch->max_pages_per_seq;
+    h.num_sms = num_sms;
+    h.num_decode_items = (int32_t)dec.size();
+    h.num_chunk_items = (int32_t)chk.size();
+    h.num_partial_slots = n_slots;
+    h.num_merge_counters = n_merge;
+    h.decode_grid = (int32_t)std::min<size_t>((size_t)num_sms, dec.size());
+    h.decode_kvh_block = kvhb;
+    h.chunk_tokens_per_tile = tpt;
+    h.items_bytes = items_bytes;
+    h.ws_counters = ws_counters;
+    h.ws_partial_o = ws_partial_o;
+    h.ws_partial_ml = ws_partial_ml;
+    h.ws_total = ws_total;
+    h.plan_bytes = need_plan;
+    uint8_t* hp = static_cast<uint8_t*>(h_plan);
+    std::memset(hp, 0, need_plan);
+    std::memcpy(hp, &h, sizeof(h));
+    uint8_t* items = hp + sizeof(PlanHeader);
+    if (!dec.empty()) std::memcpy(items, dec.data(), dec.size() * sizeof(DecodeItem));
+    if (!chk.empty())
+      std::memcpy(items + dec.size() * sizeof(DecodeItem), chk.data(), chk.size() * sizeof(ChunkItem));
+
+    if (d_workspace == nullptr) return ok();  // host plan only
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemcpyAsync(d_workspace, items, items_bytes, cudaMemcpyHostToDevice, st);
+    if (e != cudaSuccess) return cuda_fail(e, "plan upload");
+    e = cudaMemsetAsync(static_cast<uint8_t*>(d_workspace) + ws_counters, 0,
+                        ws_partial_o - ws_counters, st);
+    if (e != cudaSuccess) return cuda_fail(e, "workspace counter reset");
+    return ok();
+  } catch (...) {
+    return fail(HB_ERR_CUDA, "unexpected exception in hb_plan");
+  }
+}
+
+hb_status hb_attention(const hb_batch* batch, const void* h_plan, const void* q,
+                       const void* k_cache, const void* v_cache, float softmax_scale,
+                       void* out, void* d_workspace, void* stream) {
+  try {
+    hb_status s = check_batch(batch);
+    if (s != HB_OK) return s;
+    if (!h_plan) return fail(HB_ERR_INVALID_ARG, "h_plan is NULL");
+    PlanHeader h;
+    std::memcpy(&h, h_plan, sizeof(h));
+    if (h.magic != kPlanMagic || h.version != kPlanVersion)
+      return fail(HB_ERR_WORKSPACE, "h_plan is not a plan written by hb_plan");
+    if (h.num_seqs != batch->num_seqs || h.total_q != batch->total_q ||
+        h.num_q_heads != batch->num_q_heads || h.num_kv_heads != batch->num_kv_heads ||
+        h.head_dim != batch->head_dim || h.page_size != batch->page_size ||
+        h.max_pages_per_seq != batch->max_pages_per_seq)
+      return fail(HB_ERR_WORKSPACE, "plan was made for a different batch geometry");
+    if (batch->total_q == 0) return ok();
+    if (!(softmax_scale > 0.f) && !(softmax_scale <= 0.f))
+      return fail(HB_ERR_INVALID_ARG, "softmax_scale is NaN");
+    if ((s = check_ptr(q, "q")) != HB_OK) return s;
+    if ((s = check_ptr(out, "out")) != HB_OK) return s;
+    if ((s = check_ptr(k_cache, "k_cache")) != HB_OK) return s;
+    if ((s = check_ptr(v_cache, "v_cache")) != HB_OK) return s;
+    if (!d_workspace || (reinterpret_cast<uintptr_t>(d_workspace) & 255u))
+      return fail(HB_ERR_INVALID_ARG, "d_workspace must be non-NULL and 256-byte aligned");
+    DevState* dev = nullptr;
+    if ((s = device_state(&dev)) != HB_OK) return s;
+    if ((s = get_encoder()) != HB_OK) return s;
+
+    const int Hq = batch->num_q_heads, Hkv = batch->num_kv_heads, D = batch->head_dim;
+    const int g = Hq / Hkv;
+    const float scale_log2 = softmax_scale * 1.4426950408889634f;
+    uint8_t* ws = static_cast<uint8_t*>(d_workspace);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+    if (h.num_decode_items > 0) {
+      const int kvhb = h.decode_kvh_block;
+      CUtensorMap kmap, vmap;
+      // pools viewed as [page][kv head][slot][head dim] boxes: dims are
+      // (D, slot, kv head, page) with the pool's own strides
+      const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)kPageSize, (cuuint64_t)Hkv,
+                                  (cuuint64_t)batch->num_pages};
+      const cuuint64_t strides[3] = {(cuuint64_t)Hkv * D * 2, (cuuint64_t)D * 2,
+                                     (cuuint64_t)kPageSize * Hkv * D * 2};
+      const cuuint32_t box[4] = {64, (cuuint32_t)kPageSize, (cuuint32_t)kvhb, 1};
+      if ((s = encode_map(&kmap, k_cache, 4, dims, strides, box, "decode K")) != HB_OK) return s;
+      if ((s = encode_map(&vmap, v_cache, 4, dims, strides, box, "decode V")) != HB_OK) return s;
+      DecodeParams p{};
+      p.items = reinterpret_cast<const DecodeItem*>(ws);
+      p.num_items = h.num_decode_items;
+      p.counters = reinterpret_cast<int32_t*>(ws + h.ws_counters);
+      p.part_o = reinterpret_cast<float*>(ws + h.ws_partial_o);
+      p.part_ml = reinterpret_cast<float*>(ws + h.ws_partial_ml);
+      p.cu_q_len = batch->cu_q_len;
+      p.context_len = batch->context_len;
+      p.block_table = batch->block_table;
+      p.max_pages_per_seq = batch->max_pages_per_seq;
+      p.num_pages = batch->num_pages;
+      p.q = static_cast<const uint16_t*>(q);
+      p.out = static_cast<uint16_t*>(out);
+      p.num_q_heads = Hq;
+      p.num_kv_heads = Hkv;
+      p.group = g;
+      p.kvh_block = kvhb;
+      p.scale_log2 = scale_log2;
+      p.dev_error = dev->err;
+      LaunchTimer t(1, st);
+      cudaError_t e = launch_decode(p, D, h.decode_grid, kmap, vmap, st);
+      t.done();
+      if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+      g_launches.fetch_add(1);
+    }
+    if (h.num_chunk_items > 0) {
+      const int tpt = h.chunk_tokens_per_tile;
+      CUtensorMap qmap, kmap, vmap;
+      const cuuint64_t qdims[3] = {(cuuint64_t)D, (cuuint64_t)Hq, (cuuint64_t)batch->total_q};
+      const cuuint64_t qstr[2] = {(cuuint64_t)D * 2, (cuuint64_t)Hq * D * 2};
+      const cuuint32_t qbox[3] = {64, (cuuint32_t)g, (cuuint32_t)tpt};
+      if ((s = encode_map(&qmap, q, 3, qdims, qstr, qbox, "chunk Q")) != HB_OK) return s;
+      const cuuint64_t kdims[3] = {(cuuint64_t)D, (cuuint64_t)Hkv,
+                                   (cuuint64_t)batch->num_pages * kPageSize};
+      const cuuint64_t kstr[2] = {(cuuint64_t)D * 2, (cuuint64_t)Hkv * D * 2};
+      const cuuint32_t kbox[3] = {64, 1, (cuuint32_t)kPageSize};
+      if ((s = encode_map(&kmap, k_cache, 3, kdims, kstr, kbox, "chunk K")) != HB_OK) return s;
+      if ((s = encode_map(&vmap, v_cache, 3, kdims, kstr, kbox, "chunk V")) != HB_OK) return s;
+      ChunkParams p{};
+      p.items = reinterpret_cast<const ChunkItem*>(ws + (size_t)h.num_decode_items * sizeof(DecodeItem));
+      p.num_items = h.num_chunk_items;
+      p.cu_q_len = batch->cu_q_len;
+      p.context_len = batch->context_len;
+      p.block_table = batch->block_table;
+      p.max_pages_per_seq = batch->max_pages_per_seq;
+      p.num_pages = batch->num_pages;
+      p.out = static_cast<uint16_t*>(out);
+      p.num_q_heads = Hq;
+      p.num_kv_heads = Hkv;
+      p.group = g;
+      p.tokens_per_tile = tpt;
+      p.scale_log2 = scale_log2;
+      p.dev_error = dev->err;
+      LaunchTimer t(2, st);
+      cudaError_t e = launch_chunk(p, D, qmap, kmap, vmap, st);
+      t.done();
+      if (e != cudaSuccess) return cuda_fail(e, "chunk launch");
+      g_launches.fetch_add(1);
+    }
+    return ok();
+  } catch (...) {
+    return fail(HB_ERR_CUDA, "unexpected exception in hb_attention");
+  }
+}
+
+hb_status hb_check(void* stream) {
+  try {
+    DevState* dev = nullptr;
+    hb_status s = device_state(&dev);
+    if (s != HB_OK) return s;
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
+    int v = 0;
+    e = cudaMemcpy(&v, dev->err, sizeof(int), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "reading the device error word");
+    if (v == 0) return ok();
+    const int zero = 0;
+    cudaMemcpy(dev->err, &zero, sizeof(int), cudaMemcpyHostToDevice);
+    if (v & HB_DEVERR_INDEX)
+      return fail(HB_ERR_DEVICE_INDEX, "a kernel met a page index outside [0, num_pages) (word %d)", v);
+    return fail(HB_ERR_TIMEOUT, "a kernel wait gave up (word %d)", v);
+  } catch (...) {
+    return fail(HB_ERR_CUDA, "unexpected exception in hb_check");
+  }
+}
+
+hb_status hb_timing_enable(int32_t enable) {
+  std::lock_guard<std::mutex> lk(g_time_mu);
+  for (auto& r : g_recs) {
+    g_event_pool.push_back(r.a);
+    g_event_pool.push_back(r.b);
+  }
+  g_recs.clear();
+  g_timing = enable != 0;
+  return ok();
+}
+
+hb_status hb_timing_read(double* total_ms, int32_t* launches) {
+  if (!total_ms || !launches) return fail(HB_ERR_INVALID_ARG, "NULL output");
+  std::lock_guard<std::mutex> lk(g_time_mu);
+  for (int k = 0; k < HB_NUM_KERNEL_IDS; ++k) {
+    total_ms[k] = 0.0;
+    launches[k] = 0;
+  }
+  for (auto& r : g_recs) {
+    cudaError_t e = cudaEventSynchronize(r.b);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaEventSynchronize");
+    float ms = 0.f;
+    e = cudaEventElapsedTime(&ms, r.a, r.b);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaEventElapsedTime");
+    if (r.kernel >= 0 && r.kernel < HB_NUM_KERNEL_IDS) {
+      total_ms[r.kernel] += ms;
+      launches[r.kernel] += 1;
+    }
+  }
+  return ok();
+}
+
+int64_t hb_launch_count(void) { return g_launches.load(); }
+
+}  // extern "C"

@@ -1,0 +1,451 @@
+// decode.cu -- attention of decode rows (one new token over a long cached
+// context), split over the keys, read through the block table.
+//
+// "Sarathi-Serve：以 chunked-prefills 与 stall-free batching 驯服 LLM 推理的吞吐—
+// 延迟权衡", §GPU / 系统数据路径 ⑤: a decode reads all earlier KV of its
+// sequence every step; "In-flight Batching", §LLM 推理的两阶段计算特征: decode is
+// memory-bound (every step reads the whole KV cache).  So this kernel is
+// built to stream KV pages at HBM speed:
+//
+//  * persistent: one CTA per SM pulls work items (a page range of one decode
+//    row and one block of <= 8 kv heads) from an atomic counter; items are
+//    ordered longest first by the host plan;
+//  * one producer warp streams whole pages (all kv heads of the block, K and
+//    V) into a ring of shared-memory stages with 4-D TMA copies laid out as
+//    [kv head][slot][64 head-dim] rows with the 128-byte swizzle, so the
+//    consumer's ldmatrix reads are bank-conflict free; the q row of each item
+//    arrives by a bulk copy into a two-slot ring;
+//  * eight consumer warps, one per kv head: the GQA group (g <= 16 q heads)
+//    forms the rows of a 16 x 16 x 16 warp MMA, so each K/V element loaded
+//    from shared memory serves all g heads; online softmax in registers with
+//    the exp2 form (scale * log2 e folded in);
+//  * split-KV partial states (m, l, unnormalised o) go to the workspace; the
+//    last split of a (row, kv block) to finish, found with an atomic counter,
+//    merges them: m = max m_i, l = sum 2^(m_i - m) l_i, o = sum 2^(m_i - m) o_i
+//    / l.  Nobody waits on another CTA.
+//
+// Bytes per decode row: 2 * context * Hkv * D * 2 (K and V read once).
+#include <cuda_runtime.h>
+
+#include "hb_internal.h"
+#include "ptx.cuh"
+
+namespace hb {
+
+constexpr int kDecConsumerWarps = 8;
+constexpr int kDecThreads = 32 * (kDecConsumerWarps + 1);
+constexpr int kDecMaxStages = 8;
+constexpr int kHdrFirst = 1, kHdrLast = 2, kHdrEnd = 4;
+
+struct StageHeader {
+  DecodeItem item;
+  int32_t lpage;
+  int32_t flags;
+  int32_t qslot;
+  int32_t ctx;
+  int32_t tok;
+  int32_t pad[3];
+};
+static_assert(sizeof(StageHeader) == 64, "stage header size");
+
+struct DecodeLayout {
+  int32_t n_stages;
+  int32_t chunk_bytes;   // one 64-wide head-dim chunk of one page, all heads
+  int32_t half_bytes;    // K (or V) part of a stage
+  int32_t stage_bytes;
+  int32_t qslot_bytes;
+  int32_t smem_bytes;    // dynamic shared memory to request (with alignment)
+};
+
+__host__ DecodeLayout decode_layout(int head_dim, int kvh_block, int group) {
+  DecodeLayout L{};
+  const int ch = head_dim / 64;
+  L.chunk_bytes = kvh_block * kPageSize * 128;
+  L.half_bytes = ch * L.chunk_bytes;
+  L.stage_bytes = 2 * L.half_bytes;
+  L.qslot_bytes = ((kvh_block * group * head_dim * 2) + 1023) / 1024 * 1024;
+  const int fixed = 1024 /*align*/ + 2 * L.qslot_bytes +
+                    kDecMaxStages * (int)sizeof(StageHeader) +
+                    (2 * kDecMaxStages + 4) * 8 + 64;
+  const int budget = 227 * 1024;
+  int s = (budget - fixed) / L.stage_bytes;
+  if (s > kDecMaxStages) s = kDecMaxStages;
+  L.n_stages = s;
+  L.smem_bytes = fixed + s * L.stage_bytes;
+  return L;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kDecThreads, 1)
+    decode_kernel(const DecodeParams p, const DecodeLayout L,
+                  const __grid_constant__ CUtensorMap kmap,
+                  const __grid_constant__ CUtensorMap vmap) {
+  constexpr int CH = D / 64;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+
+  const int S = L.n_stages;
+  uint8_t* stages = smem;
+  uint8_t* qbuf = smem + S * L.stage_bytes;
+  StageHeader* hdr = reinterpret_cast<StageHeader*>(qbuf + 2 * L.qslot_bytes);
+  uint64_t* full = reinterpret_cast<uint64_t*>(hdr + kDecMaxStages);
+  uint64_t* empty = full + kDecMaxStages;
+  uint64_t* qfull = empty + kDecMaxStages;
+  uint64_t* qempty = qfull + 2;
+  int* flags = reinterpret_cast<int*>(qempty + 2);  // [0] abort, [1] merge
+  volatile int* abort_flag = flags;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int g = p.group;
+  const int kvhb = p.kvh_block;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kDecConsumerWarps);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&qfull[i], 1);
+      mbar_init(&qempty[i], kDecConsumerWarps);
+    }
+    flags[0] = 0;
+    flags[1] = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == kDecConsumerWarps) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&kmap);
+      tma_prefetch_desc(&vmap);
+      int st = 0;
+      uint32_t ph = 0;
+      int qslot = 0;
+      uint32_t qph[2] = {0u, 0u};
+      bool issued[kDecMaxStages];
+      uint32_t last_par[kDecMaxStages];
+      for (int s = 0; s < kDecMaxStages; ++s) {
+        issued[s] = false;
+        last_par[s] = 0;
+      }
+      const uint32_t page_tx = 2u * (uint32_t)L.half_bytes;
+      const uint32_t qbytes = (uint32_t)(kvhb * g * D * 2);
+      bool ok = true;
+      while (ok) {
+        const int idx = atomicAdd(&p.counters[kCounterWork], 1);
+        if (idx >= p.num_items) break;
+        const DecodeItem it = p.items[idx];
+        const int ctx = __ldg(&p.context_len[it.seq]);
+        const int tok = __ldg(&p.cu_q_len[it.seq]);
+        if (!mbar_wait(&qempty[qslot], qph[qslot] ^ 1u, abort_flag)) {
+          ok = false;
+          break;
+        }
+        qph[qslot] ^= 1u;
+        mbar_arrive_expect_tx(&qfull[qslot], qbytes);
+        bulk_load(qbuf + qslot * L.qslot_bytes,
+                  p.q + ((size_t)tok * p.num_q_heads + (size_t)it.kvh0 * g) * D,
+                  qbytes, &qfull[qslot]);
+        for (int lp = it.page_begin; lp < it.page_end; ++lp) {
+          if (!mbar_wait(&empty[st], ph ^ 1u, abort_flag)) {
+            ok = false;
+            break;
+          }
+          StageHeader& h = hdr[st];
+          h.item = it;
+          h.lpage = lp;
+          h.flags = (lp == it.page_begin ? kHdrFirst : 0) |
+                    (lp == it.page_end - 1 ? kHdrLast : 0);
+          h.qslot = qslot;
+          h.ctx = ctx;
+          h.tok = tok;
+          int phys = -1;
+          if (lp < p.max_pages_per_seq)
+            phys = __ldg(&p.block_table[(size_t)it.seq * p.max_pages_per_seq + lp]);
+          if (phys < 0 || phys >= p.num_pages) {
+            report_error(p.dev_error, HB_DEVERR_INDEX);
+            phys = p.num_pages;  // whole box out of range: the copy reads zeros
+          }
+          mbar_arrive_expect_tx(&full[st], page_tx);
+          uint8_t* kd = stages + st * L.stage_bytes;
+#pragma unroll
+          for (int c = 0; c < CH; ++c) {
+            tma_load_4d(kd + c * L.chunk_bytes, &kmap, &full[st], c * 64, 0,
+                        it.kvh0, phys);
+            tma_load_4d(kd + L.half_bytes + c * L.chunk_bytes, &vmap, &full[st],
+                        c * 64, 0, it.kvh0, phys);
+          }
+          issued[st] = true;
+          last_par[st] = ph;
+          if (++st == S) {
+            st = 0;
+            ph ^= 1u;
+          }
+        }
+        qslot ^= 1;
+      }
+      if (ok && mbar_wait(&empty[st], ph ^ 1u, abort_flag)) {
+        hdr[st].flags = kHdrEnd;
+        issued[st] = false;  // its earlier copy was consumed
+        mbar_arrive(&full[st]);
+      }
+      for (int s = 0; s < S; ++s)
+        if (issued[s]) drain_wait(&full[s], last_par[s], abort_flag);
+      const int done = atomicAdd(&p.counters[kCounterDone], 1);
+      if (done == (int)gridDim.x - 1) {
+        p.counters[kCounterWork] = 0;
+        p.counters[kCounterDone] = 0;
+        __threadfence();
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ consumers
+    const int w = warp;                  // local kv head of this warp
+    const bool active = w < kvhb;
+    const bool hi_rows = g > 8;          // rows 8..15 of the MMA in use
+    const int r = lane >> 2;             // MMA row (q head in group)
+    const int cq = lane & 3;
+    uint32_t qa[D / 16][4];
+    float o[D / 8][4];
+    float m_run[2], l_run[2];
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk)
+      qa[kk][0] = qa[kk][1] = qa[kk][2] = qa[kk][3] = 0u;
+#pragma unroll
+    for (int nt = 0; nt < D / 8; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
+    m_run[0] = m_run[1] = -INFINITY;
+    l_run[0] = l_run[1] = 0.f;
+
+    int st = 0;
+    uint32_t ph = 0;
+    uint32_t qph[2] = {0u, 0u};
+    while (true) {
+      if (!mbar_wait(&full[st], ph, abort_flag)) break;
+      const StageHeader h = hdr[st];
+      if (h.flags & kHdrEnd) break;
+      if (h.flags & kHdrFirst) {
+        if (!mbar_wait(&qfull[h.qslot], qph[h.qslot], abort_flag)) break;
+        qph[h.qslot] ^= 1u;
+        if (active) {
+          const uint16_t* qs =
+              reinterpret_cast<const uint16_t*>(qbuf + h.qslot * L.qslot_bytes) +
+              (size_t)w * g * D;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const int c0 = kk * 16 + cq * 2;
+            qa[kk][0] = (r < g) ? *reinterpret_cast<const uint32_t*>(qs + r * D + c0) : 0u;
+            qa[kk][1] = (r + 8 < g) ? *reinterpret_cast<const uint32_t*>(qs + (r + 8) * D + c0) : 0u;
+            qa[kk][2] = (r < g) ? *reinterpret_cast<const uint32_t*>(qs + r * D + c0 + 8) : 0u;
+            qa[kk][3] = (r + 8 < g) ? *reinterpret_cast<const uint32_t*>(qs + (r + 8) * D + c0 + 8) : 0u;
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&qempty[h.qslot]);
+#pragma unroll
+        for (int nt = 0; nt < D / 8; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
+        m_run[0] = m_run[1] = -INFINITY;
+        l_run[0] = l_run[1] = 0.f;
+      }
+
+      if (active) {
+        uint8_t* kst = stages + st * L.stage_bytes;
+        uint8_t* vst = kst + L.half_bytes;
+        const uint32_t kbase = smem_u32(kst);
+        const uint32_t vbase = smem_u32(vst);
+        const int valid = min(kPageSize, h.ctx - h.lpage * kPageSize);
+        if (valid < kPageSize) {
+          // Slots past the context were never written: clear this kv head's
+          // V rows there so that P = 0 never meets a NaN in the PV product.
+          const int nrow = kPageSize - valid;
+          for (int e = lane; e < nrow * CH * 8; e += 32) {
+            const int row = valid + e / (CH * 8);
+            const int rem = e % (CH * 8);
+            const int c = rem / 8, u = rem % 8;
+            uint4* dst = reinterpret_cast<uint4*>(vst + c * L.chunk_bytes +
+                                                  (w * kPageSize + row) * 128 + u * 16);
+            *dst = make_uint4(0u, 0u, 0u, 0u);
+          }
+          fence_async_shared();
+          __syncwarp();
+        }
+        // S = Q K^T over the page's 16 tokens (two n8 tiles)
+        float s[2][4];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+        {
+          const int mi = lane >> 3, r8 = lane & 7;
+          const int tokr = ((mi >> 1) << 3) + r8;
+          const uint32_t rowaddr = kbase + (uint32_t)((w * kPageSize + tokr) * 128);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const int unit = ((kk & 3) << 1) + (mi & 1);
+            const uint32_t addr = rowaddr + (uint32_t)((kk >> 2) * L.chunk_bytes) +
+                                  (uint32_t)(((unit ^ (tokr & 7)) << 4));
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4(addr, b0, b1, b2, b3);
+            mma_bf16_16816(s[0], qa[kk], b0, b1);
+            mma_bf16_16816(s[1], qa[kk], b2, b3);
+          }
+        }
+        // scale, mask, online softmax (rows r and r + 8)
+        uint32_t pa[4];
+#pragma unroll
+        for (int hr = 0; hr < 2; ++hr) {
+          if (hr == 1 && !hi_rows) {
+            pa[1] = pa[3] = 0u;
+            continue;
+          }
+          float v[4];
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int t = nt * 8 + cq * 2 + e;
+              v[nt * 2 + e] = (t < valid) ? s[nt][hr * 2 + e] * p.scale_log2 : -INFINITY;
+            }
+          float mx = fmaxf(fmaxf(v[0], v[1]), fmaxf(v[2], v[3]));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+          const float m_new = fmaxf(m_run[hr], mx);
+          const float alpha = fast_exp2(m_run[hr] - m_new);
+          m_run[hr] = m_new;
+          const uint32_t lo = pack_bf16x2(fast_exp2(v[0] - m_new), fast_exp2(v[1] - m_new));
+          const uint32_t hi = pack_bf16x2(fast_exp2(v[2] - m_new), fast_exp2(v[3] - m_new));
+          // the row sum uses the same bf16-rounded P that feeds the MMA
+          l_run[hr] = l_run[hr] * alpha + (bf16lo_to_f32(lo) + bf16hi_to_f32(lo)) +
+                      (bf16lo_to_f32(hi) + bf16hi_to_f32(hi));
+#pragma unroll
+          for (int nt = 0; nt < D / 8; ++nt) {
+            o[nt][hr * 2] *= alpha;
+            o[nt][hr * 2 + 1] *= alpha;
+          }
+          pa[hr] = lo;       // A rows r (+8), tokens 0..7
+          pa[hr + 2] = hi;   // tokens 8..15
+        }
+        // O += P V
+        {
+          const int mi = lane >> 3, r8 = lane & 7;
+          const int tokr = ((mi & 1) << 3) + r8;
+          const uint32_t rowaddr = vbase + (uint32_t)((w * kPageSize + tokr) * 128);
+#pragma unroll
+          for (int jj = 0; jj < D / 16; ++jj) {
+            const int u = 2 * jj + (mi >> 1);   // 8-wide head-dim block
+            const uint32_t addr = rowaddr + (uint32_t)((u >> 3) * L.chunk_bytes) +
+                                  (uint32_t)((((u & 7) ^ (tokr & 7)) << 4));
+            uint32_t v0, v1, v2, v3;
+            ldsm_x4_trans(addr, v0, v1, v2, v3);
+            mma_bf16_16816(o[2 * jj], pa, v0, v1);
+            mma_bf16_16816(o[2 * jj + 1], pa, v2, v3);
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[st]);
+
+      if (h.flags & kHdrLast) {
+        const DecodeItem& it = h.item;
+        const int Hq = p.num_q_heads;
+        if (active) {
+          float l_tot[2];
+#pragma unroll
+          for (int hr = 0; hr < 2; ++hr) {
+            float t = l_run[hr];
+            t += __shfl_xor_sync(0xffffffffu, t, 1);
+            t += __shfl_xor_sync(0xffffffffu, t, 2);
+            l_tot[hr] = t;
+          }
+          const int head0 = (it.kvh0 + w) * g;
+#pragma unroll
+          for (int hr = 0; hr < 2; ++hr) {
+            const int row = r + 8 * hr;
+            if (row >= g) continue;
+            if (it.n_splits == 1) {
+              const float inv = 1.f / l_tot[hr];
+              uint32_t* dst = reinterpret_cast<uint32_t*>(
+                  p.out + ((size_t)h.tok * Hq + head0 + row) * D + cq * 2);
+#pragma unroll
+              for (int nt = 0; nt < D / 8; ++nt)
+                dst[nt * 4] = pack_bf16x2(o[nt][hr * 2] * inv, o[nt][hr * 2 + 1] * inv);
+            } else {
+              const size_t slot = (size_t)(it.slot + it.split);
+              float2* dst = reinterpret_cast<float2*>(
+                  p.part_o + (slot * Hq + head0 + row) * D + cq * 2);
+#pragma unroll
+              for (int nt = 0; nt < D / 8; ++nt)
+                dst[nt * 4] = make_float2(o[nt][hr * 2], o[nt][hr * 2 + 1]);
+              if (cq == 0) {
+                float2* ml = reinterpret_cast<float2*>(p.part_ml) + slot * Hq + head0 + row;
+                *ml = make_float2(m_run[hr], l_tot[hr]);
+              }
+            }
+          }
+        }
+        if (it.n_splits > 1) {
+          __threadfence();
+          named_bar_sync(1, 32 * kDecConsumerWarps);
+          if (threadIdx.x == 0) {
+            const int old = atomicAdd(&p.counters[kCounterMerge0 + it.merge_id], 1);
+            flags[1] = (old == it.n_splits - 1) ? 1 : 0;
+          }
+          named_bar_sync(1, 32 * kDecConsumerWarps);
+          if (flags[1]) {
+            __threadfence();
+            const int n_el = kvhb * g * D;
+            const float2* ml = reinterpret_cast<const float2*>(p.part_ml);
+            for (int e = threadIdx.x; e < n_el; e += 32 * kDecConsumerWarps) {
+              const int hh = it.kvh0 * g + e / D;
+              const int d = e % D;
+              float mmax = -INFINITY;
+              for (int i = 0; i < it.n_splits; ++i)
+                mmax = fmaxf(mmax, __ldcg(&ml[(size_t)(it.slot + i) * Hq + hh]).x);
+              float acc = 0.f, lsum = 0.f;
+              for (int i = 0; i < it.n_splits; ++i) {
+                const size_t slot = (size_t)(it.slot + i);
+                const float2 st2 = __ldcg(&ml[slot * Hq + hh]);
+                const float wgt = fast_exp2(st2.x - mmax);
+                lsum += wgt * st2.y;
+                acc += wgt * __ldcg(&p.part_o[(slot * Hq + hh) * D + d]);
+              }
+              const float val = acc / lsum;
+              p.out[((size_t)h.tok * Hq + hh) * D + d] =
+                  (uint16_t)(pack_bf16x2(val, 0.f) & 0xFFFFu);
+            }
+            if (threadIdx.x == 0) p.counters[kCounterMerge0 + it.merge_id] = 0;
+          }
+        }
+      }
+      if (++st == S) {
+        st = 0;
+        ph ^= 1u;
+      }
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && *abort_flag) report_error(p.dev_error, HB_DEVERR_TIMEOUT);
+}
+
+cudaError_t launch_decode(const DecodeParams& p, int head_dim, int grid,
+                          const CUtensorMap& kmap, const CUtensorMap& vmap,
+                          cudaStream_t stream) {
+  if (p.num_items == 0 || grid == 0) return cudaSuccess;
+  const DecodeLayout L = decode_layout(head_dim, p.kvh_block, p.group);
+  if (L.n_stages < 2) return cudaErrorInvalidConfiguration;
+  cudaError_t e;
+  if (head_dim == 128) {
+    e = cudaFuncSetAttribute(decode_kernel<128>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, L.smem_bytes);
+    if (e != cudaSuccess) return e;
+    decode_kernel<128><<<grid, kDecThreads, L.smem_bytes, stream>>>(p, L, kmap, vmap);
+  } else {
+    e = cudaFuncSetAttribute(decode_kernel<64>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, L.smem_bytes);
+    if (e != cudaSuccess) return e;
+    decode_kernel<64><<<grid, kDecThreads, L.smem_bytes, stream>>>(p, L, kmap, vmap);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace hb

@@ -1,0 +1,132 @@
+// hb_internal.h -- plan layout, work items and kernel parameter blocks shared
+// by the host side of libhb (api.cu) and its kernels.  Not part of the ABI.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#define HB_DEVERR_INDEX 1
+#define HB_DEVERR_TIMEOUT 2
+
+#if defined(__CUDACC__)
+#define HB_HD __host__ __device__
+#else
+#define HB_HD
+#endif
+
+namespace hb {
+
+constexpr int kPageSize = 16;
+constexpr int kChunkRows = 128;        // M of the tensor-core query tile
+constexpr int kChunkKeys = 128;        // keys per tensor-core KV tile
+constexpr int kDecodeKvhBlock = 8;     // kv heads per decode work item (max)
+constexpr int kMaxGroup = 16;          // max q heads per kv head
+constexpr uint32_t kPlanMagic = 0x31504248u;  // "HBP1"
+constexpr uint32_t kPlanVersion = 1;
+
+// One decode work item: a range of logical pages of one decode row, for one
+// block of kv heads.  Rows of the same (sequence, kv block) with n_splits > 1
+// leave partial softmax states in slots slot .. slot+n_splits-1; the last
+// split to finish merges them.
+struct DecodeItem {
+  int32_t seq;
+  int32_t kvh0;         // first kv head of the block
+  int32_t page_begin;   // first logical page
+  int32_t page_end;     // one past the last logical page
+  int32_t split;        // index of this split within its (seq, block)
+  int32_t n_splits;
+  int32_t slot;         // first partial slot of its (seq, block)
+  int32_t merge_id;     // index of the (seq, block) merge counter
+};
+
+// One tensor-core work item: query tokens tok0 .. tok0+ntok-1 (relative to
+// the sequence's first new token) of one kv head, all q heads of its group.
+struct ChunkItem {
+  int32_t seq;
+  int32_t kv_head;
+  int32_t tok0;
+  int32_t ntok;
+  int32_t kv_tiles;     // 128-key tiles visited
+  int32_t pad0, pad1, pad2;
+};
+
+// Host plan = header, then DecodeItem[num_decode_items], then
+// ChunkItem[num_chunk_items].  The items are copied verbatim to the start of
+// the device workspace; the header records where everything else lives.
+struct PlanHeader {
+  uint32_t magic;
+  uint32_t version;
+  int32_t num_seqs, total_q, num_q_heads, num_kv_heads, head_dim, page_size;
+  int32_t max_pages_per_seq;
+  int32_t num_sms;
+  int32_t num_decode_items;
+  int32_t num_chunk_items;
+  int32_t num_partial_slots;
+  int32_t num_merge_counters;
+  int32_t decode_grid;
+  int32_t decode_kvh_block;
+  int32_t chunk_tokens_per_tile;
+  int32_t pad0;
+  uint64_t reserved;
+  uint64_t items_bytes;     // bytes of the item arrays (host and device)
+  uint64_t ws_counters;     // device offsets (bytes from workspace start)
+  uint64_t ws_partial_o;
+  uint64_t ws_partial_ml;
+  uint64_t ws_total;
+  uint64_t plan_bytes;
+  uint64_t pad1[2];
+};
+static_assert(sizeof(PlanHeader) % 16 == 0, "header alignment");
+
+// Workspace counters: [0] decode work counter, [1] decode CTAs done,
+// [2 .. 2+num_merge_counters) per-(sequence, kv block) split arrivals.
+constexpr int kCounterWork = 0;
+constexpr int kCounterDone = 1;
+constexpr int kCounterMerge0 = 2;
+
+struct DecodeParams {
+  const DecodeItem* items;
+  int32_t num_items;
+  int32_t* counters;
+  float* part_o;          // [slots, Hq, D]
+  float* part_ml;         // [slots, Hq, 2]: (m in log2 units, l)
+  const int32_t* cu_q_len;
+  const int32_t* context_len;
+  const int32_t* block_table;
+  int32_t max_pages_per_seq;
+  int32_t num_pages;
+  const uint16_t* q;
+  uint16_t* out;
+  int32_t num_q_heads, num_kv_heads, group, kvh_block;
+  float scale_log2;       // softmax scale * log2(e)
+  int* dev_error;         // device error word
+};
+
+struct ChunkParams {
+  const ChunkItem* items;
+  int32_t num_items;
+  const int32_t* cu_q_len;
+  const int32_t* context_len;
+  const int32_t* block_table;
+  int32_t max_pages_per_seq;
+  int32_t num_pages;
+  uint16_t* out;
+  int32_t num_q_heads, num_kv_heads, group, tokens_per_tile;
+  float scale_log2;
+  int* dev_error;
+};
+
+struct AppendParams {
+  const int32_t* cu_q_len;
+  const int32_t* context_len;
+  const int32_t* block_table;
+  int32_t num_seqs, total_q, max_pages_per_seq, num_pages;
+  int32_t row_vec16;      // 16-byte vectors per token row (Hkv * D * 2 / 16)
+  const uint16_t* k_new;
+  const uint16_t* v_new;
+  uint16_t* k_cache;
+  uint16_t* v_cache;
+  int* dev_error;
+};
+
+}  // namespace hb

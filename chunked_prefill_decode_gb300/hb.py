@@ -1,0 +1,326 @@
+"""ctypes binding of libhb.so (the C ABI declared in include/hb.h).
+
+Argument marshalling only: every function here turns torch tensors / numpy
+arrays into the pointers and sizes the C calls take, calls them, and raises
+HbError on a non-zero status.  All computation runs in the library's CUDA
+kernels; there is no fallback, and loading fails loudly when the library is
+missing.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libhb.so")
+_lib = None
+
+HB_OK = 0
+HB_NUM_KERNEL_IDS = 3
+KERNEL_NAMES = ("kv_append", "decode", "chunk")
+
+STATUS_NAMES = {
+    0: "HB_OK", 1: "HB_ERR_INVALID_ARG", 2: "HB_ERR_SHAPE", 3: "HB_ERR_UNSUPPORTED",
+    4: "HB_ERR_WORKSPACE", 5: "HB_ERR_CUDA", 6: "HB_ERR_DEVICE_INDEX",
+    7: "HB_ERR_TIMEOUT", 8: "HB_ERR_OUT_OF_PAGES",
+}
+
+
+class HbError(RuntimeError):
+    def __init__(self, status, message):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+class HbBatch(ctypes.Structure):
+    _fields_ = [
+        ("num_seqs", ctypes.c_int32),
+        ("total_q", ctypes.c_int32),
+        ("max_pages_per_seq", ctypes.c_int32),
+        ("num_pages", ctypes.c_int32),
+        ("num_q_heads", ctypes.c_int32),
+        ("num_kv_heads", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32),
+        ("page_size", ctypes.c_int32),
+        ("cu_q_len", ctypes.c_void_p),
+        ("context_len", ctypes.c_void_p),
+        ("block_table", ctypes.c_void_p),
+    ]
+
+
+EXPORTED = (
+    "hb_last_error", "hb_status_string", "hb_kv_append", "hb_plan", "hb_attention",
+    "hb_check", "hb_timing_enable", "hb_timing_read", "hb_launch_count",
+    "hb_builder_create", "hb_builder_destroy", "hb_builder_add_request",
+    "hb_builder_step", "hb_builder_complete", "hb_builder_counts",
+    "hb_builder_free_list", "hb_builder_last_error",
+)
+
+
+def lib_path() -> str:
+    return _LIB_PATH
+
+
+def load():
+    """Load libhb.so (raising if it has not been built) and declare its calls."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_LIB_PATH):
+        raise RuntimeError(
+            f"{_LIB_PATH} is missing: build it with "
+            "`python -c 'import __graft_entry__ as g; g.build()'`")
+    L = ctypes.CDLL(_LIB_PATH)
+    vp, i32, i64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+    P = ctypes.POINTER
+    L.hb_last_error.restype = ctypes.c_char_p
+    L.hb_last_error.argtypes = []
+    L.hb_builder_last_error.restype = ctypes.c_char_p
+    L.hb_builder_last_error.argtypes = []
+    L.hb_status_string.restype = ctypes.c_char_p
+    L.hb_status_string.argtypes = [ctypes.c_int]
+    L.hb_kv_append.restype = ctypes.c_int
+    L.hb_kv_append.argtypes = [P(HbBatch), vp, vp, vp, vp, vp]
+    L.hb_plan.restype = ctypes.c_int
+    L.hb_plan.argtypes = [P(HbBatch), vp, vp, i32, vp, P(sz), vp, P(sz), vp]
+    L.hb_attention.restype = ctypes.c_int
+    L.hb_attention.argtypes = [P(HbBatch), vp, vp, vp, vp, ctypes.c_float, vp, vp, vp]
+    L.hb_check.restype = ctypes.c_int
+    L.hb_check.argtypes = [vp]
+    L.hb_timing_enable.restype = ctypes.c_int
+    L.hb_timing_enable.argtypes = [i32]
+    L.hb_timing_read.restype = ctypes.c_int
+    L.hb_timing_read.argtypes = [P(ctypes.c_double), P(i32)]
+    L.hb_launch_count.restype = i64
+    L.hb_launch_count.argtypes = []
+    L.hb_builder_create.restype = ctypes.c_int
+    L.hb_builder_create.argtypes = [i32, i32, i32, i32, vp, P(vp)]
+    L.hb_builder_destroy.restype = None
+    L.hb_builder_destroy.argtypes = [vp]
+    L.hb_builder_add_request.restype = ctypes.c_int
+    L.hb_builder_add_request.argtypes = [vp, i64, i32, i32]
+    L.hb_builder_step.restype = ctypes.c_int
+    L.hb_builder_step.argtypes = [vp, i32, P(i32), vp, vp, vp, vp, vp, P(i32)]
+    L.hb_builder_complete.restype = ctypes.c_int
+    L.hb_builder_complete.argtypes = [vp, i32, P(i32), vp]
+    L.hb_builder_counts.restype = ctypes.c_int
+    L.hb_builder_counts.argtypes = [vp, P(i32), P(i32), P(i32)]
+    L.hb_builder_free_list.restype = ctypes.c_int
+    L.hb_builder_free_list.argtypes = [vp, i32, P(i32), vp]
+    _lib = L
+    return L
+
+
+def _check(status, builder=False):
+    if status != HB_OK:
+        L = load()
+        msg = (L.hb_builder_last_error() if builder else L.hb_last_error()) or b""
+        raise HbError(status, msg.decode(errors="replace"))
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, torch.Tensor):
+        return ctypes.c_void_p(t.data_ptr()) if t.numel() else None
+    if isinstance(t, np.ndarray):
+        return t.ctypes.data_as(ctypes.c_void_p)
+    return t
+
+
+def _stream(stream):
+    if stream is None:
+        if torch.cuda.is_available():
+            return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+        return None
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def make_batch(num_seqs, total_q, max_pages_per_seq, num_pages, num_q_heads,
+               num_kv_heads, head_dim, cu_q_len, context_len, block_table,
+               page_size=16) -> HbBatch:
+    """hb_batch over device int32 tensors (kept alive by the caller)."""
+    for name, t in (("cu_q_len", cu_q_len), ("context_len", context_len),
+                    ("block_table", block_table)):
+        if t is not None and isinstance(t, torch.Tensor):
+            if t.dtype != torch.int32 or not t.is_contiguous():
+                raise ValueError(f"{name} must be a contiguous int32 tensor")
+    b = HbBatch()
+    b.num_seqs, b.total_q = int(num_seqs), int(total_q)
+    b.max_pages_per_seq, b.num_pages = int(max_pages_per_seq), int(num_pages)
+    b.num_q_heads, b.num_kv_heads = int(num_q_heads), int(num_kv_heads)
+    b.head_dim, b.page_size = int(head_dim), int(page_size)
+    b.cu_q_len = _ptr(cu_q_len).value if _ptr(cu_q_len) is not None else None
+    b.context_len = _ptr(context_len).value if _ptr(context_len) is not None else None
+    b.block_table = _ptr(block_table).value if _ptr(block_table) is not None else None
+    return b
+
+
+def _bf16(t, name):
+    if t.dtype != torch.bfloat16 or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous bfloat16 tensor")
+    return _ptr(t)
+
+
+def hb_kv_append(batch, k_new, v_new, k_cache, v_cache, stream=None):
+    _check(load().hb_kv_append(ctypes.byref(batch), _bf16(k_new, "k_new"),
+                               _bf16(v_new, "v_new"), _bf16(k_cache, "k_cache"),
+                               _bf16(v_cache, "v_cache"), _stream(stream)))
+
+
+def hb_plan_sizes(batch, q_len, context_len, num_sms):
+    """(plan_bytes, workspace_bytes) for the batch; host-only."""
+    ql = np.ascontiguousarray(q_len, dtype=np.int32)
+    cl = np.ascontiguousarray(context_len, dtype=np.int32)
+    pb, wb = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    _check(load().hb_plan(ctypes.byref(batch), _ptr(ql), _ptr(cl), int(num_sms), None,
+                          ctypes.byref(pb), None, ctypes.byref(wb), None))
+    return pb.value, wb.value
+
+
+def hb_plan(batch, q_len, context_len, num_sms, workspace=None, stream=None,
+            plan=None, upload=True):
+    """Write the plan; returns (plan as a host uint8 array, device workspace).
+
+    `workspace` (a uint8 device tensor) is allocated when None or too small.
+    With upload=False only the host plan is built (no CUDA call)."""
+    ql = np.ascontiguousarray(q_len, dtype=np.int32)
+    cl = np.ascontiguousarray(context_len, dtype=np.int32)
+    need_p, need_w = hb_plan_sizes(batch, ql, cl, num_sms)
+    if plan is None or plan.nbytes < need_p:
+        plan = np.zeros(need_p, dtype=np.uint8)
+    if upload and (workspace is None or workspace.numel() < need_w):
+        workspace = torch.empty(need_w, dtype=torch.uint8, device="cuda")
+    if not upload:
+        workspace = None
+    pb = ctypes.c_size_t(plan.nbytes)
+    wb = ctypes.c_size_t(workspace.numel() if workspace is not None else 0)
+    _check(load().hb_plan(ctypes.byref(batch), _ptr(ql), _ptr(cl), int(num_sms),
+                          _ptr(plan), ctypes.byref(pb), _ptr(workspace),
+                          ctypes.byref(wb), _stream(stream) if upload else None))
+    return plan, workspace
+
+
+def plan_header(plan):
+    """Decode the leading fields of a host plan (for tests and reports)."""
+    h = np.frombuffer(plan[:72].tobytes(), dtype=np.int32)
+    keys = ("magic", "version", "num_seqs", "total_q", "num_q_heads", "num_kv_heads",
+            "head_dim", "page_size", "max_pages_per_seq", "num_sms",
+            "num_decode_items", "num_chunk_items", "num_partial_slots",
+            "num_merge_counters", "decode_grid", "decode_kvh_block",
+            "chunk_tokens_per_tile", "pad0")
+    return {k: int(v) for k, v in zip(keys, h)}
+
+
+def plan_items(plan):
+    """(decode items [n, 8] int32, chunk items [m, 8] int32) of a host plan."""
+    hd = plan_header(plan)
+    body = np.frombuffer(plan[144:].tobytes(), dtype=np.int32)
+    nd, nc = hd["num_decode_items"], hd["num_chunk_items"]
+    dec = body[: nd * 8].reshape(nd, 8)
+    chk = body[nd * 8: nd * 8 + nc * 8].reshape(nc, 8)
+    return dec, chk
+
+
+def hb_attention(batch, plan, q, k_cache, v_cache, scale, out, workspace, stream=None):
+    _check(load().hb_attention(ctypes.byref(batch), _ptr(plan), _bf16(q, "q"),
+                               _bf16(k_cache, "k_cache"), _bf16(v_cache, "v_cache"),
+                               ctypes.c_float(scale), _bf16(out, "out"), _ptr(workspace),
+                               _stream(stream)))
+
+
+def hb_check(stream=None):
+    _check(load().hb_check(_stream(stream)))
+
+
+def hb_timing_enable(on: bool):
+    _check(load().hb_timing_enable(1 if on else 0))
+
+
+def hb_timing_read():
+    """{kernel name: (total ms, launches)} since timing was enabled."""
+    ms = (ctypes.c_double * HB_NUM_KERNEL_IDS)()
+    n = (ctypes.c_int32 * HB_NUM_KERNEL_IDS)()
+    _check(load().hb_timing_read(ms, n))
+    return {KERNEL_NAMES[i]: (ms[i], n[i]) for i in range(HB_NUM_KERNEL_IDS)}
+
+
+def hb_launch_count() -> int:
+    return int(load().hb_launch_count())
+
+
+class Builder:
+    """The library's stall-free batch builder (host only)."""
+
+    def __init__(self, budget, page_size, num_pages, max_pages_per_seq, page_order=None):
+        self.max_pages_per_seq = max_pages_per_seq
+        handle = ctypes.c_void_p()
+        order = None
+        if page_order is not None:
+            order = np.ascontiguousarray(page_order, dtype=np.int32)
+        _check(load().hb_builder_create(budget, page_size, num_pages, max_pages_per_seq,
+                                        _ptr(order), ctypes.byref(handle)), builder=True)
+        self._h = handle
+        self._max_rows = 64
+
+    def close(self):
+        if self._h:
+            load().hb_builder_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def add_request(self, rid, prompt_len, max_new):
+        _check(load().hb_builder_add_request(self._h, int(rid), int(prompt_len),
+                                             int(max_new)), builder=True)
+
+    def step(self):
+        """Next batch as a dict of numpy arrays, or None when there is nothing to run."""
+        while True:
+            mr, mp = self._max_rows, self.max_pages_per_seq
+            ql = np.zeros(mr, np.int32)
+            cl = np.zeros(mr, np.int32)
+            bt = np.zeros((mr, mp), np.int32)
+            ids = np.zeros(mr, np.int64)
+            kind = np.zeros(mr, np.int32)
+            n, over = ctypes.c_int32(0), ctypes.c_int32(0)
+            st = load().hb_builder_step(self._h, mr, ctypes.byref(n), _ptr(ql), _ptr(cl),
+                                        _ptr(bt), _ptr(ids), _ptr(kind), ctypes.byref(over))
+            if st == 4 and n.value > mr:      # HB_ERR_WORKSPACE: grow and retry
+                self._max_rows = n.value
+                continue
+            _check(st, builder=True)
+            k = n.value
+            if k == 0:
+                return None
+            return {"q_len": ql[:k], "context_len": cl[:k], "block_table": bt[:k],
+                    "ids": ids[:k], "kind": kind[:k], "over_budget": bool(over.value)}
+
+    def complete(self):
+        out = np.zeros(max(self._max_rows, 1), np.int64)
+        n = ctypes.c_int32(0)
+        _check(load().hb_builder_complete(self._h, out.size, ctypes.byref(n), _ptr(out)),
+               builder=True)
+        return [int(x) for x in out[: n.value]]
+
+    def counts(self):
+        w, r, f = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
+        _check(load().hb_builder_counts(self._h, ctypes.byref(w), ctypes.byref(r),
+                                        ctypes.byref(f)), builder=True)
+        return w.value, r.value, f.value
+
+    def free_list(self):
+        _, _, nfree = self.counts()
+        out = np.zeros(max(nfree, 1), np.int32)
+        n = ctypes.c_int32(0)
+        _check(load().hb_builder_free_list(self._h, out.size, ctypes.byref(n), _ptr(out)),
+               builder=True)
+        return [int(x) for x in out[: n.value]]

@@ -1,0 +1,250 @@
+/*
+ * hb.h -- C ABI of the hybrid-batch paged-attention library (libhb.so).
+ *
+ * One call sequence runs one attention layer of a hybrid batch: many decode
+ * rows (one new token each, over a long cached context) plus prefill chunks
+ * (q_len > 1 new tokens that attend causally to themselves and re-read the
+ * KV of the earlier chunks of their prompt), all over a paged KV cache.
+ *
+ *   hb_kv_append  scatter the batch's new K/V rows into their pages
+ *   hb_plan       (host) split the batch into work items; upload the plan
+ *   hb_attention  attention of every new token over its sequence's pages
+ *
+ * The operation follows "Sarathi-Serve：以 chunked-prefills 与 stall-free batching
+ * 驯服 LLM 推理的吞吐—延迟权衡", §GPU / 系统数据路径 ③ (a batch of decode tokens
+ * plus prefill chunks within a token budget) and ⑤ (attention reads and
+ * writes the KV cache through the page table; a chunk appends its KV, decodes
+ * read all earlier KV, chunk i re-reads chunks 1..i-1), and "In-flight
+ * Batching", §KV Cache 管理的协同优化 (16-token pages, a block table mapping
+ * logical pages to non-contiguous physical ones) and §Batch 内的异构执行
+ * (different lengths handled inside the kernel, no padding).
+ *
+ * Conventions shared by every call
+ *  - Pointers are borrowed: the library allocates no device memory and keeps
+ *    no pointer after the call returns (work already queued on `stream` uses
+ *    them until it completes).  The caller owns all memory and streams.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default).
+ *  - Argument errors are detected on the host and returned synchronously;
+ *    nothing is launched then.  Device-side index errors (a block-table entry
+ *    outside [0, num_pages)) set a device error word and skip the access;
+ *    hb_check() turns it into HB_ERR_DEVICE_INDEX.  A device wait that runs
+ *    out of time sets HB_ERR_TIMEOUT the same way.  No C++ exception crosses
+ *    this boundary.  hb_last_error() gives a message for the last failure of
+ *    the calling thread.
+ *  - All calls are asynchronous on `stream` unless stated otherwise; append
+ *    must be ordered before attention on the same stream.
+ *
+ * Data layout (bf16 = IEEE bfloat16 stored as uint16)
+ *  - q      [total_q, num_q_heads,  head_dim] bf16, rows in batch order
+ *  - k_new  [total_q, num_kv_heads, head_dim] bf16 (same for v_new)
+ *  - cache  [num_pages, page_size, num_kv_heads, head_dim] bf16, separate
+ *           K and V pools ("NHD" pages)
+ *  - out    [total_q, num_q_heads,  head_dim] bf16
+ *  - Rows of sequence s are q rows cu_q_len[s] .. cu_q_len[s+1]-1.  Its new
+ *    token j sits at logical position p = context_len[s] - q_len[s] + j in
+ *    physical page block_table[s*max_pages_per_seq + p/page_size], slot
+ *    p % page_size, and attends to logical keys 0..p (causal, aligned to the
+ *    absolute position).  Query head h reads kv head h / (Hq/Hkv).
+ *
+ * Supported shapes: page_size 16, head_dim 64 or 128, Hq a multiple of Hkv
+ * with group size Hq/Hkv <= 16, 1 <= q_len <= context_len per sequence.
+ */
+#ifndef HB_H_
+#define HB_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum hb_status {
+  HB_OK = 0,
+  HB_ERR_INVALID_ARG = 1,   /* null pointer, bad enum, misaligned pointer   */
+  HB_ERR_SHAPE = 2,         /* inconsistent sizes or a row breaking          */
+                            /* 1 <= q_len <= context_len                      */
+  HB_ERR_UNSUPPORTED = 3,   /* valid but not built (page size, head_dim ...) */
+  HB_ERR_WORKSPACE = 4,     /* plan or workspace buffer too small / stale    */
+  HB_ERR_CUDA = 5,          /* a CUDA runtime/driver call failed             */
+  HB_ERR_DEVICE_INDEX = 6,  /* a kernel met an out-of-range page index       */
+  HB_ERR_TIMEOUT = 7,       /* a kernel wait gave up                         */
+  HB_ERR_OUT_OF_PAGES = 8   /* batch builder: no free page for a decode      */
+} hb_status;
+
+/* Message for the last failed call on this thread ("" if none).  The string
+ * is owned by the library and valid until the next call on this thread. */
+const char* hb_last_error(void);
+
+/* Name of a status code (static string). */
+const char* hb_status_string(hb_status s);
+
+/* Descriptor of one hybrid batch.  The three arrays are DEVICE pointers. */
+typedef struct hb_batch {
+  int32_t num_seqs;            /* sequences (rows of the batch), >= 0         */
+  int32_t total_q;             /* sum of q_len = rows of q / k_new / out      */
+  int32_t max_pages_per_seq;   /* row stride of block_table                   */
+  int32_t num_pages;           /* physical pages in each cache pool           */
+  int32_t num_q_heads;
+  int32_t num_kv_heads;
+  int32_t head_dim;
+  int32_t page_size;           /* tokens per page; must be 16                 */
+  const int32_t* cu_q_len;     /* [num_seqs+1] prefix sums of q_len, [0] = 0  */
+  const int32_t* context_len;  /* [num_seqs] tokens in cache AFTER append     */
+  const int32_t* block_table;  /* [num_seqs * max_pages_per_seq] page ids     */
+} hb_batch;
+
+/*
+ * KV append (scatter).  For every new token j of sequence s, copy row
+ * cu_q_len[s]+j of k_new / v_new ([num_kv_heads*head_dim] contiguous bf16)
+ * to its page slot in k_cache / v_cache (see the layout above).  The copy is
+ * bit-exact; no other slot is written.  Cited passage: the first page,
+ * §GPU / 系统数据路径 ⑤ ("a prefill chunk appends new KV").
+ *   k_new, v_new     device, [total_q, Hkv, D] bf16, 16-byte aligned
+ *   k_cache, v_cache device, [num_pages, 16, Hkv, D] bf16, 16-byte aligned
+ * Errors: HB_ERR_INVALID_ARG / HB_ERR_SHAPE / HB_ERR_UNSUPPORTED on the host;
+ * a page id outside [0, num_pages) is skipped and reported by hb_check().
+ */
+hb_status hb_kv_append(const hb_batch* batch, const void* k_new,
+                       const void* v_new, void* k_cache, void* v_cache,
+                       void* stream);
+
+/*
+ * Plan (host).  Cuts the batch into work items for hb_attention: decode rows
+ * (q_len == 1) become split-KV items over page ranges, chunk rows (q_len > 1)
+ * become (kv head, query tile) items; both lists are ordered longest first.
+ * Needs HOST copies of q_len and context_len (the same values the device
+ * arrays of `batch` hold) and the number of SMs of the device.
+ *   h_q_len, h_context_len  host, [num_seqs] int32
+ *   h_plan                  host buffer for the plan, or NULL
+ *   plan_bytes              in: size of h_plan; out: bytes needed
+ *   d_workspace             device buffer (256-byte aligned), or NULL
+ *   workspace_bytes         in: size of d_workspace; out: bytes needed
+ * The sizes are always reported.  With h_plan == NULL nothing else happens;
+ * otherwise the plan is written into h_plan, and if d_workspace is not NULL
+ * it is also copied into d_workspace and the workspace counters are cleared,
+ * asynchronously on `stream` (only this step makes CUDA calls): h_plan must
+ * stay unchanged until that copy has completed, and a workspace must not be
+ * shared by attention calls in flight at once.
+ * The plan stays valid for any later hb_attention on a batch with the same
+ * q_len / context_len / head geometry (block tables and tensors may change).
+ * Errors: HB_ERR_SHAPE for rows outside 1 <= q_len <= context_len, or
+ * context_len > max_pages_per_seq*page_size; HB_ERR_WORKSPACE if a buffer is
+ * too small.
+ */
+hb_status hb_plan(const hb_batch* batch, const int32_t* h_q_len,
+                  const int32_t* h_context_len, int32_t num_sms, void* h_plan,
+                  size_t* plan_bytes, void* d_workspace,
+                  size_t* workspace_bytes, void* stream);
+
+/*
+ * Attention.  out[row, h, :] = sum_t softmax_t(scale * <q[row,h], K[t]>) V[t]
+ * over keys t = 0..p of the row's sequence (p its absolute position), K/V of
+ * kv head h/(Hq/Hkv) read through the block table from the caches as they
+ * stand after hb_kv_append.  fp32 accumulation, one bf16 rounding at the
+ * store.  Decode rows use a split-KV kernel whose partial softmax states are
+ * merged by the last split to finish; chunk rows use a tensor-core kernel.
+ * Cited passages: the first page, §GPU / 系统数据路径 ③-⑤, and §核心机制 3
+ * (chunk i re-reads the KV of chunks 1..i-1; same computation as unchunked).
+ *   h_plan      host plan written by hb_plan for this batch
+ *   q, out      device, [total_q, Hq, D] bf16, 16-byte aligned
+ *   k_cache, v_cache device pools as in hb_kv_append
+ *   d_workspace the workspace hb_plan prepared
+ * Errors: HB_ERR_WORKSPACE if h_plan does not match the batch; argument
+ * errors as above; launch failures as HB_ERR_CUDA.
+ */
+hb_status hb_attention(const hb_batch* batch, const void* h_plan,
+                       const void* q, const void* k_cache,
+                       const void* v_cache, float softmax_scale, void* out,
+                       void* d_workspace, void* stream);
+
+/*
+ * Synchronise `stream`, then read and clear the device error word of the
+ * current device: HB_OK, HB_ERR_DEVICE_INDEX or HB_ERR_TIMEOUT (or
+ * HB_ERR_CUDA if the stream itself failed).  Blocking.
+ */
+hb_status hb_check(void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Instrumentation.  When enabled, every kernel launch of this library is
+ * bracketed by CUDA events recorded on its launch stream.
+ *   kernel ids: 0 = kv append, 1 = decode split-KV, 2 = chunk (tensor core)
+ * ------------------------------------------------------------------------- */
+#define HB_NUM_KERNEL_IDS 3
+
+/* Start (clearing earlier records) or stop recording.  Not thread-safe with
+ * concurrent launches from other threads. */
+hb_status hb_timing_enable(int32_t enable);
+
+/* Synchronise the recorded events and return, per kernel id, the summed
+ * duration in milliseconds and the number of launches recorded.  Both arrays
+ * have HB_NUM_KERNEL_IDS entries. */
+hb_status hb_timing_read(double* total_ms, int32_t* launches);
+
+/* Number of kernels this library has launched in this process so far. */
+int64_t hb_launch_count(void);
+
+/* ---------------------------------------------------------------------------
+ * Stall-free batch builder (host only, no CUDA).  Each step forms the next
+ * hybrid batch: (1) one decode token of every request past its prefill,
+ * (2) a chunk of every unfinished prefill, (3) first chunks of waiting
+ * requests, first come first served, while the token budget lasts; then the
+ * caller runs the batch and calls hb_builder_complete, which advances every
+ * request and retires finished ones, returning their pages.  Cited passages:
+ * the first page, §核心机制 2 (the four steps; decodes always in the batch,
+ * at most B tokens per iteration); "In-flight Batching", §调度状态机 (waiting
+ * -> prefill (chunked) -> decode -> completed).  Readings where the pages
+ * are silent: chunk = min(prompt left, budget left); ongoing chunks shrink to
+ * the pages available; admission stops at the first request whose first
+ * chunk's pages cannot be allocated; pages come from the front of a FIFO free
+ * list and return to its back; no preemption (a decode that finds no page
+ * fails with HB_ERR_OUT_OF_PAGES); decodes that alone exceed the budget are
+ * all kept and flagged over_budget.
+ * ------------------------------------------------------------------------- */
+typedef struct hb_builder hb_builder;
+
+/* page_order: NULL for 0..num_pages-1, else a host permutation of it that
+ * seeds the free list.  *out receives a new builder. */
+hb_status hb_builder_create(int32_t budget, int32_t page_size,
+                            int32_t num_pages, int32_t max_pages_per_seq,
+                            const int32_t* page_order, hb_builder** out);
+void hb_builder_destroy(hb_builder* b);
+
+/* Queue a request (arrival order = call order).  HB_ERR_SHAPE if
+ * prompt_len < 1, max_new < 1 or the request cannot fit max_pages_per_seq;
+ * HB_ERR_INVALID_ARG for a duplicate id. */
+hb_status hb_builder_add_request(hb_builder* b, int64_t id, int32_t prompt_len,
+                                 int32_t max_new);
+
+/* Form the next batch into caller-owned host arrays with room for max_rows
+ * rows: q_len, context_len [max_rows], block_table [max_rows *
+ * max_pages_per_seq] (unused entries -1), row_ids [max_rows], row_kind
+ * [max_rows] (0 decode, 1 prefill).  *num_rows = 0 means nothing to run.
+ * HB_ERR_WORKSPACE if max_rows is too small (the builder is then unchanged).
+ * Call hb_builder_complete before the next step. */
+hb_status hb_builder_step(hb_builder* b, int32_t max_rows, int32_t* num_rows,
+                          int32_t* q_len, int32_t* context_len,
+                          int32_t* block_table, int64_t* row_ids,
+                          int32_t* row_kind, int32_t* over_budget);
+
+/* The batch of the last step ran.  Writes up to max_finished ids of the
+ * requests that finished (in batch order) and their count. */
+hb_status hb_builder_complete(hb_builder* b, int32_t max_finished,
+                              int32_t* num_finished, int64_t* finished_ids);
+
+/* Message for the last failed hb_builder_* call on this thread. */
+const char* hb_builder_last_error(void);
+
+/* Counts: waiting requests, running requests, free pages. */
+hb_status hb_builder_counts(const hb_builder* b, int32_t* waiting,
+                            int32_t* running, int32_t* free_pages);
+
+/* The free list, front first (up to max entries; *n receives its length). */
+hb_status hb_builder_free_list(const hb_builder* b, int32_t max, int32_t* n,
+                               int32_t* pages);
+
+#ifdef __cplusplus
+}  /* extern "C" */
+#endif
+
+#endif  /* HB_H_ */

@@ -1,0 +1,179 @@
+"""The C ABI on the host (no GPU): the library loads and exports every call
+include/hb.h declares; argument errors come back as status codes; the plan
+is checked against its own definition (coverage, splits, ordering)."""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+from _hbutil import header_functions, host_batch, lib
+
+
+def test_library_exports_every_declared_function():
+    hb = lib()
+    L = hb.load()
+    declared = header_functions()
+    assert "hb_kv_append" in declared and "hb_plan" in declared and "hb_attention" in declared
+    for name in declared:
+        assert hasattr(L, name), f"{name} declared in hb.h but not exported"
+    assert set(hb.EXPORTED) == set(declared)
+
+
+def test_status_strings():
+    L = lib().load()
+    for code, name in lib().STATUS_NAMES.items():
+        assert L.hb_status_string(code).decode() == name
+
+
+@pytest.mark.parametrize("field,value,status", [
+    ("page_size", 8, 3), ("head_dim", 96, 3), ("num_kv_heads", 3, 2),
+    ("num_q_heads", 0, 2), ("num_pages", 0, 2), ("max_pages_per_seq", 0, 2),
+    ("num_seqs", -1, 2), ("total_q", -5, 2),
+])
+def test_bad_batch_is_rejected_on_the_host(field, value, status):
+    hb = lib()
+    b, ql, cl = host_batch(hb, [(1, 40), (5, 9)])
+    setattr(b, field, value)
+    with pytest.raises(hb.HbError) as e:
+        hb.hb_plan_sizes(b, ql, cl, 148)
+    assert e.value.status == status
+
+
+def test_group_too_large_and_odd_kv_heads_unsupported():
+    hb = lib()
+    b, ql, cl = host_batch(hb, [(1, 40)], hq=34, hkv=2)
+    with pytest.raises(hb.HbError) as e:
+        hb.hb_plan_sizes(b, ql, cl, 148)
+    assert e.value.status == 3
+    b, ql, cl = host_batch(hb, [(1, 40)], hq=12, hkv=12)
+    with pytest.raises(hb.HbError) as e:
+        hb.hb_plan_sizes(b, ql, cl, 148)
+    assert e.value.status == 3
+
+
+@pytest.mark.parametrize("rows", [[(0, 5)], [(6, 5)], [(1, 4000)]])
+def test_bad_rows_rejected(rows):
+    hb = lib()
+    b, ql, cl = host_batch(hb, rows, max_pages=8)
+    with pytest.raises(hb.HbError) as e:
+        hb.hb_plan_sizes(b, ql, cl, 148)
+    assert e.value.status == 2
+
+
+def test_total_q_mismatch_rejected():
+    hb = lib()
+    b, ql, cl = host_batch(hb, [(3, 9)])
+    b.total_q = 4
+    with pytest.raises(hb.HbError) as e:
+        hb.hb_plan_sizes(b, ql, cl, 148)
+    assert e.value.status == 2
+
+
+def test_null_arguments():
+    hb = lib()
+    L = hb.load()
+    assert L.hb_kv_append(None, None, None, None, None, None) == 1
+    b, ql, cl = host_batch(hb, [(2, 9)])
+    # total_q > 0 with NULL tensors
+    assert L.hb_kv_append(ctypes.byref(b), None, None, None, None, None) == 1
+    assert L.hb_attention(ctypes.byref(b), None, None, None, None, 1.0, None, None, None) == 1
+    assert "NULL" in L.hb_last_error().decode()
+
+
+def test_empty_batch_is_a_no_op():
+    hb = lib()
+    L = hb.load()
+    b, ql, cl = host_batch(hb, [])
+    assert L.hb_kv_append(ctypes.byref(b), None, None, None, None, None) == 0
+    p, w = hb.hb_plan_sizes(b, ql, cl, 148)
+    plan, _ = hb.hb_plan(b, ql, cl, 148, upload=False)
+    assert hb.plan_header(plan)["num_decode_items"] == 0
+    assert L.hb_attention(ctypes.byref(b), hb._ptr(plan), None, None, None, 1.0,
+                          None, None, None) == 0
+
+
+def test_attention_rejects_foreign_plan():
+    hb = lib()
+    L = hb.load()
+    b, ql, cl = host_batch(hb, [(1, 50), (7, 7)])
+    plan, _ = hb.hb_plan(b, ql, cl, 148, upload=False)
+    b2, _, _ = host_batch(hb, [(1, 50), (8, 8)])
+    assert L.hb_attention(ctypes.byref(b2), hb._ptr(plan), None, None, None, 1.0,
+                          None, None, None) == 4
+    junk = np.zeros_like(plan)
+    assert L.hb_attention(ctypes.byref(b), hb._ptr(junk), None, None, None, 1.0,
+                          None, None, None) == 4
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU error path")
+def test_cuda_calls_fail_cleanly_without_a_gpu():
+    hb = lib()
+    L = hb.load()
+    b, ql, cl = host_batch(hb, [(2, 9)])
+    buf = (ctypes.c_uint8 * 64)()
+    ptr = ctypes.cast(buf, ctypes.c_void_p)
+    aligned = ctypes.c_void_p((ptr.value + 15) // 16 * 16)
+    st = L.hb_kv_append(ctypes.byref(b), aligned, aligned, aligned, aligned, None)
+    assert st == 5
+
+
+def _check_plan(rows, hq, hkv, d, sms):
+    hb = lib()
+    b, ql, cl = host_batch(hb, rows, hq=hq, hkv=hkv, d=d)
+    plan, _ = hb.hb_plan(b, ql, cl, sms, upload=False)
+    h = hb.plan_header(plan)
+    dec, chk = hb.plan_items(plan)
+    g = hq // hkv
+    kvhb = min(hkv, 8)
+    assert h["decode_kvh_block"] == kvhb
+    assert h["chunk_tokens_per_tile"] == 128 // g
+    # decode items tile every decode row's pages exactly once per kv block
+    cover = {}
+    for seq, kvh0, pb, pe, split, ns, slot, mid in dec:
+        assert ql[seq] == 1 and 0 <= pb < pe and kvh0 % kvhb == 0
+        cover.setdefault((seq, kvh0), []).append((pb, pe, split, ns, slot, mid))
+    for s in range(len(rows)):
+        if ql[s] != 1:
+            continue
+        npg = -(-cl[s] // 16)
+        for kvh0 in range(0, hkv, kvhb):
+            parts = sorted(cover[(s, kvh0)])
+            assert parts[0][0] == 0 and parts[-1][1] == npg
+            assert all(a[1] == b_[0] for a, b_ in zip(parts, parts[1:]))
+            ns = parts[0][3]
+            assert len(parts) == ns and sorted(p[2] for p in parts) == list(range(ns))
+            assert len({(p[4], p[5]) for p in parts}) == 1
+    lens = [pe - pb for _, _, pb, pe, *_ in dec]
+    assert lens == sorted(lens, reverse=True)
+    # chunk items cover every (token, kv head) of every chunk row once
+    tpt = 128 // g
+    seen = set()
+    for seq, kvh, t0, nt, tiles, *_ in chk:
+        assert ql[seq] > 1 and 1 <= nt <= tpt and t0 % tpt == 0
+        off = cl[seq] - ql[seq]
+        assert tiles == -(-(off + t0 + nt) // 128)
+        for t in range(t0, t0 + nt):
+            assert (seq, kvh, t) not in seen
+            seen.add((seq, kvh, t))
+    assert len(seen) == sum(int(q) * hkv for q in ql if q > 1)
+    tiles = [c[4] for c in chk]
+    assert tiles == sorted(tiles, reverse=True)
+    return h
+
+
+@pytest.mark.parametrize("name", ["tiny", "mistral_b512", "yi_b2048", "decode_only"])
+def test_plan_covers_workloads(name):
+    from chunked_prefill_decode_gb300 import workloads
+    lay = workloads.WORKLOADS[name]()
+    sh = lay.shape
+    rows = list(zip(lay.q_len.tolist(), lay.context_len.tolist()))
+    h = _check_plan(rows, sh.num_q_heads, sh.num_kv_heads, sh.head_dim, 152)
+    assert h["decode_grid"] <= 152
+
+
+def test_plan_edge_shapes():
+    _check_plan([(1, 1), (1, 16), (1, 17), (2, 2), (17, 17), (129, 300)], 8, 8, 64, 4)
+    _check_plan([(1, 5000), (257, 8192)], 56, 8, 128, 152)
+    _check_plan([(1, 333), (9, 40)], 16, 16, 128, 8)    # 2 kv blocks of 8
+    _check_plan([(1, 100), (3, 3)], 4, 2, 64, 152)      # kv block of 2

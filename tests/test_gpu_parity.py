@@ -1,0 +1,190 @@
+"""CUDA path against the fp64 oracle, through the C ABI (GB300).
+
+Small batches are compared element by element; full-size workloads on the
+rows the oracle can afford (every decode row of a sample of sequences, a
+sample of chunk tokens).  Bars: KV append bit-exact, attention max-abs <= 1e-2
+and mean-abs <= 1e-3 (bf16 inputs, fp32 accumulation).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from _gpu import MAX_ABS, MEAN_ABS, bits, compact_layout, compare, gpu_step, oracle_step, sms
+from _hbutil import lib
+from chunked_prefill_decode_gb300 import workloads
+from chunked_prefill_decode_gb300.workloads import Shape, layout_from_rows
+
+pytestmark = pytest.mark.gpu
+
+
+def _full_check(layout, seed=0, scale=None, repeats=1):
+    ten = workloads.make_tensors(layout, seed)
+    kc, vc, out = gpu_step(layout, ten, scale=scale, repeats=repeats)
+    kp, vp, ref = oracle_step(layout, ten, scale=scale)
+    assert np.array_equal(bits(kc), kp), "K append differs"
+    assert np.array_equal(bits(vc), vp), "V append differs"
+    return compare(out, ref)
+
+
+def test_tiny_workload():
+    _full_check(workloads.tiny(0))
+
+
+@pytest.mark.parametrize("seed", [1, 2, 3])
+def test_tiny_workload_seeds(seed):
+    _full_check(workloads.tiny(seed), seed=seed)
+
+
+def test_repeated_attention_reuses_plan():
+    # counters in the workspace must reset themselves between launches
+    lay = layout_from_rows(Shape(32, 8, 128), [(1, 3000)] * 6 + [(1, 700), (40, 300)], 5)
+    _full_check(lay, seed=5, repeats=4)
+
+
+@pytest.mark.parametrize("rows", [
+    [(1, 1)], [(1, 16)], [(1, 17)], [(1, 128)], [(1, 129)], [(1, 2047)],
+    [(2, 2)], [(15, 15)], [(16, 16)], [(17, 17)], [(127, 127)], [(128, 128)],
+    [(129, 129)], [(257, 257)], [(64, 1000)], [(100, 1029)], [(33, 4096)],
+    [(1, 50), (1, 700), (5, 37), (130, 700), (1, 3)],
+])
+@pytest.mark.parametrize("geom", [(8, 8, 64), (32, 8, 128), (56, 8, 128)])
+def test_edge_rows(rows, geom):
+    hq, hkv, d = geom
+    _full_check(layout_from_rows(Shape(hq, hkv, d), rows, 11), seed=11)
+
+
+@pytest.mark.parametrize("geom", [(4, 4, 128), (16, 2, 64), (64, 16, 128), (16, 1, 128),
+                                  (8, 1, 64), (128, 8, 128)])
+def test_other_head_geometries(geom):
+    hq, hkv, d = geom
+    rows = [(1, 200), (1, 37), (24, 90), (1, 1000)]
+    _full_check(layout_from_rows(Shape(hq, hkv, d), rows, 12), seed=12)
+
+
+def test_several_chunks_and_decodes():
+    rows = [(1, 900)] * 7 + [(200, 456), (57, 57), (300, 2000), (1, 5)]
+    _full_check(layout_from_rows(Shape(32, 8, 128), rows, 13), seed=13)
+
+
+def test_constant_v_returns_v_exactly():
+    lay = layout_from_rows(Shape(32, 8, 128), [(1, 1500), (1, 40), (150, 400)], 14)
+    ten = workloads.make_tensors(lay, 14)
+    hkv, d = 8, 128
+    c = torch.randn(hkv, d).to(torch.bfloat16)
+    ten.v_new[:] = c
+    keep = torch.from_numpy(workloads.cached_slot_mask(lay))
+    ten.v_cache[keep] = c
+    _, _, out = gpu_step(lay, ten)
+    expect = c.repeat_interleave(4, dim=0)
+    assert torch.equal(out.cpu(), expect[None].expand_as(out.cpu()))
+
+
+def test_chunked_prefill_equals_unchunked_on_gpu():
+    """A 700-token prompt prefilled in chunks of 1, 100, 128, 257 and at once:
+    every chunking matches the oracle, and they agree with each other."""
+    L, sh = 700, Shape(32, 8, 128)
+    g = torch.Generator().manual_seed(15)
+    q = torch.randn(L, 32, 128, generator=g).to(torch.bfloat16)
+    kn = torch.randn(L, 8, 128, generator=g).to(torch.bfloat16)
+    vn = torch.randn(L, 8, 128, generator=g).to(torch.bfloat16)
+    base = layout_from_rows(sh, [(L, L)], 15)
+    pool_k = torch.zeros(base.num_pages, 16, 8, 128, dtype=torch.bfloat16)
+    pool_v = torch.zeros_like(pool_k)
+    outs = {}
+    for c in (L, 1, 100, 128, 257):
+        kp, vp = pool_k.clone(), pool_v.clone()
+        res = []
+        for start in range(0, L, c) if c > 1 else range(0, 40):  # chunk 1: first 40 tokens
+            n = min(c, L - start)
+            lay = workloads.BatchLayout(sh, np.array([n], np.int32),
+                                        np.array([start + n], np.int32),
+                                        base.block_table, base.num_pages)
+            ten = workloads.BatchTensors(q[start:start + n].clone(), kn[start:start + n].clone(),
+                                         vn[start:start + n].clone(), kp, vp)
+            kc, vc, out = gpu_step(lay, ten)
+            _, _, ref = oracle_step(lay, ten)
+            compare(out, ref)
+            kp, vp = kc.cpu(), vc.cpu()
+            res.append(out.float().cpu())
+        outs[c] = torch.cat(res)
+    for c in (100, 128, 257):
+        assert (outs[c] - outs[L]).abs().max().item() <= 2 * MAX_ABS
+    assert (outs[1] - outs[L][:40]).abs().max().item() <= 2 * MAX_ABS
+
+
+def test_device_index_error_is_reported():
+    hb = lib()
+    lay = layout_from_rows(Shape(8, 8, 64), [(1, 40), (20, 50)], 16)
+    lay.block_table[0, 1] = lay.num_pages + 5      # out of range
+    lay.block_table[1, 0] = -3
+    ten = workloads.make_tensors(lay, 16)
+    gpu_step(lay, ten, check=False)
+    with pytest.raises(hb.HbError) as e:
+        hb.hb_check()
+    assert e.value.status == 6
+    hb.hb_check()   # the word was cleared
+
+
+def test_timing_and_launch_count():
+    hb = lib()
+    lay = workloads.tiny(0)
+    ten = workloads.make_tensors(lay, 0)
+    n0 = hb.hb_launch_count()
+    hb.hb_timing_enable(True)
+    gpu_step(lay, ten)
+    t = hb.hb_timing_read()
+    hb.hb_timing_enable(False)
+    assert hb.hb_launch_count() - n0 == 3
+    for name in ("kv_append", "decode", "chunk"):
+        assert t[name][1] == 1 and t[name][0] > 0
+
+
+# ---------------------------------------------------------------- full size
+def _full_size(name, n_seq_sample=6, n_chunk_tok=48, seed=None):
+    lay = workloads.WORKLOADS[name]()
+    seed = {"mistral_b512": 1, "yi_b2048": 2, "decode_only": 3}.get(name, 0) if seed is None else seed
+    ten = workloads.make_tensors(lay, seed, device="cuda")
+    kc, vc, out = gpu_step(lay, ten)
+    rng = np.random.default_rng(seed)
+    dec = [s for s in range(lay.num_seqs) if lay.q_len[s] == 1]
+    chk = [s for s in range(lay.num_seqs) if lay.q_len[s] > 1]
+    # append: bit-exact at every written slot, untouched elsewhere (device)
+    cu = lay.cu_q_len
+    P = lay.shape.page_size
+    pos = np.concatenate([np.arange(lay.context_len[s] - lay.q_len[s], lay.context_len[s])
+                          for s in range(lay.num_seqs)])
+    seq_of = np.repeat(np.arange(lay.num_seqs), lay.q_len)
+    pages = lay.block_table[seq_of, pos // P]
+    slots = pos % P
+    pg = torch.from_numpy(pages.astype(np.int64)).cuda()
+    sl = torch.from_numpy(slots.astype(np.int64)).cuda()
+    assert torch.equal(kc[pg, sl].view(torch.int16), ten.k_new.view(torch.int16))
+    assert torch.equal(vc[pg, sl].view(torch.int16), ten.v_new.view(torch.int16))
+    written = torch.zeros(kc.shape[:2], dtype=torch.bool, device="cuda")
+    written[pg, sl] = True
+    assert torch.equal(kc.view(torch.int16)[~written], ten.k_cache.view(torch.int16)[~written])
+    assert torch.equal(vc.view(torch.int16)[~written], ten.v_cache.view(torch.int16)[~written])
+    # attention on sampled sequences
+    seqs = sorted(set(rng.choice(dec, size=min(n_seq_sample, len(dec)), replace=False).tolist()) | set(chk))
+    sub, sub_ten, tok = compact_layout(lay, ten, seqs)
+    sub_cu = sub.cu_q_len
+    want = []
+    for i, s in enumerate(seqs):
+        n = int(sub.q_len[i])
+        if n == 1:
+            want.append(int(sub_cu[i]))
+        else:
+            pick = rng.choice(n, size=min(n, n_chunk_tok), replace=False)
+            pick = np.union1d(pick, [0, n - 1])
+            want.extend((int(sub_cu[i]) + pick).tolist())
+    _, _, ref = oracle_step(sub, sub_ten, tokens=want)
+    got = out[torch.from_numpy(tok).cuda()]
+    return compare(got, ref, tokens=want)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["mistral_b512", "yi_b2048", "decode_only"])
+def test_full_size_workloads(name):
+    _full_size(name)
