@@ -184,15 +184,14 @@ def oracle_sample_rate(layout, ten_host, budget_s=12.0, rows=None):
         order = dec + chk
     scale = 1.0 / math.sqrt(sh.head_dim)
     done, t0 = 0, time.perf_counter()
-    for tok in order:
+    while time.perf_counter() - t0 < budget_s:
+        tok = order[done % len(order)]
         pa.attention(q, kp, vp, layout.q_len, layout.context_len, layout.block_table,
                      sh.page_size, sh.num_q_heads, sh.num_kv_heads, scale, tokens=[tok])
         done += 1
-        if time.perf_counter() - t0 > budget_s:
-            break
     dt = time.perf_counter() - t0
     return done / dt, f"{done} new tokens (all {sh.num_q_heads} heads) of this batch, " \
-                      f"decode rows first, {dt:.1f} s"
+                      f"decode rows then every 7th chunk token, cycled, {dt:.1f} s"
 
 
 def run_reference(args):

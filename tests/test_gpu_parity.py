@@ -117,9 +117,9 @@ def test_chunked_prefill_equals_unchunked_on_gpu():
 def test_device_index_error_is_reported():
     hb = lib()
     lay = layout_from_rows(Shape(8, 8, 64), [(1, 40), (20, 50)], 16)
+    ten = workloads.make_tensors(lay, 16)
     lay.block_table[0, 1] = lay.num_pages + 5      # out of range
     lay.block_table[1, 0] = -3
-    ten = workloads.make_tensors(lay, 16)
     gpu_step(lay, ten, check=False)
     with pytest.raises(hb.HbError) as e:
         hb.hb_check()
