@@ -296,6 +296,8 @@ hb_status hb_plan(const hb_batch* batch, const int32_t* h_q_len,
     const int64_t target_items = 3LL * num_sms;
     int split_pages = (int)std::max<int64_t>(8, (total_pages + target_items - 1) / std::max<int64_t>(1, target_items));
     std::vector<DecodeItem> dec;
+    std::vector<int32_t> cu(S + 1, 0);
+    for (int i = 0; i < S; ++i) cu[i + 1] = cu[i] + h_q_len[i];
     int n_slots = 0, n_merge = 0;
     for (int i = 0; i < S; ++i) {
       if (h_q_len[i] != 1) continue;
@@ -319,6 +321,8 @@ hb_status hb_plan(const hb_batch* batch, const int32_t* h_q_len,
           it.n_splits = ns;
           it.slot = slot;
           it.merge_id = merge_id;
+          it.ctx = h_context_len[i];
+          it.tok = cu[i];
           if (it.page_begin < it.page_end) dec.push_back(it);
         }
       }
@@ -343,6 +347,9 @@ hb_status hb_plan(const hb_batch* batch, const int32_t* h_q_len,
           c.tok0 = t0;
           c.ntok = std::min(tpt, h_q_len[i] - t0);
           c.kv_tiles = (off + t0 + c.ntok + kChunkKeys - 1) / kChunkKeys;
+          c.q0 = cu[i];
+          c.q_len = h_q_len[i];
+          c.ctx = h_context_len[i];
           chk.push_back(c);
         }
     }

@@ -42,9 +42,7 @@ struct StageHeader {
   int32_t lpage;
   int32_t flags;
   int32_t qslot;
-  int32_t ctx;
-  int32_t tok;
-  int32_t pad[3];
+  int32_t pad;
 };
 static_assert(sizeof(StageHeader) == 64, "stage header size");
 
@@ -118,82 +116,106 @@ __global__ void __launch_bounds__(kDecThreads, 1)
 
   if (warp == kDecConsumerWarps) {
     // ------------------------------------------------------------ producer
+    // The whole warp runs the loop: each lane holds one block-table entry of
+    // a 32-page window (one coalesced load, fetched a window ahead) and lane
+    // 0 issues the barrier operations and copies.  The next item's index is
+    // fetched while the current item streams.
     if (lane == 0) {
       tma_prefetch_desc(&kmap);
       tma_prefetch_desc(&vmap);
-      int st = 0;
-      uint32_t ph = 0;
-      int qslot = 0;
-      uint32_t qph[2] = {0u, 0u};
-      bool issued[kDecMaxStages];
-      uint32_t last_par[kDecMaxStages];
-      for (int s = 0; s < kDecMaxStages; ++s) {
-        issued[s] = false;
-        last_par[s] = 0;
-      }
-      const uint32_t page_tx = 2u * (uint32_t)L.half_bytes;
-      const uint32_t qbytes = (uint32_t)(kvhb * g * D * 2);
-      bool ok = true;
-      while (ok) {
-        const int idx = atomicAdd(&p.counters[kCounterWork], 1);
-        if (idx >= p.num_items) break;
-        const DecodeItem it = p.items[idx];
-        const int ctx = __ldg(&p.context_len[it.seq]);
-        const int tok = __ldg(&p.cu_q_len[it.seq]);
-        if (!mbar_wait(&qempty[qslot], qph[qslot] ^ 1u, abort_flag)) {
-          ok = false;
-          break;
-        }
-        qph[qslot] ^= 1u;
-        mbar_arrive_expect_tx(&qfull[qslot], qbytes);
-        bulk_load(qbuf + qslot * L.qslot_bytes,
-                  p.q + ((size_t)tok * p.num_q_heads + (size_t)it.kvh0 * g) * D,
-                  qbytes, &qfull[qslot]);
-        for (int lp = it.page_begin; lp < it.page_end; ++lp) {
-          if (!mbar_wait(&empty[st], ph ^ 1u, abort_flag)) {
-            ok = false;
-            break;
-          }
-          StageHeader& h = hdr[st];
-          h.item = it;
-          h.lpage = lp;
-          h.flags = (lp == it.page_begin ? kHdrFirst : 0) |
-                    (lp == it.page_end - 1 ? kHdrLast : 0);
-          h.qslot = qslot;
-          h.ctx = ctx;
-          h.tok = tok;
-          int phys = -1;
-          if (lp < p.max_pages_per_seq)
-            phys = __ldg(&p.block_table[(size_t)it.seq * p.max_pages_per_seq + lp]);
+    }
+    int st = 0;
+    uint32_t ph = 0;
+    int qslot = 0;
+    uint32_t qph[2] = {0u, 0u};
+    uint32_t issued_mask = 0, last_par_mask = 0;
+    const uint32_t page_tx = 2u * (uint32_t)L.half_bytes;
+    const uint32_t qbytes = (uint32_t)(kvhb * g * D * 2);
+    bool ok = true;
+    int idx = 0;
+    if (lane == 0) idx = atomicAdd(&p.counters[kCounterWork], 1);
+    idx = __shfl_sync(0xffffffffu, idx, 0);
+    while (ok && idx < p.num_items) {
+      const DecodeItem it = p.items[idx];
+      // the next item is claimed only while the last pages of this one are
+      // issued (early enough to hide the claim, late enough to keep the
+      // longest-first order balancing the tail)
+      const int claim_at = max(it.page_begin, it.page_end - 2);
+      int next = p.num_items;
+      const int32_t* bt_row = p.block_table + (size_t)it.seq * p.max_pages_per_seq;
+      auto load_window = [&](int base) -> int {
+        const int lp = base + lane;
+        int phys = p.num_pages;  // out of range: the copy reads zeros
+        if (lp < it.page_end) {
+          phys = (lp < p.max_pages_per_seq) ? __ldg(&bt_row[lp]) : -1;
           if (phys < 0 || phys >= p.num_pages) {
             report_error(p.dev_error, HB_DEVERR_INDEX);
-            phys = p.num_pages;  // whole box out of range: the copy reads zeros
-          }
-          mbar_arrive_expect_tx(&full[st], page_tx);
-          uint8_t* kd = stages + st * L.stage_bytes;
-#pragma unroll
-          for (int c = 0; c < CH; ++c) {
-            tma_load_4d(kd + c * L.chunk_bytes, &kmap, &full[st], c * 64, 0,
-                        it.kvh0, phys);
-            tma_load_4d(kd + L.half_bytes + c * L.chunk_bytes, &vmap, &full[st],
-                        c * 64, 0, it.kvh0, phys);
-          }
-          issued[st] = true;
-          last_par[st] = ph;
-          if (++st == S) {
-            st = 0;
-            ph ^= 1u;
+            phys = p.num_pages;
           }
         }
-        qslot ^= 1;
+        return phys;
+      };
+      int win = load_window(it.page_begin);
+      int win_next = load_window(it.page_begin + 32);
+      if (lane == 0) {
+        ok = mbar_wait(&qempty[qslot], qph[qslot] ^ 1u, abort_flag);
+        if (ok) {
+          mbar_arrive_expect_tx(&qfull[qslot], qbytes);
+          bulk_load(qbuf + qslot * L.qslot_bytes,
+                    p.q + ((size_t)it.tok * p.num_q_heads + (size_t)it.kvh0 * g) * D,
+                    qbytes, &qfull[qslot]);
+        }
       }
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      qph[qslot] ^= 1u;
+      for (int lp = it.page_begin; ok && lp < it.page_end; ++lp) {
+        const int k = (lp - it.page_begin) & 31;
+        if (k == 0 && lp != it.page_begin) {
+          win = win_next;
+          win_next = load_window(lp + 32);
+        }
+        const int phys = __shfl_sync(0xffffffffu, win, k);
+        if (lane == 0 && lp == claim_at) next = atomicAdd(&p.counters[kCounterWork], 1);
+        if (lane == 0) {
+          ok = mbar_wait(&empty[st], ph ^ 1u, abort_flag);
+          if (ok) {
+            StageHeader& h = hdr[st];
+            h.item = it;
+            h.lpage = lp;
+            h.flags = (lp == it.page_begin ? kHdrFirst : 0) |
+                      (lp == it.page_end - 1 ? kHdrLast : 0);
+            h.qslot = qslot;
+            mbar_arrive_expect_tx(&full[st], page_tx);
+            uint8_t* kd = stages + st * L.stage_bytes;
+#pragma unroll
+            for (int c = 0; c < CH; ++c) {
+              tma_load_4d(kd + c * L.chunk_bytes, &kmap, &full[st], c * 64, 0,
+                          it.kvh0, phys);
+              tma_load_4d(kd + L.half_bytes + c * L.chunk_bytes, &vmap, &full[st],
+                          c * 64, 0, it.kvh0, phys);
+            }
+            issued_mask |= 1u << st;
+            last_par_mask = (last_par_mask & ~(1u << st)) | (ph << st);
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (++st == S) {
+          st = 0;
+          ph ^= 1u;
+        }
+      }
+      qslot ^= 1;
+      idx = __shfl_sync(0xffffffffu, next, 0);
+    }
+    if (lane == 0) {
       if (ok && mbar_wait(&empty[st], ph ^ 1u, abort_flag)) {
         hdr[st].flags = kHdrEnd;
-        issued[st] = false;  // its earlier copy was consumed
+        issued_mask &= ~(1u << st);  // its earlier copy was consumed
         mbar_arrive(&full[st]);
       }
-      for (int s = 0; s < S; ++s)
-        if (issued[s]) drain_wait(&full[s], last_par[s], abort_flag);
+      for (int s2 = 0; s2 < S; ++s2)
+        if (issued_mask & (1u << s2))
+          drain_wait(&full[s2], (last_par_mask >> s2) & 1u, abort_flag);
       const int done = atomicAdd(&p.counters[kCounterDone], 1);
       if (done == (int)gridDim.x - 1) {
         p.counters[kCounterWork] = 0;
@@ -255,7 +277,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         uint8_t* vst = kst + L.half_bytes;
         const uint32_t kbase = smem_u32(kst);
         const uint32_t vbase = smem_u32(vst);
-        const int valid = min(kPageSize, h.ctx - h.lpage * kPageSize);
+        const int valid = min(kPageSize, h.item.ctx - h.lpage * kPageSize);
         if (valid < kPageSize) {
           // Slots past the context were never written: clear this kv head's
           // V rows there so that P = 0 never meets a NaN in the PV product.
@@ -365,7 +387,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
             if (it.n_splits == 1) {
               const float inv = 1.f / l_tot[hr];
               uint32_t* dst = reinterpret_cast<uint32_t*>(
-                  p.out + ((size_t)h.tok * Hq + head0 + row) * D + cq * 2);
+                  p.out + ((size_t)h.item.tok * Hq + head0 + row) * D + cq * 2);
 #pragma unroll
               for (int nt = 0; nt < D / 8; ++nt)
                 dst[nt * 4] = pack_bf16x2(o[nt][hr * 2] * inv, o[nt][hr * 2 + 1] * inv);
@@ -384,34 +406,53 @@ __global__ void __launch_bounds__(kDecThreads, 1)
           }
         }
         if (it.n_splits > 1) {
-          __threadfence();
+          // publish this split's partial state: the CTA barrier orders every
+          // consumer's stores before thread 0's device-scope fence + atomic
           named_bar_sync(1, 32 * kDecConsumerWarps);
           if (threadIdx.x == 0) {
+            __threadfence();
             const int old = atomicAdd(&p.counters[kCounterMerge0 + it.merge_id], 1);
+            __threadfence();  // acquire: the other splits' states are visible
             flags[1] = (old == it.n_splits - 1) ? 1 : 0;
           }
           named_bar_sync(1, 32 * kDecConsumerWarps);
           if (flags[1]) {
             __threadfence();
-            const int n_el = kvhb * g * D;
+            // one warp per head of the block; each lane owns D/32 head-dim
+            // elements; every split's (m, l) is read once per head
+            constexpr int E = D / 32;
             const float2* ml = reinterpret_cast<const float2*>(p.part_ml);
-            for (int e = threadIdx.x; e < n_el; e += 32 * kDecConsumerWarps) {
-              const int hh = it.kvh0 * g + e / D;
-              const int d = e % D;
+            const int nh = kvhb * g;
+            for (int hl = warp; hl < nh; hl += kDecConsumerWarps) {
+              const int hh = it.kvh0 * g + hl;
               float mmax = -INFINITY;
               for (int i = 0; i < it.n_splits; ++i)
                 mmax = fmaxf(mmax, __ldcg(&ml[(size_t)(it.slot + i) * Hq + hh]).x);
-              float acc = 0.f, lsum = 0.f;
+              float acc[E];
+#pragma unroll
+              for (int e = 0; e < E; ++e) acc[e] = 0.f;
+              float lsum = 0.f;
+#pragma unroll 4
               for (int i = 0; i < it.n_splits; ++i) {
                 const size_t slot = (size_t)(it.slot + i);
                 const float2 st2 = __ldcg(&ml[slot * Hq + hh]);
                 const float wgt = fast_exp2(st2.x - mmax);
                 lsum += wgt * st2.y;
-                acc += wgt * __ldcg(&p.part_o[(slot * Hq + hh) * D + d]);
+                const float* po = p.part_o + (slot * Hq + hh) * D + lane * E;
+                if constexpr (E == 4) {
+                  const float4 v = __ldcg(reinterpret_cast<const float4*>(po));
+                  acc[0] += wgt * v.x; acc[1] += wgt * v.y;
+                  acc[2] += wgt * v.z; acc[3] += wgt * v.w;
+                } else {
+                  const float2 v = __ldcg(reinterpret_cast<const float2*>(po));
+                  acc[0] += wgt * v.x; acc[1] += wgt * v.y;
+                }
               }
-              const float val = acc / lsum;
-              p.out[((size_t)h.tok * Hq + hh) * D + d] =
-                  (uint16_t)(pack_bf16x2(val, 0.f) & 0xFFFFu);
+              const float inv = 1.f / lsum;
+              uint32_t* dst = reinterpret_cast<uint32_t*>(
+                  p.out + ((size_t)h.item.tok * Hq + hh) * D + lane * E);
+#pragma unroll
+              for (int e = 0; e < E; e += 2) dst[e / 2] = pack_bf16x2(acc[e] * inv, acc[e + 1] * inv);
             }
             if (threadIdx.x == 0) p.counters[kCounterMerge0 + it.merge_id] = 0;
           }

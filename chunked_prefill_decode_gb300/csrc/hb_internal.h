@@ -37,7 +37,11 @@ struct DecodeItem {
   int32_t n_splits;
   int32_t slot;         // first partial slot of its (seq, block)
   int32_t merge_id;     // index of the (seq, block) merge counter
+  int32_t ctx;          // context_len of the row (copied from the plan input)
+  int32_t tok;          // its q / out row (cu_q_len of the sequence)
+  int32_t pad0, pad1;
 };
+static_assert(sizeof(DecodeItem) == 48, "decode item size");
 
 // One tensor-core work item: query tokens tok0 .. tok0+ntok-1 (relative to
 // the sequence's first new token) of one kv head, all q heads of its group.
@@ -47,8 +51,11 @@ struct ChunkItem {
   int32_t tok0;
   int32_t ntok;
   int32_t kv_tiles;     // 128-key tiles visited
-  int32_t pad0, pad1, pad2;
+  int32_t q0;           // first q row of the sequence (cu_q_len[seq])
+  int32_t q_len;
+  int32_t ctx;          // context_len of the sequence
 };
+static_assert(sizeof(ChunkItem) == 32, "chunk item size");
 
 // Host plan = header, then DecodeItem[num_decode_items], then
 // ChunkItem[num_chunk_items].  The items are copied verbatim to the start of

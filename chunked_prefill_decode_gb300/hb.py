@@ -221,8 +221,8 @@ def plan_items(plan):
     hd = plan_header(plan)
     body = np.frombuffer(plan[144:].tobytes(), dtype=np.int32)
     nd, nc = hd["num_decode_items"], hd["num_chunk_items"]
-    dec = body[: nd * 8].reshape(nd, 8)
-    chk = body[nd * 8: nd * 8 + nc * 8].reshape(nc, 8)
+    dec = body[: nd * 12].reshape(nd, 12)
+    chk = body[nd * 12: nd * 12 + nc * 8].reshape(nc, 8)
     return dec, chk
 
 

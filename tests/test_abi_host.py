@@ -130,8 +130,10 @@ def _check_plan(rows, hq, hkv, d, sms):
     assert h["chunk_tokens_per_tile"] == 128 // g
     # decode items tile every decode row's pages exactly once per kv block
     cover = {}
-    for seq, kvh0, pb, pe, split, ns, slot, mid in dec:
+    cu = np.concatenate([[0], np.cumsum(ql)])
+    for seq, kvh0, pb, pe, split, ns, slot, mid, ctx, tok, _, _ in dec:
         assert ql[seq] == 1 and 0 <= pb < pe and kvh0 % kvhb == 0
+        assert ctx == cl[seq] and tok == cu[seq]
         cover.setdefault((seq, kvh0), []).append((pb, pe, split, ns, slot, mid))
     for s in range(len(rows)):
         if ql[s] != 1:
@@ -149,8 +151,9 @@ def _check_plan(rows, hq, hkv, d, sms):
     # chunk items cover every (token, kv head) of every chunk row once
     tpt = 128 // g
     seen = set()
-    for seq, kvh, t0, nt, tiles, *_ in chk:
+    for seq, kvh, t0, nt, tiles, q0, qn, ctx in chk:
         assert ql[seq] > 1 and 1 <= nt <= tpt and t0 % tpt == 0
+        assert q0 == cu[seq] and qn == ql[seq] and ctx == cl[seq]
         off = cl[seq] - ql[seq]
         assert tiles == -(-(off + t0 + nt) // 128)
         for t in range(t0, t0 + nt):
