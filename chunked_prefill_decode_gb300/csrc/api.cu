@@ -200,6 +200,44 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 }  // namespace
 
+// ---------------------------------------------------------------- internal
+// Hooks for other translation units of the library (not part of the ABI).
+namespace hb {
+
+hb_status internal_fail(hb_status s, const char* msg) { return fail(s, "%s", msg); }
+
+hb_status internal_ok() { return ok(); }
+
+hb_status internal_check_batch(const hb_batch* b) { return check_batch(b); }
+
+hb_status internal_device(int** err, int* num_sms) {
+  DevState* d = nullptr;
+  hb_status s = device_state(&d);
+  if (s != HB_OK) return s;
+  *err = d->err;
+  *num_sms = d->num_sms;
+  return HB_OK;
+}
+
+// TMA maps of the decode kernel over the K and V pools.
+hb_status internal_decode_maps(const hb_batch* b, int kvhb, const void* k_cache,
+                               const void* v_cache, CUtensorMap* kmap, CUtensorMap* vmap) {
+  hb_status s = get_encoder();
+  if (s != HB_OK) return s;
+  const int Hkv = b->num_kv_heads, D = b->head_dim;
+  const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)kPageSize, (cuuint64_t)Hkv,
+                              (cuuint64_t)b->num_pages};
+  const cuuint64_t strides[3] = {(cuuint64_t)Hkv * D * 2, (cuuint64_t)D * 2,
+                                 (cuuint64_t)kPageSize * Hkv * D * 2};
+  const cuuint32_t box[4] = {64, (cuuint32_t)kPageSize, (cuuint32_t)kvhb, 1};
+  if ((s = encode_map(kmap, k_cache, 4, dims, strides, box, "decode K")) != HB_OK) return s;
+  return encode_map(vmap, v_cache, 4, dims, strides, box, "decode V");
+}
+
+void internal_count_launch() { g_launches.fetch_add(1); }
+
+}  // namespace hb
+
 // =========================================================================
 extern "C" {
 

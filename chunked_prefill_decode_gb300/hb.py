@@ -55,7 +55,7 @@ EXPORTED = (
     "hb_check", "hb_timing_enable", "hb_timing_read", "hb_launch_count",
     "hb_builder_create", "hb_builder_destroy", "hb_builder_add_request",
     "hb_builder_step", "hb_builder_complete", "hb_builder_counts",
-    "hb_builder_free_list", "hb_builder_last_error",
+    "hb_builder_free_list", "hb_builder_last_error", "hb_decode_attention_noalloc",
 )
 
 
@@ -87,6 +87,9 @@ def load():
     L.hb_plan.argtypes = [P(HbBatch), vp, vp, i32, vp, P(sz), vp, P(sz), vp]
     L.hb_attention.restype = ctypes.c_int
     L.hb_attention.argtypes = [P(HbBatch), vp, vp, vp, vp, ctypes.c_float, vp, vp, vp]
+    L.hb_decode_attention_noalloc.restype = ctypes.c_int
+    L.hb_decode_attention_noalloc.argtypes = [P(HbBatch), vp, vp, vp, vp, vp, ctypes.c_float,
+                                              vp, vp]
     L.hb_check.restype = ctypes.c_int
     L.hb_check.argtypes = [vp]
     L.hb_timing_enable.restype = ctypes.c_int
@@ -231,6 +234,18 @@ def hb_attention(batch, plan, q, k_cache, v_cache, scale, out, workspace, stream
                                _bf16(k_cache, "k_cache"), _bf16(v_cache, "v_cache"),
                                ctypes.c_float(scale), _bf16(out, "out"), _ptr(workspace),
                                _stream(stream)))
+
+
+def hb_decode_attention_noalloc(batch, q_len, context_len, q, k_cache, v_cache, scale,
+                                out, stream=None):
+    """Decode-row attention with the library's static scratch (no workspace,
+    no device allocation by the library); all rows must have q_len == 1."""
+    ql = np.ascontiguousarray(q_len, dtype=np.int32)
+    cl = np.ascontiguousarray(context_len, dtype=np.int32)
+    _check(load().hb_decode_attention_noalloc(
+        ctypes.byref(batch), _ptr(ql), _ptr(cl), _bf16(q, "q"), _bf16(k_cache, "k_cache"),
+        _bf16(v_cache, "v_cache"), ctypes.c_float(scale), _bf16(out, "out"),
+        _stream(stream)))
 
 
 def hb_check(stream=None):

@@ -159,6 +159,44 @@ hb_status hb_attention(const hb_batch* batch, const void* h_plan,
                        void* d_workspace, void* stream);
 
 /*
+ * Decode attention without a workspace, for callers that cannot allocate
+ * device memory.  (The pages have no counterpart of this call: it exists for
+ * callers such as a serving engine that gives nearly all free HBM to its
+ * KV-cache pool at start-up and allows no device allocation afterwards, or a
+ * plugin that is handed raw tensor pointers but no allocator.)
+ *
+ * Same result as hb_plan + hb_attention on a batch whose rows are all decode
+ * rows (q_len == 1), using the same split-KV kernel, but its scratch (work
+ * items, counters, split partial states) is a fixed device array of
+ * HB_NOALLOC_SCRATCH_BYTES inside the library, which every device that loads
+ * the library holds until the process exits.  The call makes no cudaMalloc /
+ * cudaFree and no other allocating call; its host-side plan also uses static
+ * storage.  The caller still owns and passes q, the caches and out (layouts as
+ * in hb_attention) plus host copies of q_len and context_len.
+ *   - The first call on a device looks up that device's copy of the array
+ *     (with the device current); make that first call before any stream
+ *     capture.
+ *   - All calls share the array and it keeps the last call's contents: each
+ *     call clears the counters it needs; calls that overlap on the GPU (other
+ *     streams or host threads) race and must be serialised by the caller.
+ *     Host calls are serialised by a lock inside the library.
+ *   - The plan's items are copied from pageable host memory, so the call
+ *     returns after the copy is staged.
+ *   - Splits are made coarser until the partial states fit the array; a batch
+ *     that needs more than 4096 work items (num_seqs times ceil(Hkv / 8)) is
+ *     rejected with HB_ERR_WORKSPACE.  Rows with q_len != 1 give
+ *     HB_ERR_UNSUPPORTED.  Other errors as hb_attention.
+ */
+#define HB_NOALLOC_SCRATCH_BYTES (8u * 1024u * 1024u)
+
+hb_status hb_decode_attention_noalloc(const hb_batch* batch,
+                                      const int32_t* h_q_len,
+                                      const int32_t* h_context_len,
+                                      const void* q, const void* k_cache,
+                                      const void* v_cache, float softmax_scale,
+                                      void* out, void* stream);
+
+/*
  * Synchronise `stream`, then read and clear the device error word of the
  * current device: HB_OK, HB_ERR_DEVICE_INDEX or HB_ERR_TIMEOUT (or
  * HB_ERR_CUDA if the stream itself failed).  Blocking.
