@@ -16,6 +16,7 @@
 #include <vector>
 
 #include "hb.h"
+#include "decode_plan.h"
 #include "hb_internal.h"
 
 __device__ int g_hb_device_error = 0;
@@ -325,51 +326,28 @@ hb_status hb_plan(const hb_batch* batch, const int32_t* h_q_len,
     if (tq != batch->total_q)
       return fail(HB_ERR_SHAPE, "sum of q_len (%lld) != total_q (%d)", (long long)tq, batch->total_q);
 
-    // ---- decode items: rows with q_len == 1, split over page ranges
+    // ---- decode items: the decode rows' pages, end to end, cut into one
+    // equal contiguous range per CTA, each range cut at row boundaries
     const int kvhb = std::min(Hkv, kDecodeKvhBlock);
     const int n_blocks = Hkv / kvhb;
-    int64_t total_pages = 0;
-    for (int i = 0; i < S; ++i)
-      if (h_q_len[i] == 1) total_pages += (int64_t)((h_context_len[i] + kPageSize - 1) / kPageSize) * n_blocks;
-    const int64_t target_items = 3LL * num_sms;
-    int split_pages = (int)std::max<int64_t>(8, (total_pages + target_items - 1) / std::max<int64_t>(1, target_items));
-    std::vector<DecodeItem> dec;
     std::vector<int32_t> cu(S + 1, 0);
     for (int i = 0; i < S; ++i) cu[i + 1] = cu[i] + h_q_len[i];
-    int n_slots = 0, n_merge = 0;
-    for (int i = 0; i < S; ++i) {
-      if (h_q_len[i] != 1) continue;
-      const int np = (h_context_len[i] + kPageSize - 1) / kPageSize;
-      const int ns = (np + split_pages - 1) / split_pages;
-      const int per = (np + ns - 1) / ns;
-      for (int b = 0; b < n_blocks; ++b) {
-        int slot = 0, merge_id = 0;
-        if (ns > 1) {
-          slot = n_slots;
-          n_slots += ns;
-          merge_id = n_merge++;
-        }
-        for (int k = 0; k < ns; ++k) {
-          DecodeItem it{};
-          it.seq = i;
-          it.kvh0 = b * kvhb;
-          it.page_begin = k * per;
-          it.page_end = std::min(np, (k + 1) * per);
-          it.split = k;
-          it.n_splits = ns;
-          it.slot = slot;
-          it.merge_id = merge_id;
-          it.ctx = h_context_len[i];
-          it.tok = cu[i];
-          if (it.page_begin < it.page_end) dec.push_back(it);
-        }
+    int64_t n_dec_rows = 0, dec_pages = 0;
+    for (int i = 0; i < S; ++i)
+      if (h_q_len[i] == 1) {
+        ++n_dec_rows;
+        dec_pages += (int64_t)((h_context_len[i] + kPageSize - 1) / kPageSize) * n_blocks;
       }
-    }
-    // a split with an empty range can only appear when per * (ns-1) >= np,
-    // which the ceil-division above rules out; keep n_splits consistent anyway
-    std::stable_sort(dec.begin(), dec.end(), [](const DecodeItem& a, const DecodeItem& b) {
-      return (a.page_end - a.page_begin) > (b.page_end - b.page_begin);
-    });
+    const int max_dec_items = (int)std::min<int64_t>(n_dec_rows * n_blocks + num_sms + 1, 1 << 30);
+    std::vector<DecodeItem> dec(std::max(1, max_dec_items));
+    std::vector<int32_t> cta_off(num_sms + 1, 0);
+    DecodePartition part;
+    if (!partition_decode(S, h_q_len, h_context_len, n_blocks, kvhb, num_sms, 4, dec.data(),
+                          (int)dec.size(), cta_off.data(), num_sms, &part))
+      return fail(HB_ERR_WORKSPACE, "decode partition overflow");
+    dec.resize(part.n_items);
+    cta_off.resize(part.grid + 1);
+    const int n_slots = part.n_slots, n_merge = part.n_merge;
 
     // ---- chunk items: rows with q_len > 1, (kv head, query tile)
     const int tpt = kChunkRows / g;
@@ -396,7 +374,8 @@ hb_status hb_plan(const hb_batch* batch, const int32_t* h_q_len,
     });
 
     // ---- sizes
-    const size_t items_bytes = align_up(dec.size() * sizeof(DecodeItem) + chk.size() * sizeof(ChunkItem), 256);
+    const size_t offsets_at = dec.size() * sizeof(DecodeItem) + chk.size() * sizeof(ChunkItem);
+    const size_t items_bytes = align_up(offsets_at + cta_off.size() * sizeof(int32_t), 256);
     const size_t need_plan = sizeof(PlanHeader) + items_bytes;
     const size_t ws_counters = items_bytes;
     const size_t ws_partial_o = align_up(ws_counters + (size_t)(kCounterMerge0 + n_merge) * 4, 256);
@@ -431,7 +410,8 @@ hb_status hb_plan(const hb_batch* batch, const int32_t* h_q_len,
     h.num_chunk_items = (int32_t)chk.size();
     h.num_partial_slots = n_slots;
     h.num_merge_counters = n_merge;
-    h.decode_grid = (int32_t)std::min<size_t>((size_t)num_sms, dec.size());
+    h.decode_grid = part.grid;
+    h.ws_decode_offsets = offsets_at;
     h.decode_kvh_block = kvhb;
     h.chunk_tokens_per_tile = tpt;
     h.items_bytes = items_bytes;
@@ -447,6 +427,7 @@ hb_status hb_plan(const hb_batch* batch, const int32_t* h_q_len,
     if (!dec.empty()) std::memcpy(items, dec.data(), dec.size() * sizeof(DecodeItem));
     if (!chk.empty())
       std::memcpy(items + dec.size() * sizeof(DecodeItem), chk.data(), chk.size() * sizeof(ChunkItem));
+    std::memcpy(items + offsets_at, cta_off.data(), cta_off.size() * sizeof(int32_t));
 
     if (d_workspace == nullptr) return ok();  // host plan only
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -510,6 +491,7 @@ hb_status hb_attention(const hb_batch* batch, const void* h_plan, const void* q,
       if ((s = encode_map(&vmap, v_cache, 4, dims, strides, box, "decode V")) != HB_OK) return s;
       DecodeParams p{};
       p.items = reinterpret_cast<const DecodeItem*>(ws);
+      p.cta_offsets = reinterpret_cast<const int32_t*>(ws + h.ws_decode_offsets);
       p.num_items = h.num_decode_items;
       p.counters = reinterpret_cast<int32_t*>(ws + h.ws_counters);
       p.part_o = reinterpret_cast<float*>(ws + h.ws_partial_o);

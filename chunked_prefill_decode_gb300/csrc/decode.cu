@@ -7,9 +7,10 @@
 // memory-bound (every step reads the whole KV cache).  So this kernel is
 // built to stream KV pages at HBM speed:
 //
-//  * persistent: one CTA per SM pulls work items (a page range of one decode
-//    row and one block of <= 8 kv heads) from an atomic counter; items are
-//    ordered longest first by the host plan;
+//  * persistent and statically balanced: the host plan lays the decode
+//    rows' pages end to end and gives each CTA (at most one per SM) an equal
+//    contiguous range, cut at row boundaries into work items (a page range of
+//    one row and one block of <= 8 kv heads);
 //  * one producer warp streams whole pages (all kv heads of the block, K and
 //    V) into a ring of shared-memory stages with 4-D TMA copies laid out as
 //    [kv head][slot][64 head-dim] rows with the 128-byte swizzle, so the
@@ -19,9 +20,9 @@
 //    forms the rows of a 16 x 16 x 16 warp MMA, so each K/V element loaded
 //    from shared memory serves all g heads; online softmax in registers with
 //    the exp2 form (scale * log2 e folded in);
-//  * split-KV partial states (m, l, unnormalised o) go to the workspace; the
-//    last split of a (row, kv block) to finish, found with an atomic counter,
-//    merges them: m = max m_i, l = sum 2^(m_i - m) l_i, o = sum 2^(m_i - m) o_i
+//  * a row that straddles ranges leaves one partial state (m, l,
+//    unnormalised o) per piece in the workspace; the last piece of a
+//    (row, kv block) to finish, found with an atomic counter, merges them: m = max m_i, l = sum 2^(m_i - m) l_i, o = sum 2^(m_i - m) o_i
 //    / l.  Nobody waits on another CTA.
 //
 // Bytes per decode row: 2 * context * Hkv * D * 2 (K and V read once).
@@ -116,10 +117,12 @@ __global__ void __launch_bounds__(kDecThreads, 1)
 
   if (warp == kDecConsumerWarps) {
     // ------------------------------------------------------------ producer
-    // The whole warp runs the loop: each lane holds one block-table entry of
-    // a 32-page window (one coalesced load, fetched a window ahead) and lane
-    // 0 issues the barrier operations and copies.  The next item's index is
-    // fetched while the current item streams.
+    // This CTA streams its own contiguous range of pages (items
+    // cta_offsets[b] .. cta_offsets[b+1], cut at row boundaries).  The whole
+    // warp runs the loop: each lane holds one block-table entry of a 32-page
+    // window (one coalesced load, fetched a window ahead; the next item's
+    // first window is fetched while the current item starts) and lane 0
+    // issues the barrier operations and copies.
     if (lane == 0) {
       tma_prefetch_desc(&kmap);
       tma_prefetch_desc(&vmap);
@@ -131,32 +134,33 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     uint32_t issued_mask = 0, last_par_mask = 0;
     const uint32_t page_tx = 2u * (uint32_t)L.half_bytes;
     const uint32_t qbytes = (uint32_t)(kvhb * g * D * 2);
-    bool ok = true;
-    int idx = 0;
-    if (lane == 0) idx = atomicAdd(&p.counters[kCounterWork], 1);
-    idx = __shfl_sync(0xffffffffu, idx, 0);
-    while (ok && idx < p.num_items) {
-      const DecodeItem it = p.items[idx];
-      // the next item is claimed only while the last pages of this one are
-      // issued (early enough to hide the claim, late enough to keep the
-      // longest-first order balancing the tail)
-      const int claim_at = max(it.page_begin, it.page_end - 2);
-      int next = p.num_items;
-      const int32_t* bt_row = p.block_table + (size_t)it.seq * p.max_pages_per_seq;
-      auto load_window = [&](int base) -> int {
-        const int lp = base + lane;
-        int phys = p.num_pages;  // out of range: the copy reads zeros
-        if (lp < it.page_end) {
-          phys = (lp < p.max_pages_per_seq) ? __ldg(&bt_row[lp]) : -1;
-          if (phys < 0 || phys >= p.num_pages) {
-            report_error(p.dev_error, HB_DEVERR_INDEX);
-            phys = p.num_pages;
-          }
+    auto window = [&](const DecodeItem& x, int base) -> int {
+      const int lp = base + lane;
+      int phys = p.num_pages;  // out of range: the copy reads zeros
+      if (lp < x.page_end) {
+        phys = (lp < p.max_pages_per_seq)
+                   ? __ldg(&p.block_table[(size_t)x.seq * p.max_pages_per_seq + lp])
+                   : -1;
+        if (phys < 0 || phys >= p.num_pages) {
+          report_error(p.dev_error, HB_DEVERR_INDEX);
+          phys = p.num_pages;
         }
-        return phys;
-      };
-      int win = load_window(it.page_begin);
-      int win_next = load_window(it.page_begin + 32);
+      }
+      return phys;
+    };
+    const int i0 = p.cta_offsets[blockIdx.x];
+    const int i1 = p.cta_offsets[blockIdx.x + 1];
+    bool ok = true;
+    DecodeItem it{}, nxt{};
+    int win = 0, win_next = 0, nxt_win = 0;
+    if (i0 < i1) {
+      it = p.items[i0];
+      win = window(it, it.page_begin);
+      win_next = window(it, it.page_begin + 32);
+    }
+    for (int i = i0; ok && i < i1; ++i) {
+      const bool has_next = i + 1 < i1;
+      if (has_next) nxt = p.items[i + 1];
       if (lane == 0) {
         ok = mbar_wait(&qempty[qslot], qph[qslot] ^ 1u, abort_flag);
         if (ok) {
@@ -168,14 +172,15 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       }
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
       qph[qslot] ^= 1u;
+      const int nxt_at = min(it.page_begin + 1, it.page_end - 1);
       for (int lp = it.page_begin; ok && lp < it.page_end; ++lp) {
         const int k = (lp - it.page_begin) & 31;
         if (k == 0 && lp != it.page_begin) {
           win = win_next;
-          win_next = load_window(lp + 32);
+          win_next = window(it, lp + 32);
         }
+        if (has_next && lp == nxt_at) nxt_win = window(nxt, nxt.page_begin);
         const int phys = __shfl_sync(0xffffffffu, win, k);
-        if (lane == 0 && lp == claim_at) next = atomicAdd(&p.counters[kCounterWork], 1);
         if (lane == 0) {
           ok = mbar_wait(&empty[st], ph ^ 1u, abort_flag);
           if (ok) {
@@ -205,7 +210,11 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         }
       }
       qslot ^= 1;
-      idx = __shfl_sync(0xffffffffu, next, 0);
+      if (has_next) {
+        it = nxt;
+        win = nxt_win;
+        win_next = window(it, it.page_begin + 32);
+      }
     }
     if (lane == 0) {
       if (ok && mbar_wait(&empty[st], ph ^ 1u, abort_flag)) {
@@ -216,12 +225,6 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       for (int s2 = 0; s2 < S; ++s2)
         if (issued_mask & (1u << s2))
           drain_wait(&full[s2], (last_par_mask >> s2) & 1u, abort_flag);
-      const int done = atomicAdd(&p.counters[kCounterDone], 1);
-      if (done == (int)gridDim.x - 1) {
-        p.counters[kCounterWork] = 0;
-        p.counters[kCounterDone] = 0;
-        __threadfence();
-      }
     }
   } else {
     // ------------------------------------------------------------ consumers

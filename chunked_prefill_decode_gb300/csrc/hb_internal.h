@@ -57,9 +57,10 @@ struct ChunkItem {
 };
 static_assert(sizeof(ChunkItem) == 32, "chunk item size");
 
-// Host plan = header, then DecodeItem[num_decode_items], then
-// ChunkItem[num_chunk_items].  The items are copied verbatim to the start of
-// the device workspace; the header records where everything else lives.
+// Host plan = header, then DecodeItem[num_decode_items] (in CTA order), then
+// ChunkItem[num_chunk_items], then int32 decode CTA offsets[decode_grid + 1].
+// That body is copied verbatim to the start of the device workspace; the
+// header records where everything else lives.
 struct PlanHeader {
   uint32_t magic;
   uint32_t version;
@@ -74,7 +75,7 @@ struct PlanHeader {
   int32_t decode_kvh_block;
   int32_t chunk_tokens_per_tile;
   int32_t pad0;
-  uint64_t reserved;
+  uint64_t ws_decode_offsets;  // device offset of the per-CTA item offsets
   uint64_t items_bytes;     // bytes of the item arrays (host and device)
   uint64_t ws_counters;     // device offsets (bytes from workspace start)
   uint64_t ws_partial_o;
@@ -92,7 +93,8 @@ constexpr int kCounterDone = 1;
 constexpr int kCounterMerge0 = 2;
 
 struct DecodeParams {
-  const DecodeItem* items;
+  const DecodeItem* items;      // in CTA order
+  const int32_t* cta_offsets;   // [grid + 1]: CTA b takes items [b], [b+1])
   int32_t num_items;
   int32_t* counters;
   float* part_o;          // [slots, Hq, D]

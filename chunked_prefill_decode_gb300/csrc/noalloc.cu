@@ -23,6 +23,7 @@
 #include <cstring>
 #include <mutex>
 
+#include "decode_plan.h"
 #include "hb.h"
 #include "hb_internal.h"
 
@@ -41,15 +42,17 @@ void internal_count_launch();
 
 using namespace hb;
 
-// The scratch: [items | counters | partial o | partial (m, l)].
+// The scratch: [items | CTA offsets | counters | partial o | partial (m, l)].
 static __device__ __align__(256) unsigned char g_noalloc_scratch[HB_NOALLOC_SCRATCH_BYTES];
 
 namespace {
 
 constexpr int kMaxItems = 4096;
 constexpr int kMaxMerges = 4096;
+constexpr int kMaxGrid = 1024;
 constexpr size_t kItemsBytes = (size_t)kMaxItems * sizeof(DecodeItem);
-constexpr size_t kCountersOff = kItemsBytes;
+constexpr size_t kOffsetsOff = kItemsBytes;
+constexpr size_t kCountersOff = kOffsetsOff + (size_t)(kMaxGrid + 1) * 4;
 constexpr size_t kCountersBytes = (size_t)(kCounterMerge0 + kMaxMerges) * 4;
 constexpr size_t kPartialOff = (kCountersOff + kCountersBytes + 255) / 256 * 256;
 static_assert(kPartialOff < HB_NOALLOC_SCRATCH_BYTES, "scratch layout");
@@ -57,6 +60,7 @@ static_assert(kPartialOff < HB_NOALLOC_SCRATCH_BYTES, "scratch layout");
 std::mutex g_mu;
 void* g_scratch[64] = {};     // device address of the array, per device
 DecodeItem g_items[kMaxItems];  // host-side plan (static: nothing is allocated)
+int32_t g_offsets[kMaxGrid + 1];
 
 // Address of this device's copy of the array; looked up on the first call on
 // each device (the device must be current).
@@ -94,7 +98,6 @@ extern "C" hb_status hb_decode_attention_noalloc(const hb_batch* batch, const in
       if (!ptr || (reinterpret_cast<uintptr_t>(ptr) & 15u))
         return internal_fail(HB_ERR_INVALID_ARG, "q, k_cache, v_cache and out must be non-NULL and 16-byte aligned");
     const int Hq = batch->num_q_heads, Hkv = batch->num_kv_heads, D = batch->head_dim;
-    const int g = Hq / Hkv;
     const int64_t max_ctx = (int64_t)batch->max_pages_per_seq * kPageSize;
     for (int i = 0; i < S; ++i) {
       if (h_q_len[i] != 1)
@@ -103,78 +106,32 @@ extern "C" hb_status hb_decode_attention_noalloc(const hb_batch* batch, const in
         return internal_fail(HB_ERR_SHAPE, "context_len outside 1 .. max_pages_per_seq * 16");
     }
     if (batch->total_q != S) return internal_fail(HB_ERR_SHAPE, "total_q must equal num_seqs");
+    const int g = Hq / Hkv;
 
-    // ---- plan into static host storage; splits shrink until the partial
-    // states fit the scratch
+    // ---- plan into static host storage: the decode partition over at most
+    // one CTA per SM; fewer, longer ranges until the partial states fit
     const int kvhb = std::min(Hkv, kDecodeKvhBlock);
     const int n_blocks = Hkv / kvhb;
     int* err = nullptr;
     int num_sms = 0;
     if ((s = internal_device(&err, &num_sms)) != HB_OK) return s;
-    int64_t total_pages = 0;
-    for (int i = 0; i < S; ++i) total_pages += (int64_t)((h_context_len[i] + kPageSize - 1) / kPageSize) * n_blocks;
-    const int64_t target = 3LL * num_sms;
-    int64_t split_pages = std::max<int64_t>(8, (total_pages + target - 1) / target);
     const size_t slot_bytes = (size_t)Hq * D * 4 + (size_t)Hq * 8;
     const size_t partial_room = HB_NOALLOC_SCRATCH_BYTES - kPartialOff;
-    int n_items = 0, n_slots = 0, n_merge = 0;
+    int max_grid = std::min(num_sms, kMaxGrid);
+    DecodePartition part;
     for (;;) {
-      n_items = n_slots = n_merge = 0;
-      for (int i = 0; i < S; ++i) {
-        const int64_t np = (h_context_len[i] + kPageSize - 1) / kPageSize;
-        const int64_t ns = (np + split_pages - 1) / split_pages;
-        n_items += (int)(ns * n_blocks);
-        if (ns > 1) {
-          n_slots += (int)(ns * n_blocks);
-          n_merge += n_blocks;
-        }
-      }
-      const bool fits = n_items <= kMaxItems && n_merge <= kMaxMerges &&
-                        (size_t)n_slots * slot_bytes <= partial_room;
-      if (fits) break;
-      if (n_slots == 0) {
+      if (!partition_decode(S, h_q_len, h_context_len, n_blocks, kvhb, num_sms, 4, g_items,
+                            kMaxItems, g_offsets, max_grid, &part))
         return internal_fail(HB_ERR_WORKSPACE,
                              "batch needs more work items than the static scratch holds "
-                             "(at most 4096 = num_seqs * kv blocks)");
-      }
-      split_pages *= 2;
+                             "(at most 4096 = num_seqs * ceil(Hkv / 8) plus one per SM)");
+      if (part.n_merge <= kMaxMerges && (size_t)part.n_slots * slot_bytes <= partial_room) break;
+      if (max_grid == 1)
+        return internal_fail(HB_ERR_WORKSPACE, "partial states do not fit the static scratch");
+      max_grid = std::max(1, max_grid / 2);
     }
-    int k = 0, slot = 0, merge_id = 0;
-    for (int i = 0; i < S; ++i) {
-      const int np = (h_context_len[i] + kPageSize - 1) / kPageSize;
-      const int ns = (int)((np + split_pages - 1) / split_pages);
-      const int per = (np + ns - 1) / ns;
-      for (int b = 0; b < n_blocks; ++b) {
-        const int my_slot = ns > 1 ? slot : 0;
-        const int my_merge = ns > 1 ? merge_id : 0;
-        if (ns > 1) {
-          slot += ns;
-          ++merge_id;
-        }
-        for (int sp = 0; sp < ns; ++sp) {
-          DecodeItem& it = g_items[k++];
-          std::memset(&it, 0, sizeof(it));
-          it.seq = i;
-          it.kvh0 = b * kvhb;
-          it.page_begin = sp * per;
-          it.page_end = std::min(np, (sp + 1) * per);
-          it.split = sp;
-          it.n_splits = ns;
-          it.slot = my_slot;
-          it.merge_id = my_merge;
-          it.ctx = h_context_len[i];
-          it.tok = i;
-        }
-      }
-    }
-    // longest first (in-place sort; ties keep the row order)
-    std::sort(g_items, g_items + k, [](const DecodeItem& a, const DecodeItem& b) {
-      const int la = a.page_end - a.page_begin, lb = b.page_end - b.page_begin;
-      if (la != lb) return la > lb;
-      if (a.seq != b.seq) return a.seq < b.seq;
-      if (a.kvh0 != b.kvh0) return a.kvh0 < b.kvh0;
-      return a.split < b.split;
-    });
+    const int k = part.n_items;
+    const int n_slots = part.n_slots, n_merge = part.n_merge;
 
     void* scratch = nullptr;
     if ((s = scratch_address(&scratch)) != HB_OK) return s;
@@ -183,6 +140,9 @@ extern "C" hb_status hb_decode_attention_noalloc(const hb_batch* batch, const in
     cudaError_t e = cudaMemcpyAsync(base, g_items, (size_t)k * sizeof(DecodeItem),
                                     cudaMemcpyHostToDevice, st);
     if (e != cudaSuccess) return internal_fail(HB_ERR_CUDA, "copy of the work items failed");
+    e = cudaMemcpyAsync(base + kOffsetsOff, g_offsets, (size_t)(part.grid + 1) * 4,
+                        cudaMemcpyHostToDevice, st);
+    if (e != cudaSuccess) return internal_fail(HB_ERR_CUDA, "copy of the CTA offsets failed");
     e = cudaMemsetAsync(base + kCountersOff, 0, (size_t)(kCounterMerge0 + n_merge) * 4, st);
     if (e != cudaSuccess) return internal_fail(HB_ERR_CUDA, "clearing the counters failed");
 
@@ -190,6 +150,7 @@ extern "C" hb_status hb_decode_attention_noalloc(const hb_batch* batch, const in
     if ((s = internal_decode_maps(batch, kvhb, k_cache, v_cache, &kmap, &vmap)) != HB_OK) return s;
     DecodeParams p{};
     p.items = reinterpret_cast<const DecodeItem*>(base);
+    p.cta_offsets = reinterpret_cast<const int32_t*>(base + kOffsetsOff);
     p.num_items = k;
     p.counters = reinterpret_cast<int32_t*>(base + kCountersOff);
     p.part_o = reinterpret_cast<float*>(base + kPartialOff);
@@ -207,7 +168,7 @@ extern "C" hb_status hb_decode_attention_noalloc(const hb_batch* batch, const in
     p.kvh_block = kvhb;
     p.scale_log2 = softmax_scale * 1.4426950408889634f;
     p.dev_error = err;
-    e = launch_decode(p, D, std::min(num_sms, k), kmap, vmap, st);
+    e = launch_decode(p, D, part.grid, kmap, vmap, st);
     if (e != cudaSuccess) return internal_fail(HB_ERR_CUDA, "decode launch failed");
     internal_count_launch();
     return internal_ok();

@@ -209,24 +209,35 @@ def hb_plan(batch, q_len, context_len, num_sms, workspace=None, stream=None,
 
 
 def plan_header(plan):
-    """Decode the leading fields of a host plan (for tests and reports)."""
+    """Decode the header of a host plan (for tests and reports)."""
     h = np.frombuffer(plan[:72].tobytes(), dtype=np.int32)
     keys = ("magic", "version", "num_seqs", "total_q", "num_q_heads", "num_kv_heads",
             "head_dim", "page_size", "max_pages_per_seq", "num_sms",
             "num_decode_items", "num_chunk_items", "num_partial_slots",
             "num_merge_counters", "decode_grid", "decode_kvh_block",
             "chunk_tokens_per_tile", "pad0")
-    return {k: int(v) for k, v in zip(keys, h)}
+    out = {k: int(v) for k, v in zip(keys, h)}
+    u = np.frombuffer(plan[72:144].tobytes(), dtype=np.uint64)
+    for k, v in zip(("ws_decode_offsets", "items_bytes", "ws_counters", "ws_partial_o",
+                     "ws_partial_ml", "ws_total", "plan_bytes"), u):
+        out[k] = int(v)
+    return out
 
 
 def plan_items(plan):
-    """(decode items [n, 8] int32, chunk items [m, 8] int32) of a host plan."""
+    """(decode items [n, 12] int32 in CTA order, chunk items [m, 8] int32,
+    decode CTA offsets [grid + 1]) of a host plan."""
     hd = plan_header(plan)
-    body = np.frombuffer(plan[144:].tobytes(), dtype=np.int32)
+    body = plan[144:]
     nd, nc = hd["num_decode_items"], hd["num_chunk_items"]
-    dec = body[: nd * 12].reshape(nd, 12)
-    chk = body[nd * 12: nd * 12 + nc * 8].reshape(nc, 8)
-    return dec, chk
+    ints = np.frombuffer(body[: nd * 48 + nc * 32].tobytes(), dtype=np.int32)
+    dec = ints[: nd * 12].reshape(nd, 12)
+    chk = ints[nd * 12: nd * 12 + nc * 8].reshape(nc, 8)
+    off = hd["ws_decode_offsets"]
+    grid = hd["decode_grid"]
+    offs = np.frombuffer(body[off: off + 4 * (grid + 1)].tobytes(), dtype=np.int32) \
+        if grid > 0 else np.zeros(1, np.int32)
+    return dec, chk, offs
 
 
 def hb_attention(batch, plan, q, k_cache, v_cache, scale, out, workspace, stream=None):

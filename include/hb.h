@@ -182,10 +182,11 @@ hb_status hb_attention(const hb_batch* batch, const void* h_plan,
  *     Host calls are serialised by a lock inside the library.
  *   - The plan's items are copied from pageable host memory, so the call
  *     returns after the copy is staged.
- *   - Splits are made coarser until the partial states fit the array; a batch
- *     that needs more than 4096 work items (num_seqs times ceil(Hkv / 8)) is
- *     rejected with HB_ERR_WORKSPACE.  Rows with q_len != 1 give
- *     HB_ERR_UNSUPPORTED.  Other errors as hb_attention.
+ *   - The work is spread over fewer CTAs when the partial states would not
+ *     fit the array; a batch that needs more than 4096 work items (about
+ *     num_seqs times ceil(Hkv / 8), plus one per SM) is rejected with
+ *     HB_ERR_WORKSPACE.  Rows with q_len != 1 give HB_ERR_UNSUPPORTED.  Other
+ *     errors as hb_attention.
  */
 #define HB_NOALLOC_SCRATCH_BYTES (8u * 1024u * 1024u)
 

@@ -123,18 +123,27 @@ def _check_plan(rows, hq, hkv, d, sms):
     b, ql, cl = host_batch(hb, rows, hq=hq, hkv=hkv, d=d)
     plan, _ = hb.hb_plan(b, ql, cl, sms, upload=False)
     h = hb.plan_header(plan)
-    dec, chk = hb.plan_items(plan)
+    dec, chk, offs = hb.plan_items(plan)
     g = hq // hkv
     kvhb = min(hkv, 8)
     assert h["decode_kvh_block"] == kvhb
     assert h["chunk_tokens_per_tile"] == 128 // g
-    # decode items tile every decode row's pages exactly once per kv block
-    cover = {}
     cu = np.concatenate([[0], np.cumsum(ql)])
+    # decode: CTA ranges are contiguous, equal (the last may be shorter),
+    # and together tile every decode row's pages once per kv block
+    grid = h["decode_grid"]
+    assert grid <= sms and offs[0] == 0 and offs[-1] == len(dec)
+    assert (np.diff(offs) >= 1).all() if grid else len(dec) == 0
+    per_cta = [int(sum(dec[i, 3] - dec[i, 2] for i in range(offs[c], offs[c + 1])))
+               for c in range(grid)]
+    if grid:
+        assert all(x == per_cta[0] for x in per_cta[:-1]) and per_cta[-1] <= per_cta[0]
+    cover = {}
     for seq, kvh0, pb, pe, split, ns, slot, mid, ctx, tok, _, _ in dec:
         assert ql[seq] == 1 and 0 <= pb < pe and kvh0 % kvhb == 0
         assert ctx == cl[seq] and tok == cu[seq]
         cover.setdefault((seq, kvh0), []).append((pb, pe, split, ns, slot, mid))
+    slots = set()
     for s in range(len(rows)):
         if ql[s] != 1:
             continue
@@ -144,10 +153,11 @@ def _check_plan(rows, hq, hkv, d, sms):
             assert parts[0][0] == 0 and parts[-1][1] == npg
             assert all(a[1] == b_[0] for a, b_ in zip(parts, parts[1:]))
             ns = parts[0][3]
-            assert len(parts) == ns and sorted(p[2] for p in parts) == list(range(ns))
+            assert len(parts) == ns and [p[2] for p in parts] == list(range(ns))
             assert len({(p[4], p[5]) for p in parts}) == 1
-    lens = [pe - pb for _, _, pb, pe, *_ in dec]
-    assert lens == sorted(lens, reverse=True)
+            if ns > 1:
+                assert parts[0][4] not in slots
+                slots.add(parts[0][4])
     # chunk items cover every (token, kv head) of every chunk row once
     tpt = 128 // g
     seen = set()
@@ -172,7 +182,6 @@ def test_plan_covers_workloads(name):
     sh = lay.shape
     rows = list(zip(lay.q_len.tolist(), lay.context_len.tolist()))
     h = _check_plan(rows, sh.num_q_heads, sh.num_kv_heads, sh.head_dim, 152)
-    assert h["decode_grid"] <= 152
 
 
 def test_plan_edge_shapes():
