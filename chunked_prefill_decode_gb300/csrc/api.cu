@@ -27,8 +27,7 @@ cudaError_t launch_decode(const DecodeParams& p, int head_dim, int grid,
                           const CUtensorMap& kmap, const CUtensorMap& vmap,
                           cudaStream_t stream);
 cudaError_t launch_chunk(const ChunkParams& p, int head_dim, const CUtensorMap& qmap,
-                         const CUtensorMap& kmap, const CUtensorMap& vmap,
-                         cudaStream_t stream);
+                         const void* k_cache, const void* v_cache, cudaStream_t stream);
 }  // namespace hb
 
 using namespace hb;
@@ -351,17 +350,24 @@ hb_status hb_plan(const hb_batch* batch, const int32_t* h_q_len,
 
     // ---- chunk items: rows with q_len > 1, (kv head, query tile)
     const int tpt = kChunkRows / g;
+    int64_t n_tiles_total = 0;
+    for (int i = 0; i < S; ++i)
+      if (h_q_len[i] > 1) n_tiles_total += (int64_t)((h_q_len[i] + tpt - 1) / tpt) * Hkv;
+    const int tiles_per_item = (n_tiles_total >= 2LL * num_sms) ? 2 : 1;
     std::vector<ChunkItem> chk;
     for (int i = 0; i < S; ++i) {
       if (h_q_len[i] == 1) continue;
       const int off = h_context_len[i] - h_q_len[i];
+      // an item is a pair of query tiles (2 * tokens_per_tile tokens) that
+      // share every K/V tile when there are enough of them to fill the GPU,
+      // else a single tile (more CTAs); the last item of a row may be short
       for (int kvh = 0; kvh < Hkv; ++kvh)
-        for (int t0 = 0; t0 < h_q_len[i]; t0 += tpt) {
+        for (int t0 = 0; t0 < h_q_len[i]; t0 += tiles_per_item * tpt) {
           ChunkItem c{};
           c.seq = i;
           c.kv_head = kvh;
           c.tok0 = t0;
-          c.ntok = std::min(tpt, h_q_len[i] - t0);
+          c.ntok = std::min(tiles_per_item * tpt, h_q_len[i] - t0);
           c.kv_tiles = (off + t0 + c.ntok + kChunkKeys - 1) / kChunkKeys;
           c.q0 = cu[i];
           c.q_len = h_q_len[i];
@@ -517,17 +523,11 @@ hb_status hb_attention(const hb_batch* batch, const void* h_plan, const void* q,
     }
     if (h.num_chunk_items > 0) {
       const int tpt = h.chunk_tokens_per_tile;
-      CUtensorMap qmap, kmap, vmap;
+      CUtensorMap qmap;
       const cuuint64_t qdims[3] = {(cuuint64_t)D, (cuuint64_t)Hq, (cuuint64_t)batch->total_q};
       const cuuint64_t qstr[2] = {(cuuint64_t)D * 2, (cuuint64_t)Hq * D * 2};
       const cuuint32_t qbox[3] = {64, (cuuint32_t)g, (cuuint32_t)tpt};
       if ((s = encode_map(&qmap, q, 3, qdims, qstr, qbox, "chunk Q")) != HB_OK) return s;
-      const cuuint64_t kdims[3] = {(cuuint64_t)D, (cuuint64_t)Hkv,
-                                   (cuuint64_t)batch->num_pages * kPageSize};
-      const cuuint64_t kstr[2] = {(cuuint64_t)D * 2, (cuuint64_t)Hkv * D * 2};
-      const cuuint32_t kbox[3] = {64, 1, (cuuint32_t)kPageSize};
-      if ((s = encode_map(&kmap, k_cache, 3, kdims, kstr, kbox, "chunk K")) != HB_OK) return s;
-      if ((s = encode_map(&vmap, v_cache, 3, kdims, kstr, kbox, "chunk V")) != HB_OK) return s;
       ChunkParams p{};
       p.items = reinterpret_cast<const ChunkItem*>(ws + (size_t)h.num_decode_items * sizeof(DecodeItem));
       p.num_items = h.num_chunk_items;
@@ -544,7 +544,7 @@ hb_status hb_attention(const hb_batch* batch, const void* h_plan, const void* q,
       p.scale_log2 = scale_log2;
       p.dev_error = dev->err;
       LaunchTimer t(2, st);
-      cudaError_t e = launch_chunk(p, D, qmap, kmap, vmap, st);
+      cudaError_t e = launch_chunk(p, D, qmap, k_cache, v_cache, st);
       t.done();
       if (e != cudaSuccess) return cuda_fail(e, "chunk launch");
       g_launches.fetch_add(1);

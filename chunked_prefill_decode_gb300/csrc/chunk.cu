@@ -7,32 +7,45 @@
 // Batching", §LLM 推理的两阶段计算特征: prefill is compute-bound, so QK^T and PV
 // run as the dense contractions they are, on the tensor cores.
 //
-// One CTA takes one work item: a 128-row query tile made of (token, q head)
-// pairs of one kv head's GQA group (tokens_per_tile = 128 / g tokens times
-// the g heads, so one K/V tile in shared memory serves the whole group), and
-// walks the 128-key tiles 0 .. (last position in the tile) of its sequence.
+// A query tile is 128 rows of (token, q head) pairs of one kv head's GQA
+// group: tokens_per_tile = 128 / g tokens times the g heads, so a K/V tile in
+// shared memory serves the whole group.  One CTA takes one work item: two
+// consecutive query tiles, A and B (B may be short or absent), which share
+// every 128-key K/V tile; the CTA walks the key tiles 0 .. (last position of
+// B) of its sequence, A stopping at its own last position.
 //
-// Warp roles (192 threads):
-//   warp 0     TMA producer: the Q tile once (3-D map over q, box
-//              64 x g x tokens), then K and V tiles into two separate rings
-//              (K runs one tile ahead of V, since QK_j comes a softmax earlier
-//              than PV_j); a tile is eight 16-token pages, one box per page
-//              and 64-wide head-dim chunk, coordinates from the block table
-//              (prefetched 32 pages at a time by the whole warp); pages past
-//              the context are fetched out of range, i.e. as zeros;
-//   warp 1     TMEM owner and MMA issuer: S_j = Q K_j^T (M 128, N 128, K D,
-//              both operands K-major in shared memory) into one of two S
-//              buffers, then O += P_j V_j (M 128, N D, K 128) with P read from
-//              TMEM and V read MN-major straight from its page layout;
-//   warps 2-5  softmax: thread = query row = TMEM lane; S row to registers
-//              (tcgen05.ld), causal mask only on tiles that cross the
-//              diagonal, p = 2^(s * scale * log2 e - m) as one FFMA + EX2, P
-//              as bf16 into TMEM (tcgen05.st), row sum from the same rounded
-//              P; O is rescaled in TMEM only when a row maximum grows by more
-//              than 2^8 (a stale maximum stays exact while it bounds P, and
-//              P <= 2^8 is safe in bf16 and fp32); epilogue O / l to bf16.
-// TMEM (512 columns): S0 0-127, S1 128-255, O 256-(256+D), P0 384-447,
-// P1 448-511 (P is 128 bf16 per row = 64 columns).
+// Warp roles (416 threads):
+//   warps 0-3  softmax of tile A, warps 4-7 softmax of tile B: thread = query
+//              row = TMEM lane (warp w owns lanes 32 (w % 4) ..).  Per key
+//              tile, pass 1 reads S in 32-column pieces (tcgen05.ld) for the
+//              row maximum, with the causal mask only on tiles that cross the
+//              diagonal; pass 2 re-reads them, forms p = 2^(s c - m) with one
+//              FFMA + EX2 (c = scale * log2 e), rounds to bf16 and writes P
+//              into the S columns it has already consumed (tcgen05.st); the
+//              row sum uses the same rounded P.  O is rescaled in TMEM only
+//              when a row maximum grows by more than 2^8 (a stale maximum
+//              stays exact while it bounds P, and P <= 2^8 is safe); epilogue
+//              O / l to bf16.
+//   warp 8     TMEM owner and MMA issuer (one thread): Q tiles by TMA (3-D map
+//              over q, box 64 x g x tokens); then, ping-ponging the two tiles,
+//              PV_A(j), QK_A(j+1), PV_B(j), QK_B(j+1), ... so that the tensor
+//              cores work on one tile while the other tile's softmax runs.
+//              S = Q K^T (M 128, N 128, K D, both operands K-major in shared
+//              memory); O += P V (M 128, N D, K 128) with P read from TMEM and
+//              V read MN-major.  QK_t(j) is issued after PV_t(j-1), and the
+//              tensor pipe runs one thread's MMAs in order, so "S_t(j) ready"
+//              also means PV_t(j-1) is done: the softmax may then rescale O_t
+//              and P_t may live in the S_t columns.
+//   warps 9-12 producers: gather each 128-key K or V tile from its eight
+//              16-token pages with 16-byte cp.async copies (adjacent lanes
+//              cover one contiguous token row, so every warp access is
+//              coalesced) straight into the 128-byte-swizzled layout the MMA
+//              reads; keys past the context are zero-filled by the copy
+//              itself.  A 16-token page holds only 2 KB per kv head, too small
+//              for one TMA box each (the per-box cost bounded an earlier
+//              design), so the gather runs on the load/store units.  K runs
+//              one tile ahead of V.
+// TMEM (512 columns): S_A 0-127, S_B 128-255, O_A 256-(256+D), O_B after it.
 #include <cuda_runtime.h>
 
 #include "hb_internal.h"
@@ -40,7 +53,10 @@
 
 namespace hb {
 
-constexpr int kChunkThreads = 192;
+constexpr int kChunkThreads = 416;
+constexpr int kMmaWarp = 8;
+constexpr int kProducerWarp0 = 9;
+constexpr int kProducerThreads = 128;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 template <int D>
@@ -48,17 +64,18 @@ struct ChunkCfg {
   static constexpr int CH = D / 64;                    // 128-byte K chunks
   static constexpr int kTileBytes = CH * 16384;         // 128 rows x D bf16
   static constexpr int NK = (D == 128) ? 3 : 4;         // K stages
-  static constexpr int NV = (D == 128) ? 3 : 4;         // V stages
-  static constexpr int kQOff = 0;
-  static constexpr int kKOff = kQOff + kTileBytes;
+  static constexpr int NV = (D == 128) ? 2 : 4;         // V stages
+  static constexpr int kQOff = 0;                       // Q_A, then Q_B
+  static constexpr int kKOff = kQOff + 2 * kTileBytes;
   static constexpr int kVOff = kKOff + NK * kTileBytes;
   static constexpr int kBarOff = kVOff + NV * kTileBytes;
-  static constexpr int kNumBars = 1 + 2 * NK + 2 * NV + 2 + 2 + 1 + 1;
+  static constexpr int kNumBars = 1 + 2 * NK + 2 * NV + 2 + 2 + 2 + 1;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kSmemBytes = kMiscOff + 64 + 1024;  // + alignment slack
   static constexpr uint32_t kTmemCols = 512;
-  static constexpr uint32_t kOCol = 256;
-  static constexpr uint32_t kPCol = 384;
+  static constexpr uint32_t kOCol = 256;                // O_A; O_B at kOCol + D
+  static constexpr int kUnits = D / 8;                  // 16-byte units per token row
+  static constexpr int kRowsPerInstr = 32 / kUnits;     // token rows per warp access
 };
 static_assert(ChunkCfg<128>::kSmemBytes <= 227 * 1024, "chunk smem (D=128)");
 static_assert(ChunkCfg<64>::kSmemBytes <= 227 * 1024, "chunk smem (D=64)");
@@ -66,8 +83,8 @@ static_assert(ChunkCfg<64>::kSmemBytes <= 227 * 1024, "chunk smem (D=64)");
 template <int D>
 __global__ void __launch_bounds__(kChunkThreads, 1)
     chunk_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap qmap,
-                 const __grid_constant__ CUtensorMap kmap,
-                 const __grid_constant__ CUtensorMap vmap) {
+                 const uint16_t* __restrict__ k_cache,
+                 const uint16_t* __restrict__ v_cache) {
   using C = ChunkCfg<D>;
   constexpr int CH = C::CH;
   constexpr int NK = C::NK;
@@ -84,10 +101,10 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
   uint64_t* k_empty = k_full + NK;
   uint64_t* v_full = k_empty + NK;
   uint64_t* v_empty = v_full + NV;
-  uint64_t* s_full = v_empty + NV;
-  uint64_t* p_full = s_full + 2;
-  uint64_t* o_full = p_full + 2;
-  uint64_t* mma_done = o_full + 1;
+  uint64_t* s_full = v_empty + NV;   // [A, B]
+  uint64_t* p_full = s_full + 2;     // [A, B]
+  uint64_t* o_done = p_full + 2;     // [A, B]
+  uint64_t* mma_done = o_done + 2;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::kMiscOff);
   int* abort_i = reinterpret_cast<int*>(smem + C::kMiscOff + 16);
   volatile int* abort_flag = abort_i;
@@ -100,28 +117,32 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
   const int q0 = it.q0;
   const int ctx = it.ctx;
   const int off = ctx - it.q_len;         // tokens cached before this chunk
-  const int n_tiles = it.kv_tiles;
+  const int ntokA = min(tpt, it.ntok);
+  const int ntokB = it.ntok - ntokA;
+  const bool hasB = ntokB > 0;
+  const int T = it.kv_tiles;              // key tiles of the later tile
+  const int TA = (off + it.tok0 + ntokA + kChunkKeys - 1) / kChunkKeys;
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
     for (int s = 0; s < NK; ++s) {
-      mbar_init(&k_full[s], 1);
+      mbar_init(&k_full[s], kProducerThreads);
       mbar_init(&k_empty[s], 1);
     }
     for (int s = 0; s < NV; ++s) {
-      mbar_init(&v_full[s], 1);
+      mbar_init(&v_full[s], kProducerThreads);
       mbar_init(&v_empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&s_full[b], 1);
-      mbar_init(&p_full[b], 128);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&s_full[t], 1);
+      mbar_init(&p_full[t], 128);
+      mbar_init(&o_done[t], 1);
     }
-    mbar_init(o_full, 1);
     mbar_init(mma_done, 1);
     *abort_i = 0;
     fence_mbar_init();
   }
-  if (warp == 1) {
+  if (warp == kMmaWarp) {
     tmem_alloc(tmem_holder, C::kTmemCols);
     tmem_relinquish();
   }
@@ -130,255 +151,261 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_holder;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    constexpr int kPagesPerTile = kChunkKeys / kPageSize;
+  if (warp >= kProducerWarp0) {
+    // ------------------------------------------------------------ producers
+    const int pw = warp - kProducerWarp0;            // 0..3: rows 32pw..32pw+31
+    const int unit = lane % C::kUnits;
+    const int sub = lane / C::kUnits;
     const int n_pages = (ctx + kPageSize - 1) / kPageSize;
     const int32_t* bt_row = p.block_table + (size_t)it.seq * p.max_pages_per_seq;
-    auto load_window = [&](int base) -> int {
-      const int lp = base + lane;
-      int phys = p.num_pages;  // out of range: the copy fills zeros
-      if (lp < n_pages) {
-        phys = (lp < p.max_pages_per_seq) ? __ldg(&bt_row[lp]) : -1;
-        if (phys < 0 || phys >= p.num_pages) {
-          report_error(p.dev_error, HB_DEVERR_INDEX);
-          phys = p.num_pages;
-        }
-      }
-      return phys;
-    };
-    // block-table windows of 32 pages (4 tiles each), one window ahead
-    int win_k = load_window(0), win_k_next = load_window(32);
-    int win_v = win_k, win_v_next = win_k_next;
-    if (lane == 0) {
-      tma_prefetch_desc(&qmap);
-      tma_prefetch_desc(&kmap);
-      tma_prefetch_desc(&vmap);
-      mbar_arrive_expect_tx(q_full, (uint32_t)(CH * g * tpt * 128));
+    const size_t row_elems = (size_t)p.num_kv_heads * D;   // one token of a pool
+    // physical pages of this warp's two pages of tile j (-1: none / invalid)
+    auto pages_of = [&](int j, int* e) {
 #pragma unroll
-      for (int c = 0; c < CH; ++c)
-        tma_load_3d(sQ + c * 16384, &qmap, q_full, c * 64, it.kv_head * g,
-                    q0 + it.tok0);
-    }
-    uint32_t k_issued = 0, k_par = 0, v_issued = 0, v_par = 0;
-    bool ok = true;
-    auto issue_tile = [&](bool is_v, int j, int win) -> bool {
-      const int s = is_v ? j % NV : j % NK;
-      const uint32_t ph = (uint32_t)(is_v ? j / NV : j / NK) & 1u;
-      const int w = j & 3;
-      int phys[kPagesPerTile];
-#pragma unroll
-      for (int pp = 0; pp < kPagesPerTile; ++pp)
-        phys[pp] = __shfl_sync(0xffffffffu, win, w * kPagesPerTile + pp);
-      bool good = true;
-      if (lane == 0) {
-        uint64_t* empty = is_v ? &v_empty[s] : &k_empty[s];
-        uint64_t* full = is_v ? &v_full[s] : &k_full[s];
-        good = mbar_wait(empty, ph ^ 1u, abort_flag);
-        if (good) {
-          mbar_arrive_expect_tx(full, (uint32_t)C::kTileBytes);
-          uint8_t* dst = (is_v ? sV : sK) + s * C::kTileBytes;
-          const CUtensorMap* map = is_v ? &vmap : &kmap;
-#pragma unroll
-          for (int pp = 0; pp < kPagesPerTile; ++pp)
-#pragma unroll
-            for (int c = 0; c < CH; ++c)
-              tma_load_3d(dst + c * 16384 + pp * 2048, map, full, c * 64,
-                          it.kv_head, phys[pp] * kPageSize);
-          if (is_v) {
-            v_issued |= 1u << s;
-            v_par = (v_par & ~(1u << s)) | (ph << s);
-          } else {
-            k_issued |= 1u << s;
-            k_par = (k_par & ~(1u << s)) | (ph << s);
+      for (int h = 0; h < 2; ++h) {
+        const int lp = j * (kChunkKeys / kPageSize) + 2 * pw + h;
+        int phys = -1;
+        if (lp < n_pages) {
+          phys = (lp < p.max_pages_per_seq) ? __ldg(&bt_row[lp]) : -1;
+          if (phys < 0 || phys >= p.num_pages) {
+            if (lane == 0) report_error(p.dev_error, HB_DEVERR_INDEX);
+            phys = -1;
           }
         }
+        e[h] = phys;
       }
-      return __shfl_sync(0xffffffffu, good ? 1 : 0, 0) != 0;
     };
-    // issue K_j (j < n_tiles) and V_{j-1} (j >= 1): K runs one tile ahead
-    for (int j = 0; ok && j <= n_tiles; ++j) {
-      if (j < n_tiles) {
-        if ((j & 3) == 0 && j > 0) {
-          win_k = win_k_next;
-          win_k_next = load_window((j + 4) * kPagesPerTile);
-        }
-        ok = issue_tile(false, j, win_k);
+    auto gather = [&](const uint16_t* pool, uint8_t* stage, int j, const int* e) {
+      const uint32_t base = smem_u32(stage);
+      const int kbase = j * kChunkKeys;
+#pragma unroll
+      for (int i = 0; i < C::kUnits; ++i) {
+        const int r = 32 * pw + i * C::kRowsPerInstr + sub;   // key row in the tile
+        const int key = kbase + r;
+        const int phys = e[(r >> 4) & 1];
+        const bool valid = key < ctx && phys >= 0;
+        const uint16_t* src = valid
+            ? pool + ((size_t)phys * kPageSize + (key & (kPageSize - 1))) * row_elems +
+                  (size_t)it.kv_head * D + unit * 8
+            : pool;
+        const uint32_t dst = base + (unit >> 3) * 16384 + r * 128 + (((unit & 7) ^ (r & 7)) << 4);
+        cp_async_16(dst, src, valid ? 16u : 0u);
       }
-      if (ok && j >= 1) {
+    };
+    int e_prev[2] = {-1, -1}, e_cur[2], e_next[2];
+    pages_of(0, e_cur);
+    pages_of(1, e_next);
+    bool ok = true;
+    for (int j = 0; ok && j <= T; ++j) {
+      if (j < T) {
+        const int s = j % NK;
+        if (!mbar_wait(&k_empty[s], ((uint32_t)(j / NK) & 1u) ^ 1u, abort_flag)) { ok = false; break; }
+        gather(k_cache, sK + s * C::kTileBytes, j, e_cur);
+        cp_async_arrive_noinc(&k_full[s]);
+      }
+      if (j >= 1) {
         const int jv = j - 1;
-        if ((jv & 3) == 0 && jv > 0) {
-          win_v = win_v_next;
-          win_v_next = load_window((jv + 4) * kPagesPerTile);
-        }
-        ok = issue_tile(true, jv, win_v);
+        const int s = jv % NV;
+        if (!mbar_wait(&v_empty[s], ((uint32_t)(jv / NV) & 1u) ^ 1u, abort_flag)) { ok = false; break; }
+        gather(v_cache, sV + s * C::kTileBytes, jv, e_prev);
+        cp_async_arrive_noinc(&v_full[s]);
       }
+      e_prev[0] = e_cur[0];
+      e_prev[1] = e_cur[1];
+      e_cur[0] = e_next[0];
+      e_cur[1] = e_next[1];
+      pages_of(j + 2, e_next);
     }
-    if (lane == 0) {
-      // copies in flight must land before the CTA exits
-      drain_wait(q_full, 0u, abort_flag);
-      for (int s = 0; s < NK; ++s)
-        if (k_issued & (1u << s)) drain_wait(&k_full[s], (k_par >> s) & 1u, abort_flag);
-      for (int s = 0; s < NV; ++s)
-        if (v_issued & (1u << s)) drain_wait(&v_full[s], (v_par >> s) & 1u, abort_flag);
-    }
-  } else if (warp == 1) {
+    // copies in flight must land before the CTA exits
+    asm volatile("cp.async.wait_all;" ::: "memory");
+  } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
+      tma_prefetch_desc(&qmap);
+      mbar_arrive_expect_tx(q_full, (uint32_t)(CH * g * tpt * 128 * (hasB ? 2 : 1)));
+#pragma unroll
+      for (int c = 0; c < CH; ++c)
+        tma_load_3d(sQ + c * 16384, &qmap, q_full, c * 64, it.kv_head * g, q0 + it.tok0);
+      if (hasB) {
+#pragma unroll
+        for (int c = 0; c < CH; ++c)
+          tma_load_3d(sQ + C::kTileBytes + c * 16384, &qmap, q_full, c * 64, it.kv_head * g,
+                      q0 + it.tok0 + tpt);
+      }
       const uint32_t idesc_qk = idesc_bf16_f32(128, kChunkKeys, false);
       const uint32_t idesc_pv = idesc_bf16_f32(128, D, true);
       const uint32_t aQ = smem_u32(sQ);
       const uint32_t aK = smem_u32(sK);
       const uint32_t aV = smem_u32(sV);
-      bool ok = mbar_wait(q_full, 0u, abort_flag);
-      auto issue_pv = [&](int i) -> bool {
-        const int pb = i & 1;
-        if (!mbar_wait(&p_full[pb], (uint32_t)(i >> 1) & 1u, abort_flag)) return false;
-        const int s = i % NV;
-        if (!mbar_wait(&v_full[s], (uint32_t)(i / NV) & 1u, abort_flag)) return false;
-        tc_fence_after_sync();
-        const uint32_t vb = aV + s * C::kTileBytes;
-#pragma unroll
-        for (int kk = 0; kk < kChunkKeys / 16; ++kk) {
-          const uint64_t b = sdesc_sw128(vb + kk * 2048, 16384, 1024);
-          tc_mma_bf16_ts(tmem + C::kOCol, tmem + C::kPCol + pb * 64 + kk * 8, b, idesc_pv,
-                         (i > 0 || kk > 0) ? 1u : 0u);
-        }
-        tc_commit(&v_empty[s]);
-        tc_commit(o_full);
-        return true;
-      };
-      for (int j = 0; ok && j < n_tiles; ++j) {
-        const int s = j % NK;
-        if (!mbar_wait(&k_full[s], (uint32_t)(j / NK) & 1u, abort_flag)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after_sync();
-        const int sb = j & 1;
-        const uint32_t kb = aK + s * C::kTileBytes;
+      auto qk = [&](int t, int j) {
+        const uint32_t kb = aK + (j % NK) * C::kTileBytes;
+        const uint32_t qb = aQ + t * C::kTileBytes;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t koff = (kk >> 2) * 16384 + (kk & 3) * 32;
-          const uint64_t a = sdesc_sw128(aQ + koff, 16, 1024);
-          const uint64_t b = sdesc_sw128(kb + koff, 16, 1024);
-          tc_mma_bf16(tmem + sb * kChunkKeys, a, b, idesc_qk, kk > 0 ? 1u : 0u);
+          tc_mma_bf16(tmem + t * kChunkKeys, sdesc_sw128(qb + koff, 16, 1024),
+                      sdesc_sw128(kb + koff, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
         }
-        tc_commit(&s_full[sb]);
-        tc_commit(&k_empty[s]);
-        if (j >= 1 && !issue_pv(j - 1)) ok = false;
+        tc_commit(&s_full[t]);
+      };
+      auto pv = [&](int t, int j) {
+        const uint32_t vb = aV + (j % NV) * C::kTileBytes;
+        const uint32_t ocol = C::kOCol + t * D;
+#pragma unroll
+        for (int kk = 0; kk < kChunkKeys / 16; ++kk)
+          tc_mma_bf16_ts(tmem + ocol, tmem + t * kChunkKeys + kk * 8,
+                         sdesc_sw128(vb + kk * 2048, 16384, 1024), idesc_pv,
+                         (j > 0 || kk > 0) ? 1u : 0u);
+      };
+      auto wait_k = [&](int j) -> bool {
+        if (!mbar_wait(&k_full[j % NK], (uint32_t)(j / NK) & 1u, abort_flag)) return false;
+        fence_async_shared();   // gathered K (generic proxy) -> tensor core
+        tc_fence_after_sync();
+        return true;
+      };
+      auto wait_v = [&](int j) -> bool {
+        if (!mbar_wait(&v_full[j % NV], (uint32_t)(j / NV) & 1u, abort_flag)) return false;
+        fence_async_shared();
+        tc_fence_after_sync();
+        return true;
+      };
+      bool ok = mbar_wait(q_full, 0u, abort_flag) && wait_k(0);
+      if (ok) {
+        qk(0, 0);
+        if (hasB) qk(1, 0);
+        tc_commit(&k_empty[0]);
       }
-      if (ok) issue_pv(n_tiles - 1);
+      for (int j = 0; ok && j < T; ++j) {
+        bool k_next_ready = false, v_ready = false;
+        if (j < TA) {
+          if (!mbar_wait(&p_full[0], (uint32_t)j & 1u, abort_flag) || !wait_v(j)) { ok = false; break; }
+          v_ready = true;
+          pv(0, j);
+          if (j == TA - 1) tc_commit(&o_done[0]);
+          if (j + 1 < TA) {
+            if (!wait_k(j + 1)) { ok = false; break; }
+            k_next_ready = true;
+            qk(0, j + 1);
+          }
+        }
+        if (hasB) {
+          if (!mbar_wait(&p_full[1], (uint32_t)j & 1u, abort_flag)) { ok = false; break; }
+          if (!v_ready && !wait_v(j)) { ok = false; break; }
+          tc_fence_after_sync();
+          pv(1, j);
+          if (j == T - 1) tc_commit(&o_done[1]);
+        }
+        tc_commit(&v_empty[j % NV]);
+        if (j + 1 < T) {
+          if (!k_next_ready && !wait_k(j + 1)) { ok = false; break; }
+          if (hasB) qk(1, j + 1);
+          tc_commit(&k_empty[(j + 1) % NK]);
+        }
+      }
       // every MMA issued must complete before TMEM is freed
       tc_commit(mma_done);
       drain_wait(mma_done, 0u, abort_flag);
+      drain_wait(q_full, 0u, abort_flag);
     }
   } else {
     // ------------------------------------------------------------ softmax
+    const int t = warp >> 2;               // 0: tile A, 1: tile B
     const int wq = warp & 3;
     const int row = wq * 32 + lane;
     const uint32_t t_lane = tmem + ((uint32_t)(wq * 32) << 16);
+    const int ntok_t = t ? ntokB : ntokA;
+    const int T_t = t ? (hasB ? T : 0) : TA;
+    const int tok0_t = it.tok0 + t * tpt;
     const int tok_local = row / g;
-    const bool valid_row = (row < g * tpt) && (tok_local < it.ntok);
-    const int tok_rel = it.tok0 + tok_local;
+    const bool valid_row = (row < g * tpt) && (tok_local < ntok_t);
+    const int tok_rel = tok0_t + tok_local;
     const int pos = valid_row ? off + tok_rel : ctx - 1;  // absolute position
-    const int min_pos = off + it.tok0;
+    const int min_pos = off + tok0_t;
     const float sl2 = p.scale_log2;
+    const uint32_t s_col = t_lane + t * kChunkKeys;
+    const uint32_t o_col = t_lane + C::kOCol + t * D;
     float m_run = -INFINITY;   // running maximum, in scaled log2 units
     float l_run = 0.f;
     bool ok = true;
-    for (int j = 0; j < n_tiles; ++j) {
-      const int sb = j & 1;
-      if (!mbar_wait(&s_full[sb], (uint32_t)(j >> 1) & 1u, abort_flag)) { ok = false; break; }
+    for (int j = 0; j < T_t; ++j) {
+      if (!mbar_wait(&s_full[t], (uint32_t)j & 1u, abort_flag)) { ok = false; break; }
       tc_fence_after_sync();
-      uint32_t sr[kChunkKeys];
-#pragma unroll
-      for (int q = 0; q < kChunkKeys / 32; ++q)
-        tmem_ld32(t_lane + sb * kChunkKeys + q * 32, &sr[q * 32]);
-      tmem_ld_wait();
       const int kbase = j * kChunkKeys;
+      const bool masked = kbase + kChunkKeys - 1 > min_pos;
+      const int lim = pos - kbase;   // keys 0..lim of this tile are visible
       float alpha = 1.f;
       bool resc = false;
-      uint32_t pk[kChunkKeys / 2];
-      if (valid_row) {
-        float mx = -INFINITY;
-        if (kbase + kChunkKeys - 1 > min_pos) {
-          const int lim = pos - kbase;   // keys 0..lim of this tile are visible
+      // tcgen05.ld / tcgen05.st are warp-collective: every lane executes each
+      // of them; rows that hold no query only change the arithmetic (P = 0)
+      float mxp[8];
 #pragma unroll
-          for (int i = 0; i < kChunkKeys; ++i) {
-            if (i > lim) sr[i] = __float_as_uint(-INFINITY);
-            mx = fmaxf(mx, __uint_as_float(sr[i]));
-          }
+      for (int i = 0; i < 8; ++i) mxp[i] = -INFINITY;
+#pragma unroll 1
+      for (int q = 0; q < kChunkKeys / 32; ++q) {
+        uint32_t sr[32];
+        tmem_ld32(s_col + q * 32, sr);
+        tmem_ld_wait();
+        if (masked) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            mxp[i & 7] = fmaxf(mxp[i & 7], (q * 32 + i > lim) ? -INFINITY : __uint_as_float(sr[i]));
         } else {
 #pragma unroll
-          for (int i = 0; i < kChunkKeys; ++i) mx = fmaxf(mx, __uint_as_float(sr[i]));
+          for (int i = 0; i < 32; ++i) mxp[i & 7] = fmaxf(mxp[i & 7], __uint_as_float(sr[i]));
         }
+      }
+      if (valid_row) {
+        const float mx = fmaxf(fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3])),
+                               fmaxf(fmaxf(mxp[4], mxp[5]), fmaxf(mxp[6], mxp[7])));
         const float m_new = fmaxf(m_run, mx * sl2);
         if (m_new > m_run + kRescaleThreshold) {
           alpha = fast_exp2(m_run - m_new);
           m_run = m_new;
           resc = true;
         }
-        float lsum = 0.f;
-#pragma unroll
-        for (int i = 0; i < kChunkKeys / 2; ++i) {
-          const float a0 = fast_exp2(fmaf(__uint_as_float(sr[2 * i]), sl2, -m_run));
-          const float a1 = fast_exp2(fmaf(__uint_as_float(sr[2 * i + 1]), sl2, -m_run));
-          pk[i] = pack_bf16x2(a0, a1);
-          lsum += bf16lo_to_f32(pk[i]) + bf16hi_to_f32(pk[i]);
-        }
-        l_run = l_run * alpha + lsum;
-      } else {
-#pragma unroll
-        for (int i = 0; i < kChunkKeys / 2; ++i) pk[i] = 0u;
       }
-      // P_j into TMEM buffer j&1 (its previous reader, PV_{j-2}, completed:
-      // this thread saw o_full for it one tile ago)
-      tmem_st32(t_lane + C::kPCol + sb * 64, pk);
-      tmem_st32(t_lane + C::kPCol + sb * 64 + 32, pk + 32);
-      if (j == n_tiles - 1) {
-        // keys past the context in the last page were never written: clear
-        // their V rows so that P = 0 never multiplies a NaN
-        const int s = j % NV;
-        const int first_bad = ctx - kbase;
-        const int end_bad = min(kChunkKeys, ((ctx + kPageSize - 1) / kPageSize) * kPageSize - kbase);
-        if (first_bad < end_bad) {
-          if (!mbar_wait(&v_full[s], (uint32_t)(j / NV) & 1u, abort_flag)) { ok = false; break; }
-          uint8_t* vt = sV + s * C::kTileBytes;
-          const int n_units = (end_bad - first_bad) * CH * 8;
-          for (int e = row; e < n_units; e += 128) {
-            const int key = first_bad + e / (CH * 8);
-            const int rem = e % (CH * 8);
-            *reinterpret_cast<uint4*>(vt + (rem >> 3) * 16384 + key * 128 + (rem & 7) * 16) =
-                make_uint4(0u, 0u, 0u, 0u);
-          }
-          fence_async_shared();
-        }
-      }
-      if (j >= 1) {
-        // PV_{j-1} must be complete before O is rescaled
-        if (!mbar_wait(o_full, (uint32_t)(j - 1) & 1u, abort_flag)) { ok = false; break; }
-        tc_fence_after_sync();
-        if (__any_sync(0xffffffffu, resc)) {
-          const float f = resc ? alpha : 1.f;
+      // pass 2: P = 2^(s c - m) as bf16 over the S columns already read
+      const float neg_m = valid_row ? -m_run : -INFINITY;   // dead rows: P = 0
+      float lsp[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 1
-          for (int q = 0; q < D / 32; ++q) {
-            uint32_t orow[32];
-            tmem_ld32(t_lane + C::kOCol + q * 32, orow);
-            tmem_ld_wait();
+      for (int q = 0; q < kChunkKeys / 32; ++q) {
+        uint32_t sr[32];
+        tmem_ld32(s_col + q * 32, sr);
+        tmem_ld_wait();
+        if (masked) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
-              orow[i] = __float_as_uint(__uint_as_float(orow[i]) * f);
-            tmem_st32(t_lane + C::kOCol + q * 32, orow);
-          }
+          for (int i = 0; i < 32; ++i)
+            if (q * 32 + i > lim) sr[i] = __float_as_uint(-INFINITY);
+        }
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          pk[i] = pack_bf16x2(fast_exp2(fmaf(__uint_as_float(sr[2 * i]), sl2, neg_m)),
+                              fast_exp2(fmaf(__uint_as_float(sr[2 * i + 1]), sl2, neg_m)));
+          lsp[i & 3] += bf16lo_to_f32(pk[i]) + bf16hi_to_f32(pk[i]);
+        }
+        tmem_st16(s_col + q * 16, pk);
+      }
+      if (valid_row) l_run = l_run * alpha + ((lsp[0] + lsp[1]) + (lsp[2] + lsp[3]));
+      // O_t is stable here (PV_t(j-1) completed before S_t(j) was ready)
+      if (j > 0 && __any_sync(0xffffffffu, resc)) {
+        const float f = resc ? alpha : 1.f;
+#pragma unroll 1
+        for (int q = 0; q < D / 32; ++q) {
+          uint32_t orow[32];
+          tmem_ld32(o_col + q * 32, orow);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) orow[i] = __float_as_uint(__uint_as_float(orow[i]) * f);
+          tmem_st32(o_col + q * 32, orow);
         }
       }
       tmem_st_wait();
       tc_fence_before_sync();
-      mbar_arrive(&p_full[sb]);
+      mbar_arrive(&p_full[t]);
     }
     // epilogue: O / l -> bf16
-    if (ok && mbar_wait(o_full, (uint32_t)(n_tiles - 1) & 1u, abort_flag)) {
+    if (T_t > 0 && ok && mbar_wait(&o_done[t], 0u, abort_flag)) {
       tc_fence_after_sync();
       const float inv = (l_run > 0.f) ? 1.f / l_run : 0.f;
       uint16_t* dst = p.out + ((size_t)(q0 + tok_rel) * p.num_q_heads +
@@ -386,7 +413,7 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
 #pragma unroll 1
       for (int q = 0; q < D / 32; ++q) {
         uint32_t orow[32];
-        tmem_ld32(t_lane + C::kOCol + q * 32, orow);
+        tmem_ld32(o_col + q * 32, orow);
         tmem_ld_wait();
         if (valid_row) {
 #pragma unroll
@@ -404,30 +431,31 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
   }
   tc_fence_before_sync();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == kMmaWarp) {
     tc_fence_after_sync();
     tmem_dealloc(tmem, C::kTmemCols);
   }
   if (threadIdx.x == 0 && *abort_flag) report_error(p.dev_error, HB_DEVERR_TIMEOUT);
 }
 
-cudaError_t launch_chunk(const ChunkParams& p, int head_dim,
-                         const CUtensorMap& qmap, const CUtensorMap& kmap,
-                         const CUtensorMap& vmap, cudaStream_t stream) {
+cudaError_t launch_chunk(const ChunkParams& p, int head_dim, const CUtensorMap& qmap,
+                         const void* k_cache, const void* v_cache, cudaStream_t stream) {
   if (p.num_items == 0) return cudaSuccess;
+  const uint16_t* kc = static_cast<const uint16_t*>(k_cache);
+  const uint16_t* vc = static_cast<const uint16_t*>(v_cache);
   cudaError_t e;
   if (head_dim == 128) {
     constexpr int smem = ChunkCfg<128>::kSmemBytes;
     e = cudaFuncSetAttribute(chunk_kernel<128>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    chunk_kernel<128><<<p.num_items, kChunkThreads, smem, stream>>>(p, qmap, kmap, vmap);
+    chunk_kernel<128><<<p.num_items, kChunkThreads, smem, stream>>>(p, qmap, kc, vc);
   } else {
     constexpr int smem = ChunkCfg<64>::kSmemBytes;
     e = cudaFuncSetAttribute(chunk_kernel<64>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    chunk_kernel<64><<<p.num_items, kChunkThreads, smem, stream>>>(p, qmap, kmap, vmap);
+    chunk_kernel<64><<<p.num_items, kChunkThreads, smem, stream>>>(p, qmap, kc, vc);
   }
   return cudaGetLastError();
 }

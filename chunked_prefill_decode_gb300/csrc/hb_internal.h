@@ -44,7 +44,9 @@ struct DecodeItem {
 static_assert(sizeof(DecodeItem) == 48, "decode item size");
 
 // One tensor-core work item: query tokens tok0 .. tok0+ntok-1 (relative to
-// the sequence's first new token) of one kv head, all q heads of its group.
+// the sequence's first new token) of one kv head, all q heads of its group,
+// as two query tiles of tokens_per_tile tokens (the second may be short or
+// empty); kv_tiles covers the later tile.
 struct ChunkItem {
   int32_t seq;
   int32_t kv_head;
