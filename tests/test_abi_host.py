@@ -160,9 +160,9 @@ def _check_plan(rows, hq, hkv, d, sms):
                 slots.add(parts[0][4])
     # chunk items cover every (token, kv head) of every chunk row once; an
     # item holds two query tiles when there are enough tiles to fill the SMs
+    tpt = 128 // g
     n_tiles = sum(-(-int(q) // tpt) * hkv for q in ql if q > 1)
     tpi = 2 if n_tiles >= 2 * sms else 1
-    tpt = 128 // g
     seen = set()
     for seq, kvh, t0, nt, tiles, q0, qn, ctx in chk:
         assert ql[seq] > 1 and 1 <= nt <= tpi * tpt and t0 % (tpi * tpt) == 0
