@@ -335,27 +335,28 @@ def run_native(args):
         return
     peaks = _peaks()
     cnt = algorithmic_counts(layout)
-    t_dec = ktimes["decode"][0] / max(1, ktimes["decode"][1])
-    t_chk = ktimes["chunk"][0] / max(1, ktimes["chunk"][1])
+    t_att = ktimes["attention"][0] / max(1, ktimes["attention"][1])
     t_app = ktimes["kv_append"][0] / max(1, ktimes["kv_append"][1])
-    # dominant kernel = the one with the largest share of the step
-    shares = {"decode": ktimes["decode"][0], "chunk": ktimes["chunk"][0],
-              "kv_append": ktimes["kv_append"][0]}
-    dom = max(shares, key=shares.get)
-    if dom == "chunk":
-        achieved = cnt["chunk_flops"] / (t_chk / 1e3) / 1e12
-        roof = {"kernel": "chunk", "bound": "tensor", "achieved": achieved,
-                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                "frac": achieved / peaks["bf16_tflops"], "traffic": None}
-    else:
-        key, t = ("decode", t_dec) if dom == "decode" else ("append", t_app)
-        byts = cnt["decode_bytes"] if dom == "decode" else cnt["append_bytes"]
-        achieved = byts / (t / 1e3) / 1e9
-        roof = {"kernel": dom, "bound": "hbm", "achieved": achieved,
+    # the attention launch (decode and chunk CTAs together) is the dominant
+    # kernel; its bound is the larger of its two roofline terms
+    att_bytes = cnt["decode_bytes"] + cnt["chunk_bytes"]
+    att_flops = cnt["flops"]
+    t_hbm = att_bytes / (peaks["hbm_gbs"] * 1e9)
+    t_tc = att_flops / (peaks["bf16_tflops"] * 1e12)
+    if t_hbm >= t_tc:
+        achieved = att_bytes / (t_att / 1e3) / 1e9
+        roof = {"kernel": "attention", "bound": "hbm", "achieved": achieved,
                 "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / peaks["hbm_gbs"], "traffic": None}
+    else:
+        achieved = att_flops / (t_att / 1e3) / 1e12
+        roof = {"kernel": "attention", "bound": "tensor", "achieved": achieved,
+                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": achieved / peaks["bf16_tflops"], "traffic": None}
     roof["peak_source"] = peaks["source"]
-    roof["avg_launch_ms"] = {"decode": t_dec, "chunk": t_chk, "kv_append": t_app}
+    roof["algorithmic"] = {"bytes": att_bytes, "flops": att_flops}
+    roof["kernel_roofline_frac"] = max(t_hbm, t_tc) * 1e3 / t_att
+    roof["avg_launch_ms"] = {"attention": t_att, "kv_append": t_app}
     step_roof_s = max(cnt["flops"] / (peaks["bf16_tflops"] * 1e12),
                       cnt["bytes"] / (peaks["hbm_gbs"] * 1e9))
     ms_step = ms_max / args.steps

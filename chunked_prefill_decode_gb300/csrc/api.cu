@@ -23,11 +23,10 @@ __device__ int g_hb_device_error = 0;
 
 namespace hb {
 cudaError_t launch_kv_append(const AppendParams& p, int num_sms, cudaStream_t stream);
-cudaError_t launch_decode(const DecodeParams& p, int head_dim, int grid,
-                          const CUtensorMap& kmap, const CUtensorMap& vmap,
-                          cudaStream_t stream);
-cudaError_t launch_chunk(const ChunkParams& p, int head_dim, const CUtensorMap& qmap,
-                         const void* k_cache, const void* v_cache, cudaStream_t stream);
+cudaError_t launch_attention(const DecodeParams& dec, int decode_grid, const ChunkParams& chk,
+                             int head_dim, const CUtensorMap& dec_k, const CUtensorMap& dec_v,
+                             const CUtensorMap& chunk_q, const void* k_cache,
+                             const void* v_cache, cudaStream_t stream);
 }  // namespace hb
 
 using namespace hb;
@@ -325,28 +324,10 @@ hb_status hb_plan(const hb_batch* batch, const int32_t* h_q_len,
     if (tq != batch->total_q)
       return fail(HB_ERR_SHAPE, "sum of q_len (%lld) != total_q (%d)", (long long)tq, batch->total_q);
 
-    // ---- decode items: the decode rows' pages, end to end, cut into one
-    // equal contiguous range per CTA, each range cut at row boundaries
     const int kvhb = std::min(Hkv, kDecodeKvhBlock);
     const int n_blocks = Hkv / kvhb;
     std::vector<int32_t> cu(S + 1, 0);
     for (int i = 0; i < S; ++i) cu[i + 1] = cu[i] + h_q_len[i];
-    int64_t n_dec_rows = 0, dec_pages = 0;
-    for (int i = 0; i < S; ++i)
-      if (h_q_len[i] == 1) {
-        ++n_dec_rows;
-        dec_pages += (int64_t)((h_context_len[i] + kPageSize - 1) / kPageSize) * n_blocks;
-      }
-    const int max_dec_items = (int)std::min<int64_t>(n_dec_rows * n_blocks + num_sms + 1, 1 << 30);
-    std::vector<DecodeItem> dec(std::max(1, max_dec_items));
-    std::vector<int32_t> cta_off(num_sms + 1, 0);
-    DecodePartition part;
-    if (!partition_decode(S, h_q_len, h_context_len, n_blocks, kvhb, num_sms, 4, dec.data(),
-                          (int)dec.size(), cta_off.data(), num_sms, &part))
-      return fail(HB_ERR_WORKSPACE, "decode partition overflow");
-    dec.resize(part.n_items);
-    cta_off.resize(part.grid + 1);
-    const int n_slots = part.n_slots, n_merge = part.n_merge;
 
     // ---- chunk items: rows with q_len > 1, (kv head, query tile)
     const int tpt = kChunkRows / g;
@@ -378,6 +359,67 @@ hb_status hb_plan(const hb_batch* batch, const int32_t* h_q_len,
     std::stable_sort(chk.begin(), chk.end(), [](const ChunkItem& a, const ChunkItem& b) {
       return a.kv_tiles > b.kv_tiles;
     });
+
+    // ---- how many CTAs stream the decode rows.  The attention kernel runs
+    // decode CTAs and chunk CTAs side by side (one CTA per SM); SMs that end
+    // their decode range go on to chunk items.  Estimated end time with G
+    // decode CTAs: decode takes its bytes over min(HBM rate, G x one SM's
+    // stream rate); everything ends no earlier than (chunk work + G x decode
+    // time) / SMs, nor before the longest chunk item.  That estimate is flat
+    // over a range of G whose ends it knows only roughly, so the middle of
+    // the range within 2% of the best is taken.  Rates measured on GB300.
+    constexpr double kHbmBytesPerUs = 7.0e6;      // whole-GPU HBM stream
+    constexpr double kSmBytesPerUs = 8.5e4;       // one SM's stream ceiling
+    constexpr double kPairTileUs = 2.7;           // 2-tile item x one key tile
+    constexpr double kSingleTileUs = 2.0;         // 1-tile item x one key tile
+    double decode_bytes = 0.0, chunk_us = 0.0, max_item_us = 0.0;
+    for (int i = 0; i < S; ++i)
+      if (h_q_len[i] == 1) decode_bytes += (double)h_context_len[i] * Hkv * D * 4.0;
+    for (const ChunkItem& c : chk) {
+      const double us = c.kv_tiles * (tiles_per_item == 2 ? kPairTileUs : kSingleTileUs);
+      chunk_us += us;
+      max_item_us = std::max(max_item_us, us);
+    }
+    int decode_ctas = 0;
+    if (decode_bytes > 0.0) {
+      decode_ctas = num_sms;
+      if (!chk.empty()) {
+        std::vector<double> t(num_sms + 1, 0.0);
+        double best = 1e300;
+        for (int G = 1; G <= num_sms; ++G) {
+          const double t_dec = decode_bytes / std::min(kHbmBytesPerUs, G * kSmBytesPerUs);
+          t[G] = std::max({t_dec, (chunk_us + G * t_dec) / num_sms, max_item_us});
+          best = std::min(best, t[G]);
+        }
+        int lo = 0, hi = 0;
+        for (int G = 1; G <= num_sms; ++G)
+          if (t[G] <= 1.02 * best) {
+            if (!lo) lo = G;
+            hi = G;
+          }
+        decode_ctas = (lo + hi) / 2;
+      }
+    }
+
+    // ---- decode items: the decode rows' pages, end to end, cut into one
+    // equal contiguous range per CTA, each range cut at row boundaries
+    int64_t n_dec_rows = 0, dec_pages = 0;
+    for (int i = 0; i < S; ++i)
+      if (h_q_len[i] == 1) {
+        ++n_dec_rows;
+        dec_pages += (int64_t)((h_context_len[i] + kPageSize - 1) / kPageSize) * n_blocks;
+      }
+    const int max_dec_items = (int)std::min<int64_t>(n_dec_rows * n_blocks + num_sms + 1, 1 << 30);
+    std::vector<DecodeItem> dec(std::max(1, max_dec_items));
+    std::vector<int32_t> cta_off(num_sms + 1, 0);
+    DecodePartition part;
+    if (!partition_decode(S, h_q_len, h_context_len, n_blocks, kvhb, std::max(1, decode_ctas), 4,
+                          dec.data(), (int)dec.size(), cta_off.data(), std::max(1, decode_ctas),
+                          &part))
+      return fail(HB_ERR_WORKSPACE, "decode partition overflow");
+    dec.resize(part.n_items);
+    cta_off.resize(part.grid + 1);
+    const int n_slots = part.n_slots, n_merge = part.n_merge;
 
     // ---- sizes
     const size_t offsets_at = dec.size() * sizeof(DecodeItem) + chk.size() * sizeof(ChunkItem);
@@ -483,9 +525,16 @@ hb_status hb_attention(const hb_batch* batch, const void* h_plan, const void* q,
     uint8_t* ws = static_cast<uint8_t*>(d_workspace);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
 
+    // one launch: decode CTAs first, then one CTA per chunk item
+    CUtensorMap dec_k, dec_v, chunk_q;
+    std::memset(&dec_k, 0, sizeof(dec_k));
+    std::memset(&dec_v, 0, sizeof(dec_v));
+    std::memset(&chunk_q, 0, sizeof(chunk_q));
+    const int kvhb = h.decode_kvh_block;
+    DecodeParams dp{};
+    dp.group = g;
+    dp.kvh_block = kvhb;
     if (h.num_decode_items > 0) {
-      const int kvhb = h.decode_kvh_block;
-      CUtensorMap kmap, vmap;
       // pools viewed as [page][kv head][slot][head dim] boxes: dims are
       // (D, slot, kv head, page) with the pool's own strides
       const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)kPageSize, (cuuint64_t)Hkv,
@@ -493,60 +542,54 @@ hb_status hb_attention(const hb_batch* batch, const void* h_plan, const void* q,
       const cuuint64_t strides[3] = {(cuuint64_t)Hkv * D * 2, (cuuint64_t)D * 2,
                                      (cuuint64_t)kPageSize * Hkv * D * 2};
       const cuuint32_t box[4] = {64, (cuuint32_t)kPageSize, (cuuint32_t)kvhb, 1};
-      if ((s = encode_map(&kmap, k_cache, 4, dims, strides, box, "decode K")) != HB_OK) return s;
-      if ((s = encode_map(&vmap, v_cache, 4, dims, strides, box, "decode V")) != HB_OK) return s;
-      DecodeParams p{};
-      p.items = reinterpret_cast<const DecodeItem*>(ws);
-      p.cta_offsets = reinterpret_cast<const int32_t*>(ws + h.ws_decode_offsets);
-      p.num_items = h.num_decode_items;
-      p.counters = reinterpret_cast<int32_t*>(ws + h.ws_counters);
-      p.part_o = reinterpret_cast<float*>(ws + h.ws_partial_o);
-      p.part_ml = reinterpret_cast<float*>(ws + h.ws_partial_ml);
-      p.cu_q_len = batch->cu_q_len;
-      p.context_len = batch->context_len;
-      p.block_table = batch->block_table;
-      p.max_pages_per_seq = batch->max_pages_per_seq;
-      p.num_pages = batch->num_pages;
-      p.q = static_cast<const uint16_t*>(q);
-      p.out = static_cast<uint16_t*>(out);
-      p.num_q_heads = Hq;
-      p.num_kv_heads = Hkv;
-      p.group = g;
-      p.kvh_block = kvhb;
-      p.scale_log2 = scale_log2;
-      p.dev_error = dev->err;
-      LaunchTimer t(1, st);
-      cudaError_t e = launch_decode(p, D, h.decode_grid, kmap, vmap, st);
-      t.done();
-      if (e != cudaSuccess) return cuda_fail(e, "decode launch");
-      g_launches.fetch_add(1);
+      if ((s = encode_map(&dec_k, k_cache, 4, dims, strides, box, "decode K")) != HB_OK) return s;
+      if ((s = encode_map(&dec_v, v_cache, 4, dims, strides, box, "decode V")) != HB_OK) return s;
+      dp.items = reinterpret_cast<const DecodeItem*>(ws);
+      dp.cta_offsets = reinterpret_cast<const int32_t*>(ws + h.ws_decode_offsets);
+      dp.num_items = h.num_decode_items;
+      dp.counters = reinterpret_cast<int32_t*>(ws + h.ws_counters);
+      dp.part_o = reinterpret_cast<float*>(ws + h.ws_partial_o);
+      dp.part_ml = reinterpret_cast<float*>(ws + h.ws_partial_ml);
+      dp.cu_q_len = batch->cu_q_len;
+      dp.context_len = batch->context_len;
+      dp.block_table = batch->block_table;
+      dp.max_pages_per_seq = batch->max_pages_per_seq;
+      dp.num_pages = batch->num_pages;
+      dp.q = static_cast<const uint16_t*>(q);
+      dp.out = static_cast<uint16_t*>(out);
+      dp.num_q_heads = Hq;
+      dp.num_kv_heads = Hkv;
+      dp.scale_log2 = scale_log2;
+      dp.dev_error = dev->err;
     }
+    ChunkParams cp{};
+    cp.group = g;
     if (h.num_chunk_items > 0) {
       const int tpt = h.chunk_tokens_per_tile;
-      CUtensorMap qmap;
       const cuuint64_t qdims[3] = {(cuuint64_t)D, (cuuint64_t)Hq, (cuuint64_t)batch->total_q};
       const cuuint64_t qstr[2] = {(cuuint64_t)D * 2, (cuuint64_t)Hq * D * 2};
       const cuuint32_t qbox[3] = {64, (cuuint32_t)g, (cuuint32_t)tpt};
-      if ((s = encode_map(&qmap, q, 3, qdims, qstr, qbox, "chunk Q")) != HB_OK) return s;
-      ChunkParams p{};
-      p.items = reinterpret_cast<const ChunkItem*>(ws + (size_t)h.num_decode_items * sizeof(DecodeItem));
-      p.num_items = h.num_chunk_items;
-      p.cu_q_len = batch->cu_q_len;
-      p.context_len = batch->context_len;
-      p.block_table = batch->block_table;
-      p.max_pages_per_seq = batch->max_pages_per_seq;
-      p.num_pages = batch->num_pages;
-      p.out = static_cast<uint16_t*>(out);
-      p.num_q_heads = Hq;
-      p.num_kv_heads = Hkv;
-      p.group = g;
-      p.tokens_per_tile = tpt;
-      p.scale_log2 = scale_log2;
-      p.dev_error = dev->err;
-      LaunchTimer t(2, st);
-      cudaError_t e = launch_chunk(p, D, qmap, k_cache, v_cache, st);
+      if ((s = encode_map(&chunk_q, q, 3, qdims, qstr, qbox, "chunk Q")) != HB_OK) return s;
+      cp.items = reinterpret_cast<const ChunkItem*>(ws + (size_t)h.num_decode_items * sizeof(DecodeItem));
+      cp.num_items = h.num_chunk_items;
+      cp.cu_q_len = batch->cu_q_len;
+      cp.context_len = batch->context_len;
+      cp.block_table = batch->block_table;
+      cp.max_pages_per_seq = batch->max_pages_per_seq;
+      cp.num_pages = batch->num_pages;
+      cp.out = static_cast<uint16_t*>(out);
+      cp.num_q_heads = Hq;
+      cp.num_kv_heads = Hkv;
+      cp.tokens_per_tile = tpt;
+      cp.scale_log2 = scale_log2;
+      cp.dev_error = dev->err;
+    }
+    if (h.num_decode_items > 0 || h.num_chunk_items > 0) {
+      LaunchTimer t(1, st);
+      cudaError_t e = launch_attention(dp, h.decode_grid, cp, D, dec_k, dec_v, chunk_q, k_cache,
+                                       v_cache, st);
       t.done();
-      if (e != cudaSuccess) return cuda_fail(e, "chunk launch");
+      if (e != cudaSuccess) return cuda_fail(e, "attention launch");
       g_launches.fetch_add(1);
     }
     return ok();

@@ -1,0 +1,91 @@
+// attention.cu -- the single attention launch of a hybrid batch.
+//
+// "Sarathi-Serve：以 chunked-prefills 与 stall-free batching 驯服 LLM 推理的吞吐—
+// 延迟权衡", §GPU / 系统数据路径 ③: one iteration's batch holds decode tokens and
+// prefill chunks together; "In-flight Batching", §Batch 内的异构执行: the
+// different lengths are handled inside one kernel launch.
+//
+// One grid serves both kinds of work.  CTAs 0 .. decode_grid-1 each stream
+// one equal range of the decode rows' pages (decode_body.cuh, HBM-bound);
+// every later CTA takes one chunk work item, longest first
+// (chunk_body.cuh, tensor-core-bound).  Every CTA uses ~220 KB of shared
+// memory, so one CTA runs per SM and the hardware hands out CTAs in index
+// order as SMs free up: the first wave runs decode ranges and chunk items
+// side by side, and SMs that finish their decode range go on to the
+// remaining chunk items.  The host plan picks decode_grid so that both kinds
+// of work end together.  No CTA waits for another.
+#include <cuda_runtime.h>
+
+#include "chunk_body.cuh"
+#include "decode_body.cuh"
+#include "hb_internal.h"
+#include "ptx.cuh"
+
+namespace hb {
+
+constexpr int kAttnThreads = 384;
+
+struct AttnParams {
+  DecodeParams dec;
+  DecodeLayout dl;
+  ChunkParams chk;
+  const uint16_t* k_cache;
+  const uint16_t* v_cache;
+  int32_t decode_grid;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kAttnThreads, 1)
+    attention_kernel(const AttnParams p, const __grid_constant__ CUtensorMap dec_k,
+                     const __grid_constant__ CUtensorMap dec_v,
+                     const __grid_constant__ CUtensorMap chunk_q) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+  if ((int)blockIdx.x < p.decode_grid)
+    decode_cta<D>(p.dec, p.dl, dec_k, dec_v, smem, blockIdx.x);
+  else
+    chunk_cta<D>(p.chk, chunk_q, p.k_cache, p.v_cache, smem, blockIdx.x - p.decode_grid);
+}
+
+// Dynamic shared memory of the attention kernel for this geometry.
+int attention_smem_bytes(int head_dim, int kvh_block, int group) {
+  const DecodeLayout L = decode_layout(head_dim, kvh_block, group);
+  const int c = head_dim == 128 ? ChunkCfg<128>::kSmemBytes : ChunkCfg<64>::kSmemBytes;
+  return L.smem_bytes > c ? L.smem_bytes : c;
+}
+
+// Launch decode_grid decode CTAs followed by one CTA per chunk item.  Either
+// part may be empty (dec.num_items == 0: no decode CTA).  dec.kvh_block and
+// dec.group must be set in every case (they size the shared memory).
+cudaError_t launch_attention(const DecodeParams& dec, int decode_grid, const ChunkParams& chk,
+                             int head_dim, const CUtensorMap& dec_k, const CUtensorMap& dec_v,
+                             const CUtensorMap& chunk_q, const void* k_cache,
+                             const void* v_cache, cudaStream_t stream) {
+  AttnParams p{};
+  p.dec = dec;
+  p.chk = chk;
+  p.decode_grid = dec.num_items > 0 ? decode_grid : 0;
+  p.dl = decode_layout(head_dim, dec.kvh_block, dec.group);
+  if (p.decode_grid > 0 && p.dl.n_stages < 2) return cudaErrorInvalidConfiguration;
+  p.k_cache = static_cast<const uint16_t*>(k_cache);
+  p.v_cache = static_cast<const uint16_t*>(v_cache);
+  const int grid = p.decode_grid + chk.num_items;
+  if (grid == 0) return cudaSuccess;
+  const int smem = attention_smem_bytes(head_dim, dec.kvh_block, dec.group);
+  cudaError_t e;
+  if (head_dim == 128) {
+    e = cudaFuncSetAttribute(attention_kernel<128>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    attention_kernel<128><<<grid, kAttnThreads, smem, stream>>>(p, dec_k, dec_v, chunk_q);
+  } else {
+    e = cudaFuncSetAttribute(attention_kernel<64>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    attention_kernel<64><<<grid, kAttnThreads, smem, stream>>>(p, dec_k, dec_v, chunk_q);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace hb

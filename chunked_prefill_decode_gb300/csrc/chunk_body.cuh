@@ -1,4 +1,6 @@
-// chunk.cu -- attention of prefill chunks on the tcgen05 tensor cores.
+// chunk_body.cuh -- attention of prefill chunks on the tcgen05 tensor cores:
+// the per-CTA body that the attention kernel (attention.cu) runs for chunk
+// items.
 //
 // "Sarathi-Serve：以 chunked-prefills 与 stall-free batching 驯服 LLM 推理的吞吐—
 // 延迟权衡", §核心机制 3 and §GPU / 系统数据路径 ⑤: chunk i of a prompt attends
@@ -14,7 +16,7 @@
 // every 128-key K/V tile; the CTA walks the key tiles 0 .. (last position of
 // B) of its sequence, A stopping at its own last position.
 //
-// Warp roles (416 threads):
+// Warp roles (384 threads):
 //   warps 0-3  softmax of tile A, warps 4-7 softmax of tile B: thread = query
 //              row = TMEM lane (warp w owns lanes 32 (w % 4) ..).  Per key
 //              tile, pass 1 reads S in 32-column pieces (tcgen05.ld) for the
@@ -36,7 +38,7 @@
 //              tensor pipe runs one thread's MMAs in order, so "S_t(j) ready"
 //              also means PV_t(j-1) is done: the softmax may then rescale O_t
 //              and P_t may live in the S_t columns.
-//   warps 9-12 producers: gather each 128-key K or V tile from its eight
+//   warps 9-11 producers: gather each 128-key K or V tile from its eight
 //              16-token pages with 16-byte cp.async copies (adjacent lanes
 //              cover one contiguous token row, so every warp access is
 //              coalesced) straight into the 128-byte-swizzled layout the MMA
@@ -46,6 +48,8 @@
 //              design), so the gather runs on the load/store units.  K runs
 //              one tile ahead of V.
 // TMEM (512 columns): S_A 0-127, S_B 128-255, O_A 256-(256+D), O_B after it.
+#pragma once
+
 #include <cuda_runtime.h>
 
 #include "hb_internal.h"
@@ -53,10 +57,10 @@
 
 namespace hb {
 
-constexpr int kChunkThreads = 416;
 constexpr int kMmaWarp = 8;
 constexpr int kProducerWarp0 = 9;
-constexpr int kProducerThreads = 128;
+constexpr int kProducerWarps = 3;
+constexpr int kProducerThreads = 32 * kProducerWarps;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 template <int D>
@@ -76,22 +80,22 @@ struct ChunkCfg {
   static constexpr uint32_t kOCol = 256;                // O_A; O_B at kOCol + D
   static constexpr int kUnits = D / 8;                  // 16-byte units per token row
   static constexpr int kRowsPerInstr = 32 / kUnits;     // token rows per warp access
+  static constexpr int kInstrPerTile = kChunkKeys / kRowsPerInstr;  // warp accesses per tile
 };
 static_assert(ChunkCfg<128>::kSmemBytes <= 227 * 1024, "chunk smem (D=128)");
 static_assert(ChunkCfg<64>::kSmemBytes <= 227 * 1024, "chunk smem (D=64)");
 
+// Body of one chunk CTA working on item `item`; `smem` is the 1024-byte-
+// aligned dynamic shared memory.
 template <int D>
-__global__ void __launch_bounds__(kChunkThreads, 1)
-    chunk_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap qmap,
-                 const uint16_t* __restrict__ k_cache,
-                 const uint16_t* __restrict__ v_cache) {
+__device__ __forceinline__ void chunk_cta(const ChunkParams& p, const CUtensorMap& qmap,
+                                          const uint16_t* __restrict__ k_cache,
+                                          const uint16_t* __restrict__ v_cache,
+                                          uint8_t* smem, int item) {
   using C = ChunkCfg<D>;
   constexpr int CH = C::CH;
   constexpr int NK = C::NK;
   constexpr int NV = C::NV;
-  extern __shared__ uint8_t smem_raw[];
-  const uint32_t raw = smem_u32(smem_raw);
-  uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
   uint8_t* sQ = smem + C::kQOff;
   uint8_t* sK = smem + C::kKOff;
   uint8_t* sV = smem + C::kVOff;
@@ -111,7 +115,7 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const ChunkItem it = p.items[blockIdx.x];
+  const ChunkItem it = p.items[item];
   const int g = p.group;
   const int tpt = p.tokens_per_tile;
   const int q0 = it.q0;
@@ -153,68 +157,69 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
 
   if (warp >= kProducerWarp0) {
     // ------------------------------------------------------------ producers
-    const int pw = warp - kProducerWarp0;            // 0..3: rows 32pw..32pw+31
+    // lane l < 8 holds the physical page of page l of a tile (one tile ahead)
+    const int pw = warp - kProducerWarp0;
     const int unit = lane % C::kUnits;
     const int sub = lane / C::kUnits;
     const int n_pages = (ctx + kPageSize - 1) / kPageSize;
     const int32_t* bt_row = p.block_table + (size_t)it.seq * p.max_pages_per_seq;
     const size_t row_elems = (size_t)p.num_kv_heads * D;   // one token of a pool
-    // physical pages of this warp's two pages of tile j (-1: none / invalid)
-    auto pages_of = [&](int j, int* e) {
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int lp = j * (kChunkKeys / kPageSize) + 2 * pw + h;
-        int phys = -1;
-        if (lp < n_pages) {
-          phys = (lp < p.max_pages_per_seq) ? __ldg(&bt_row[lp]) : -1;
-          if (phys < 0 || phys >= p.num_pages) {
-            if (lane == 0) report_error(p.dev_error, HB_DEVERR_INDEX);
-            phys = -1;
-          }
+    auto page_of = [&](int j) -> int {   // lane l: page l of tile j (-1: none)
+      const int lp = j * (kChunkKeys / kPageSize) + (lane & 7);
+      int phys = -1;
+      if (lp < n_pages) {
+        phys = (lp < p.max_pages_per_seq) ? __ldg(&bt_row[lp]) : -1;
+        if (phys < 0 || phys >= p.num_pages) {
+          if (lane < 8) report_error(p.dev_error, HB_DEVERR_INDEX);
+          phys = -1;
         }
-        e[h] = phys;
       }
+      return phys;
     };
-    auto gather = [&](const uint16_t* pool, uint8_t* stage, int j, const int* e) {
-      const uint32_t base = smem_u32(stage);
+    // Each warp copies whole pages (pages pw, pw + 3, pw + 6 of a tile): one
+    // block-table shuffle per page, then kRowsPerPage accesses that step
+    // through the page's rows; only the swizzle term depends on the row.
+    constexpr int kRowsPerPage = kPageSize / C::kRowsPerInstr;   // accesses per page
+    const uint32_t unit_off = (uint32_t)((unit >> 3) * 16384);
+    const size_t src_unit = (size_t)it.kv_head * D + unit * 8;
+    auto gather = [&](const uint16_t* pool, uint8_t* stage, int j, int pages) {
+      const uint32_t base = smem_u32(stage) + unit_off;
       const int kbase = j * kChunkKeys;
 #pragma unroll
-      for (int i = 0; i < C::kUnits; ++i) {
-        const int r = 32 * pw + i * C::kRowsPerInstr + sub;   // key row in the tile
-        const int key = kbase + r;
-        const int phys = e[(r >> 4) & 1];
-        const bool valid = key < ctx && phys >= 0;
-        const uint16_t* src = valid
-            ? pool + ((size_t)phys * kPageSize + (key & (kPageSize - 1))) * row_elems +
-                  (size_t)it.kv_head * D + unit * 8
-            : pool;
-        const uint32_t dst = base + (unit >> 3) * 16384 + r * 128 + (((unit & 7) ^ (r & 7)) << 4);
-        cp_async_16(dst, src, valid ? 16u : 0u);
+      for (int pi = 0; pi < (kChunkKeys / kPageSize + kProducerWarps - 1) / kProducerWarps; ++pi) {
+        const int pp = pw + pi * kProducerWarps;          // page of the tile (warp-uniform)
+        const int phys = __shfl_sync(0xffffffffu, pages, pp & 7);
+        if (pp >= kChunkKeys / kPageSize) break;
+        const uint16_t* src_page = pool + (size_t)(phys < 0 ? 0 : phys) * kPageSize * row_elems + src_unit;
+#pragma unroll
+        for (int k = 0; k < kRowsPerPage; ++k) {
+          const int slot = k * C::kRowsPerInstr + sub;      // row within the page
+          const int r = pp * kPageSize + slot;              // row within the tile
+          const bool valid = phys >= 0 && kbase + r < ctx;
+          const uint16_t* src = valid ? src_page + (size_t)slot * row_elems : pool;
+          cp_async_16(base + r * 128 + (((unit & 7) ^ (r & 7)) << 4), src, valid ? 16u : 0u);
+        }
       }
     };
-    int e_prev[2] = {-1, -1}, e_cur[2], e_next[2];
-    pages_of(0, e_cur);
-    pages_of(1, e_next);
+    int pg_prev = -1, pg_cur = page_of(0), pg_next = page_of(1);
     bool ok = true;
     for (int j = 0; ok && j <= T; ++j) {
       if (j < T) {
         const int s = j % NK;
         if (!mbar_wait(&k_empty[s], ((uint32_t)(j / NK) & 1u) ^ 1u, abort_flag)) { ok = false; break; }
-        gather(k_cache, sK + s * C::kTileBytes, j, e_cur);
+        gather(k_cache, sK + s * C::kTileBytes, j, pg_cur);
         cp_async_arrive_noinc(&k_full[s]);
       }
       if (j >= 1) {
         const int jv = j - 1;
         const int s = jv % NV;
         if (!mbar_wait(&v_empty[s], ((uint32_t)(jv / NV) & 1u) ^ 1u, abort_flag)) { ok = false; break; }
-        gather(v_cache, sV + s * C::kTileBytes, jv, e_prev);
+        gather(v_cache, sV + s * C::kTileBytes, jv, pg_prev);
         cp_async_arrive_noinc(&v_full[s]);
       }
-      e_prev[0] = e_cur[0];
-      e_prev[1] = e_cur[1];
-      e_cur[0] = e_next[0];
-      e_cur[1] = e_next[1];
-      pages_of(j + 2, e_next);
+      pg_prev = pg_cur;
+      pg_cur = pg_next;
+      pg_next = page_of(j + 2);
     }
     // copies in flight must land before the CTA exits
     asm volatile("cp.async.wait_all;" ::: "memory");
@@ -436,28 +441,6 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
     tmem_dealloc(tmem, C::kTmemCols);
   }
   if (threadIdx.x == 0 && *abort_flag) report_error(p.dev_error, HB_DEVERR_TIMEOUT);
-}
-
-cudaError_t launch_chunk(const ChunkParams& p, int head_dim, const CUtensorMap& qmap,
-                         const void* k_cache, const void* v_cache, cudaStream_t stream) {
-  if (p.num_items == 0) return cudaSuccess;
-  const uint16_t* kc = static_cast<const uint16_t*>(k_cache);
-  const uint16_t* vc = static_cast<const uint16_t*>(v_cache);
-  cudaError_t e;
-  if (head_dim == 128) {
-    constexpr int smem = ChunkCfg<128>::kSmemBytes;
-    e = cudaFuncSetAttribute(chunk_kernel<128>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    chunk_kernel<128><<<p.num_items, kChunkThreads, smem, stream>>>(p, qmap, kc, vc);
-  } else {
-    constexpr int smem = ChunkCfg<64>::kSmemBytes;
-    e = cudaFuncSetAttribute(chunk_kernel<64>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    chunk_kernel<64><<<p.num_items, kChunkThreads, smem, stream>>>(p, qmap, kc, vc);
-  }
-  return cudaGetLastError();
 }
 
 }  // namespace hb

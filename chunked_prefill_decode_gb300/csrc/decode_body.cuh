@@ -1,5 +1,6 @@
-// decode.cu -- attention of decode rows (one new token over a long cached
-// context), split over the keys, read through the block table.
+// decode_body.cuh -- attention of decode rows (one new token over a long
+// cached context), split over the keys, read through the block table: the
+// per-CTA body that the attention kernel (attention.cu) runs for decode CTAs.
 //
 // "Sarathi-Serve：以 chunked-prefills 与 stall-free batching 驯服 LLM 推理的吞吐—
 // 延迟权衡", §GPU / 系统数据路径 ⑤: a decode reads all earlier KV of its
@@ -26,6 +27,8 @@
 //    / l.  Nobody waits on another CTA.
 //
 // Bytes per decode row: 2 * context * Hkv * D * 2 (K and V read once).
+#pragma once
+
 #include <cuda_runtime.h>
 
 #include "hb_internal.h"
@@ -33,8 +36,7 @@
 
 namespace hb {
 
-constexpr int kDecConsumerWarps = 8;
-constexpr int kDecThreads = 32 * (kDecConsumerWarps + 1);
+constexpr int kDecConsumerWarps = 8;   // warps 0-7; warp 8 is the producer
 constexpr int kDecMaxStages = 8;
 constexpr int kHdrFirst = 1, kHdrLast = 2, kHdrEnd = 4;
 
@@ -56,7 +58,7 @@ struct DecodeLayout {
   int32_t smem_bytes;    // dynamic shared memory to request (with alignment)
 };
 
-__host__ DecodeLayout decode_layout(int head_dim, int kvh_block, int group) {
+inline __host__ DecodeLayout decode_layout(int head_dim, int kvh_block, int group) {
   DecodeLayout L{};
   const int ch = head_dim / 64;
   L.chunk_bytes = kvh_block * kPageSize * 128;
@@ -74,15 +76,14 @@ __host__ DecodeLayout decode_layout(int head_dim, int kvh_block, int group) {
   return L;
 }
 
+// Body of one decode CTA (index `cta` among the decode CTAs); `smem` is the
+// 1024-byte-aligned dynamic shared memory.  Warps 0-7 consume, warp 8
+// produces, any further warps of the block only join the barriers.
 template <int D>
-__global__ void __launch_bounds__(kDecThreads, 1)
-    decode_kernel(const DecodeParams p, const DecodeLayout L,
-                  const __grid_constant__ CUtensorMap kmap,
-                  const __grid_constant__ CUtensorMap vmap) {
+__device__ __forceinline__ void decode_cta(const DecodeParams& p, const DecodeLayout& L,
+                                           const CUtensorMap& kmap, const CUtensorMap& vmap,
+                                           uint8_t* smem, int cta) {
   constexpr int CH = D / 64;
-  extern __shared__ uint8_t smem_raw[];
-  const uint32_t raw = smem_u32(smem_raw);
-  uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
 
   const int S = L.n_stages;
   uint8_t* stages = smem;
@@ -148,8 +149,8 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       }
       return phys;
     };
-    const int i0 = p.cta_offsets[blockIdx.x];
-    const int i1 = p.cta_offsets[blockIdx.x + 1];
+    const int i0 = p.cta_offsets[cta];
+    const int i1 = p.cta_offsets[cta + 1];
     bool ok = true;
     DecodeItem it{}, nxt{};
     int win = 0, win_next = 0, nxt_win = 0;
@@ -226,7 +227,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         if (issued_mask & (1u << s2))
           drain_wait(&full[s2], (last_par_mask >> s2) & 1u, abort_flag);
     }
-  } else {
+  } else if (warp < kDecConsumerWarps) {
     // ------------------------------------------------------------ consumers
     const int w = warp;                  // local kv head of this warp
     const bool active = w < kvhb;
@@ -469,27 +470,6 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   }
   __syncthreads();
   if (threadIdx.x == 0 && *abort_flag) report_error(p.dev_error, HB_DEVERR_TIMEOUT);
-}
-
-cudaError_t launch_decode(const DecodeParams& p, int head_dim, int grid,
-                          const CUtensorMap& kmap, const CUtensorMap& vmap,
-                          cudaStream_t stream) {
-  if (p.num_items == 0 || grid == 0) return cudaSuccess;
-  const DecodeLayout L = decode_layout(head_dim, p.kvh_block, p.group);
-  if (L.n_stages < 2) return cudaErrorInvalidConfiguration;
-  cudaError_t e;
-  if (head_dim == 128) {
-    e = cudaFuncSetAttribute(decode_kernel<128>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, L.smem_bytes);
-    if (e != cudaSuccess) return e;
-    decode_kernel<128><<<grid, kDecThreads, L.smem_bytes, stream>>>(p, L, kmap, vmap);
-  } else {
-    e = cudaFuncSetAttribute(decode_kernel<64>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, L.smem_bytes);
-    if (e != cudaSuccess) return e;
-    decode_kernel<64><<<grid, kDecThreads, L.smem_bytes, stream>>>(p, L, kmap, vmap);
-  }
-  return cudaGetLastError();
 }
 
 }  // namespace hb

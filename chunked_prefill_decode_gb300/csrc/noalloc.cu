@@ -5,7 +5,8 @@
 // one: a serving engine that hands nearly all free HBM to its KV-cache pool
 // at start-up and forbids device allocations afterwards, or a plugin that
 // receives raw tensor pointers but no allocator.  hb_decode_attention_noalloc
-// serves them: it runs the same split-KV decode kernel with its scratch in a
+// serves them: it runs the same attention kernel (decode CTAs only) with its
+// scratch in a
 // fixed array of HB_NOALLOC_SCRATCH_BYTES that lives in this file and is
 // created when the library is loaded (every device that loads the library
 // holds it until the process exits).  It makes no cudaMalloc / cudaFree call
@@ -28,9 +29,10 @@
 #include "hb_internal.h"
 
 namespace hb {
-cudaError_t launch_decode(const DecodeParams& p, int head_dim, int grid,
-                          const CUtensorMap& kmap, const CUtensorMap& vmap,
-                          cudaStream_t stream);
+cudaError_t launch_attention(const DecodeParams& dec, int decode_grid, const ChunkParams& chk,
+                             int head_dim, const CUtensorMap& dec_k, const CUtensorMap& dec_v,
+                             const CUtensorMap& chunk_q, const void* k_cache,
+                             const void* v_cache, cudaStream_t stream);
 hb_status internal_fail(hb_status s, const char* msg);
 hb_status internal_ok();
 hb_status internal_check_batch(const hb_batch* b);
@@ -168,7 +170,11 @@ extern "C" hb_status hb_decode_attention_noalloc(const hb_batch* batch, const in
     p.kvh_block = kvhb;
     p.scale_log2 = softmax_scale * 1.4426950408889634f;
     p.dev_error = err;
-    e = launch_decode(p, D, part.grid, kmap, vmap, st);
+    ChunkParams none{};
+    none.group = g;
+    CUtensorMap unused;
+    std::memset(&unused, 0, sizeof(unused));
+    e = launch_attention(p, part.grid, none, D, kmap, vmap, unused, k_cache, v_cache, st);
     if (e != cudaSuccess) return internal_fail(HB_ERR_CUDA, "decode launch failed");
     internal_count_launch();
     return internal_ok();

@@ -18,8 +18,8 @@ _LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libhb.so")
 _lib = None
 
 HB_OK = 0
-HB_NUM_KERNEL_IDS = 3
-KERNEL_NAMES = ("kv_append", "decode", "chunk")
+HB_NUM_KERNEL_IDS = 2
+KERNEL_NAMES = ("kv_append", "attention")
 
 STATUS_NAMES = {
     0: "HB_OK", 1: "HB_ERR_INVALID_ARG", 2: "HB_ERR_SHAPE", 3: "HB_ERR_UNSUPPORTED",

@@ -142,8 +142,10 @@ hb_status hb_plan(const hb_batch* batch, const int32_t* h_q_len,
  * over keys t = 0..p of the row's sequence (p its absolute position), K/V of
  * kv head h/(Hq/Hkv) read through the block table from the caches as they
  * stand after hb_kv_append.  fp32 accumulation, one bf16 rounding at the
- * store.  Decode rows use a split-KV kernel whose partial softmax states are
- * merged by the last split to finish; chunk rows use a tensor-core kernel.
+ * store.  One kernel launch does all of it: decode rows are streamed as equal
+ * page ranges per CTA (a row that straddles ranges leaves partial softmax
+ * states, merged by the last piece to finish) and chunk rows are tiled for
+ * the tensor cores, the two kinds of CTAs running side by side.
  * Cited passages: the first page, §GPU / 系统数据路径 ③-⑤, and §核心机制 3
  * (chunk i re-reads the KV of chunks 1..i-1; same computation as unchunked).
  *   h_plan      host plan written by hb_plan for this batch
@@ -207,9 +209,10 @@ hb_status hb_check(void* stream);
 /* ---------------------------------------------------------------------------
  * Instrumentation.  When enabled, every kernel launch of this library is
  * bracketed by CUDA events recorded on its launch stream.
- *   kernel ids: 0 = kv append, 1 = decode split-KV, 2 = chunk (tensor core)
+ *   kernel ids: 0 = kv append, 1 = attention (decode and chunk work in one
+ *   launch)
  * ------------------------------------------------------------------------- */
-#define HB_NUM_KERNEL_IDS 3
+#define HB_NUM_KERNEL_IDS 2
 
 /* Start (clearing earlier records) or stop recording.  Not thread-safe with
  * concurrent launches from other threads. */

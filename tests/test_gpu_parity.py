@@ -136,8 +136,8 @@ def test_timing_and_launch_count():
     gpu_step(lay, ten)
     t = hb.hb_timing_read()
     hb.hb_timing_enable(False)
-    assert hb.hb_launch_count() - n0 == 3
-    for name in ("kv_append", "decode", "chunk"):
+    assert hb.hb_launch_count() - n0 == 2
+    for name in ("kv_append", "attention"):
         assert t[name][1] == 1 and t[name][0] > 0
 
 
