@@ -57,6 +57,31 @@ def _peaks():
                 "source": "fallback"}
 
 
+ATTN_SOURCES = ("attention.cu", "decode_body.cuh", "chunk_body.cuh", "ptx.cuh",
+                "hb_internal.h", "decode_plan.h", "api.cu")
+
+
+def profiled_traffic(workload):
+    """DRAM bytes per attention launch from the committed ncu summary of this
+    workload, if the summary was taken on the current kernel sources."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", f"attention_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    fields = {}
+    for line in open(path):
+        if ":" in line and line.split(":")[0] in ("traffic_bytes_per_launch", "sources_sha256"):
+            k, v = line.split(":", 1)
+            fields[k.strip()] = v.strip()
+    h = hashlib.sha256()
+    for src in ATTN_SOURCES:
+        with open(os.path.join(ROOT, "chunked_prefill_decode_gb300", "csrc", src), "rb") as f:
+            h.update(f.read())
+    if fields.get("sources_sha256") != h.hexdigest()[:16]:
+        return None
+    return int(fields["traffic_bytes_per_launch"])
+
+
 def algorithmic_counts(layout):
     """FLOPs and bytes of one step, by kernel, counted from the definition.
 
@@ -140,10 +165,10 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def _dist():
+def _dist(backend="nccl"):
     n = int(os.environ.get("WORLD_SIZE", "1"))
     if n > 1 and not torch.distributed.is_initialized():
-        torch.distributed.init_process_group("nccl")
+        torch.distributed.init_process_group(backend)
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return n, rank, local
@@ -155,11 +180,19 @@ def _barrier(n):
 
 
 def max_over_ranks(x: float, n: int) -> float:
+    """Largest value over the ranks (the job ends when its slowest rank does)."""
     if n <= 1:
         return x
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if torch.distributed.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_tokens_per_s(tokens_per_step: int, steps: int, n: int, ms_local: float) -> float:
+    """Whole-job rate of n independent replicas: every rank's tokens over the
+    slowest rank's time."""
+    return n * tokens_per_step * steps / (max_over_ranks(ms_local, n) / 1e3)
 
 
 # ---------------------------------------------------------------------------
@@ -289,7 +322,7 @@ def run_native(args):
     _barrier(n)
     ms = ev0.elapsed_time(ev1)
     ms_max = max_over_ranks(ms, n)
-    value = n * T * args.steps / (ms_max / 1e3)
+    value = job_tokens_per_s(T, args.steps, n, ms)
 
     # ---- end to end through the public API with host buffers
     pin = lambda t: t.detach().cpu().pin_memory()
@@ -354,6 +387,7 @@ def run_native(args):
                 "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                 "frac": achieved / peaks["bf16_tflops"], "traffic": None}
     roof["peak_source"] = peaks["source"]
+    roof["traffic"] = profiled_traffic(args.workload)
     roof["algorithmic"] = {"bytes": att_bytes, "flops": att_flops}
     roof["kernel_roofline_frac"] = max(t_hbm, t_tc) * 1e3 / t_att
     roof["avg_launch_ms"] = {"attention": t_att, "kv_append": t_app}
