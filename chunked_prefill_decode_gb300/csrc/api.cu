@@ -25,7 +25,8 @@ namespace hb {
 cudaError_t launch_kv_append(const AppendParams& p, int num_sms, cudaStream_t stream);
 cudaError_t launch_attention(const DecodeParams& dec, int decode_grid, const ChunkParams& chk,
                              int head_dim, const CUtensorMap& dec_k, const CUtensorMap& dec_v,
-                             const CUtensorMap& chunk_q, const void* k_cache,
+                             const CUtensorMap& chunk_q, const CUtensorMap& chunk_k,
+                             const CUtensorMap& chunk_v, const void* k_cache,
                              const void* v_cache, cudaStream_t stream);
 }  // namespace hb
 
@@ -526,7 +527,9 @@ hb_status hb_attention(const hb_batch* batch, const void* h_plan, const void* q,
     cudaStream_t st = static_cast<cudaStream_t>(stream);
 
     // one launch: decode CTAs first, then one CTA per chunk item
-    CUtensorMap dec_k, dec_v, chunk_q;
+    CUtensorMap dec_k, dec_v, chunk_q, chunk_k, chunk_v;
+    std::memset(&chunk_k, 0, sizeof(chunk_k));
+    std::memset(&chunk_v, 0, sizeof(chunk_v));
     std::memset(&dec_k, 0, sizeof(dec_k));
     std::memset(&dec_v, 0, sizeof(dec_v));
     std::memset(&chunk_q, 0, sizeof(chunk_q));
@@ -570,6 +573,13 @@ hb_status hb_attention(const hb_batch* batch, const void* h_plan, const void* q,
       const cuuint64_t qstr[2] = {(cuuint64_t)D * 2, (cuuint64_t)Hq * D * 2};
       const cuuint32_t qbox[3] = {64, (cuuint32_t)g, (cuuint32_t)tpt};
       if ((s = encode_map(&chunk_q, q, 3, qdims, qstr, qbox, "chunk Q")) != HB_OK) return s;
+      // pools viewed as (D, kv head, token slot) with one box per page
+      const cuuint64_t kdims[3] = {(cuuint64_t)D, (cuuint64_t)Hkv,
+                                   (cuuint64_t)batch->num_pages * kPageSize};
+      const cuuint64_t kstr[2] = {(cuuint64_t)D * 2, (cuuint64_t)Hkv * D * 2};
+      const cuuint32_t kbox[3] = {64, 1, (cuuint32_t)kPageSize};
+      if ((s = encode_map(&chunk_k, k_cache, 3, kdims, kstr, kbox, "chunk K")) != HB_OK) return s;
+      if ((s = encode_map(&chunk_v, v_cache, 3, kdims, kstr, kbox, "chunk V")) != HB_OK) return s;
       cp.items = reinterpret_cast<const ChunkItem*>(ws + (size_t)h.num_decode_items * sizeof(DecodeItem));
       cp.num_items = h.num_chunk_items;
       cp.cu_q_len = batch->cu_q_len;
@@ -586,8 +596,8 @@ hb_status hb_attention(const hb_batch* batch, const void* h_plan, const void* q,
     }
     if (h.num_decode_items > 0 || h.num_chunk_items > 0) {
       LaunchTimer t(1, st);
-      cudaError_t e = launch_attention(dp, h.decode_grid, cp, D, dec_k, dec_v, chunk_q, k_cache,
-                                       v_cache, st);
+      cudaError_t e = launch_attention(dp, h.decode_grid, cp, D, dec_k, dec_v, chunk_q, chunk_k,
+                                       chunk_v, k_cache, v_cache, st);
       t.done();
       if (e != cudaSuccess) return cuda_fail(e, "attention launch");
       g_launches.fetch_add(1);

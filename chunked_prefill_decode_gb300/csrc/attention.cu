@@ -38,14 +38,16 @@ template <int D>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     attention_kernel(const AttnParams p, const __grid_constant__ CUtensorMap dec_k,
                      const __grid_constant__ CUtensorMap dec_v,
-                     const __grid_constant__ CUtensorMap chunk_q) {
+                     const __grid_constant__ CUtensorMap chunk_q,
+                     const __grid_constant__ CUtensorMap chunk_k,
+                     const __grid_constant__ CUtensorMap chunk_v) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
   if ((int)blockIdx.x < p.decode_grid)
     decode_cta<D>(p.dec, p.dl, dec_k, dec_v, smem, blockIdx.x);
   else
-    chunk_cta<D>(p.chk, chunk_q, p.k_cache, p.v_cache, smem, blockIdx.x - p.decode_grid);
+    chunk_cta<D>(p.chk, chunk_q, chunk_k, chunk_v, p.k_cache, p.v_cache, smem, blockIdx.x - p.decode_grid);
 }
 
 // Dynamic shared memory of the attention kernel for this geometry.
@@ -60,7 +62,8 @@ int attention_smem_bytes(int head_dim, int kvh_block, int group) {
 // dec.group must be set in every case (they size the shared memory).
 cudaError_t launch_attention(const DecodeParams& dec, int decode_grid, const ChunkParams& chk,
                              int head_dim, const CUtensorMap& dec_k, const CUtensorMap& dec_v,
-                             const CUtensorMap& chunk_q, const void* k_cache,
+                             const CUtensorMap& chunk_q, const CUtensorMap& chunk_k,
+                             const CUtensorMap& chunk_v, const void* k_cache,
                              const void* v_cache, cudaStream_t stream) {
   AttnParams p{};
   p.dec = dec;
@@ -78,12 +81,12 @@ cudaError_t launch_attention(const DecodeParams& dec, int decode_grid, const Chu
     e = cudaFuncSetAttribute(attention_kernel<128>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    attention_kernel<128><<<grid, kAttnThreads, smem, stream>>>(p, dec_k, dec_v, chunk_q);
+    attention_kernel<128><<<grid, kAttnThreads, smem, stream>>>(p, dec_k, dec_v, chunk_q, chunk_k, chunk_v);
   } else {
     e = cudaFuncSetAttribute(attention_kernel<64>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    attention_kernel<64><<<grid, kAttnThreads, smem, stream>>>(p, dec_k, dec_v, chunk_q);
+    attention_kernel<64><<<grid, kAttnThreads, smem, stream>>>(p, dec_k, dec_v, chunk_q, chunk_k, chunk_v);
   }
   return cudaGetLastError();
 }

@@ -38,15 +38,14 @@
 //              tensor pipe runs one thread's MMAs in order, so "S_t(j) ready"
 //              also means PV_t(j-1) is done: the softmax may then rescale O_t
 //              and P_t may live in the S_t columns.
-//   warps 9-11 producers: gather each 128-key K or V tile from its eight
-//              16-token pages with 16-byte cp.async copies (adjacent lanes
-//              cover one contiguous token row, so every warp access is
-//              coalesced) straight into the 128-byte-swizzled layout the MMA
-//              reads; keys past the context are zero-filled by the copy
-//              itself.  A 16-token page holds only 2 KB per kv head, too small
-//              for one TMA box each (the per-box cost bounded an earlier
-//              design), so the gather runs on the load/store units.  K runs
-//              one tile ahead of V.
+//   warps 9-11 producers: fetch each 128-key K or V tile as its eight
+//              16-token pages, one TMA box per page and 64-column head-dim
+//              chunk (2 KB), coordinates from the block table; each warp's
+//              lane 0 issues the boxes of its pages, so three threads share
+//              the per-box issue cost.  Pages past the context are fetched out
+//              of range (zeros); the unwritten tail slots of the last page
+//              are zeroed in V by the softmax group that reads that tile
+//              first.  K runs one tile ahead of V.
 // TMEM (512 columns): S_A 0-127, S_B 128-255, O_A 256-(256+D), O_B after it.
 #pragma once
 
@@ -89,6 +88,7 @@ static_assert(ChunkCfg<64>::kSmemBytes <= 227 * 1024, "chunk smem (D=64)");
 // aligned dynamic shared memory.
 template <int D>
 __device__ __forceinline__ void chunk_cta(const ChunkParams& p, const CUtensorMap& qmap,
+                                          const CUtensorMap& kmap, const CUtensorMap& vmap,
                                           const uint16_t* __restrict__ k_cache,
                                           const uint16_t* __restrict__ v_cache,
                                           uint8_t* smem, int item) {
@@ -130,11 +130,11 @@ __device__ __forceinline__ void chunk_cta(const ChunkParams& p, const CUtensorMa
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
     for (int s = 0; s < NK; ++s) {
-      mbar_init(&k_full[s], kProducerThreads);
+      mbar_init(&k_full[s], kProducerWarps);
       mbar_init(&k_empty[s], 1);
     }
     for (int s = 0; s < NV; ++s) {
-      mbar_init(&v_full[s], kProducerThreads);
+      mbar_init(&v_full[s], kProducerWarps);
       mbar_init(&v_empty[s], 1);
     }
     for (int t = 0; t < 2; ++t) {
@@ -157,72 +157,82 @@ __device__ __forceinline__ void chunk_cta(const ChunkParams& p, const CUtensorMa
 
   if (warp >= kProducerWarp0) {
     // ------------------------------------------------------------ producers
-    // lane l < 8 holds the physical page of page l of a tile (one tile ahead)
+    // Each of the three producer warps owns pages pw, pw + 3, pw + 6 of every
+    // tile and its lane 0 issues their TMA boxes (one 16-token x 64-column box
+    // per page and head-dim chunk, 2 KB each): spreading the issue over three
+    // threads hides the per-box issue latency.  Lane l < 8 holds the physical
+    // page of page l of a tile; pages past the context are fetched out of
+    // range, i.e. as zeros.
     const int pw = warp - kProducerWarp0;
-    const int unit = lane % C::kUnits;
-    const int sub = lane / C::kUnits;
     const int n_pages = (ctx + kPageSize - 1) / kPageSize;
     const int32_t* bt_row = p.block_table + (size_t)it.seq * p.max_pages_per_seq;
-    const size_t row_elems = (size_t)p.num_kv_heads * D;   // one token of a pool
-    auto page_of = [&](int j) -> int {   // lane l: page l of tile j (-1: none)
+    auto page_of = [&](int j) -> int {   // lane l: page l of tile j
       const int lp = j * (kChunkKeys / kPageSize) + (lane & 7);
-      int phys = -1;
+      int phys = p.num_pages;
       if (lp < n_pages) {
         phys = (lp < p.max_pages_per_seq) ? __ldg(&bt_row[lp]) : -1;
         if (phys < 0 || phys >= p.num_pages) {
           if (lane < 8) report_error(p.dev_error, HB_DEVERR_INDEX);
-          phys = -1;
+          phys = p.num_pages;
         }
       }
       return phys;
     };
-    // Each warp copies whole pages (pages pw, pw + 3, pw + 6 of a tile): one
-    // block-table shuffle per page, then kRowsPerPage accesses that step
-    // through the page's rows; only the swizzle term depends on the row.
-    constexpr int kRowsPerPage = kPageSize / C::kRowsPerInstr;   // accesses per page
-    const uint32_t unit_off = (uint32_t)((unit >> 3) * 16384);
-    const size_t src_unit = (size_t)it.kv_head * D + unit * 8;
-    auto gather = [&](const uint16_t* pool, uint8_t* stage, int j, int pages) {
-      const uint32_t base = smem_u32(stage) + unit_off;
-      const int kbase = j * kChunkKeys;
+    constexpr int kMyPages = (kChunkKeys / kPageSize + kProducerWarps - 1) / kProducerWarps;
+    int my_pages = 0;
+    for (int pp = pw; pp < kChunkKeys / kPageSize; pp += kProducerWarps) ++my_pages;
+    uint32_t issued = 0, par = 0;   // bit s: stage s (K in 0..NK-1, V from NK)
+    auto tma_tile = [&](const CUtensorMap* map, uint8_t* stage, uint64_t* full, int pages,
+                        int bit, uint32_t ph) {
+      int phys[kMyPages];
 #pragma unroll
-      for (int pi = 0; pi < (kChunkKeys / kPageSize + kProducerWarps - 1) / kProducerWarps; ++pi) {
-        const int pp = pw + pi * kProducerWarps;          // page of the tile (warp-uniform)
-        const int phys = __shfl_sync(0xffffffffu, pages, pp & 7);
-        if (pp >= kChunkKeys / kPageSize) break;
-        const uint16_t* src_page = pool + (size_t)(phys < 0 ? 0 : phys) * kPageSize * row_elems + src_unit;
+      for (int pi = 0; pi < kMyPages; ++pi)
+        phys[pi] = __shfl_sync(0xffffffffu, pages, (pw + pi * kProducerWarps) & 7);
+      if (lane == 0) {
+        mbar_arrive_expect_tx(full, (uint32_t)(my_pages * CH * 2048));
 #pragma unroll
-        for (int k = 0; k < kRowsPerPage; ++k) {
-          const int slot = k * C::kRowsPerInstr + sub;      // row within the page
-          const int r = pp * kPageSize + slot;              // row within the tile
-          const bool valid = phys >= 0 && kbase + r < ctx;
-          const uint16_t* src = valid ? src_page + (size_t)slot * row_elems : pool;
-          cp_async_16(base + r * 128 + (((unit & 7) ^ (r & 7)) << 4), src, valid ? 16u : 0u);
+        for (int pi = 0; pi < kMyPages; ++pi) {
+          const int pp = pw + pi * kProducerWarps;
+          if (pp >= kChunkKeys / kPageSize) break;
+#pragma unroll
+          for (int c = 0; c < CH; ++c)
+            tma_load_3d(stage + c * 16384 + pp * 2048, map, full, c * 64, it.kv_head,
+                        phys[pi] * kPageSize);
         }
+        issued |= 1u << bit;
+        par = (par & ~(1u << bit)) | (ph << bit);
       }
     };
-    int pg_prev = -1, pg_cur = page_of(0), pg_next = page_of(1);
+    int pg_prev = p.num_pages, pg_cur = page_of(0), pg_next = page_of(1);
     bool ok = true;
     for (int j = 0; ok && j <= T; ++j) {
       if (j < T) {
         const int s = j % NK;
-        if (!mbar_wait(&k_empty[s], ((uint32_t)(j / NK) & 1u) ^ 1u, abort_flag)) { ok = false; break; }
-        gather(k_cache, sK + s * C::kTileBytes, j, pg_cur);
-        cp_async_arrive_noinc(&k_full[s]);
+        const uint32_t ph = (uint32_t)(j / NK) & 1u;
+        ok = lane != 0 || mbar_wait(&k_empty[s], ph ^ 1u, abort_flag);
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (!ok) break;
+        tma_tile(&kmap, sK + s * C::kTileBytes, &k_full[s], pg_cur, s, ph);
       }
       if (j >= 1) {
         const int jv = j - 1;
         const int s = jv % NV;
-        if (!mbar_wait(&v_empty[s], ((uint32_t)(jv / NV) & 1u) ^ 1u, abort_flag)) { ok = false; break; }
-        gather(v_cache, sV + s * C::kTileBytes, jv, pg_prev);
-        cp_async_arrive_noinc(&v_full[s]);
+        const uint32_t ph = (uint32_t)(jv / NV) & 1u;
+        ok = lane != 0 || mbar_wait(&v_empty[s], ph ^ 1u, abort_flag);
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (!ok) break;
+        tma_tile(&vmap, sV + s * C::kTileBytes, &v_full[s], pg_prev, NK + s, ph);
       }
       pg_prev = pg_cur;
       pg_cur = pg_next;
       pg_next = page_of(j + 2);
     }
-    // copies in flight must land before the CTA exits
-    asm volatile("cp.async.wait_all;" ::: "memory");
+    if (lane == 0) {
+      // copies in flight must land before the CTA exits
+      for (int b = 0; b < NK + NV; ++b)
+        if (issued & (1u << b))
+          drain_wait(b < NK ? &k_full[b] : &v_full[b - NK], (par >> b) & 1u, abort_flag);
+    }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
@@ -353,10 +363,14 @@ __device__ __forceinline__ void chunk_cta(const ChunkParams& p, const CUtensorMa
         if (masked) {
 #pragma unroll
           for (int i = 0; i < 32; ++i)
-            mxp[i & 7] = fmaxf(mxp[i & 7], (q * 32 + i > lim) ? -INFINITY : __uint_as_float(sr[i]));
-        } else {
+            if (q * 32 + i > lim) sr[i] = __float_as_uint(-INFINITY);
+        }
 #pragma unroll
-          for (int i = 0; i < 32; ++i) mxp[i & 7] = fmaxf(mxp[i & 7], __uint_as_float(sr[i]));
+        for (int i = 0; i < 32; i += 8) {
+          mxp[(i >> 3) & 3] = fmax3(mxp[(i >> 3) & 3], __uint_as_float(sr[i]), __uint_as_float(sr[i + 1]));
+          mxp[4 + ((i >> 3) & 3)] = fmax3(mxp[4 + ((i >> 3) & 3)], __uint_as_float(sr[i + 2]), __uint_as_float(sr[i + 3]));
+          mxp[(i >> 3) & 3] = fmax3(mxp[(i >> 3) & 3], __uint_as_float(sr[i + 4]), __uint_as_float(sr[i + 5]));
+          mxp[4 + ((i >> 3) & 3)] = fmax3(mxp[4 + ((i >> 3) & 3)], __uint_as_float(sr[i + 6]), __uint_as_float(sr[i + 7]));
         }
       }
       if (valid_row) {
@@ -371,7 +385,9 @@ __device__ __forceinline__ void chunk_cta(const ChunkParams& p, const CUtensorMa
       }
       // pass 2: P = 2^(s c - m) as bf16 over the S columns already read
       const float neg_m = valid_row ? -m_run : -INFINITY;   // dead rows: P = 0
-      float lsp[4] = {0.f, 0.f, 0.f, 0.f};
+      const uint64_t c2 = pack_f32x2(sl2, sl2);
+      const uint64_t nm2 = pack_f32x2(neg_m, neg_m);
+      uint64_t lsum2[2] = {pack_f32x2(0.f, 0.f), pack_f32x2(0.f, 0.f)};
 #pragma unroll 1
       for (int q = 0; q < kChunkKeys / 32; ++q) {
         uint32_t sr[32];
@@ -385,13 +401,39 @@ __device__ __forceinline__ void chunk_cta(const ChunkParams& p, const CUtensorMa
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          pk[i] = pack_bf16x2(fast_exp2(fmaf(__uint_as_float(sr[2 * i]), sl2, neg_m)),
-                              fast_exp2(fmaf(__uint_as_float(sr[2 * i + 1]), sl2, neg_m)));
-          lsp[i & 3] += bf16lo_to_f32(pk[i]) + bf16hi_to_f32(pk[i]);
+          float x0, x1;
+          unpack_f32x2(fma_f32x2(pack_f32x2(__uint_as_float(sr[2 * i]), __uint_as_float(sr[2 * i + 1])),
+                                 c2, nm2), x0, x1);
+          pk[i] = pack_bf16x2(fast_exp2(x0), fast_exp2(x1));
+          lsum2[i & 1] = add_f32x2(lsum2[i & 1], bf16x2_to_f32x2(pk[i]));
         }
         tmem_st16(s_col + q * 16, pk);
       }
+      float lsp[4];
+      unpack_f32x2(lsum2[0], lsp[0], lsp[1]);
+      unpack_f32x2(lsum2[1], lsp[2], lsp[3]);
       if (valid_row) l_run = l_run * alpha + ((lsp[0] + lsp[1]) + (lsp[2] + lsp[3]));
+      if (j == T - 1 && t == (TA == T ? 0 : 1)) {
+        // the last page's slots past the context were never written (its TMA
+        // box brings them in as they are): clear those V rows before the
+        // first PV that reads this tile, so that P = 0 never meets a NaN
+        const int kb = j * kChunkKeys;
+        const int first_bad = ctx - kb;
+        const int end_bad = min(kChunkKeys, ((ctx + kPageSize - 1) / kPageSize) * kPageSize - kb);
+        if (first_bad < end_bad) {
+          const int s = j % NV;
+          if (!mbar_wait(&v_full[s], (uint32_t)(j / NV) & 1u, abort_flag)) { ok = false; break; }
+          uint8_t* vt = sV + s * C::kTileBytes;
+          const int n_units = (end_bad - first_bad) * CH * 8;
+          for (int e = row; e < n_units; e += 128) {
+            const int key = first_bad + e / (CH * 8);
+            const int rem = e % (CH * 8);
+            *reinterpret_cast<uint4*>(vt + (rem >> 3) * 16384 + key * 128 + (rem & 7) * 16) =
+                make_uint4(0u, 0u, 0u, 0u);
+          }
+          fence_async_shared();
+        }
+      }
       // O_t is stable here (PV_t(j-1) completed before S_t(j) was ready)
       if (j > 0 && __any_sync(0xffffffffu, resc)) {
         const float f = resc ? alpha : 1.f;
