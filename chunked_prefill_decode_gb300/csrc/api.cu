@@ -23,6 +23,7 @@ __device__ int g_hb_device_error = 0;
 
 namespace hb {
 cudaError_t launch_kv_append(const AppendParams& p, int num_sms, cudaStream_t stream);
+cudaError_t launch_wait_timeout(int* dev_error, cudaStream_t stream);
 cudaError_t launch_attention(const DecodeParams& dec, int decode_grid, const ChunkParams& chk,
                              int head_dim, const CUtensorMap& dec_k, const CUtensorMap& dec_v,
                              const CUtensorMap& chunk_q, const CUtensorMap& chunk_k,
@@ -371,7 +372,7 @@ hb_status hb_plan(const hb_batch* batch, const int32_t* h_q_len,
     // the range within 2% of the best is taken.  Rates measured on GB300.
     constexpr double kHbmBytesPerUs = 7.0e6;      // whole-GPU HBM stream
     constexpr double kSmBytesPerUs = 8.5e4;       // one SM's stream ceiling
-    constexpr double kPairTileUs = 2.7;           // 2-tile item x one key tile
+    constexpr double kPairTileUs = 2.2;           // 2-tile item x one key tile
     constexpr double kSingleTileUs = 2.0;         // 1-tile item x one key tile
     double decode_bytes = 0.0, chunk_us = 0.0, max_item_us = 0.0;
     for (int i = 0; i < S; ++i)
@@ -626,6 +627,20 @@ hb_status hb_check(void* stream) {
     return fail(HB_ERR_TIMEOUT, "a kernel wait gave up (word %d)", v);
   } catch (...) {
     return fail(HB_ERR_CUDA, "unexpected exception in hb_check");
+  }
+}
+
+hb_status hb_selftest_wait_timeout(void* stream) {
+  try {
+    DevState* dev = nullptr;
+    hb_status s = device_state(&dev);
+    if (s != HB_OK) return s;
+    cudaError_t e = launch_wait_timeout(dev->err, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "self-test launch");
+    g_launches.fetch_add(1);
+    return ok();
+  } catch (...) {
+    return fail(HB_ERR_CUDA, "unexpected exception in hb_selftest_wait_timeout");
   }
 }
 

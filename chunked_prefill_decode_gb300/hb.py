@@ -56,6 +56,7 @@ EXPORTED = (
     "hb_builder_create", "hb_builder_destroy", "hb_builder_add_request",
     "hb_builder_step", "hb_builder_complete", "hb_builder_counts",
     "hb_builder_free_list", "hb_builder_last_error", "hb_decode_attention_noalloc",
+    "hb_selftest_wait_timeout",
 )
 
 
@@ -90,6 +91,8 @@ def load():
     L.hb_decode_attention_noalloc.restype = ctypes.c_int
     L.hb_decode_attention_noalloc.argtypes = [P(HbBatch), vp, vp, vp, vp, vp, ctypes.c_float,
                                               vp, vp]
+    L.hb_selftest_wait_timeout.restype = ctypes.c_int
+    L.hb_selftest_wait_timeout.argtypes = [vp]
     L.hb_check.restype = ctypes.c_int
     L.hb_check.argtypes = [vp]
     L.hb_timing_enable.restype = ctypes.c_int
@@ -261,6 +264,10 @@ def hb_decode_attention_noalloc(batch, q_len, context_len, q, k_cache, v_cache, 
 
 def hb_check(stream=None):
     _check(load().hb_check(_stream(stream)))
+
+
+def hb_selftest_wait_timeout(stream=None):
+    _check(load().hb_selftest_wait_timeout(_stream(stream)))
 
 
 def hb_timing_enable(on: bool):

@@ -206,6 +206,15 @@ hb_status hb_decode_attention_noalloc(const hb_batch* batch,
  */
 hb_status hb_check(void* stream);
 
+/*
+ * Self-test of the failure path: launches one CTA that waits on a barrier
+ * nothing arrives at, using the bounded wait every kernel of the library
+ * uses.  After the wait's time limit (about one second) the kernel records a
+ * timeout in the device error word and returns; hb_check() then gives
+ * HB_ERR_TIMEOUT and the CUDA context stays usable.  No fault or hang.
+ */
+hb_status hb_selftest_wait_timeout(void* stream);
+
 /* ---------------------------------------------------------------------------
  * Instrumentation.  When enabled, every kernel launch of this library is
  * bracketed by CUDA events recorded on its launch stream.

@@ -188,3 +188,15 @@ def _full_size(name, n_seq_sample=6, n_chunk_tok=48, seed=None):
 @pytest.mark.parametrize("name", ["mistral_b512", "yi_b2048", "decode_only"])
 def test_full_size_workloads(name):
     _full_size(name)
+
+
+def test_wait_timeout_is_reported_and_context_survives():
+    """A kernel wait that runs out ends the kernel with a status, not a hang:
+    the library's bounded wait on a barrier nothing arrives at."""
+    hb = lib()
+    hb.hb_selftest_wait_timeout()
+    with pytest.raises(hb.HbError) as e:
+        hb.hb_check()
+    assert e.value.status == 7
+    hb.hb_check()                      # the word was cleared
+    _full_check(workloads.tiny(0))     # the context still works
