@@ -25,8 +25,19 @@ __device__ __forceinline__ uint4 ld_stream(const uint4* p) {
   return v;
 }
 
+// cu_q_len is staged in shared memory for batches up to this many sequences
+constexpr int kAppendSmemSeqs = 8191;
+
 __global__ void __launch_bounds__(256) kv_append_kernel(AppendParams p) {
+  extern __shared__ int32_t s_cu[];
   const int lane = threadIdx.x & 31;
+  // the row -> sequence search runs on a shared-memory copy of cu_q_len (one
+  // coalesced load per CTA instead of a chain of dependent global loads)
+  const bool staged = p.num_seqs <= kAppendSmemSeqs;
+  if (staged)
+    for (int i = threadIdx.x; i <= p.num_seqs; i += blockDim.x) s_cu[i] = __ldg(&p.cu_q_len[i]);
+  __syncthreads();
+  const int32_t* cu = staged ? s_cu : p.cu_q_len;
   const int warps_total = gridDim.x * (blockDim.x >> 5);
   const int n_rows = 2 * p.total_q;
   for (int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < n_rows;
@@ -37,11 +48,11 @@ __global__ void __launch_bounds__(256) kv_append_kernel(AppendParams p) {
     int lo = 0, hi = p.num_seqs - 1;
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
-      if (__ldg(&p.cu_q_len[mid]) <= tok) lo = mid; else hi = mid - 1;
+      if (cu[mid] <= tok) lo = mid; else hi = mid - 1;
     }
     const int s = lo;
-    const int q0 = __ldg(&p.cu_q_len[s]);
-    const int q_len = __ldg(&p.cu_q_len[s + 1]) - q0;
+    const int q0 = cu[s];
+    const int q_len = cu[s + 1] - q0;
     const int pos = __ldg(&p.context_len[s]) - q_len + (tok - q0);
     const int lp = pos / kPageSize;
     int page = -1;
@@ -67,7 +78,8 @@ cudaError_t launch_kv_append(const AppendParams& p, int num_sms,
   long blocks = (2L * p.total_q + warps_per_block - 1) / warps_per_block;
   const long cap = 16L * num_sms;
   if (blocks > cap) blocks = cap;
-  kv_append_kernel<<<(unsigned)blocks, 32 * warps_per_block, 0, stream>>>(p);
+  const size_t smem = p.num_seqs <= kAppendSmemSeqs ? (size_t)(p.num_seqs + 1) * 4 : 0;
+  kv_append_kernel<<<(unsigned)blocks, 32 * warps_per_block, smem, stream>>>(p);
   return cudaGetLastError();
 }
 
