@@ -1,7 +1,7 @@
 """Benchmark of one hybrid-batch attention step (KV append + attention).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
-                    [--impl native|reference]
+                    [--impl native|reference] [--sweep chunk]
 
 A step is one pass of the hot path over one synthetic hybrid batch: the KV
 append of the batch's new tokens and the attention of every new token (decode
@@ -17,6 +17,9 @@ step's fraction of its roofline, the CPU oracle timed on a bounded sample, and
 the SM clocks sampled during the timed region.
 
 `--impl reference` times the fp64 CPU oracle instead (rank 0 only).
+`--sweep chunk` prefills one 8192-token prompt in chunks of several sizes,
+with and without decode rows beside each chunk, and prints one JSON line per
+chunk size (the chunk-size sweep; not the step benchmark).
 Under torchrun (N > 1) each rank runs an independent replica of the workload;
 timing is the max over ranks and `value` counts every rank's tokens.
 """
@@ -425,6 +428,81 @@ def run_native(args):
     print(json.dumps(line), flush=True)
 
 
+SWEEP_CHUNKS = (256, 257, 512, 1024, 2048, 8192)
+
+
+def run_chunk_sweep(args):
+    """Prefill of one 8192-token prompt in chunks of c tokens, each chunk in a
+    hybrid batch with 32 decode rows at context 2048, and the same chunks
+    alone.  Per c: the summed step time over all chunks of the prompt (append
+    + attention, L2 flushed before every timed step, median over repetitions),
+    the chunk work's FLOPs and the KV bytes its re-reads of earlier chunks
+    cost.  One JSON line per chunk size; c = 8192 is the unchunked prefill."""
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    import __graft_entry__
+    __graft_entry__.build()
+    from chunked_prefill_decode_gb300 import hb
+    from chunked_prefill_decode_gb300.device import device_batch
+
+    peaks = _peaks()
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    reps = max(3, args.sweep_reps)
+
+    def time_layout(lay):
+        sh = lay.shape
+        ten = workloads.make_tensors(lay, seed=7, device=dev)
+        db = device_batch(lay.q_len, lay.context_len, lay.block_table, lay.num_pages,
+                          sh.num_q_heads, sh.num_kv_heads, sh.head_dim, sh.page_size, dev)
+        plan, ws = hb.hb_plan(db.batch, db.q_len, db.context_len, sms)
+        out = torch.empty_like(ten.q)
+        scale = 1.0 / math.sqrt(sh.head_dim)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(reps + 3)]
+        for e0, e1 in evs:
+            flush.fill_(1)
+            e0.record(stream)
+            hb.hb_kv_append(db.batch, ten.k_new, ten.v_new, ten.k_cache, ten.v_cache)
+            hb.hb_attention(db.batch, plan, ten.q, ten.k_cache, ten.v_cache, scale, out, ws)
+            e1.record(stream)
+        torch.cuda.synchronize(dev)
+        hb.hb_check()
+        return statistics.median(e0.elapsed_time(e1) for e0, e1 in evs[3:])
+
+    rows = []
+    with ClockSampler(0) as clk:
+        for c in SWEEP_CHUNKS:
+            n_chunks = -(-8192 // c)
+            r = {"sweep": "chunk", "chunk": c, "n_chunks": n_chunks, "prefill_ms_with_decodes": 0.0,
+                 "prefill_ms_chunk_only": 0.0, "chunk_flops": 0, "chunk_kv_bytes": 0}
+            for i in range(n_chunks):
+                alone = workloads.chunk_sweep(c, i, n_decode=0)
+                cnt = algorithmic_counts(alone)
+                r["chunk_flops"] += cnt["chunk_flops"]
+                r["chunk_kv_bytes"] += cnt["chunk_bytes"]
+                r["prefill_ms_chunk_only"] += time_layout(alone)
+                r["prefill_ms_with_decodes"] += time_layout(workloads.chunk_sweep(c, i))
+            t = r["prefill_ms_chunk_only"] * 1e-3
+            r["chunk_only_tflops"] = r["chunk_flops"] / t / 1e12
+            r["chunk_only_tc_frac"] = r["chunk_only_tflops"] / peaks["bf16_tflops"]
+            r["decode_ms_per_iteration"] = (r["prefill_ms_with_decodes"] -
+                                            r["prefill_ms_chunk_only"]) / n_chunks
+            rows.append(r)
+    base = rows[-1]
+    clocks = clk.summary()
+    for r in rows:
+        r["chunk_only_vs_unchunked"] = r["prefill_ms_chunk_only"] / base["prefill_ms_chunk_only"]
+        r["with_decodes_vs_unchunked"] = (r["prefill_ms_with_decodes"] /
+                                          base["prefill_ms_with_decodes"])
+        r["peak"] = {"bf16_tflops": peaks["bf16_tflops"], "source": peaks["source"]}
+        r["l2"] = "flushed before every timed step (%d MB written)" % (flush.numel() >> 20)
+        r["reps"] = reps
+        r["clocks"] = clocks
+        print(json.dumps(r), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -433,8 +511,14 @@ def main():
     ap.add_argument("--workload", default="mistral_b512", choices=sorted(workloads.WORKLOADS))
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--sweep", choices=["chunk"], default=None,
+                    help="instead of the step benchmark: prefill one 8192-token prompt "
+                         "in chunks of 256/257/512/1024/2048/8192 tokens")
+    ap.add_argument("--sweep-reps", type=int, default=10)
     args = ap.parse_args()
-    if args.impl == "reference":
+    if args.sweep == "chunk":
+        run_chunk_sweep(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_native(args)

@@ -61,6 +61,8 @@ constexpr int kProducerWarp0 = 9;
 constexpr int kProducerWarps = 3;
 constexpr int kProducerThreads = 32 * kProducerWarps;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
+constexpr int kSoftmaxRegs = 176;   // per thread, softmax warpgroups (warps 0-7)
+constexpr int kLightRegs = 152;     // per thread, MMA + producer warpgroup (8-11)
 
 template <int D>
 struct ChunkCfg {
@@ -154,6 +156,11 @@ __device__ __forceinline__ void chunk_cta(const ChunkParams& p, const CUtensorMa
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_holder;
+  // registers move from the MMA / producer warpgroup (warps 8-11) to the two
+  // softmax warpgroups, which hold a whole S row: 2 x 128 x 176 + 128 x 152 =
+  // 384 x 168, the CTA's launch allocation
+  if (warp >= kMmaWarp) setmaxnreg_dec<kLightRegs>();
+  else setmaxnreg_inc<kSoftmaxRegs>();
 
   if (warp >= kProducerWarp0) {
     // ------------------------------------------------------------ producers
@@ -351,27 +358,25 @@ __device__ __forceinline__ void chunk_cta(const ChunkParams& p, const CUtensorMa
       float alpha = 1.f;
       bool resc = false;
       // tcgen05.ld / tcgen05.st are warp-collective: every lane executes each
-      // of them; rows that hold no query only change the arithmetic (P = 0)
+      // of them; rows that hold no query only change the arithmetic (P = 0).
+      // The whole 128-column S row comes in with one wait.
+      uint32_t sr[kChunkKeys];
+#pragma unroll
+      for (int q = 0; q < kChunkKeys / 32; ++q) tmem_ld32(s_col + q * 32, sr + q * 32);
+      tmem_ld_wait();
+      if (masked) {
+#pragma unroll
+        for (int i = 0; i < kChunkKeys; ++i)
+          if (i > lim) sr[i] = __float_as_uint(-INFINITY);
+      }
       float mxp[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) mxp[i] = -INFINITY;
-#pragma unroll 1
-      for (int q = 0; q < kChunkKeys / 32; ++q) {
-        uint32_t sr[32];
-        tmem_ld32(s_col + q * 32, sr);
-        tmem_ld_wait();
-        if (masked) {
+      for (int u = 0; u < 8; ++u) mxp[u] = -INFINITY;
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if (q * 32 + i > lim) sr[i] = __float_as_uint(-INFINITY);
-        }
+      for (int i = 0; i < kChunkKeys; i += 16) {
 #pragma unroll
-        for (int i = 0; i < 32; i += 8) {
-          mxp[(i >> 3) & 3] = fmax3(mxp[(i >> 3) & 3], __uint_as_float(sr[i]), __uint_as_float(sr[i + 1]));
-          mxp[4 + ((i >> 3) & 3)] = fmax3(mxp[4 + ((i >> 3) & 3)], __uint_as_float(sr[i + 2]), __uint_as_float(sr[i + 3]));
-          mxp[(i >> 3) & 3] = fmax3(mxp[(i >> 3) & 3], __uint_as_float(sr[i + 4]), __uint_as_float(sr[i + 5]));
-          mxp[4 + ((i >> 3) & 3)] = fmax3(mxp[4 + ((i >> 3) & 3)], __uint_as_float(sr[i + 6]), __uint_as_float(sr[i + 7]));
-        }
+        for (int u = 0; u < 8; ++u)
+          mxp[u] = fmax3(mxp[u], __uint_as_float(sr[i + 2 * u]), __uint_as_float(sr[i + 2 * u + 1]));
       }
       if (valid_row) {
         const float mx = fmaxf(fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3])),
@@ -383,26 +388,20 @@ __device__ __forceinline__ void chunk_cta(const ChunkParams& p, const CUtensorMa
           resc = true;
         }
       }
-      // pass 2: P = 2^(s c - m) as bf16 over the S columns already read
+      // P = 2^(s c - m) as bf16, written over the S columns (all of S is in
+      // registers by now)
       const float neg_m = valid_row ? -m_run : -INFINITY;   // dead rows: P = 0
       const uint64_t c2 = pack_f32x2(sl2, sl2);
       const uint64_t nm2 = pack_f32x2(neg_m, neg_m);
       uint64_t lsum2[2] = {pack_f32x2(0.f, 0.f), pack_f32x2(0.f, 0.f)};
-#pragma unroll 1
-      for (int q = 0; q < kChunkKeys / 32; ++q) {
-        uint32_t sr[32];
-        tmem_ld32(s_col + q * 32, sr);
-        tmem_ld_wait();
-        if (masked) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if (q * 32 + i > lim) sr[i] = __float_as_uint(-INFINITY);
-        }
+      for (int q = 0; q < kChunkKeys / 32; ++q) {
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           float x0, x1;
-          unpack_f32x2(fma_f32x2(pack_f32x2(__uint_as_float(sr[2 * i]), __uint_as_float(sr[2 * i + 1])),
+          unpack_f32x2(fma_f32x2(pack_f32x2(__uint_as_float(sr[q * 32 + 2 * i]),
+                                            __uint_as_float(sr[q * 32 + 2 * i + 1])),
                                  c2, nm2), x0, x1);
           pk[i] = pack_bf16x2(fast_exp2(x0), fast_exp2(x1));
           lsum2[i & 1] = add_f32x2(lsum2[i & 1], bf16x2_to_f32x2(pk[i]));

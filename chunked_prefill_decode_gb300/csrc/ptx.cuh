@@ -205,6 +205,21 @@ __device__ __forceinline__ void mma_bf16_16816(float* c, const uint32_t* a,
 }
 
 // max(a, b, c) in one instruction.
+// Register re-balancing between warpgroups (all four warps of a warpgroup
+// execute it).  `dec` returns registers to the CTA's pool, `inc` waits until
+// the pool holds enough; the counts of all warpgroups must add up to at most
+// the registers the CTA was launched with.
+template <int N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  static_assert(N % 8 == 0 && N >= 24 && N <= 256, "setmaxnreg count");
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  static_assert(N % 8 == 0 && N >= 24 && N <= 256, "setmaxnreg count");
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float d;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));

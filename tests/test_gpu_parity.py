@@ -142,8 +142,9 @@ def test_timing_and_launch_count():
 
 
 # ---------------------------------------------------------------- full size
-def _full_size(name, n_seq_sample=6, n_chunk_tok=48, seed=None):
-    lay = workloads.WORKLOADS[name]()
+def _full_size(name, n_seq_sample=6, n_chunk_tok=48, seed=None, lay=None):
+    if lay is None:
+        lay = workloads.WORKLOADS[name]()
     seed = {"mistral_b512": 1, "yi_b2048": 2, "decode_only": 3}.get(name, 0) if seed is None else seed
     ten = workloads.make_tensors(lay, seed, device="cuda")
     kc, vc, out = gpu_step(lay, ten)
@@ -188,6 +189,16 @@ def _full_size(name, n_seq_sample=6, n_chunk_tok=48, seed=None):
 @pytest.mark.parametrize("name", ["mistral_b512", "yi_b2048", "decode_only"])
 def test_full_size_workloads(name):
     _full_size(name)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("chunk,index", [(256, 31), (257, 0), (257, 31), (512, 7),
+                                         (1024, 5), (2048, 3), (8192, 0)])
+def test_chunk_sweep_batches(chunk, index):
+    """The chunk-size sweep's batches: chunk `index` of an 8192-token prompt
+    beside 32 decode rows at context 2048 (257 leaves a ragged last chunk of
+    225 tokens and chunks that straddle pages)."""
+    _full_size(None, seed=4, lay=workloads.chunk_sweep(chunk, index))
 
 
 def test_wait_timeout_is_reported_and_context_survives():
