@@ -362,8 +362,7 @@ def run_native(args):
         e2e_step()
     torch.cuda.synchronize(dev)
     e2e_s = max_over_ranks(time.perf_counter() - t0, n)
-    plan_bytes = int(hb.plan_header(plan)["num_decode_items"]) * 48 + \
-        int(hb.plan_header(plan)["num_chunk_items"]) * 32
+    plan_bytes = int(hb.plan_header(plan)["items_bytes"])
     e2e = {"value": n * T * e2e_steps / e2e_s, "unit": "tokens/s",
            "h2d_bytes_per_step": h2d + plan_bytes, "d2h_bytes_per_step": d2h}
 

@@ -11,7 +11,9 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <functional>
 #include <mutex>
+#include <queue>
 #include <string>
 #include <vector>
 
@@ -362,46 +364,135 @@ hb_status hb_plan(const hb_batch* batch, const int32_t* h_q_len,
       return a.kv_tiles > b.kv_tiles;
     });
 
-    // ---- how many CTAs stream the decode rows.  The attention kernel runs
-    // decode CTAs and chunk CTAs side by side (one CTA per SM); SMs that end
-    // their decode range go on to chunk items.  Estimated end time with G
-    // decode CTAs: decode takes its bytes over min(HBM rate, G x one SM's
+    // ---- cost model, in microseconds, from rates measured on GB300.  The
+    // attention kernel runs decode CTAs and chunk CTAs side by side (one CTA
+    // per SM); SMs that end their decode range go on to chunk items.  With G
+    // decode CTAs, decode takes its bytes over min(HBM rate, G x one SM's
     // stream rate); everything ends no earlier than (chunk work + G x decode
     // time) / SMs, nor before the longest chunk item.  That estimate is flat
     // over a range of G whose ends it knows only roughly, so the middle of
-    // the range within 2% of the best is taken.  Rates measured on GB300.
+    // the range within 2% of the best is taken.
     constexpr double kHbmBytesPerUs = 7.0e6;      // whole-GPU HBM stream
     constexpr double kSmBytesPerUs = 8.5e4;       // one SM's stream ceiling
-    constexpr double kPairTileUs = 2.2;           // 2-tile item x one key tile
-    constexpr double kSingleTileUs = 2.0;         // 1-tile item x one key tile
-    double decode_bytes = 0.0, chunk_us = 0.0, max_item_us = 0.0;
+    constexpr double kPairTileUs = 2.0;           // 2-tile item x one key tile
+    constexpr double kSingleTileUs = 1.1;         // 1-tile item x one key tile
+    constexpr double kPieceUs = 3.0;              // extra cost of one split piece
+    constexpr int kMinPieceTiles = 4;             // key tiles per split piece (min)
+    const double tile_us = tiles_per_item == 2 ? kPairTileUs : kSingleTileUs;
+    double decode_bytes = 0.0;
     for (int i = 0; i < S; ++i)
       if (h_q_len[i] == 1) decode_bytes += (double)h_context_len[i] * Hkv * D * 4.0;
+    auto t_decode = [&](int G) {
+      return decode_bytes / std::min(kHbmBytesPerUs, G * kSmBytesPerUs);
+    };
+    auto pick_decode = [&](double chunk_us, double max_item_us) -> int {
+      if (decode_bytes <= 0.0) return 0;
+      if (chunk_us <= 0.0) return num_sms;
+      std::vector<double> t(num_sms + 1, 0.0);
+      double best = 1e300;
+      for (int G = 1; G <= num_sms; ++G) {
+        const double td = t_decode(G);
+        t[G] = std::max({td, (chunk_us + G * td) / num_sms, max_item_us});
+        best = std::min(best, t[G]);
+      }
+      int lo = 0, hi = 0;
+      for (int G = 1; G <= num_sms; ++G)
+        if (t[G] <= 1.02 * best) {
+          if (!lo) lo = G;
+          hi = G;
+        }
+      return (lo + hi) / 2;
+    };
+    // pieces per item when each piece holds about L key tiles
+    auto pieces_of = [&](int kv, int L) {
+      int n = std::min(kMaxChunkSplits, (kv + L - 1) / L);
+      return std::max(1, std::min(n, kv / kMinPieceTiles));
+    };
+    // end time of the launch: CTAs start in index order on the SM that frees
+    // up first; the G decode CTAs come first and hold their SMs for the
+    // decode time
+    auto simulate = [&](const std::vector<double>& durs, int G) {
+      std::priority_queue<double, std::vector<double>, std::greater<double>> free_at;
+      const double td = G > 0 ? t_decode(G) : 0.0;
+      for (int i = 0; i < num_sms; ++i) free_at.push(i < G ? td : 0.0);
+      double end = td;
+      for (double d : durs) {
+        const double t0 = free_at.top();
+        free_at.pop();
+        free_at.push(t0 + d);
+        end = std::max(end, t0 + d);
+      }
+      return end;
+    };
+
+    // ---- split-KV: when single query tiles are too few to fill the SMs, a
+    // tile's key range may be cut into up to kMaxChunkSplits pieces (each its
+    // own CTA, merged by the last to finish).  The piece length is the one
+    // with the earliest estimated end among a few candidates (no split
+    // included).
+    int best_L = 0;   // 0: no split
+    if (tiles_per_item == 1 && !chk.empty()) {
+      const int kmax = chk.front().kv_tiles;
+      double best_t = 1e300;
+      int prev_L = -1;
+      for (int n = 1; n <= kMaxChunkSplits; ++n) {
+        const int L = (kmax + n - 1) / n;
+        if (L == prev_L || (n > 1 && L < kMinPieceTiles)) continue;
+        prev_L = L;
+        std::vector<double> durs;
+        double sum = 0.0, mx = 0.0;
+        for (const ChunkItem& c : chk) {
+          const int np = pieces_of(c.kv_tiles, L);
+          for (int k = 0; k < np; ++k) {
+            const int len = (k + 1) * c.kv_tiles / np - k * c.kv_tiles / np;
+            const double d = len * tile_us + (np > 1 ? kPieceUs : 0.0);
+            durs.push_back(d);
+            sum += d;
+            mx = std::max(mx, d);
+          }
+        }
+        if (n > 1 && durs.size() > (size_t)(2 * num_sms)) break;   // at most two waves
+        std::sort(durs.begin(), durs.end(), std::greater<double>());
+        const double t = simulate(durs, pick_decode(sum, mx));
+        if (t < 0.97 * best_t) {   // a split has to pay for itself clearly
+          best_t = t;
+          best_L = n == 1 ? 0 : L;
+        }
+      }
+    }
+    int n_cslots = 0, n_cmerge = 0;
+    {
+      std::vector<ChunkItem> out;
+      for (ChunkItem c : chk) {
+        const int np = best_L > 0 ? pieces_of(c.kv_tiles, best_L) : 1;
+        const int kv = c.kv_tiles;
+        c.n_splits = np;
+        c.slot = np > 1 ? n_cslots : 0;
+        c.merge_id = np > 1 ? n_cmerge : 0;
+        for (int k = 0; k < np; ++k) {
+          c.split = k;
+          c.kv_begin = k * kv / np;
+          c.kv_tiles = (k + 1) * kv / np;
+          out.push_back(c);
+        }
+        if (np > 1) {
+          n_cslots += np;
+          n_cmerge += 1;
+        }
+      }
+      // longest first, so that short pieces fill the end of the launch
+      std::stable_sort(out.begin(), out.end(), [](const ChunkItem& a, const ChunkItem& b) {
+        return a.kv_tiles - a.kv_begin > b.kv_tiles - b.kv_begin;
+      });
+      chk.swap(out);
+    }
+    double chunk_us = 0.0, max_item_us = 0.0;
     for (const ChunkItem& c : chk) {
-      const double us = c.kv_tiles * (tiles_per_item == 2 ? kPairTileUs : kSingleTileUs);
+      const double us = (c.kv_tiles - c.kv_begin) * tile_us + (c.n_splits > 1 ? kPieceUs : 0.0);
       chunk_us += us;
       max_item_us = std::max(max_item_us, us);
     }
-    int decode_ctas = 0;
-    if (decode_bytes > 0.0) {
-      decode_ctas = num_sms;
-      if (!chk.empty()) {
-        std::vector<double> t(num_sms + 1, 0.0);
-        double best = 1e300;
-        for (int G = 1; G <= num_sms; ++G) {
-          const double t_dec = decode_bytes / std::min(kHbmBytesPerUs, G * kSmBytesPerUs);
-          t[G] = std::max({t_dec, (chunk_us + G * t_dec) / num_sms, max_item_us});
-          best = std::min(best, t[G]);
-        }
-        int lo = 0, hi = 0;
-        for (int G = 1; G <= num_sms; ++G)
-          if (t[G] <= 1.02 * best) {
-            if (!lo) lo = G;
-            hi = G;
-          }
-        decode_ctas = (lo + hi) / 2;
-      }
-    }
+    const int decode_ctas = pick_decode(chunk_us, max_item_us);
 
     // ---- decode items: the decode rows' pages, end to end, cut into one
     // equal contiguous range per CTA, each range cut at row boundaries
@@ -430,7 +521,11 @@ hb_status hb_plan(const hb_batch* batch, const int32_t* h_q_len,
     const size_t ws_counters = items_bytes;
     const size_t ws_partial_o = align_up(ws_counters + (size_t)(kCounterMerge0 + n_merge) * 4, 256);
     const size_t ws_partial_ml = align_up(ws_partial_o + (size_t)n_slots * Hq * D * 4, 256);
-    const size_t ws_total = std::max<size_t>(256, align_up(ws_partial_ml + (size_t)n_slots * Hq * 8, 256));
+    const size_t ws_chunk_counters = align_up(ws_partial_ml + (size_t)n_slots * Hq * 8, 256);
+    const size_t ws_chunk_o = align_up(ws_chunk_counters + (size_t)n_cmerge * 4, 256);
+    const size_t ws_chunk_ml = align_up(ws_chunk_o + (size_t)n_cslots * D * kChunkRows * 4, 256);
+    const size_t ws_total =
+        std::max<size_t>(256, align_up(ws_chunk_ml + (size_t)n_cslots * 2 * kChunkRows * 4, 256));
 
     const size_t have_plan = *plan_bytes, have_ws = *workspace_bytes;
     *plan_bytes = need_plan;
@@ -464,6 +559,11 @@ hb_status hb_plan(const hb_batch* batch, const int32_t* h_q_len,
     h.ws_decode_offsets = offsets_at;
     h.decode_kvh_block = kvhb;
     h.chunk_tokens_per_tile = tpt;
+    h.num_chunk_slots = n_cslots;
+    h.num_chunk_merges = n_cmerge;
+    h.ws_chunk_counters = ws_chunk_counters;
+    h.ws_chunk_o = ws_chunk_o;
+    h.ws_chunk_ml = ws_chunk_ml;
     h.items_bytes = items_bytes;
     h.ws_counters = ws_counters;
     h.ws_partial_o = ws_partial_o;
@@ -486,6 +586,11 @@ hb_status hb_plan(const hb_batch* batch, const int32_t* h_q_len,
     e = cudaMemsetAsync(static_cast<uint8_t*>(d_workspace) + ws_counters, 0,
                         ws_partial_o - ws_counters, st);
     if (e != cudaSuccess) return cuda_fail(e, "workspace counter reset");
+    if (n_cmerge > 0) {
+      e = cudaMemsetAsync(static_cast<uint8_t*>(d_workspace) + ws_chunk_counters, 0,
+                          ws_chunk_o - ws_chunk_counters, st);
+      if (e != cudaSuccess) return cuda_fail(e, "workspace counter reset");
+    }
     return ok();
   } catch (...) {
     return fail(HB_ERR_CUDA, "unexpected exception in hb_plan");
@@ -594,6 +699,9 @@ hb_status hb_attention(const hb_batch* batch, const void* h_plan, const void* q,
       cp.tokens_per_tile = tpt;
       cp.scale_log2 = scale_log2;
       cp.dev_error = dev->err;
+      cp.counters = reinterpret_cast<int32_t*>(ws + h.ws_chunk_counters);
+      cp.part_o = reinterpret_cast<float*>(ws + h.ws_chunk_o);
+      cp.part_ml = reinterpret_cast<float*>(ws + h.ws_chunk_ml);
     }
     if (h.num_decode_items > 0 || h.num_chunk_items > 0) {
       LaunchTimer t(1, st);

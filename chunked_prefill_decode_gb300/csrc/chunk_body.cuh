@@ -11,45 +11,54 @@
 //
 // A query tile is 128 rows of (token, q head) pairs of one kv head's GQA
 // group: tokens_per_tile = 128 / g tokens times the g heads, so a K/V tile in
-// shared memory serves the whole group.  One CTA takes one work item: two
-// consecutive query tiles, A and B (B may be short or absent), which share
-// every 128-key K/V tile; the CTA walks the key tiles 0 .. (last position of
-// B) of its sequence, A stopping at its own last position.
+// shared memory serves the whole group.  One CTA takes one work item over key
+// tiles kv_begin .. kv_tiles-1 of its sequence, in one of two modes:
+//   pair:        two consecutive query tiles, A and B (B may be short), that
+//                share every 128-key K/V tile; A stops at its own last
+//                position.  Used when there are enough tiles to fill the SMs.
+//   interleaved: one query tile; the even key tiles go to half 0 (S_0, O_0,
+//                softmax warps 0-3) and the odd ones to half 1 (S_1, O_1,
+//                warps 4-7), so one half's softmax overlaps the other half's
+//                MMAs; at the end warps 0-3 merge the two partial softmax
+//                states.  A tile whose key range is split over several CTAs
+//                (split-KV) publishes its state to the workspace instead,
+//                and the last piece to finish merges all pieces.
 //
 // Warp roles (384 threads):
-//   warps 0-3  softmax of tile A, warps 4-7 softmax of tile B: thread = query
-//              row = TMEM lane (warp w owns lanes 32 (w % 4) ..).  Per key
-//              tile, pass 1 reads S in 32-column pieces (tcgen05.ld) for the
-//              row maximum, with the causal mask only on tiles that cross the
-//              diagonal; pass 2 re-reads them, forms p = 2^(s c - m) with one
-//              FFMA + EX2 (c = scale * log2 e), rounds to bf16 and writes P
-//              into the S columns it has already consumed (tcgen05.st); the
-//              row sum uses the same rounded P.  O is rescaled in TMEM only
-//              when a row maximum grows by more than 2^8 (a stale maximum
-//              stays exact while it bounds P, and P <= 2^8 is safe); epilogue
-//              O / l to bf16.
+//   warps 0-3, 4-7  softmax of half 0 and half 1 (tile A and tile B in pair
+//              mode): thread = query row = TMEM lane (warp w owns lanes
+//              32 (w % 4) ..).  Per key tile the whole 128-column S row is
+//              read with one wait (tcgen05.ld), masked causally only on tiles
+//              that cross the diagonal, reduced to its maximum, and turned
+//              into p = 2^(s c - m) with one FFMA + EX2 (c = scale * log2 e),
+//              rounded to bf16 and written over the S columns (tcgen05.st);
+//              the row sum uses the same rounded P.  O is rescaled in TMEM
+//              only when a row maximum grows by more than 2^8 (a stale
+//              maximum stays exact while it bounds P, and P <= 2^8 is safe);
+//              epilogue O / l to bf16.  These warps hold 176 registers (the
+//              MMA / producer warpgroup gives up 16 with setmaxnreg).
 //   warp 8     TMEM owner and MMA issuer (one thread): Q tiles by TMA (3-D map
-//              over q, box 64 x g x tokens); then, ping-ponging the two tiles,
-//              PV_A(j), QK_A(j+1), PV_B(j), QK_B(j+1), ... so that the tensor
-//              cores work on one tile while the other tile's softmax runs.
-//              S = Q K^T (M 128, N 128, K D, both operands K-major in shared
-//              memory); O += P V (M 128, N D, K 128) with P read from TMEM and
-//              V read MN-major.  QK_t(j) is issued after PV_t(j-1), and the
-//              tensor pipe runs one thread's MMAs in order, so "S_t(j) ready"
-//              also means PV_t(j-1) is done: the softmax may then rescale O_t
-//              and P_t may live in the S_t columns.
+//              over q, box 64 x g x tokens); S = Q K^T (M 128, N 128, K D,
+//              both operands K-major in shared memory); O += P V (M 128, N D,
+//              K 128) with P read from TMEM and V read MN-major.  A half's
+//              next QK is issued after its PV, and the tensor pipe runs one
+//              thread's MMAs in order, so "S ready" also means that half's
+//              previous PV is done: the softmax may then rescale O and P may
+//              live in the S columns.
 //   warps 9-11 producers: fetch each 128-key K or V tile as its eight
 //              16-token pages, one TMA box per page and 64-column head-dim
-//              chunk (2 KB), coordinates from the block table; each warp's
-//              lane 0 issues the boxes of its pages, so three threads share
-//              the per-box issue cost.  Pages past the context are fetched out
+//              chunk (2 KB), coordinates from the block table (read a
+//              batch of four key tiles ahead); the lanes of the three warps
+//              issue the boxes side by side.  Pages past the context are fetched out
 //              of range (zeros); the unwritten tail slots of the last page
 //              are zeroed in V by the softmax group that reads that tile
 //              first.  K runs one tile ahead of V.
-// TMEM (512 columns): S_A 0-127, S_B 128-255, O_A 256-(256+D), O_B after it.
+// TMEM (512 columns): S_0 0-127, S_1 128-255, O_0 256-(256+D), O_1 after it.
 #pragma once
 
 #include <cuda_runtime.h>
+
+#include <climits>
 
 #include "hb_internal.h"
 #include "ptx.cuh"
@@ -126,8 +135,16 @@ __device__ __forceinline__ void chunk_cta(const ChunkParams& p, const CUtensorMa
   const int ntokA = min(tpt, it.ntok);
   const int ntokB = it.ntok - ntokA;
   const bool hasB = ntokB > 0;
-  const int T = it.kv_tiles;              // key tiles of the later tile
-  const int TA = (off + it.tok0 + ntokA + kChunkKeys - 1) / kChunkKeys;
+  // key tiles jb .. T-1 of this item; tile A ends at TA.  Stage and phase
+  // counters below run over r = j - jb.
+  const int jb = it.kv_begin;
+  const int T = it.kv_tiles;
+  const int TA = min(T, (off + it.tok0 + ntokA + kChunkKeys - 1) / kChunkKeys);
+  const int n_all = T - jb;
+  const int nA = TA - jb;
+  // one query tile: the two softmax groups take alternate key tiles of it
+  // (even: S_0/O_0, odd: S_1/O_1) and merge their states at the end
+  const bool inter = !hasB;
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
@@ -141,7 +158,7 @@ __device__ __forceinline__ void chunk_cta(const ChunkParams& p, const CUtensorMa
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&s_full[t], 1);
-      mbar_init(&p_full[t], 128);
+      mbar_init(&p_full[t], inter ? 2 * kChunkRows : kChunkRows);   // softmax threads per S tile
       mbar_init(&o_done[t], 1);
     }
     mbar_init(mma_done, 1);
@@ -165,61 +182,68 @@ __device__ __forceinline__ void chunk_cta(const ChunkParams& p, const CUtensorMa
   if (warp >= kProducerWarp0) {
     // ------------------------------------------------------------ producers
     // Each of the three producer warps owns pages pw, pw + 3, pw + 6 of every
-    // tile and its lane 0 issues their TMA boxes (one 16-token x 64-column box
-    // per page and head-dim chunk, 2 KB each): spreading the issue over three
-    // threads hides the per-box issue latency.  Lane l < 8 holds the physical
-    // page of page l of a tile; pages past the context are fetched out of
-    // range, i.e. as zeros.
+    // tile; its lanes issue their TMA boxes side by side, one box each (a
+    // 16-token x 64-column box per page and head-dim chunk, 2 KB).
     const int pw = warp - kProducerWarp0;
     const int n_pages = (ctx + kPageSize - 1) / kPageSize;
     const int32_t* bt_row = p.block_table + (size_t)it.seq * p.max_pages_per_seq;
-    auto page_of = [&](int j) -> int {   // lane l: page l of tile j
-      const int lp = j * (kChunkKeys / kPageSize) + (lane & 7);
-      int phys = p.num_pages;
-      if (lp < n_pages) {
-        phys = (lp < p.max_pages_per_seq) ? __ldg(&bt_row[lp]) : -1;
-        if (phys < 0 || phys >= p.num_pages) {
-          if (lane < 8) report_error(p.dev_error, HB_DEVERR_INDEX);
-          phys = p.num_pages;
-        }
-      }
-      return phys;
+    constexpr int kPagesPerTile = kChunkKeys / kPageSize;
+    constexpr int kTilesPerBatch = 32 / kPagesPerTile;
+    // Block-table entries arrive 32 at a time, one batch of key tiles ahead
+    // of their use: lane l holds the entry of page l of the batch (raw; it is
+    // checked where it is used, so no instruction waits on the load before
+    // then).  Pages past the context are marked and fetched out of range,
+    // i.e. as zeros.
+    constexpr int kPastContext = INT_MIN;
+    auto load_batch = [&](int b) -> int {
+      const int lp = (jb + b * kTilesPerBatch) * kPagesPerTile + lane;
+      if (lp >= n_pages) return kPastContext;
+      return lp < p.max_pages_per_seq ? __ldg(&bt_row[lp]) : -1;
     };
-    constexpr int kMyPages = (kChunkKeys / kPageSize + kProducerWarps - 1) / kProducerWarps;
+    auto phys_of = [&](int raw) -> int {
+      if (raw == kPastContext) return p.num_pages;
+      if ((unsigned)raw >= (unsigned)p.num_pages) {
+        report_error(p.dev_error, HB_DEVERR_INDEX);
+        return p.num_pages;
+      }
+      return raw;
+    };
     int my_pages = 0;
-    for (int pp = pw; pp < kChunkKeys / kPageSize; pp += kProducerWarps) ++my_pages;
+    for (int pp = pw; pp < kPagesPerTile; pp += kProducerWarps) ++my_pages;
+    // lane l < my_pages * CH issues one box: page pw + 3 (l / CH), chunk l % CH
+    const int pp_l = pw + (lane / CH) * kProducerWarps;
+    const int c_l = lane % CH;
+    const bool issuer = lane < my_pages * CH;
     uint32_t issued = 0, par = 0;   // bit s: stage s (K in 0..NK-1, V from NK)
-    auto tma_tile = [&](const CUtensorMap* map, uint8_t* stage, uint64_t* full, int pages,
-                        int bit, uint32_t ph) {
-      int phys[kMyPages];
-#pragma unroll
-      for (int pi = 0; pi < kMyPages; ++pi)
-        phys[pi] = __shfl_sync(0xffffffffu, pages, (pw + pi * kProducerWarps) & 7);
+    auto tma_tile = [&](const CUtensorMap* map, uint8_t* stage, uint64_t* full, int batch_reg,
+                        int jt, int bit, uint32_t ph) {
+      const int raw = __shfl_sync(0xffffffffu, batch_reg,
+                                  ((jt % kTilesPerBatch) * kPagesPerTile + (pp_l & 7)) & 31);
+      if (lane == 0) mbar_arrive_expect_tx(full, (uint32_t)(my_pages * CH * 2048));
+      __syncwarp();
+      if (issuer)
+        tma_load_3d(stage + c_l * 16384 + pp_l * 2048, map, full, c_l * 64, it.kv_head,
+                    phys_of(raw) * kPageSize);
       if (lane == 0) {
-        mbar_arrive_expect_tx(full, (uint32_t)(my_pages * CH * 2048));
-#pragma unroll
-        for (int pi = 0; pi < kMyPages; ++pi) {
-          const int pp = pw + pi * kProducerWarps;
-          if (pp >= kChunkKeys / kPageSize) break;
-#pragma unroll
-          for (int c = 0; c < CH; ++c)
-            tma_load_3d(stage + c * 16384 + pp * 2048, map, full, c * 64, it.kv_head,
-                        phys[pi] * kPageSize);
-        }
         issued |= 1u << bit;
         par = (par & ~(1u << bit)) | (ph << bit);
       }
     };
-    int pg_prev = p.num_pages, pg_cur = page_of(0), pg_next = page_of(1);
+    int bt_prev = kPastContext, bt_cur = load_batch(0), bt_next = load_batch(1);
     bool ok = true;
-    for (int j = 0; ok && j <= T; ++j) {
-      if (j < T) {
+    for (int j = 0; ok && j <= n_all; ++j) {   // j: tile jb + j
+      if (j > 0 && j % kTilesPerBatch == 0) {
+        bt_prev = bt_cur;
+        bt_cur = bt_next;
+        bt_next = load_batch(j / kTilesPerBatch + 1);
+      }
+      if (j < n_all) {
         const int s = j % NK;
         const uint32_t ph = (uint32_t)(j / NK) & 1u;
         ok = lane != 0 || mbar_wait(&k_empty[s], ph ^ 1u, abort_flag);
         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
         if (!ok) break;
-        tma_tile(&kmap, sK + s * C::kTileBytes, &k_full[s], pg_cur, s, ph);
+        tma_tile(&kmap, sK + s * C::kTileBytes, &k_full[s], bt_cur, j, s, ph);
       }
       if (j >= 1) {
         const int jv = j - 1;
@@ -228,11 +252,9 @@ __device__ __forceinline__ void chunk_cta(const ChunkParams& p, const CUtensorMa
         ok = lane != 0 || mbar_wait(&v_empty[s], ph ^ 1u, abort_flag);
         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
         if (!ok) break;
-        tma_tile(&vmap, sV + s * C::kTileBytes, &v_full[s], pg_prev, NK + s, ph);
+        const int breg = (jv / kTilesPerBatch == j / kTilesPerBatch) ? bt_cur : bt_prev;
+        tma_tile(&vmap, sV + s * C::kTileBytes, &v_full[s], breg, jv, NK + s, ph);
       }
-      pg_prev = pg_cur;
-      pg_cur = pg_next;
-      pg_next = page_of(j + 2);
     }
     if (lane == 0) {
       // copies in flight must land before the CTA exits
@@ -259,9 +281,10 @@ __device__ __forceinline__ void chunk_cta(const ChunkParams& p, const CUtensorMa
       const uint32_t aQ = smem_u32(sQ);
       const uint32_t aK = smem_u32(sK);
       const uint32_t aV = smem_u32(sV);
-      auto qk = [&](int t, int j) {
+      // S_t = Q_qt K(j)^T
+      auto qk = [&](int t, int qt, int j) {
         const uint32_t kb = aK + (j % NK) * C::kTileBytes;
-        const uint32_t qb = aQ + t * C::kTileBytes;
+        const uint32_t qb = aQ + qt * C::kTileBytes;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t koff = (kk >> 2) * 16384 + (kk & 3) * 32;
@@ -270,14 +293,15 @@ __device__ __forceinline__ void chunk_cta(const ChunkParams& p, const CUtensorMa
         }
         tc_commit(&s_full[t]);
       };
-      auto pv = [&](int t, int j) {
+      // O_t (+)= P_t V(j); `first` starts O_t
+      auto pv = [&](int t, int j, bool first) {
         const uint32_t vb = aV + (j % NV) * C::kTileBytes;
         const uint32_t ocol = C::kOCol + t * D;
 #pragma unroll
         for (int kk = 0; kk < kChunkKeys / 16; ++kk)
-          tc_mma_bf16_ts(tmem + ocol, tmem + t * kChunkKeys + kk * 8,
+          tc_mma_bf16_ts(tmem + ocol, tmem + t * kChunkKeys + (kk >> 2) * 64 + (kk & 3) * 8,
                          sdesc_sw128(vb + kk * 2048, 16384, 1024), idesc_pv,
-                         (j > 0 || kk > 0) ? 1u : 0u);
+                         (!first || kk > 0) ? 1u : 0u);
       };
       auto wait_k = [&](int j) -> bool {
         if (!mbar_wait(&k_full[j % NK], (uint32_t)(j / NK) & 1u, abort_flag)) return false;
@@ -292,36 +316,63 @@ __device__ __forceinline__ void chunk_cta(const ChunkParams& p, const CUtensorMa
         return true;
       };
       bool ok = mbar_wait(q_full, 0u, abort_flag) && wait_k(0);
-      if (ok) {
-        qk(0, 0);
-        if (hasB) qk(1, 0);
-        tc_commit(&k_empty[0]);
-      }
-      for (int j = 0; ok && j < T; ++j) {
-        bool k_next_ready = false, v_ready = false;
-        if (j < TA) {
-          if (!mbar_wait(&p_full[0], (uint32_t)j & 1u, abort_flag) || !wait_v(j)) { ok = false; break; }
-          v_ready = true;
-          pv(0, j);
-          if (j == TA - 1) tc_commit(&o_done[0]);
-          if (j + 1 < TA) {
-            if (!wait_k(j + 1)) { ok = false; break; }
-            k_next_ready = true;
-            qk(0, j + 1);
+      if (inter) {
+        // one query tile, key tiles alternating between S_0/O_0 (even) and
+        // S_1/O_1 (odd): QK of tile j + 2 follows PV of tile j on the same
+        // half, so each half's softmax overlaps the other half's MMAs
+        if (ok) {
+          qk(0, 0, 0);
+          tc_commit(&k_empty[0]);
+        }
+        if (ok && n_all > 1) {
+          ok = wait_k(1);
+          if (ok) {
+            qk(1, 0, 1);
+            tc_commit(&k_empty[1 % NK]);
           }
         }
-        if (hasB) {
+        for (int j = 0; ok && j < n_all; ++j) {   // j: tile jb + j, half j & 1
+          const int t = j & 1;
+          if (!mbar_wait(&p_full[t], (uint32_t)(j >> 1) & 1u, abort_flag) || !wait_v(j)) { ok = false; break; }
+          pv(t, j, j < 2);
+          if (j + 2 >= n_all) tc_commit(&o_done[t]);
+          tc_commit(&v_empty[j % NV]);
+          if (j + 2 < n_all) {
+            if (!wait_k(j + 2)) { ok = false; break; }
+            qk(t, 0, j + 2);
+            tc_commit(&k_empty[(j + 2) % NK]);
+          }
+        }
+      } else {
+        if (ok) {
+          qk(0, 0, 0);
+          qk(1, 1, 0);
+          tc_commit(&k_empty[0]);
+        }
+        for (int j = 0; ok && j < n_all; ++j) {   // j: tile jb + j
+          bool k_next_ready = false, v_ready = false;
+          if (j < nA) {
+            if (!mbar_wait(&p_full[0], (uint32_t)j & 1u, abort_flag) || !wait_v(j)) { ok = false; break; }
+            v_ready = true;
+            pv(0, j, j == 0);
+            if (j == nA - 1) tc_commit(&o_done[0]);
+            if (j + 1 < nA) {
+              if (!wait_k(j + 1)) { ok = false; break; }
+              k_next_ready = true;
+              qk(0, 0, j + 1);
+            }
+          }
           if (!mbar_wait(&p_full[1], (uint32_t)j & 1u, abort_flag)) { ok = false; break; }
           if (!v_ready && !wait_v(j)) { ok = false; break; }
           tc_fence_after_sync();
-          pv(1, j);
-          if (j == T - 1) tc_commit(&o_done[1]);
-        }
-        tc_commit(&v_empty[j % NV]);
-        if (j + 1 < T) {
-          if (!k_next_ready && !wait_k(j + 1)) { ok = false; break; }
-          if (hasB) qk(1, j + 1);
-          tc_commit(&k_empty[(j + 1) % NK]);
+          pv(1, j, j == 0);
+          if (j == n_all - 1) tc_commit(&o_done[1]);
+          tc_commit(&v_empty[j % NV]);
+          if (j + 1 < n_all) {
+            if (!k_next_ready && !wait_k(j + 1)) { ok = false; break; }
+            qk(1, 1, j + 1);
+            tc_commit(&k_empty[(j + 1) % NK]);
+          }
         }
       }
       // every MMA issued must complete before TMEM is freed
@@ -329,37 +380,37 @@ __device__ __forceinline__ void chunk_cta(const ChunkParams& p, const CUtensorMa
       drain_wait(mma_done, 0u, abort_flag);
       drain_wait(q_full, 0u, abort_flag);
     }
-  } else {
-    // ------------------------------------------------------------ softmax
-    const int t = warp >> 2;               // 0: tile A, 1: tile B
+  } else if (!inter) {
+    // ------------------------------------------------------------ softmax (pair)
+    // Warps 4t .. 4t+3 own tile t (A or B): thread = query row = TMEM lane,
+    // the whole 128-column S row in registers.  P of keys 0-63 goes to S
+    // columns 0-31 and of keys 64-127 to columns 64-95.
+    const int t = warp >> 2;
     const int wq = warp & 3;
     const int row = wq * 32 + lane;
     const uint32_t t_lane = tmem + ((uint32_t)(wq * 32) << 16);
-    const int ntok_t = t ? ntokB : ntokA;
-    const int T_t = t ? (hasB ? T : 0) : TA;
+    const int n_t = t ? n_all : nA;
     const int tok0_t = it.tok0 + t * tpt;
     const int tok_local = row / g;
-    const bool valid_row = (row < g * tpt) && (tok_local < ntok_t);
+    const bool valid_row = (row < g * tpt) && (tok_local < (t ? ntokB : ntokA));
     const int tok_rel = tok0_t + tok_local;
-    const int pos = valid_row ? off + tok_rel : ctx - 1;  // absolute position
+    const int pos = valid_row ? off + tok_rel : ctx - 1;   // absolute position
     const int min_pos = off + tok0_t;
     const float sl2 = p.scale_log2;
     const uint32_t s_col = t_lane + t * kChunkKeys;
     const uint32_t o_col = t_lane + C::kOCol + t * D;
-    float m_run = -INFINITY;   // running maximum, in scaled log2 units
+    const int zero_t = (TA == T) ? 0 : 1;    // the tile whose PV reads V(T-1) first
+    float m_run = -INFINITY;   // running maximum, scaled log2 units
     float l_run = 0.f;
     bool ok = true;
-    for (int j = 0; j < T_t; ++j) {
-      if (!mbar_wait(&s_full[t], (uint32_t)j & 1u, abort_flag)) { ok = false; break; }
+    for (int j = 0; j < n_t; ++j) {   // key tile jb + j
+      // waits are made warp-uniform: a lane that gave up must not leave its
+      // warp's collective TMEM accesses
+      if (!__all_sync(0xffffffffu, mbar_wait(&s_full[t], (uint32_t)j & 1u, abort_flag))) { ok = false; break; }
       tc_fence_after_sync();
-      const int kbase = j * kChunkKeys;
+      const int kbase = (jb + j) * kChunkKeys;
       const bool masked = kbase + kChunkKeys - 1 > min_pos;
       const int lim = pos - kbase;   // keys 0..lim of this tile are visible
-      float alpha = 1.f;
-      bool resc = false;
-      // tcgen05.ld / tcgen05.st are warp-collective: every lane executes each
-      // of them; rows that hold no query only change the arithmetic (P = 0).
-      // The whole 128-column S row comes in with one wait.
       uint32_t sr[kChunkKeys];
 #pragma unroll
       for (int q = 0; q < kChunkKeys / 32; ++q) tmem_ld32(s_col + q * 32, sr + q * 32);
@@ -371,13 +422,15 @@ __device__ __forceinline__ void chunk_cta(const ChunkParams& p, const CUtensorMa
       }
       float mxp[8];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) mxp[u] = -INFINITY;
+      for (int e = 0; e < 8; ++e) mxp[e] = -INFINITY;
 #pragma unroll
       for (int i = 0; i < kChunkKeys; i += 16) {
 #pragma unroll
-        for (int u = 0; u < 8; ++u)
-          mxp[u] = fmax3(mxp[u], __uint_as_float(sr[i + 2 * u]), __uint_as_float(sr[i + 2 * u + 1]));
+        for (int e = 0; e < 8; ++e)
+          mxp[e] = fmax3(mxp[e], __uint_as_float(sr[i + 2 * e]), __uint_as_float(sr[i + 2 * e + 1]));
       }
+      float alpha = 1.f;
+      bool resc = false;
       if (valid_row) {
         const float mx = fmaxf(fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3])),
                                fmaxf(fmaxf(mxp[4], mxp[5]), fmaxf(mxp[6], mxp[7])));
@@ -388,9 +441,9 @@ __device__ __forceinline__ void chunk_cta(const ChunkParams& p, const CUtensorMa
           resc = true;
         }
       }
-      // P = 2^(s c - m) as bf16, written over the S columns (all of S is in
-      // registers by now)
-      const float neg_m = valid_row ? -m_run : -INFINITY;   // dead rows: P = 0
+      // P = 2^(s c - m) as bf16; dead rows and rows that have seen no key
+      // yet get P = 0
+      const float neg_m = (valid_row && m_run != -INFINITY) ? -m_run : -INFINITY;
       const uint64_t c2 = pack_f32x2(sl2, sl2);
       const uint64_t nm2 = pack_f32x2(neg_m, neg_m);
       uint64_t lsum2[2] = {pack_f32x2(0.f, 0.f), pack_f32x2(0.f, 0.f)};
@@ -403,28 +456,28 @@ __device__ __forceinline__ void chunk_cta(const ChunkParams& p, const CUtensorMa
           unpack_f32x2(fma_f32x2(pack_f32x2(__uint_as_float(sr[q * 32 + 2 * i]),
                                             __uint_as_float(sr[q * 32 + 2 * i + 1])),
                                  c2, nm2), x0, x1);
-          pk[i] = pack_bf16x2(fast_exp2(x0), fast_exp2(x1));
-          lsum2[i & 1] = add_f32x2(lsum2[i & 1], bf16x2_to_f32x2(pk[i]));
+          const float e0 = fast_exp2(x0), e1 = fast_exp2(x1);
+          pk[i] = pack_bf16x2(e0, e1);
+          lsum2[i & 1] = add_f32x2(lsum2[i & 1], pack_f32x2(e0, e1));
         }
-        tmem_st16(s_col + q * 16, pk);
+        tmem_st16(s_col + (q >> 1) * 64 + (q & 1) * 16, pk);
       }
       float lsp[4];
       unpack_f32x2(lsum2[0], lsp[0], lsp[1]);
       unpack_f32x2(lsum2[1], lsp[2], lsp[3]);
       if (valid_row) l_run = l_run * alpha + ((lsp[0] + lsp[1]) + (lsp[2] + lsp[3]));
-      if (j == T - 1 && t == (TA == T ? 0 : 1)) {
+      if (jb + j == T - 1 && t == zero_t) {
         // the last page's slots past the context were never written (its TMA
         // box brings them in as they are): clear those V rows before the
         // first PV that reads this tile, so that P = 0 never meets a NaN
-        const int kb = j * kChunkKeys;
-        const int first_bad = ctx - kb;
-        const int end_bad = min(kChunkKeys, ((ctx + kPageSize - 1) / kPageSize) * kPageSize - kb);
+        const int first_bad = ctx - kbase;
+        const int end_bad = min(kChunkKeys, ((ctx + kPageSize - 1) / kPageSize) * kPageSize - kbase);
         if (first_bad < end_bad) {
           const int s = j % NV;
-          if (!mbar_wait(&v_full[s], (uint32_t)(j / NV) & 1u, abort_flag)) { ok = false; break; }
+          if (!__all_sync(0xffffffffu, mbar_wait(&v_full[s], (uint32_t)(j / NV) & 1u, abort_flag))) { ok = false; break; }
           uint8_t* vt = sV + s * C::kTileBytes;
           const int n_units = (end_bad - first_bad) * CH * 8;
-          for (int e = row; e < n_units; e += 128) {
+          for (int e = row; e < n_units; e += kChunkRows) {
             const int key = first_bad + e / (CH * 8);
             const int rem = e % (CH * 8);
             *reinterpret_cast<uint4*>(vt + (rem >> 3) * 16384 + key * 128 + (rem & 7) * 16) =
@@ -433,7 +486,8 @@ __device__ __forceinline__ void chunk_cta(const ChunkParams& p, const CUtensorMa
           fence_async_shared();
         }
       }
-      // O_t is stable here (PV_t(j-1) completed before S_t(j) was ready)
+      // O_t is stable here (PV_t of the previous key tile completed before
+      // S_t was ready)
       if (j > 0 && __any_sync(0xffffffffu, resc)) {
         const float f = resc ? alpha : 1.f;
 #pragma unroll 1
@@ -451,7 +505,7 @@ __device__ __forceinline__ void chunk_cta(const ChunkParams& p, const CUtensorMa
       mbar_arrive(&p_full[t]);
     }
     // epilogue: O / l -> bf16
-    if (T_t > 0 && ok && mbar_wait(&o_done[t], 0u, abort_flag)) {
+    if (__all_sync(0xffffffffu, n_t > 0 && ok && mbar_wait(&o_done[t], 0u, abort_flag))) {
       tc_fence_after_sync();
       const float inv = (l_run > 0.f) ? 1.f / l_run : 0.f;
       uint16_t* dst = p.out + ((size_t)(q0 + tok_rel) * p.num_q_heads +
@@ -471,6 +525,299 @@ __device__ __forceinline__ void chunk_cta(const ChunkParams& p, const CUtensorMa
             pk4.w = pack_bf16x2(__uint_as_float(orow[v * 8 + 6]) * inv, __uint_as_float(orow[v * 8 + 7]) * inv);
             *reinterpret_cast<uint4*>(dst + q * 32 + v * 8) = pk4;
           }
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ softmax (interleaved)
+    // One query tile; its S tiles come in two slots (the even and odd key
+    // tiles, S_0/O_0 and S_1/O_1).  Every S tile passes through all eight
+    // warps: warp w serves TMEM lanes 32 (w % 4) .. (its query rows) and
+    // column half h = w / 4 (keys 64 h .. 64 h + 63 and head-dim columns
+    // h D / 2 ..).  Both halves read the whole row for its maximum, and warps
+    // w and w + 4 meet at named barrier 4 + w % 4 before either writes its P
+    // over the S columns.  P of keys 0-63 goes to S columns 0-31 and of keys
+    // 64-127 to columns 64-95.
+    const int h = warp >> 2;
+    const int wq = warp & 3;
+    const int row = wq * 32 + lane;
+    const uint32_t bar_pair = 4u + (uint32_t)wq;
+    const uint32_t t_lane = tmem + ((uint32_t)(wq * 32) << 16);
+    const float sl2 = p.scale_log2;
+    const int c_own = h * 64, c_oth = (1 - h) * 64;   // S columns: exponentiated / max only
+    const int o_c0 = h * (D / 2);                     // head-dim columns of O
+    constexpr int o_nc = D / 2;
+    const int tok_local = row / g;
+    const bool valid_row = (row < g * tpt) && (tok_local < ntokA);
+    const int tok_rel = it.tok0 + tok_local;
+    const int pos = valid_row ? off + tok_rel : ctx - 1;   // absolute position
+    const int min_pos = off + it.tok0;
+    // per slot: running maximum (scaled log2 units) and this half's row sum
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    const int zero_slot = (n_all - 1) & 1;
+    bool ok = true;
+    for (int j = 0; j < n_all; ++j) {   // key tile jb + j, slot j & 1
+      const int t = j & 1;
+      const uint32_t u = (uint32_t)j >> 1;      // S tiles of slot t before this one
+      float m_run = t ? m1 : m0;
+      float l_run = t ? l1 : l0;
+      const bool got_s = mbar_wait(&s_full[t], u & 1u, abort_flag);
+      tc_fence_after_sync();
+      const int kbase = (jb + j) * kChunkKeys;
+      const bool masked = kbase + kChunkKeys - 1 > min_pos;
+      const int lim = pos - kbase;   // keys 0..lim of this tile are visible
+      const uint32_t s_col = t_lane + t * kChunkKeys;
+      // tcgen05.ld / tcgen05.st are warp-collective: every lane executes
+      // each of them; rows that hold no query only change the arithmetic
+      uint32_t own[64], oth[64];
+      tmem_ld32(s_col + c_own, own);
+      tmem_ld32(s_col + c_own + 32, own + 32);
+      tmem_ld32(s_col + c_oth, oth);
+      tmem_ld32(s_col + c_oth + 32, oth + 32);
+      tmem_ld_wait();
+      // both halves hold the row before either overwrites it; a failed wait
+      // ends the loop for both
+      if (!named_bar_and(bar_pair, 64, got_s)) { ok = false; break; }
+      if (masked) {
+        const int lim_own = lim - c_own, lim_oth = lim - c_oth;
+#pragma unroll
+        for (int i = 0; i < 64; ++i) {
+          if (i > lim_own) own[i] = __float_as_uint(-INFINITY);
+          if (i > lim_oth) oth[i] = __float_as_uint(-INFINITY);
+        }
+      }
+      float mxp[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) mxp[e] = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < 64; i += 8) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          mxp[e] = fmax3(mxp[e], __uint_as_float(own[i + 2 * e]), __uint_as_float(own[i + 2 * e + 1]));
+          mxp[4 + e] = fmax3(mxp[4 + e], __uint_as_float(oth[i + 2 * e]), __uint_as_float(oth[i + 2 * e + 1]));
+        }
+      }
+      float alpha = 1.f;
+      bool resc = false;
+      if (valid_row) {
+        const float mx = fmaxf(fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3])),
+                               fmaxf(fmaxf(mxp[4], mxp[5]), fmaxf(mxp[6], mxp[7])));
+        const float m_new = fmaxf(m_run, mx * sl2);
+        if (m_new > m_run + kRescaleThreshold) {
+          alpha = fast_exp2(m_run - m_new);
+          m_run = m_new;
+          resc = true;
+        }
+      }
+      // P = 2^(s c - m) as bf16 for this half's 64 keys; dead rows and rows
+      // that have seen no key yet get P = 0
+      const float neg_m = (valid_row && m_run != -INFINITY) ? -m_run : -INFINITY;
+      const uint64_t c2 = pack_f32x2(sl2, sl2);
+      const uint64_t nm2 = pack_f32x2(neg_m, neg_m);
+      uint64_t lsum2[2] = {pack_f32x2(0.f, 0.f), pack_f32x2(0.f, 0.f)};
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int k = q * 32 + 2 * i;
+          float x0, x1;
+          unpack_f32x2(fma_f32x2(pack_f32x2(__uint_as_float(own[k]), __uint_as_float(own[k + 1])),
+                                 c2, nm2), x0, x1);
+          const float e0 = fast_exp2(x0), e1 = fast_exp2(x1);
+          pk[i] = pack_bf16x2(e0, e1);
+          lsum2[i & 1] = add_f32x2(lsum2[i & 1], pack_f32x2(e0, e1));
+        }
+        tmem_st16(s_col + c_own + q * 16, pk);
+      }
+      float lsp[4];
+      unpack_f32x2(lsum2[0], lsp[0], lsp[1]);
+      unpack_f32x2(lsum2[1], lsp[2], lsp[3]);
+      if (valid_row) l_run = l_run * alpha + ((lsp[0] + lsp[1]) + (lsp[2] + lsp[3]));
+      if (t) {
+        m1 = m_run;
+        l1 = l_run;
+      } else {
+        m0 = m_run;
+        l0 = l_run;
+      }
+      if (jb + j == T - 1 && t == zero_slot) {
+        // the last page's slots past the context were never written (its
+        // TMA box brings them in as they are): clear those V rows before
+        // the first PV that reads this tile, so that P = 0 never meets a NaN
+        const int first_bad = ctx - kbase;
+        const int end_bad = min(kChunkKeys, ((ctx + kPageSize - 1) / kPageSize) * kPageSize - kbase);
+        if (first_bad < end_bad) {
+          const int s = j % NV;
+          const bool got_v = mbar_wait(&v_full[s], (uint32_t)(j / NV) & 1u, abort_flag);
+          if (!named_bar_and(bar_pair, 64, got_v)) { ok = false; break; }
+          uint8_t* vt = sV + s * C::kTileBytes;
+          const int n_units = (end_bad - first_bad) * CH * 8;
+          for (int e = (int)threadIdx.x; e < n_units; e += 2 * kChunkRows) {
+            const int key = first_bad + e / (CH * 8);
+            const int rem = e % (CH * 8);
+            *reinterpret_cast<uint4*>(vt + (rem >> 3) * 16384 + key * 128 + (rem & 7) * 16) =
+                make_uint4(0u, 0u, 0u, 0u);
+          }
+          fence_async_shared();
+        }
+      }
+      // O_t is stable here (slot t's previous PV completed before its S was
+      // ready); each half rescales its own head-dim columns
+      if (u > 0 && __any_sync(0xffffffffu, resc)) {
+        const float f = resc ? alpha : 1.f;
+        const uint32_t oc = t_lane + C::kOCol + t * D + o_c0;
+#pragma unroll 1
+        for (int q = 0; q < o_nc / 32; ++q) {
+          uint32_t orow[32];
+          tmem_ld32(oc + q * 32, orow);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) orow[i] = __float_as_uint(__uint_as_float(orow[i]) * f);
+          tmem_st32(oc + q * 32, orow);
+        }
+      }
+      tmem_st_wait();
+      tc_fence_before_sync();
+      mbar_arrive(&p_full[t]);
+    }
+    // ---- epilogue: every MMA is complete once both slots' last PV is (slot
+    // 1 is empty with one key tile)
+    bool have_o = ok && mbar_wait(&o_done[0], 0u, abort_flag);
+    if (n_all > 1) have_o = have_o && mbar_wait(&o_done[1], 0u, abort_flag);
+    tc_fence_after_sync();
+    // row sums over both column halves, through the second Q tile's room
+    // (unused with one query tile)
+    float* xl = reinterpret_cast<float*>(sQ + C::kTileBytes);
+    xl[(h * 2 + 0) * kChunkRows + row] = l0;
+    xl[(h * 2 + 1) * kChunkRows + row] = l1;
+    have_o = named_bar_and(bar_pair, 64, have_o);
+    const float l_tot0 = l0 + xl[((1 - h) * 2 + 0) * kChunkRows + row];
+    const float l_tot1 = l1 + xl[((1 - h) * 2 + 1) * kChunkRows + row];
+    // the two slots merge: O = w0 O_0 + w1 O_1 relative to 2^m_fin, l_fin
+    // likewise
+    const bool merge_slots = n_all > 1;
+    float m_fin = m0, l_fin = l_tot0, w0 = 1.f, w1 = 0.f;
+    if (merge_slots) {
+      m_fin = fmaxf(m0, m1);
+      w0 = (m0 == -INFINITY) ? 0.f : fast_exp2(m0 - m_fin);
+      w1 = (m1 == -INFINITY) ? 0.f : fast_exp2(m1 - m_fin);
+      l_fin = w0 * l_tot0 + w1 * l_tot1;
+    }
+    // 32 head-dim columns c0 .. c0 + 31 of the final O (warp-collective)
+    auto load_o = [&](int c0, uint32_t (&o)[32]) {
+      tmem_ld32(t_lane + C::kOCol + c0, o);
+      if (merge_slots) {
+        uint32_t o1[32];
+        tmem_ld32(t_lane + C::kOCol + D + c0, o1);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          o[i] = __float_as_uint(w0 * __uint_as_float(o[i]) + w1 * __uint_as_float(o1[i]));
+      } else {
+        tmem_ld_wait();
+      }
+    };
+    if (it.n_splits == 1) {
+      // O / l -> bf16, this half's columns
+      if (have_o) {
+        const float inv = (l_fin > 0.f) ? 1.f / l_fin : 0.f;
+        uint16_t* dst = p.out + ((size_t)(q0 + tok_rel) * p.num_q_heads +
+                                 (size_t)it.kv_head * g + (row % g)) * D + o_c0;
+#pragma unroll 1
+        for (int q = 0; q < o_nc / 32; ++q) {
+          uint32_t orow[32];
+          load_o(o_c0 + q * 32, orow);
+          if (valid_row) {
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              uint4 pk4;
+              pk4.x = pack_bf16x2(__uint_as_float(orow[v * 8 + 0]) * inv, __uint_as_float(orow[v * 8 + 1]) * inv);
+              pk4.y = pack_bf16x2(__uint_as_float(orow[v * 8 + 2]) * inv, __uint_as_float(orow[v * 8 + 3]) * inv);
+              pk4.z = pack_bf16x2(__uint_as_float(orow[v * 8 + 4]) * inv, __uint_as_float(orow[v * 8 + 5]) * inv);
+              pk4.w = pack_bf16x2(__uint_as_float(orow[v * 8 + 6]) * inv, __uint_as_float(orow[v * 8 + 7]) * inv);
+              *reinterpret_cast<uint4*>(dst + q * 32 + v * 8) = pk4;
+            }
+          }
+        }
+      }
+    } else {
+      // one piece of a split key range (an interleaved tile): publish the
+      // unnormalised O and (m, l) of every row; the last piece to arrive
+      // merges all pieces, o = sum_k 2^(m_k - M) o_k / sum_k 2^(m_k - M) l_k
+      const size_t slot = (size_t)(it.slot + it.split);
+      float* po = p.part_o + slot * D * kChunkRows + row;
+      float* pml = p.part_ml + slot * 2 * kChunkRows + row;
+      if (have_o) {
+#pragma unroll 1
+        for (int q = 0; q < o_nc / 32; ++q) {
+          uint32_t orow[32];
+          load_o(o_c0 + q * 32, orow);
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            po[(size_t)(o_c0 + q * 32 + i) * kChunkRows] = __uint_as_float(orow[i]);
+        }
+        if (h == 0) {
+          pml[0] = m_fin;
+          pml[kChunkRows] = l_fin;
+        }
+        __threadfence();
+      }
+      // all 256 softmax threads reach these barriers; a piece whose waits
+      // gave up does not arrive (the error word reports it)
+      volatile int* last_flag = reinterpret_cast<volatile int*>(smem + C::kMiscOff + 32);
+      if (named_bar_and(2, 2 * kChunkRows, have_o)) {
+        if (threadIdx.x == 0) {
+          __threadfence();
+          const int old = atomicAdd(&p.counters[it.merge_id], 1);
+          __threadfence();
+          *last_flag = (old == it.n_splits - 1) ? 1 : 0;
+        }
+        named_bar_sync(2, 2 * kChunkRows);
+        if (*last_flag) {
+          __threadfence();
+          const int ns = it.n_splits;
+          const float* o0 = p.part_o + (size_t)it.slot * D * kChunkRows + row;
+          const float* ml0 = p.part_ml + (size_t)it.slot * 2 * kChunkRows + row;
+          float mk[kMaxChunkSplits], w[kMaxChunkSplits];
+          float mmax = -INFINITY;
+#pragma unroll
+          for (int k = 0; k < kMaxChunkSplits; ++k) {
+            mk[k] = k < ns ? __ldcg(ml0 + (size_t)k * 2 * kChunkRows) : -INFINITY;
+            mmax = fmaxf(mmax, mk[k]);
+          }
+          float lsum = 0.f;
+#pragma unroll
+          for (int k = 0; k < kMaxChunkSplits; ++k) {
+            w[k] = (mk[k] == -INFINITY) ? 0.f : fast_exp2(mk[k] - mmax);
+            if (k < ns) lsum += w[k] * __ldcg(ml0 + (size_t)k * 2 * kChunkRows + kChunkRows);
+          }
+          const float inv = (lsum > 0.f) ? 1.f / lsum : 0.f;
+          if (valid_row) {
+            uint16_t* dst = p.out + ((size_t)(q0 + tok_rel) * p.num_q_heads +
+                                     (size_t)it.kv_head * g + (row % g)) * D;
+#pragma unroll 1
+            for (int d0 = o_c0; d0 < o_c0 + o_nc; d0 += 8) {
+              float acc[8];
+#pragma unroll
+              for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+#pragma unroll
+              for (int k = 0; k < kMaxChunkSplits; ++k) {
+                if (k < ns) {
+                  const float* src = o0 + ((size_t)k * D + d0) * kChunkRows;
+#pragma unroll
+                  for (int i = 0; i < 8; ++i) acc[i] += w[k] * __ldcg(src + (size_t)i * kChunkRows);
+                }
+              }
+              uint4 pk4;
+              pk4.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+              pk4.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+              pk4.z = pack_bf16x2(acc[4] * inv, acc[5] * inv);
+              pk4.w = pack_bf16x2(acc[6] * inv, acc[7] * inv);
+              *reinterpret_cast<uint4*>(dst + d0) = pk4;
+            }
+          }
+          if (threadIdx.x == 0) p.counters[it.merge_id] = 0;   // ready for the next launch
         }
       }
     }

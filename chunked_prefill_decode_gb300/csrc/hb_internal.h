@@ -22,7 +22,8 @@ constexpr int kChunkKeys = 128;        // keys per tensor-core KV tile
 constexpr int kDecodeKvhBlock = 8;     // kv heads per decode work item (max)
 constexpr int kMaxGroup = 16;          // max q heads per kv head
 constexpr uint32_t kPlanMagic = 0x31504248u;  // "HBP1"
-constexpr uint32_t kPlanVersion = 1;
+constexpr uint32_t kPlanVersion = 2;
+constexpr int kMaxChunkSplits = 16;    // key-range pieces of one query tile (max)
 
 // One decode work item: a range of logical pages of one decode row, for one
 // block of kv heads.  Rows of the same (sequence, kv block) with n_splits > 1
@@ -46,18 +47,27 @@ static_assert(sizeof(DecodeItem) == 48, "decode item size");
 // One tensor-core work item: query tokens tok0 .. tok0+ntok-1 (relative to
 // the sequence's first new token) of one kv head, all q heads of its group,
 // as two query tiles of tokens_per_tile tokens (the second may be short or
-// empty); kv_tiles covers the later tile.
+// empty), over key tiles kv_begin .. kv_tiles-1 (kv_tiles covers the later
+// tile).  A single-tile item may be one of n_splits > 1 pieces of its tile's
+// key range (split-KV): each piece leaves a partial softmax state in slot
+// slot + split, and the last piece to finish merges them.
 struct ChunkItem {
   int32_t seq;
   int32_t kv_head;
   int32_t tok0;
   int32_t ntok;
-  int32_t kv_tiles;     // 128-key tiles visited
+  int32_t kv_tiles;     // one past the last 128-key tile visited
   int32_t q0;           // first q row of the sequence (cu_q_len[seq])
   int32_t q_len;
   int32_t ctx;          // context_len of the sequence
+  int32_t kv_begin;     // first 128-key tile visited
+  int32_t split;        // index of this piece within its tile's key range
+  int32_t n_splits;     // 1: the item covers the whole key range
+  int32_t slot;         // first partial slot of the tile (n_splits > 1)
+  int32_t merge_id;     // the tile's merge counter (n_splits > 1)
+  int32_t pad0, pad1, pad2;
 };
-static_assert(sizeof(ChunkItem) == 32, "chunk item size");
+static_assert(sizeof(ChunkItem) == 64, "chunk item size");
 
 // Host plan = header, then DecodeItem[num_decode_items] (in CTA order), then
 // ChunkItem[num_chunk_items], then int32 decode CTA offsets[decode_grid + 1].
@@ -76,6 +86,8 @@ struct PlanHeader {
   int32_t decode_grid;
   int32_t decode_kvh_block;
   int32_t chunk_tokens_per_tile;
+  int32_t num_chunk_slots;     // partial states of split chunk tiles
+  int32_t num_chunk_merges;    // split chunk tiles
   int32_t pad0;
   uint64_t ws_decode_offsets;  // device offset of the per-CTA item offsets
   uint64_t items_bytes;     // bytes of the item arrays (host and device)
@@ -84,8 +96,11 @@ struct PlanHeader {
   uint64_t ws_partial_ml;
   uint64_t ws_total;
   uint64_t plan_bytes;
-  uint64_t pad1[2];
+  uint64_t ws_chunk_counters;   // [num_chunk_merges] arrivals per split tile
+  uint64_t ws_chunk_o;          // [num_chunk_slots, D, 128] fp32
+  uint64_t ws_chunk_ml;         // [num_chunk_slots, 2, 128] fp32: (m in log2 units, l)
 };
+static_assert(sizeof(PlanHeader) == 160, "header size");
 static_assert(sizeof(PlanHeader) % 16 == 0, "header alignment");
 
 // Workspace counters: [0] decode work counter, [1] decode CTAs done,
@@ -125,6 +140,9 @@ struct ChunkParams {
   int32_t num_q_heads, num_kv_heads, group, tokens_per_tile;
   float scale_log2;
   int* dev_error;
+  int32_t* counters;      // [merges]: arrivals of the pieces of a split tile
+  float* part_o;          // [slots, D, 128]: unnormalised O, row fastest
+  float* part_ml;         // [slots, 2, 128]: row maximum (log2 units), row sum
 };
 
 struct AppendParams {

@@ -196,6 +196,19 @@ def hb_plan(batch, q_len, context_len, num_sms, workspace=None, stream=None,
     With upload=False only the host plan is built (no CUDA call)."""
     ql = np.ascontiguousarray(q_len, dtype=np.int32)
     cl = np.ascontiguousarray(context_len, dtype=np.int32)
+    if plan is not None and (workspace is not None or not upload):
+        # buffers given: plan straight into them; ask for sizes only if they
+        # turn out too small
+        ws = workspace if upload else None
+        pb = ctypes.c_size_t(plan.nbytes)
+        wb = ctypes.c_size_t(ws.numel() if ws is not None else 0)
+        st = load().hb_plan(ctypes.byref(batch), _ptr(ql), _ptr(cl), int(num_sms), _ptr(plan),
+                            ctypes.byref(pb), _ptr(ws), ctypes.byref(wb),
+                            _stream(stream) if upload else None)
+        if st == 0:
+            return plan, ws
+        if st != 4:   # anything but HB_ERR_WORKSPACE
+            _check(st)
     need_p, need_w = hb_plan_sizes(batch, ql, cl, num_sms)
     if plan is None or plan.nbytes < need_p:
         plan = np.zeros(need_p, dtype=np.uint8)
@@ -211,31 +224,41 @@ def hb_plan(batch, q_len, context_len, num_sms, workspace=None, stream=None,
     return plan, workspace
 
 
+HEADER_BYTES = 160
+DECODE_ITEM_INTS = 12
+CHUNK_ITEM_INTS = 16
+
+
 def plan_header(plan):
     """Decode the header of a host plan (for tests and reports)."""
-    h = np.frombuffer(plan[:72].tobytes(), dtype=np.int32)
+    h = np.frombuffer(plan[:80].tobytes(), dtype=np.int32)
     keys = ("magic", "version", "num_seqs", "total_q", "num_q_heads", "num_kv_heads",
             "head_dim", "page_size", "max_pages_per_seq", "num_sms",
             "num_decode_items", "num_chunk_items", "num_partial_slots",
             "num_merge_counters", "decode_grid", "decode_kvh_block",
-            "chunk_tokens_per_tile", "pad0")
+            "chunk_tokens_per_tile", "num_chunk_slots", "num_chunk_merges", "pad0")
     out = {k: int(v) for k, v in zip(keys, h)}
-    u = np.frombuffer(plan[72:144].tobytes(), dtype=np.uint64)
+    u = np.frombuffer(plan[80:HEADER_BYTES].tobytes(), dtype=np.uint64)
     for k, v in zip(("ws_decode_offsets", "items_bytes", "ws_counters", "ws_partial_o",
-                     "ws_partial_ml", "ws_total", "plan_bytes"), u):
+                     "ws_partial_ml", "ws_total", "plan_bytes", "ws_chunk_counters",
+                     "ws_chunk_o", "ws_chunk_ml"), u):
         out[k] = int(v)
     return out
 
 
 def plan_items(plan):
-    """(decode items [n, 12] int32 in CTA order, chunk items [m, 8] int32,
-    decode CTA offsets [grid + 1]) of a host plan."""
+    """(decode items [n, 12] int32 in CTA order, chunk items [m, 16] int32,
+    decode CTA offsets [grid + 1]) of a host plan.
+
+    Chunk item columns: seq, kv_head, tok0, ntok, kv_tiles (end), q0, q_len,
+    ctx, kv_begin, split, n_splits, slot, merge_id, 3 x padding."""
     hd = plan_header(plan)
-    body = plan[144:]
+    body = plan[HEADER_BYTES:]
     nd, nc = hd["num_decode_items"], hd["num_chunk_items"]
-    ints = np.frombuffer(body[: nd * 48 + nc * 32].tobytes(), dtype=np.int32)
-    dec = ints[: nd * 12].reshape(nd, 12)
-    chk = ints[nd * 12: nd * 12 + nc * 8].reshape(nc, 8)
+    n_int = nd * DECODE_ITEM_INTS + nc * CHUNK_ITEM_INTS
+    ints = np.frombuffer(body[: 4 * n_int].tobytes(), dtype=np.int32)
+    dec = ints[: nd * DECODE_ITEM_INTS].reshape(nd, DECODE_ITEM_INTS)
+    chk = ints[nd * DECODE_ITEM_INTS: n_int].reshape(nc, CHUNK_ITEM_INTS)
     off = hd["ws_decode_offsets"]
     grid = hd["decode_grid"]
     offs = np.frombuffer(body[off: off + 4 * (grid + 1)].tobytes(), dtype=np.int32) \

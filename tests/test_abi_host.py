@@ -164,17 +164,39 @@ def _check_plan(rows, hq, hkv, d, sms):
     n_tiles = sum(-(-int(q) // tpt) * hkv for q in ql if q > 1)
     tpi = 2 if n_tiles >= 2 * sms else 1
     seen = set()
-    for seq, kvh, t0, nt, tiles, q0, qn, ctx in chk:
+    groups = {}
+    for seq, kvh, t0, nt, end, q0, qn, ctx, kb, split, ns, slot, mid, *_ in chk:
         assert ql[seq] > 1 and 1 <= nt <= tpi * tpt and t0 % (tpi * tpt) == 0
         assert q0 == cu[seq] and qn == ql[seq] and ctx == cl[seq]
+        assert 1 <= ns <= 16 and 0 <= split < ns and 0 <= kb < end
+        if ns > 1:
+            assert tpi == 1 and end - kb >= 4      # only single tiles are split
+        groups.setdefault((seq, kvh, t0), []).append((split, kb, end, ns, slot, mid, nt))
+    slots, merges = set(), set()
+    for (seq, kvh, t0), parts in groups.items():
+        parts.sort()
+        ns = parts[0][3]
+        nt = parts[0][6]
         off = cl[seq] - ql[seq]
-        assert tiles == -(-(off + t0 + nt) // 128)
+        # the pieces tile the key range of the query tile(s) exactly once
+        assert [p[0] for p in parts] == list(range(ns))
+        assert parts[0][1] == 0 and parts[-1][2] == -(-(off + t0 + nt) // 128)
+        assert all(a[2] == b_[1] for a, b_ in zip(parts, parts[1:]))
+        assert len({(p[3], p[4], p[5], p[6]) for p in parts}) == 1
+        if ns > 1:
+            assert parts[0][5] not in merges
+            merges.add(parts[0][5])
+            rng_ = set(range(parts[0][4], parts[0][4] + ns))
+            assert not (rng_ & slots)
+            slots |= rng_
         for t in range(t0, t0 + nt):
             assert (seq, kvh, t) not in seen
             seen.add((seq, kvh, t))
     assert len(seen) == sum(int(q) * hkv for q in ql if q > 1)
-    tiles = [c[4] for c in chk]
-    assert tiles == sorted(tiles, reverse=True)
+    assert h["num_chunk_slots"] == len(slots) and h["num_chunk_merges"] == len(merges)
+    assert slots == set(range(len(slots))) and merges == set(range(len(merges)))
+    lengths = [c[4] - c[8] for c in chk]
+    assert lengths == sorted(lengths, reverse=True)
     return h
 
 
@@ -192,3 +214,18 @@ def test_plan_edge_shapes():
     _check_plan([(1, 5000), (257, 8192)], 56, 8, 128, 152)
     _check_plan([(1, 333), (9, 40)], 16, 16, 128, 8)    # 2 kv blocks of 8
     _check_plan([(1, 100), (3, 3)], 4, 2, 64, 152)      # kv block of 2
+
+
+def test_plan_splits_short_chunks_at_long_offsets():
+    """A 256-token chunk at offset 7936 (64 query tiles of 64 key tiles) cannot
+    fill 148 SMs as whole tiles: its key ranges are split; a chunk with enough
+    tiles to pair is not."""
+    h = _check_plan([(256, 8192)], 32, 8, 128, 148)
+    assert h["num_chunk_merges"] == 64 and h["num_chunk_slots"] >= 128
+    h = _check_plan([(1, 2048)] * 32 + [(256, 8192)], 32, 8, 128, 148)
+    assert h["num_chunk_merges"] > 0
+    h = _check_plan([(4096, 8192)], 32, 8, 128, 148)
+    assert h["num_chunk_merges"] == 0
+    # short key ranges are never split below 4 tiles per piece
+    h = _check_plan([(64, 64 + 200)], 8, 8, 64, 148)
+    assert h["num_chunk_merges"] == 0

@@ -63,6 +63,27 @@ def test_other_head_geometries(geom):
     _full_check(layout_from_rows(Shape(hq, hkv, d), rows, 12), seed=12)
 
 
+@pytest.mark.parametrize("geom,rows", [
+    ((32, 8, 128), [(64, 4160)]),
+    ((32, 8, 128), [(1, 2048)] * 8 + [(96, 6000)]),
+    ((8, 8, 64), [(100, 3000)]),
+    ((56, 8, 128), [(1, 5000), (40, 5040)]),
+    ((16, 1, 128), [(300, 9000)]),
+])
+def test_split_key_ranges(geom, rows):
+    """Chunks with too few query tiles to fill the SMs, at long offsets: the
+    plan cuts each tile's key range into pieces that the last piece to finish
+    merges.  Three launches on one plan also check that the merge counters
+    reset themselves."""
+    from _hbutil import host_batch
+    hq, hkv, d = geom
+    hb = lib()
+    b, ql, cl = host_batch(hb, rows, hq=hq, hkv=hkv, d=d)
+    plan, _ = hb.hb_plan(b, ql, cl, sms(), upload=False)
+    assert hb.plan_header(plan)["num_chunk_merges"] > 0
+    _full_check(layout_from_rows(Shape(hq, hkv, d), rows, 14), seed=14, repeats=3)
+
+
 def test_several_chunks_and_decodes():
     rows = [(1, 900)] * 7 + [(200, 456), (57, 57), (300, 2000), (1, 5)]
     _full_check(layout_from_rows(Shape(32, 8, 128), rows, 13), seed=13)
