@@ -27,6 +27,8 @@ __device__ __forceinline__ uint4 ld_stream(const uint4* p) {
 
 // cu_q_len is staged in shared memory for batches up to this many sequences
 constexpr int kAppendSmemSeqs = 8191;
+// 16-byte vectors per lane held in registers (rows up to 32 x 8 x 16 B = 4 KB)
+constexpr int kAppendVecsPerLane = 8;
 
 __global__ void __launch_bounds__(256) kv_append_kernel(AppendParams p) {
   extern __shared__ int32_t s_cu[];
@@ -34,16 +36,34 @@ __global__ void __launch_bounds__(256) kv_append_kernel(AppendParams p) {
   // the row -> sequence search runs on a shared-memory copy of cu_q_len (one
   // coalesced load per CTA instead of a chain of dependent global loads)
   const bool staged = p.num_seqs <= kAppendSmemSeqs;
+  const int warps_total = gridDim.x * (blockDim.x >> 5);
+  const int n_rows = 2 * p.total_q;
+  const size_t row_vecs = (size_t)p.row_vec16;
+  // a row's data does not depend on where it goes: its loads are issued
+  // before the sequence / page lookups (for the first row, even before the
+  // staging of cu_q_len) and overlap them
+  uint4 buf[kAppendVecsPerLane];
+  auto load_row = [&](int r) {
+    const uint4* src = reinterpret_cast<const uint4*>((r & 1) ? p.v_new : p.k_new) +
+                       (size_t)(r >> 1) * row_vecs;
+#pragma unroll
+    for (int i = 0; i < kAppendVecsPerLane; ++i) {
+      const int v = lane + 32 * i;
+      if (v < p.row_vec16) buf[i] = ld_stream(src + v);
+    }
+  };
+  int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  if (r < n_rows) load_row(r);
   if (staged)
     for (int i = threadIdx.x; i <= p.num_seqs; i += blockDim.x) s_cu[i] = __ldg(&p.cu_q_len[i]);
   __syncthreads();
   const int32_t* cu = staged ? s_cu : p.cu_q_len;
-  const int warps_total = gridDim.x * (blockDim.x >> 5);
-  const int n_rows = 2 * p.total_q;
-  for (int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < n_rows;
-       r += warps_total) {
+  for (bool first = true; r < n_rows; r += warps_total, first = false) {
     const int tok = r >> 1;
     const bool is_v = (r & 1) != 0;
+    if (!first) load_row(r);
+    const uint4* src = reinterpret_cast<const uint4*>(is_v ? p.v_new : p.k_new) +
+                       (size_t)tok * row_vecs;
     // sequence owning this token: the largest s with cu_q_len[s] <= tok
     int lo = 0, hi = p.num_seqs - 1;
     while (lo < hi) {
@@ -62,12 +82,15 @@ __global__ void __launch_bounds__(256) kv_append_kernel(AppendParams p) {
       if (lane == 0) report_error(p.dev_error, HB_DEVERR_INDEX);
       continue;
     }
-    const size_t row_vecs = (size_t)p.row_vec16;
-    const uint4* src = reinterpret_cast<const uint4*>(is_v ? p.v_new : p.k_new) +
-                       (size_t)tok * row_vecs;
     uint4* dst = reinterpret_cast<uint4*>(is_v ? p.v_cache : p.k_cache) +
                  ((size_t)page * kPageSize + (pos % kPageSize)) * row_vecs;
-    for (int v = lane; v < p.row_vec16; v += 32) dst[v] = ld_stream(src + v);
+#pragma unroll
+    for (int i = 0; i < kAppendVecsPerLane; ++i) {
+      const int v = lane + 32 * i;
+      if (v < p.row_vec16) dst[v] = buf[i];
+    }
+    // rows of more than 4 KB (Hkv * D > 2048) copy the rest directly
+    for (int v = lane + 32 * kAppendVecsPerLane; v < p.row_vec16; v += 32) dst[v] = ld_stream(src + v);
   }
 }
 

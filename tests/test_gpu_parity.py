@@ -55,7 +55,7 @@ def test_edge_rows(rows, geom):
     _full_check(layout_from_rows(Shape(hq, hkv, d), rows, 11), seed=11)
 
 
-@pytest.mark.parametrize("geom", [(4, 4, 128), (16, 2, 64), (64, 16, 128), (16, 1, 128),
+@pytest.mark.parametrize("geom", [(4, 4, 128), (16, 2, 64), (64, 16, 128), (32, 32, 128), (16, 1, 128),
                                   (8, 1, 64), (128, 8, 128)])
 def test_other_head_geometries(geom):
     hq, hkv, d = geom
