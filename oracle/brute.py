@@ -19,9 +19,11 @@ def _val(x):
 
 
 def attention_bruteforce(q, k_pool, v_pool, q_len, context_len, block_table,
-                         page_size, num_q_heads, num_kv_heads, scale):
+                         page_size, num_q_heads, num_kv_heads, scale, window=0):
     """Nested-loop attention; q, pools are float64 arrays; returns a list
-    out[token][head][d] of Python floats."""
+    out[token][head][d] of Python floats.  With window > 0 the query at p
+    sees keys p - window + 1 .. p only ("Sarathi-Serve: Chunked Prefills for
+    Stall-Free LLM Inference", §Results and evidence, names such variants)."""
     g = num_q_heads // num_kv_heads
     D = len(q[0][0])
     out = []
@@ -31,11 +33,13 @@ def attention_bruteforce(q, k_pool, v_pool, q_len, context_len, block_table,
         ctx = int(context_len[s])
         for j in range(ql):
             p = ctx - ql + j
+            first = max(0, p - window + 1) if window > 0 else 0
+            keys = list(range(first, p + 1))
             row = []
             for h in range(num_q_heads):
                 kv = h // g
                 scores = []
-                for t in range(p + 1):
+                for t in keys:
                     page = int(block_table[s][t // page_size])
                     slot = t % page_size
                     acc = 0.0
@@ -48,9 +52,9 @@ def attention_bruteforce(q, k_pool, v_pool, q_len, context_len, block_table,
                 o = []
                 for d in range(D):
                     acc = 0.0
-                    for t in range(p + 1):
+                    for i, t in enumerate(keys):
                         page = int(block_table[s][t // page_size])
-                        acc += w[t] * _val(v_pool[page][t % page_size][kv][d])
+                        acc += w[i] * _val(v_pool[page][t % page_size][kv][d])
                     o.append(acc / z)
                 row.append(o)
             out.append(row)

@@ -29,7 +29,11 @@ Readings taken where the pages are silent (each is listed in the design doc):
     p = context_len - q_len + j and sees keys 0..p;
   * grouped-query attention maps q head h to kv head h // (Hq / Hkv);
   * pages are laid out [page][slot][kv_head][head_dim], separate K and V pools;
-    the oracle only ever looks at the logical view through the block table.
+    the oracle only ever looks at the logical view through the block table;
+  * "Sarathi-Serve: Chunked Prefills for Stall-Free LLM Inference", §Results
+    and evidence, names sliding-window model variants without a size: with a
+    window of W tokens the query at position p sees keys p - W + 1 .. p (W
+    keys, itself included); W = 0 means no window.
 
 Parity pins (tests/test_oracle_pins.py) tie this module to things other than
 itself: a pure-Python brute force, closed forms (constant V, q = 0, one key,
@@ -96,24 +100,38 @@ def kv_append(k_pool, v_pool, k_new, v_new, q_len, context_len, block_table,
     return k_out, v_out
 
 
-def gather_logical(pool, block_table_row, n_tokens, page_size) -> np.ndarray:
-    """The first n_tokens tokens of one sequence, in logical order: [n, Hkv, D]."""
-    pos = np.arange(n_tokens, dtype=np.int64)
+def gather_logical(pool, block_table_row, n_tokens, page_size, start=0) -> np.ndarray:
+    """Tokens start .. n_tokens-1 of one sequence, in logical order: [n, Hkv, D]."""
+    pos = np.arange(start, n_tokens, dtype=np.int64)
     return np.asarray(pool)[np.asarray(block_table_row)[pos // page_size],
                             pos % page_size]
 
 
+def visible_mask(keys, pos, window=0) -> np.ndarray:
+    """[n, K] bool: key position keys[k] is visible to the query at position
+    pos[i] -- causal (key <= query) and, with a sliding window of W tokens,
+    no more than W - 1 positions back."""
+    keys = np.asarray(keys, dtype=np.int64)[None, :]
+    pos = np.asarray(pos, dtype=np.int64)[:, None]
+    vis = keys <= pos
+    if window > 0:
+        vis &= keys > pos - window
+    return vis
+
+
 def attention(q, k_pool, v_pool, q_len, context_len, block_table, page_size,
-              num_q_heads, num_kv_heads, scale, tokens=None) -> np.ndarray:
+              num_q_heads, num_kv_heads, scale, tokens=None, window=0) -> np.ndarray:
     """fp64 output [T, Hq, D] of the hybrid batch's attention.
 
     For sequence s, new token j, q head h (kv head h // g, g = Hq / Hkv):
         p    = context_len[s] - q_len[s] + j
-        s_t  = scale * <q[s, j, h], K[t, kv]>            for t = 0 .. p
+        s_t  = scale * <q[s, j, h], K[t, kv]>            for t = t0 .. p
         o    = sum_t softmax(s)_t * V[t, kv]
-    with K, V read through the block table after the append.  `tokens`, if
-    given, restricts the computation to those global token indices (other
-    rows of the result are NaN), for spot checks of large batches.
+    with t0 = 0, or t0 = max(0, p - window + 1) with a sliding window, and K,
+    V read through the block table after the append (only the pages holding
+    keys some query sees).  `tokens`, if given, restricts the computation to
+    those global token indices (other rows of the result are NaN), for spot
+    checks of large batches.
     """
     qf = _as_f64(q)
     T, Hq, D = qf.shape
@@ -132,10 +150,11 @@ def attention(q, k_pool, v_pool, q_len, context_len, block_table, page_size,
                 continue
         else:
             sel = np.ones(ql, dtype=bool)
-        K = _as_f64(gather_logical(k_pool, block_table[s], ctx, page_size))
-        V = _as_f64(gather_logical(v_pool, block_table[s], ctx, page_size))
         pos = query_positions(ql, ctx)[sel]                  # [n]
-        visible = np.arange(ctx)[None, :] <= pos[:, None]    # [n, ctx]
+        t0 = max(0, int(pos.min()) - window + 1) if window > 0 else 0
+        K = _as_f64(gather_logical(k_pool, block_table[s], ctx, page_size, t0))
+        V = _as_f64(gather_logical(v_pool, block_table[s], ctx, page_size, t0))
+        visible = visible_mask(np.arange(t0, ctx), pos, window)   # [n, ctx - t0]
         for h in range(Hq):
             kv = h // g
             scores = scale * (qf[rows[sel], h, :] @ K[:, kv, :].T)

@@ -318,9 +318,105 @@ def test_pin_catches_transposed_page_index(monkeypatch):
     q, kp, vp, ql, cl, bt = _random_batch(rng, [(2, 10)], 2, 2, 8)
     ref = np.array(attention_bruteforce(q, kp, vp, ql, cl, bt, P, 2, 2, 0.5))
 
-    def wrong_gather(pool, row, n, page):
-        pos = np.arange(n)
+    def wrong_gather(pool, row, n, page, start=0):
+        pos = np.arange(start, n)
         return np.asarray(pool)[np.asarray(row)[pos % len(row)], pos // len(row) % page]
     monkeypatch.setattr(pa, "gather_logical", wrong_gather)
     out = _attn(q, kp, vp, ql, cl, bt, 2, 2, 0.5)
     assert not np.allclose(out, ref)
+
+
+# --------------------------------------------------------------- sliding window
+@pytest.mark.parametrize("seed,window", [(0, 1), (1, 3), (2, 5), (3, 9)])
+def test_windowed_oracle_matches_bruteforce(seed, window):
+    rng = np.random.default_rng(100 + seed)
+    hq, hkv, d = 4, 2, 8
+    rows = [(1, 11), (6, 17), (3, 3), (1, 2)]
+    q, kp, vp, ql, cl, bt = _random_batch(rng, rows, hq, hkv, d)
+    ref = np.array(attention_bruteforce(q, kp, vp, ql, cl, bt, P, hq, hkv, 0.3, window=window))
+    out = _attn(q, kp, vp, ql, cl, bt, hq, hkv, 0.3, window=window)
+    np.testing.assert_allclose(out, ref, rtol=0, atol=1e-12)
+
+
+def test_window_covering_the_context_is_full_attention():
+    rng = np.random.default_rng(110)
+    q, kp, vp, ql, cl, bt = _random_batch(rng, [(1, 9), (5, 14)], 2, 2, 8)
+    full = _attn(q, kp, vp, ql, cl, bt, 2, 2, 0.4)
+    for w in (14, 15, 1000):
+        np.testing.assert_array_equal(_attn(q, kp, vp, ql, cl, bt, 2, 2, 0.4, window=w), full)
+
+
+def test_window_of_one_returns_own_value():
+    """Closed form: with W = 1 each query sees only its own key, so o = v_p."""
+    rng = np.random.default_rng(111)
+    rows = [(1, 9), (5, 14)]
+    q, kp, vp, ql, cl, bt = _random_batch(rng, rows, 4, 2, 8)
+    out = _attn(q, kp, vp, ql, cl, bt, 4, 2, 0.4, window=1)
+    r = 0
+    for s, (qn, c) in enumerate(rows):
+        for j in range(qn):
+            p = c - qn + j
+            v = vp[bt[s, p // P], p % P]          # [Hkv, D]
+            np.testing.assert_allclose(out[r], np.repeat(v, 2, axis=0), rtol=0, atol=1e-15)
+            r += 1
+
+
+def test_windowed_chunked_prefill_equals_unchunked():
+    """Chunking changes cost, not the result -- with a window as well."""
+    rng = np.random.default_rng(112)
+    L, W, hq, hkv, d = 23, 6, 2, 1, 8
+    kp, vp = _pools(rng, 8, hkv, d)
+    bt = np.array([rng.permutation(8)[:6]])
+    qs = rng.standard_normal((L, hq, d))
+    full = _attn(qs, kp, vp, [L], [L], bt, hq, hkv, 0.5, window=W)
+    for c in (1, 4, 5, 9):
+        got = []
+        for o in range(0, L, c):
+            n = min(c, L - o)
+            got.append(_attn(qs[o:o + n], kp, vp, [n], [o + n], bt, hq, hkv, 0.5, window=W))
+        np.testing.assert_allclose(np.concatenate(got), full, rtol=0, atol=1e-12)
+
+
+def test_windowed_matches_torch_sdpa_band_mask():
+    """One contiguous sequence: torch fp64 SDPA with an explicit band mask."""
+    rng = np.random.default_rng(113)
+    ctx, qn, W, h, d = 21, 8, 5, 3, 16
+    q, kp, vp, ql, cl, bt = _random_batch(rng, [(qn, ctx)], h, h, d)
+    out = _attn(q, kp, vp, ql, cl, bt, h, h, 0.25, window=W)
+    K = pa.gather_logical(kp, bt[0], ctx, P)
+    V = pa.gather_logical(vp, bt[0], ctx, P)
+    pos = torch.arange(ctx - qn, ctx)[:, None]
+    key = torch.arange(ctx)[None, :]
+    mask = (key <= pos) & (key > pos - W)
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        torch.from_numpy(q).permute(1, 0, 2), torch.from_numpy(K).permute(1, 0, 2),
+        torch.from_numpy(V).permute(1, 0, 2), attn_mask=mask, scale=0.25).permute(1, 0, 2)
+    np.testing.assert_allclose(out, ref.numpy(), rtol=0, atol=1e-12)
+
+
+def test_window_reads_no_page_below_it():
+    """Pages holding no key inside any row's window are never looked up: an
+    invalid block-table entry there changes nothing."""
+    rng = np.random.default_rng(114)
+    q, kp, vp, ql, cl, bt = _random_batch(rng, [(1, 30), (3, 27)], 2, 2, 8)
+    W = 9
+    ref = _attn(q, kp, vp, ql, cl, bt, 2, 2, 0.4, window=W)
+    bt2 = bt.copy()
+    bt2[0, :(30 - W) // P] = -999999        # row 0 sees keys 21 .. 29
+    bt2[1, :(24 - W + 1) // P] = -999999    # row 1's first query (24) sees 16 ..
+    np.testing.assert_array_equal(_attn(q, kp, vp, ql, cl, bt2, 2, 2, 0.4, window=W), ref)
+
+
+def test_pin_catches_window_off_by_one(monkeypatch):
+    """A window one key too narrow breaks the brute-force pin."""
+    rng = np.random.default_rng(115)
+    q, kp, vp, ql, cl, bt = _random_batch(rng, [(4, 13)], 2, 2, 8)
+    ref = np.array(attention_bruteforce(q, kp, vp, ql, cl, bt, P, 2, 2, 0.5, window=5))
+
+    def narrow(keys, pos, window=0):
+        keys = np.asarray(keys)[None, :]
+        pos = np.asarray(pos)[:, None]
+        return (keys <= pos) & (keys > pos - window + 1)
+    monkeypatch.setattr(pa, "visible_mask", narrow)
+    out = _attn(q, kp, vp, ql, cl, bt, 2, 2, 0.5, window=5)
+    assert not np.allclose(out, ref, atol=1e-6)
