@@ -95,13 +95,17 @@ def algorithmic_counts(layout):
     written."""
     sh = layout.shape
     Hq, Hkv, D = sh.num_q_heads, sh.num_kv_heads, sh.head_dim
+    W = sh.sliding_window
     kv_tok = 2 * Hkv * D * 2               # K+V bytes per cached token
     qo_tok = 2 * Hq * D * 2                # q read + out written per new token
     c = {"decode_bytes": 0, "decode_flops": 0, "chunk_bytes": 0, "chunk_flops": 0}
     for q, ctx in zip(layout.q_len.tolist(), layout.context_len.tolist()):
-        seen = sum(ctx - q + j + 1 for j in range(q))
+        # keys each new token sees (a sliding window caps them at W), and the
+        # keys the row needs at all
+        seen = sum(min(ctx - q + j + 1, W) if W > 0 else ctx - q + j + 1 for j in range(q))
+        first_key = max(0, ctx - q - W + 1) if W > 0 else 0
         flops = 4 * Hq * D * seen
-        byts = ctx * kv_tok + q * qo_tok
+        byts = (ctx - first_key) * kv_tok + q * qo_tok
         kind = "decode" if q == 1 else "chunk"
         c[kind + "_bytes"] += byts
         c[kind + "_flops"] += flops
@@ -223,7 +227,8 @@ def oracle_sample_rate(layout, ten_host, budget_s=12.0, rows=None):
     while time.perf_counter() - t0 < budget_s:
         tok = order[done % len(order)]
         pa.attention(q, kp, vp, layout.q_len, layout.context_len, layout.block_table,
-                     sh.page_size, sh.num_q_heads, sh.num_kv_heads, scale, tokens=[tok])
+                     sh.page_size, sh.num_q_heads, sh.num_kv_heads, scale, tokens=[tok],
+                     window=sh.sliding_window)
         done += 1
     dt = time.perf_counter() - t0
     return done / dt, f"{done} new tokens (all {sh.num_q_heads} heads) of this batch, " \
@@ -251,7 +256,8 @@ def run_reference(args):
     def step(i):
         tok = dec[i % len(dec)]
         pa.attention(qb, kp, vp, layout.q_len, layout.context_len, layout.block_table,
-                     sh.page_size, sh.num_q_heads, sh.num_kv_heads, scale, tokens=[tok])
+                     sh.page_size, sh.num_q_heads, sh.num_kv_heads, scale, tokens=[tok],
+                     window=sh.sliding_window)
 
     for i in range(args.warmup):
         step(i)
@@ -290,7 +296,7 @@ def run_native(args):
     ten = workloads.make_tensors(layout, seed=1 + rank, device=dev)
     db = device_batch(layout.q_len, layout.context_len, layout.block_table,
                       layout.num_pages, sh.num_q_heads, sh.num_kv_heads, sh.head_dim,
-                      sh.page_size, dev)
+                      sh.page_size, dev, sliding_window=sh.sliding_window)
     scale = 1.0 / math.sqrt(sh.head_dim)
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     out = torch.empty_like(ten.q)
@@ -405,7 +411,8 @@ def run_native(args):
         "dtype": "bf16", "data": "synthetic",
         "config": {"workload": args.workload, "num_q_heads": sh.num_q_heads,
                    "num_kv_heads": sh.num_kv_heads, "head_dim": sh.head_dim,
-                   "page_size": sh.page_size, "tokens_per_step": T,
+                   "page_size": sh.page_size, "sliding_window": sh.sliding_window,
+                   "tokens_per_step": T,
                    "decode_rows": int((layout.q_len == 1).sum()),
                    "chunk_rows": int((layout.q_len > 1).sum()),
                    "kv_bytes_per_step": cnt["bytes"],

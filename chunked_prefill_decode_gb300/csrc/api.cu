@@ -188,6 +188,8 @@ hb_status check_batch(const hb_batch* b) {
     return fail(HB_ERR_SHAPE, "max_pages_per_seq and num_pages must be > 0");
   if ((int64_t)b->num_pages * kPageSize > 0x7fffffffLL)
     return fail(HB_ERR_UNSUPPORTED, "num_pages %d too large", b->num_pages);
+  if (b->sliding_window < 0) return fail(HB_ERR_SHAPE, "sliding_window %d < 0", b->sliding_window);
+  if (b->reserved != 0) return fail(HB_ERR_INVALID_ARG, "hb_batch.reserved must be 0");
   if (b->num_seqs > 0 && (!b->cu_q_len || !b->context_len || !b->block_table))
     return fail(HB_ERR_INVALID_ARG, "cu_q_len, context_len and block_table must be non-NULL");
   return HB_OK;
@@ -314,6 +316,7 @@ hb_status hb_plan(const hb_batch* batch, const int32_t* h_q_len,
       return fail(HB_ERR_INVALID_ARG, "h_q_len and h_context_len must be non-NULL");
     const int Hq = batch->num_q_heads, Hkv = batch->num_kv_heads, D = batch->head_dim;
     const int g = Hq / Hkv;
+    const int W = batch->sliding_window;
     const int64_t max_ctx = (int64_t)batch->max_pages_per_seq * kPageSize;
     int64_t tq = 0;
     for (int i = 0; i < S; ++i) {
@@ -354,14 +357,18 @@ hb_status hb_plan(const hb_batch* batch, const int32_t* h_q_len,
           c.tok0 = t0;
           c.ntok = std::min(tiles_per_item * tpt, h_q_len[i] - t0);
           c.kv_tiles = (off + t0 + c.ntok + kChunkKeys - 1) / kChunkKeys;
+          // with a sliding window the first row sees keys from off+t0-W+1 on
+          c.kv_begin = W > 0 ? std::max(0, off + t0 - W + 1) / kChunkKeys : 0;
+          c.n_splits = 1;
           c.q0 = cu[i];
           c.q_len = h_q_len[i];
           c.ctx = h_context_len[i];
           chk.push_back(c);
         }
     }
-    std::stable_sort(chk.begin(), chk.end(), [](const ChunkItem& a, const ChunkItem& b) {
-      return a.kv_tiles > b.kv_tiles;
+    auto key_tiles = [](const ChunkItem& c) { return c.kv_tiles - c.kv_begin; };
+    std::stable_sort(chk.begin(), chk.end(), [&](const ChunkItem& a, const ChunkItem& b) {
+      return key_tiles(a) > key_tiles(b);
     });
 
     // ---- cost model, in microseconds, from rates measured on GB300.  The
@@ -381,7 +388,8 @@ hb_status hb_plan(const hb_batch* batch, const int32_t* h_q_len,
     const double tile_us = tiles_per_item == 2 ? kPairTileUs : kSingleTileUs;
     double decode_bytes = 0.0;
     for (int i = 0; i < S; ++i)
-      if (h_q_len[i] == 1) decode_bytes += (double)h_context_len[i] * Hkv * D * 4.0;
+      if (h_q_len[i] == 1)
+        decode_bytes += (double)(W > 0 ? std::min(h_context_len[i], W) : h_context_len[i]) * Hkv * D * 4.0;
     auto t_decode = [&](int G) {
       return decode_bytes / std::min(kHbmBytesPerUs, G * kSmBytesPerUs);
     };
@@ -432,7 +440,7 @@ hb_status hb_plan(const hb_batch* batch, const int32_t* h_q_len,
     // included).
     int best_L = 0;   // 0: no split
     if (tiles_per_item == 1 && !chk.empty()) {
-      const int kmax = chk.front().kv_tiles;
+      const int kmax = key_tiles(chk.front());
       double best_t = 1e300;
       int prev_L = -1;
       for (int n = 1; n <= kMaxChunkSplits; ++n) {
@@ -442,9 +450,10 @@ hb_status hb_plan(const hb_batch* batch, const int32_t* h_q_len,
         std::vector<double> durs;
         double sum = 0.0, mx = 0.0;
         for (const ChunkItem& c : chk) {
-          const int np = pieces_of(c.kv_tiles, L);
+          const int kv = key_tiles(c);
+          const int np = pieces_of(kv, L);
           for (int k = 0; k < np; ++k) {
-            const int len = (k + 1) * c.kv_tiles / np - k * c.kv_tiles / np;
+            const int len = (k + 1) * kv / np - k * kv / np;
             const double d = len * tile_us + (np > 1 ? kPieceUs : 0.0);
             durs.push_back(d);
             sum += d;
@@ -464,15 +473,16 @@ hb_status hb_plan(const hb_batch* batch, const int32_t* h_q_len,
     {
       std::vector<ChunkItem> out;
       for (ChunkItem c : chk) {
-        const int np = best_L > 0 ? pieces_of(c.kv_tiles, best_L) : 1;
-        const int kv = c.kv_tiles;
+        const int kv = key_tiles(c);
+        const int kb0 = c.kv_begin;
+        const int np = best_L > 0 ? pieces_of(kv, best_L) : 1;
         c.n_splits = np;
         c.slot = np > 1 ? n_cslots : 0;
         c.merge_id = np > 1 ? n_cmerge : 0;
         for (int k = 0; k < np; ++k) {
           c.split = k;
-          c.kv_begin = k * kv / np;
-          c.kv_tiles = (k + 1) * kv / np;
+          c.kv_begin = kb0 + k * kv / np;
+          c.kv_tiles = kb0 + (k + 1) * kv / np;
           out.push_back(c);
         }
         if (np > 1) {
@@ -508,7 +518,7 @@ hb_status hb_plan(const hb_batch* batch, const int32_t* h_q_len,
     DecodePartition part;
     if (!partition_decode(S, h_q_len, h_context_len, n_blocks, kvhb, std::max(1, decode_ctas), 4,
                           dec.data(), (int)dec.size(), cta_off.data(), std::max(1, decode_ctas),
-                          &part))
+                          &part, W))
       return fail(HB_ERR_WORKSPACE, "decode partition overflow");
     dec.resize(part.n_items);
     cta_off.resize(part.grid + 1);
@@ -561,6 +571,7 @@ hb_status hb_plan(const hb_batch* batch, const int32_t* h_q_len,
     h.chunk_tokens_per_tile = tpt;
     h.num_chunk_slots = n_cslots;
     h.num_chunk_merges = n_cmerge;
+    h.sliding_window = W;
     h.ws_chunk_counters = ws_chunk_counters;
     h.ws_chunk_o = ws_chunk_o;
     h.ws_chunk_ml = ws_chunk_ml;
@@ -611,7 +622,8 @@ hb_status hb_attention(const hb_batch* batch, const void* h_plan, const void* q,
     if (h.num_seqs != batch->num_seqs || h.total_q != batch->total_q ||
         h.num_q_heads != batch->num_q_heads || h.num_kv_heads != batch->num_kv_heads ||
         h.head_dim != batch->head_dim || h.page_size != batch->page_size ||
-        h.max_pages_per_seq != batch->max_pages_per_seq)
+        h.max_pages_per_seq != batch->max_pages_per_seq ||
+        h.sliding_window != batch->sliding_window)
       return fail(HB_ERR_WORKSPACE, "plan was made for a different batch geometry");
     if (batch->total_q == 0) return ok();
     if (!(softmax_scale > 0.f) && !(softmax_scale <= 0.f))
@@ -670,6 +682,7 @@ hb_status hb_attention(const hb_batch* batch, const void* h_plan, const void* q,
       dp.num_kv_heads = Hkv;
       dp.scale_log2 = scale_log2;
       dp.dev_error = dev->err;
+      dp.window = batch->sliding_window;
     }
     ChunkParams cp{};
     cp.group = g;
@@ -699,6 +712,7 @@ hb_status hb_attention(const hb_batch* batch, const void* h_plan, const void* q,
       cp.tokens_per_tile = tpt;
       cp.scale_log2 = scale_log2;
       cp.dev_error = dev->err;
+      cp.window = batch->sliding_window;
       cp.counters = reinterpret_cast<int32_t*>(ws + h.ws_chunk_counters);
       cp.part_o = reinterpret_cast<float*>(ws + h.ws_chunk_o);
       cp.part_ml = reinterpret_cast<float*>(ws + h.ws_chunk_ml);

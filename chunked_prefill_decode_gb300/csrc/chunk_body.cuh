@@ -195,9 +195,12 @@ __device__ __forceinline__ void chunk_cta(const ChunkParams& p, const CUtensorMa
     // then).  Pages past the context are marked and fetched out of range,
     // i.e. as zeros.
     constexpr int kPastContext = INT_MIN;
+    // with a sliding window, pages that end at or below the item's lowest
+    // visible key are never looked up either (their entries may be stale)
+    const int lowest_key = p.window > 0 ? off + it.tok0 - p.window + 1 : 0;
     auto load_batch = [&](int b) -> int {
       const int lp = (jb + b * kTilesPerBatch) * kPagesPerTile + lane;
-      if (lp >= n_pages) return kPastContext;
+      if (lp >= n_pages || (lp + 1) * kPageSize <= lowest_key) return kPastContext;
       return lp < p.max_pages_per_seq ? __ldg(&bt_row[lp]) : -1;
     };
     auto phys_of = [&](int raw) -> int {
@@ -396,6 +399,11 @@ __device__ __forceinline__ void chunk_cta(const ChunkParams& p, const CUtensorMa
     const int tok_rel = tok0_t + tok_local;
     const int pos = valid_row ? off + tok_rel : ctx - 1;   // absolute position
     const int min_pos = off + tok0_t;
+    // sliding window: row sees keys pos - W + 1 .. pos; a key tile below the
+    // window edge of the tile's last row needs the lower mask
+    const int max_pos = off + tok0_t + (t ? ntokB : ntokA) - 1;
+    const int win_lo = p.window > 0 ? pos - p.window + 1 : INT_MIN;
+    const int tile_lo = p.window > 0 ? max_pos - p.window + 1 : INT_MIN;
     const float sl2 = p.scale_log2;
     const uint32_t s_col = t_lane + t * kChunkKeys;
     const uint32_t o_col = t_lane + C::kOCol + t * D;
@@ -409,8 +417,9 @@ __device__ __forceinline__ void chunk_cta(const ChunkParams& p, const CUtensorMa
       if (!__all_sync(0xffffffffu, mbar_wait(&s_full[t], (uint32_t)j & 1u, abort_flag))) { ok = false; break; }
       tc_fence_after_sync();
       const int kbase = (jb + j) * kChunkKeys;
-      const bool masked = kbase + kChunkKeys - 1 > min_pos;
+      const bool masked = kbase + kChunkKeys - 1 > min_pos || kbase < tile_lo;
       const int lim = pos - kbase;   // keys 0..lim of this tile are visible
+      const int lo_lim = win_lo == INT_MIN ? INT_MIN : win_lo - kbase;   // .. and lo_lim..
       uint32_t sr[kChunkKeys];
 #pragma unroll
       for (int q = 0; q < kChunkKeys / 32; ++q) tmem_ld32(s_col + q * 32, sr + q * 32);
@@ -418,7 +427,7 @@ __device__ __forceinline__ void chunk_cta(const ChunkParams& p, const CUtensorMa
       if (masked) {
 #pragma unroll
         for (int i = 0; i < kChunkKeys; ++i)
-          if (i > lim) sr[i] = __float_as_uint(-INFINITY);
+          if (i > lim || i < lo_lim) sr[i] = __float_as_uint(-INFINITY);
       }
       float mxp[8];
 #pragma unroll
@@ -552,6 +561,9 @@ __device__ __forceinline__ void chunk_cta(const ChunkParams& p, const CUtensorMa
     const int tok_rel = it.tok0 + tok_local;
     const int pos = valid_row ? off + tok_rel : ctx - 1;   // absolute position
     const int min_pos = off + it.tok0;
+    // sliding window: row sees keys pos - W + 1 .. pos
+    const int win_lo = p.window > 0 ? pos - p.window + 1 : INT_MIN;
+    const int tile_lo = p.window > 0 ? off + it.tok0 + ntokA - p.window : INT_MIN;
     // per slot: running maximum (scaled log2 units) and this half's row sum
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
     const int zero_slot = (n_all - 1) & 1;
@@ -564,8 +576,9 @@ __device__ __forceinline__ void chunk_cta(const ChunkParams& p, const CUtensorMa
       const bool got_s = mbar_wait(&s_full[t], u & 1u, abort_flag);
       tc_fence_after_sync();
       const int kbase = (jb + j) * kChunkKeys;
-      const bool masked = kbase + kChunkKeys - 1 > min_pos;
+      const bool masked = kbase + kChunkKeys - 1 > min_pos || kbase < tile_lo;
       const int lim = pos - kbase;   // keys 0..lim of this tile are visible
+      const int lo_lim = win_lo == INT_MIN ? INT_MIN : win_lo - kbase;   // .. and lo_lim..
       const uint32_t s_col = t_lane + t * kChunkKeys;
       // tcgen05.ld / tcgen05.st are warp-collective: every lane executes
       // each of them; rows that hold no query only change the arithmetic
@@ -580,10 +593,12 @@ __device__ __forceinline__ void chunk_cta(const ChunkParams& p, const CUtensorMa
       if (!named_bar_and(bar_pair, 64, got_s)) { ok = false; break; }
       if (masked) {
         const int lim_own = lim - c_own, lim_oth = lim - c_oth;
+        const int lo_own = lo_lim == INT_MIN ? INT_MIN : lo_lim - c_own;
+        const int lo_oth = lo_lim == INT_MIN ? INT_MIN : lo_lim - c_oth;
 #pragma unroll
         for (int i = 0; i < 64; ++i) {
-          if (i > lim_own) own[i] = __float_as_uint(-INFINITY);
-          if (i > lim_oth) oth[i] = __float_as_uint(-INFINITY);
+          if (i > lim_own || i < lo_own) own[i] = __float_as_uint(-INFINITY);
+          if (i > lim_oth || i < lo_oth) oth[i] = __float_as_uint(-INFINITY);
         }
       }
       float mxp[8];

@@ -282,6 +282,8 @@ __device__ __forceinline__ void decode_cta(const DecodeParams& p, const DecodeLa
         const uint32_t kbase = smem_u32(kst);
         const uint32_t vbase = smem_u32(vst);
         const int valid = min(kPageSize, h.item.ctx - h.lpage * kPageSize);
+        // with a sliding window the row sees keys ctx - W .. ctx - 1 only
+        const int lo_valid = p.window > 0 ? h.item.ctx - p.window - h.lpage * kPageSize : 0;
         if (valid < kPageSize) {
           // Slots past the context were never written: clear this kv head's
           // V rows there so that P = 0 never meets a NaN in the PV product.
@@ -330,7 +332,7 @@ __device__ __forceinline__ void decode_cta(const DecodeParams& p, const DecodeLa
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
               const int t = nt * 8 + cq * 2 + e;
-              v[nt * 2 + e] = (t < valid) ? s[nt][hr * 2 + e] * p.scale_log2 : -INFINITY;
+              v[nt * 2 + e] = (t < valid && t >= lo_valid) ? s[nt][hr * 2 + e] * p.scale_log2 : -INFINITY;
             }
           float mx = fmaxf(fmaxf(v[0], v[1]), fmaxf(v[2], v[3]));
           mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));

@@ -26,18 +26,26 @@ struct DecodePartition {
   int64_t pages_per_cta = 0;
 };
 
+// First logical page a decode row of context ctx reads: 0, or with a sliding
+// window of W tokens the page of key ctx - W (the row sees keys ctx-W .. ctx-1).
+inline int decode_first_page(int ctx, int window) {
+  return window > 0 && ctx > window ? (ctx - window) / kPageSize : 0;
+}
+
 // rows: S sequences with q_len[i], ctx[i]; rows with q_len != 1 are skipped.
 // Writes items (capacity max_items) in CTA order and cta_offsets[grid + 1].
 // Returns false if max_items (or max_grid + 1 offsets) would overflow.
 inline bool partition_decode(int S, const int32_t* q_len, const int32_t* ctx, int n_blocks,
                              int kvhb, int num_sms, int min_pages_per_cta,
                              DecodeItem* items, int max_items, int32_t* cta_offsets,
-                             int max_grid, DecodePartition* out) {
+                             int max_grid, DecodePartition* out, int window = 0) {
   DecodePartition r;
   int64_t total = 0;
   int32_t tok = 0;
   for (int i = 0; i < S; ++i)
-    if (q_len[i] == 1) total += (int64_t)((ctx[i] + kPageSize - 1) / kPageSize) * n_blocks;
+    if (q_len[i] == 1)
+      total += (int64_t)((ctx[i] + kPageSize - 1) / kPageSize - decode_first_page(ctx[i], window)) *
+               n_blocks;
   if (total == 0) {
     *out = r;
     return true;
@@ -55,7 +63,8 @@ inline bool partition_decode(int S, const int32_t* q_len, const int32_t* ctx, in
     const int32_t this_tok = tok;
     tok += q_len[i];
     if (q_len[i] != 1) continue;
-    const int64_t np = (ctx[i] + kPageSize - 1) / kPageSize;
+    const int first = decode_first_page(ctx[i], window);
+    const int64_t np = (ctx[i] + kPageSize - 1) / kPageSize - first;
     for (int blk = 0; blk < n_blocks; ++blk) {
       const int64_t a = pos, e = pos + np;
       const int64_t first_cta = a / per, last_cta = (e - 1) / per;
@@ -72,8 +81,8 @@ inline bool partition_decode(int S, const int32_t* q_len, const int32_t* ctx, in
         it = DecodeItem{};
         it.seq = i;
         it.kvh0 = blk * kvhb;
-        it.page_begin = (int32_t)(std::max(a, c * per) - a);
-        it.page_end = (int32_t)(std::min(e, (c + 1) * per) - a);
+        it.page_begin = first + (int32_t)(std::max(a, c * per) - a);
+        it.page_end = first + (int32_t)(std::min(e, (c + 1) * per) - a);
         it.split = (int32_t)(c - first_cta);
         it.n_splits = pieces;
         it.slot = slot;

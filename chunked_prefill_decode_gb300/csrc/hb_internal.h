@@ -88,7 +88,7 @@ struct PlanHeader {
   int32_t chunk_tokens_per_tile;
   int32_t num_chunk_slots;     // partial states of split chunk tiles
   int32_t num_chunk_merges;    // split chunk tiles
-  int32_t pad0;
+  int32_t sliding_window;      // the batch's window (the plan depends on it)
   uint64_t ws_decode_offsets;  // device offset of the per-CTA item offsets
   uint64_t items_bytes;     // bytes of the item arrays (host and device)
   uint64_t ws_counters;     // device offsets (bytes from workspace start)
@@ -126,6 +126,7 @@ struct DecodeParams {
   int32_t num_q_heads, num_kv_heads, group, kvh_block;
   float scale_log2;       // softmax scale * log2(e)
   int* dev_error;         // device error word
+  int32_t window;         // sliding window in tokens, 0 = none
 };
 
 struct ChunkParams {
@@ -143,6 +144,7 @@ struct ChunkParams {
   int32_t* counters;      // [merges]: arrivals of the pieces of a split tile
   float* part_o;          // [slots, D, 128]: unnormalised O, row fastest
   float* part_ml;         // [slots, 2, 128]: row maximum (log2 units), row sum
+  int32_t window;         // sliding window in tokens, 0 = none
 };
 
 struct AppendParams {

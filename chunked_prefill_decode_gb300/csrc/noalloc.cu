@@ -124,7 +124,7 @@ extern "C" hb_status hb_decode_attention_noalloc(const hb_batch* batch, const in
     DecodePartition part;
     for (;;) {
       if (!partition_decode(S, h_q_len, h_context_len, n_blocks, kvhb, num_sms, 4, g_items,
-                            kMaxItems, g_offsets, max_grid, &part))
+                            kMaxItems, g_offsets, max_grid, &part, batch->sliding_window))
         return internal_fail(HB_ERR_WORKSPACE,
                              "batch needs more work items than the static scratch holds "
                              "(at most 4096 = num_seqs * ceil(Hkv / 8) plus one per SM)");
@@ -171,6 +171,7 @@ extern "C" hb_status hb_decode_attention_noalloc(const hb_batch* batch, const in
     p.kvh_block = kvhb;
     p.scale_log2 = softmax_scale * 1.4426950408889634f;
     p.dev_error = err;
+    p.window = batch->sliding_window;
     ChunkParams none{};
     none.group = g;
     CUtensorMap unused;

@@ -26,7 +26,7 @@ class DeviceBatch:
 
 def device_batch(q_len, context_len, block_table, num_pages, num_q_heads,
                  num_kv_heads, head_dim, page_size=16, device="cuda",
-                 non_blocking=False) -> DeviceBatch:
+                 non_blocking=False, sliding_window=0) -> DeviceBatch:
     ql = np.ascontiguousarray(q_len, dtype=np.int32)
     cl = np.ascontiguousarray(context_len, dtype=np.int32)
     bt = np.ascontiguousarray(block_table, dtype=np.int32)
@@ -39,7 +39,7 @@ def device_batch(q_len, context_len, block_table, num_pages, num_q_heads,
     bt_d = torch.from_numpy(bt).to(device, non_blocking=non_blocking)
     b = hb.make_batch(ql.shape[0], int(cu[-1]), max(1, bt.shape[1]), num_pages,
                       num_q_heads, num_kv_heads, head_dim, cu_d, cl_d, bt_d,
-                      page_size=page_size)
+                      page_size=page_size, sliding_window=sliding_window)
     return DeviceBatch(b, ql, cl, cu_d, cl_d, bt_d)
 
 
@@ -48,4 +48,5 @@ def from_layout(layout, device="cuda") -> DeviceBatch:
     sh = layout.shape
     return device_batch(layout.q_len, layout.context_len, layout.block_table,
                         layout.num_pages, sh.num_q_heads, sh.num_kv_heads,
-                        sh.head_dim, sh.page_size, device)
+                        sh.head_dim, sh.page_size, device,
+                        sliding_window=sh.sliding_window)

@@ -44,6 +44,8 @@ class HbBatch(ctypes.Structure):
         ("num_kv_heads", ctypes.c_int32),
         ("head_dim", ctypes.c_int32),
         ("page_size", ctypes.c_int32),
+        ("sliding_window", ctypes.c_int32),
+        ("reserved", ctypes.c_int32),
         ("cu_q_len", ctypes.c_void_p),
         ("context_len", ctypes.c_void_p),
         ("block_table", ctypes.c_void_p),
@@ -148,7 +150,7 @@ def _stream(stream):
 
 def make_batch(num_seqs, total_q, max_pages_per_seq, num_pages, num_q_heads,
                num_kv_heads, head_dim, cu_q_len, context_len, block_table,
-               page_size=16) -> HbBatch:
+               page_size=16, sliding_window=0) -> HbBatch:
     """hb_batch over device int32 tensors (kept alive by the caller)."""
     for name, t in (("cu_q_len", cu_q_len), ("context_len", context_len),
                     ("block_table", block_table)):
@@ -160,6 +162,7 @@ def make_batch(num_seqs, total_q, max_pages_per_seq, num_pages, num_q_heads,
     b.max_pages_per_seq, b.num_pages = int(max_pages_per_seq), int(num_pages)
     b.num_q_heads, b.num_kv_heads = int(num_q_heads), int(num_kv_heads)
     b.head_dim, b.page_size = int(head_dim), int(page_size)
+    b.sliding_window, b.reserved = int(sliding_window), 0
     b.cu_q_len = _ptr(cu_q_len).value if _ptr(cu_q_len) is not None else None
     b.context_len = _ptr(context_len).value if _ptr(context_len) is not None else None
     b.block_table = _ptr(block_table).value if _ptr(block_table) is not None else None
@@ -236,7 +239,7 @@ def plan_header(plan):
             "head_dim", "page_size", "max_pages_per_seq", "num_sms",
             "num_decode_items", "num_chunk_items", "num_partial_slots",
             "num_merge_counters", "decode_grid", "decode_kvh_block",
-            "chunk_tokens_per_tile", "num_chunk_slots", "num_chunk_merges", "pad0")
+            "chunk_tokens_per_tile", "num_chunk_slots", "num_chunk_merges", "sliding_window")
     out = {k: int(v) for k, v in zip(keys, h)}
     u = np.frombuffer(plan[80:HEADER_BYTES].tobytes(), dtype=np.uint64)
     for k, v in zip(("ws_decode_offsets", "items_bytes", "ws_counters", "ws_partial_o",

@@ -37,11 +37,13 @@ SENTINEL_BITS = 0x7FC1
 
 @dataclass
 class Shape:
-    """Head geometry of one attention layer."""
+    """Head geometry of one attention layer (sliding_window 0: full causal;
+    W > 0: a query at position p sees keys p - W + 1 .. p)."""
     num_q_heads: int
     num_kv_heads: int
     head_dim: int
     page_size: int = PAGE_SIZE
+    sliding_window: int = 0
 
 
 @dataclass
@@ -145,6 +147,16 @@ def mistral_b512(seed: int = 1) -> BatchLayout:
     return layout_from_rows(shape, rows, seed)
 
 
+def mistral_b512_window(seed: int = 1, window: int = 1024) -> BatchLayout:
+    """The Mistral-7B batch of mistral_b512 with sliding-window attention of
+    `window` tokens.  The pages name sliding-window variants without a size;
+    1024 is below the decode rows' median context (2145), so the window
+    binds for most rows."""
+    lay = mistral_b512(seed)
+    lay.shape = Shape(32, 8, 128, sliding_window=window)
+    return lay
+
+
 def yi_b2048(seed: int = 2, offset: int = 6048) -> BatchLayout:
     """Yi-34B attention shape (56 q / 8 kv heads, head_dim 128), budget 2048:
     32 decode rows with context ~ lognormal(median 7267 = 7059 + 208) clipped
@@ -187,6 +199,7 @@ def chunk_sweep(chunk: int, index: int | None = None, seed: int = 4,
 WORKLOADS = {
     "tiny": tiny,
     "mistral_b512": mistral_b512,
+    "mistral_b512_window": mistral_b512_window,
     "yi_b2048": yi_b2048,
     "decode_only": decode_only,
 }

@@ -79,7 +79,15 @@ const char* hb_last_error(void);
 /* Name of a status code (static string). */
 const char* hb_status_string(hb_status s);
 
-/* Descriptor of one hybrid batch.  The three arrays are DEVICE pointers. */
+/* Descriptor of one hybrid batch.  The three arrays are DEVICE pointers.
+ *
+ * sliding_window: 0 for full causal attention; W > 0 restricts the query at
+ * absolute position p to the keys p-W+1 .. p (W keys, itself included).  The
+ * pages name sliding-window model variants ("Sarathi-Serve: Chunked Prefills
+ * for Stall-Free LLM Inference", §Results and evidence) without a size, so W
+ * is a parameter.  With W > 0 the kernels never read the block-table entry
+ * of a page that holds no key inside any of its row's windows (such entries
+ * may be stale). */
 typedef struct hb_batch {
   int32_t num_seqs;            /* sequences (rows of the batch), >= 0         */
   int32_t total_q;             /* sum of q_len = rows of q / k_new / out      */
@@ -89,6 +97,8 @@ typedef struct hb_batch {
   int32_t num_kv_heads;
   int32_t head_dim;
   int32_t page_size;           /* tokens per page; must be 16                 */
+  int32_t sliding_window;      /* 0: none; W > 0: keys p-W+1 .. p (above)     */
+  int32_t reserved;            /* must be 0                                   */
   const int32_t* cu_q_len;     /* [num_seqs+1] prefix sums of q_len, [0] = 0  */
   const int32_t* context_len;  /* [num_seqs] tokens in cache AFTER append     */
   const int32_t* block_table;  /* [num_seqs * max_pages_per_seq] page ids     */

@@ -27,7 +27,7 @@ def gpu_step(layout, ten, scale=None, repeats=1, check=True):
     dev = torch.device("cuda:0")
     db = device_batch(layout.q_len, layout.context_len, layout.block_table,
                       layout.num_pages, sh.num_q_heads, sh.num_kv_heads, sh.head_dim,
-                      sh.page_size, dev)
+                      sh.page_size, dev, sliding_window=sh.sliding_window)
     q, kn, vn = (t.to(dev) for t in (ten.q, ten.k_new, ten.v_new))
     kc, vc = ten.k_cache.to(dev).clone(), ten.v_cache.to(dev).clone()
     out = torch.full_like(q, float("nan"))
@@ -49,7 +49,7 @@ def oracle_step(layout, ten, scale=None, tokens=None):
                           layout.block_table, sh.page_size)
     ref = pa.attention(bits(ten.q), kp, vp, layout.q_len, layout.context_len,
                        layout.block_table, sh.page_size, sh.num_q_heads,
-                       sh.num_kv_heads, scale, tokens=tokens)
+                       sh.num_kv_heads, scale, tokens=tokens, window=sh.sliding_window)
     return kp, vp, ref
 
 

@@ -31,7 +31,7 @@ def header_functions():
     return sorted(names)
 
 
-def host_batch(hb, rows, hq=32, hkv=8, d=128, max_pages=None, num_pages=None):
+def host_batch(hb, rows, hq=32, hkv=8, d=128, max_pages=None, num_pages=None, window=0):
     """hb_batch with fake (never dereferenced) device pointers, for host-only
     calls such as hb_plan without a workspace."""
     import numpy as np
@@ -41,7 +41,7 @@ def host_batch(hb, rows, hq=32, hkv=8, d=128, max_pages=None, num_pages=None):
     npg = num_pages or max(1, int(sum(-(-c // 16) for c in cl)))
     fake = 0x1000
     b = hb.make_batch(len(rows), int(ql.sum()), mp, npg, hq, hkv, d,
-                      None, None, None)
+                      None, None, None, sliding_window=window)
     if len(rows):
         b.cu_q_len = b.context_len = b.block_table = fake
     return b, ql, cl

@@ -118,9 +118,9 @@ def test_cuda_calls_fail_cleanly_without_a_gpu():
     assert st == 5
 
 
-def _check_plan(rows, hq, hkv, d, sms):
+def _check_plan(rows, hq, hkv, d, sms, window=0):
     hb = lib()
-    b, ql, cl = host_batch(hb, rows, hq=hq, hkv=hkv, d=d)
+    b, ql, cl = host_batch(hb, rows, hq=hq, hkv=hkv, d=d, window=window)
     plan, _ = hb.hb_plan(b, ql, cl, sms, upload=False)
     h = hb.plan_header(plan)
     dec, chk, offs = hb.plan_items(plan)
@@ -148,9 +148,10 @@ def _check_plan(rows, hq, hkv, d, sms):
         if ql[s] != 1:
             continue
         npg = -(-cl[s] // 16)
+        first = (cl[s] - window) // 16 if 0 < window < cl[s] else 0
         for kvh0 in range(0, hkv, kvhb):
             parts = sorted(cover[(s, kvh0)])
-            assert parts[0][0] == 0 and parts[-1][1] == npg
+            assert parts[0][0] == first and parts[-1][1] == npg
             assert all(a[1] == b_[0] for a, b_ in zip(parts, parts[1:]))
             ns = parts[0][3]
             assert len(parts) == ns and [p[2] for p in parts] == list(range(ns))
@@ -180,7 +181,8 @@ def _check_plan(rows, hq, hkv, d, sms):
         off = cl[seq] - ql[seq]
         # the pieces tile the key range of the query tile(s) exactly once
         assert [p[0] for p in parts] == list(range(ns))
-        assert parts[0][1] == 0 and parts[-1][2] == -(-(off + t0 + nt) // 128)
+        kb0 = max(0, off + t0 - window + 1) // 128 if window > 0 else 0
+        assert parts[0][1] == kb0 and parts[-1][2] == -(-(off + t0 + nt) // 128)
         assert all(a[2] == b_[1] for a, b_ in zip(parts, parts[1:]))
         assert len({(p[3], p[4], p[5], p[6]) for p in parts}) == 1
         if ns > 1:
@@ -200,13 +202,15 @@ def _check_plan(rows, hq, hkv, d, sms):
     return h
 
 
-@pytest.mark.parametrize("name", ["tiny", "mistral_b512", "yi_b2048", "decode_only"])
+@pytest.mark.parametrize("name", ["tiny", "mistral_b512", "mistral_b512_window", "yi_b2048",
+                                  "decode_only"])
 def test_plan_covers_workloads(name):
     from chunked_prefill_decode_gb300 import workloads
     lay = workloads.WORKLOADS[name]()
     sh = lay.shape
     rows = list(zip(lay.q_len.tolist(), lay.context_len.tolist()))
-    h = _check_plan(rows, sh.num_q_heads, sh.num_kv_heads, sh.head_dim, 152)
+    h = _check_plan(rows, sh.num_q_heads, sh.num_kv_heads, sh.head_dim, 152,
+                    window=sh.sliding_window)
 
 
 def test_plan_edge_shapes():
@@ -214,6 +218,40 @@ def test_plan_edge_shapes():
     _check_plan([(1, 5000), (257, 8192)], 56, 8, 128, 152)
     _check_plan([(1, 333), (9, 40)], 16, 16, 128, 8)    # 2 kv blocks of 8
     _check_plan([(1, 100), (3, 3)], 4, 2, 64, 152)      # kv block of 2
+
+
+@pytest.mark.parametrize("window", [1, 15, 16, 17, 300, 4096, 100000])
+def test_plan_with_sliding_window(window):
+    """Decode ranges start at the window's first page; chunk items start at
+    the first key tile their first row sees; the header records the window."""
+    rows = [(1, 1), (1, 17), (1, 5000), (1, 333), (257, 8192), (40, 45), (1, 3000)]
+    h = _check_plan(rows, 32, 8, 128, 148, window=window)
+    assert h["sliding_window"] == window
+    _check_plan(rows, 8, 8, 64, 8, window=window)
+
+
+def test_attention_rejects_plan_of_another_window():
+    hb = lib()
+    L = hb.load()
+    b, ql, cl = host_batch(hb, [(1, 500), (9, 90)], window=64)
+    plan, _ = hb.hb_plan(b, ql, cl, 148, upload=False)
+    b2, _, _ = host_batch(hb, [(1, 500), (9, 90)], window=0)
+    assert L.hb_attention(ctypes.byref(b2), hb._ptr(plan), None, None, None, 1.0,
+                          None, None, None) == 4
+
+
+def test_negative_window_and_reserved_field_are_rejected():
+    hb = lib()
+    L = hb.load()
+    b, ql, cl = host_batch(hb, [(1, 50)])
+    b.sliding_window = -1
+    assert L.hb_plan(ctypes.byref(b), hb._ptr(ql), hb._ptr(cl), 148, None,
+                     ctypes.byref(ctypes.c_size_t(0)), None,
+                     ctypes.byref(ctypes.c_size_t(0)), None) == 2
+    b.sliding_window, b.reserved = 0, 7
+    assert L.hb_plan(ctypes.byref(b), hb._ptr(ql), hb._ptr(cl), 148, None,
+                     ctypes.byref(ctypes.c_size_t(0)), None,
+                     ctypes.byref(ctypes.c_size_t(0)), None) == 1
 
 
 def test_plan_splits_short_chunks_at_long_offsets():

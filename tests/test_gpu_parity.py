@@ -84,6 +84,36 @@ def test_split_key_ranges(geom, rows):
     _full_check(layout_from_rows(Shape(hq, hkv, d), rows, 14), seed=14, repeats=3)
 
 
+WINDOW_ROWS = [(1, 1), (1, 17), (1, 700), (1, 3000), (5, 37), (130, 700), (64, 4160),
+               (257, 2000), (1, 129)]
+
+
+@pytest.mark.parametrize("window", [1, 7, 16, 100, 1000, 5000])
+@pytest.mark.parametrize("geom", [(8, 8, 64), (32, 8, 128), (56, 8, 128)])
+def test_sliding_window(window, geom):
+    """Sliding-window attention: decode rows start their page range at the
+    window, chunk tiles their key range, and both mask the window's edge."""
+    hq, hkv, d = geom
+    _full_check(layout_from_rows(Shape(hq, hkv, d, sliding_window=window), WINDOW_ROWS, 15),
+                seed=15, repeats=2)
+
+
+@pytest.mark.parametrize("window", [16, 100, 1000])
+def test_sliding_window_never_reads_pages_below_it(window):
+    """Block-table entries of pages below every window of their row are set
+    to -1 (as a cache that has freed them would): no index error, same result."""
+    lay = layout_from_rows(Shape(32, 8, 128, sliding_window=window), WINDOW_ROWS, 16)
+    ten = workloads.make_tensors(lay, 16)
+    P = lay.shape.page_size
+    for s in range(lay.num_seqs):
+        lowest = int(lay.context_len[s] - lay.q_len[s]) - window + 1
+        n_below = max(0, lowest) // P
+        lay.block_table[s, :n_below] = -1
+    kc, vc, out = gpu_step(lay, ten)          # hb_check raises on an index error
+    _, _, ref = oracle_step(lay, ten)
+    compare(out, ref)
+
+
 def test_several_chunks_and_decodes():
     rows = [(1, 900)] * 7 + [(200, 456), (57, 57), (300, 2000), (1, 5)]
     _full_check(layout_from_rows(Shape(32, 8, 128), rows, 13), seed=13)
@@ -166,7 +196,8 @@ def test_timing_and_launch_count():
 def _full_size(name, n_seq_sample=6, n_chunk_tok=48, seed=None, lay=None):
     if lay is None:
         lay = workloads.WORKLOADS[name]()
-    seed = {"mistral_b512": 1, "yi_b2048": 2, "decode_only": 3}.get(name, 0) if seed is None else seed
+    seed = {"mistral_b512": 1, "mistral_b512_window": 1, "yi_b2048": 2,
+            "decode_only": 3}.get(name, 0) if seed is None else seed
     ten = workloads.make_tensors(lay, seed, device="cuda")
     kc, vc, out = gpu_step(lay, ten)
     rng = np.random.default_rng(seed)
@@ -207,7 +238,7 @@ def _full_size(name, n_seq_sample=6, n_chunk_tok=48, seed=None, lay=None):
 
 
 @pytest.mark.slow
-@pytest.mark.parametrize("name", ["mistral_b512", "yi_b2048", "decode_only"])
+@pytest.mark.parametrize("name", ["mistral_b512", "mistral_b512_window", "yi_b2048", "decode_only"])
 def test_full_size_workloads(name):
     _full_size(name)
 
