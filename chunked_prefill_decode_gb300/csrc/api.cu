@@ -25,6 +25,8 @@ __device__ int g_hb_device_error = 0;
 
 namespace hb {
 cudaError_t launch_kv_append(const AppendParams& p, int num_sms, cudaStream_t stream);
+cudaError_t launch_linear(const LinearParams& p, const CUtensorMap& xmap, const CUtensorMap& wmap,
+                          int num_sms, cudaStream_t stream);
 cudaError_t launch_wait_timeout(int* dev_error, cudaStream_t stream);
 cudaError_t launch_attention(const DecodeParams& dec, int decode_grid, const ChunkParams& chk,
                              int head_dim, const CUtensorMap& dec_k, const CUtensorMap& dec_v,
@@ -298,6 +300,68 @@ hb_status hb_kv_append(const hb_batch* batch, const void* k_new, const void* v_n
     return ok();
   } catch (...) {
     return fail(HB_ERR_CUDA, "unexpected exception in hb_kv_append");
+  }
+}
+
+hb_status hb_linear(const void* x, const void* w, int32_t M, int32_t N, int32_t K,
+                    int32_t epilogue, const hb_linear_out* out, void* stream) {
+  try {
+    if (!out) return fail(HB_ERR_INVALID_ARG, "out is NULL");
+    if (epilogue < HB_LINEAR_STORE || epilogue > HB_LINEAR_RESIDUAL)
+      return fail(HB_ERR_INVALID_ARG, "unknown epilogue %d", epilogue);
+    if (M < 0 || N <= 0 || K <= 0) return fail(HB_ERR_SHAPE, "M %d, N %d, K %d", M, N, K);
+    if (K % 64) return fail(HB_ERR_SHAPE, "K (%d) must be a multiple of 64", K);
+    hb_status s;
+    if ((s = check_ptr(x, "x")) != HB_OK) return s;
+    if ((s = check_ptr(w, "w")) != HB_OK) return s;
+    LinearParams p{};
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.epilogue = epilogue;
+    if (epilogue == HB_LINEAR_GATED) {
+      if (N % 256) return fail(HB_ERR_SHAPE, "gated: N = 2F (%d) must be a multiple of 256", N);
+      p.F = N / 2;
+      if (out->cols[0] != p.F || out->cols[1] != 0 || out->cols[2] != 0)
+        return fail(HB_ERR_SHAPE, "gated: cols must be {F, 0, 0} with F = %d", p.F);
+    } else {
+      if (N % 256) return fail(HB_ERR_SHAPE, "N (%d) must be a multiple of 256", N);
+      int64_t sum = 0;
+      for (int i = 0; i < 3; ++i) {
+        if (out->cols[i] < 0 || out->cols[i] % 256)
+          return fail(HB_ERR_SHAPE, "cols[%d] = %d: multiples of 256 needed", i, out->cols[i]);
+        sum += out->cols[i];
+      }
+      if (sum != N) return fail(HB_ERR_SHAPE, "cols sum to %lld, N is %d", (long long)sum, N);
+    }
+    for (int i = 0; i < 3; ++i) {
+      if (out->cols[i] == 0) continue;
+      if ((s = check_ptr(out->y[i], "out->y[i]")) != HB_OK) return s;
+      p.y[i] = static_cast<uint16_t*>(out->y[i]);
+      p.seg_cols[i] = out->cols[i];
+    }
+    if (M == 0) return ok();
+    DevState* dev = nullptr;
+    if ((s = device_state(&dev)) != HB_OK) return s;
+    if ((s = get_encoder()) != HB_OK) return s;
+    p.dev_error = dev->err;
+    CUtensorMap xmap, wmap;
+    const cuuint64_t xdims[2] = {(cuuint64_t)K, (cuuint64_t)M};
+    const cuuint64_t xstr[1] = {(cuuint64_t)K * 2};
+    const cuuint32_t xbox[2] = {64, 128};
+    if ((s = encode_map(&xmap, x, 2, xdims, xstr, xbox, "linear x")) != HB_OK) return s;
+    const cuuint64_t wdims[2] = {(cuuint64_t)K, (cuuint64_t)N};
+    const cuuint32_t wbox[2] = {64, (cuuint32_t)(epilogue == HB_LINEAR_GATED ? 128 : 256)};
+    if ((s = encode_map(&wmap, w, 2, wdims, xstr, wbox, "linear w")) != HB_OK) return s;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    LaunchTimer t(2, st);
+    cudaError_t e = launch_linear(p, xmap, wmap, dev->num_sms, st);
+    t.done();
+    if (e != cudaSuccess) return cuda_fail(e, "linear launch");
+    g_launches.fetch_add(1);
+    return ok();
+  } catch (...) {
+    return fail(HB_ERR_CUDA, "unexpected exception in hb_linear");
   }
 }
 

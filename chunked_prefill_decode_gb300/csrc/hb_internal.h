@@ -147,6 +147,19 @@ struct ChunkParams {
   int32_t window;         // sliding window in tokens, 0 = none
 };
 
+// Linear layer y = x W^T (linear.cu).  epilogue: 0 store, 1 gated (W has
+// 2F rows [gate; up], y[0] receives silu(g) * u, F columns), 2 residual
+// (y += x W^T).  Output columns are split over up to three destinations:
+// y[i] receives seg_cols[i] consecutive columns with row stride seg_cols[i].
+struct LinearParams {
+  int32_t M, N, K;
+  int32_t epilogue;
+  int32_t F;
+  uint16_t* y[3];
+  int32_t seg_cols[3];
+  int* dev_error;
+};
+
 struct AppendParams {
   const int32_t* cu_q_len;
   const int32_t* context_len;

@@ -1,0 +1,274 @@
+// linear.cu -- the linear layers around the attention step, on the tcgen05
+// tensor cores.
+//
+// "Sarathi-Serve：以 chunked-prefills 与 stall-free batching 驯服 LLM 推理的吞吐—
+// 延迟权衡", §问题背景 (两阶段天然不对称): every token of a hybrid batch goes
+// through the model's linear layers, which take most of the iteration --
+// compute-bound for prefill tokens, bound by the weight read for decodes.
+//
+// y = x W^T with x [M, K] (one row per token) and W [N, K], bf16 in, fp32
+// accumulation in tensor memory, bf16 out.  A persistent kernel: one CTA per
+// SM walks output tiles of 128 rows x 256 columns (m fastest, so CTAs that
+// run together share the weight tile through L2); per tile, 64-wide slices of
+// K stream through a 4-stage ring of shared memory by TMA (128-byte swizzle)
+// and feed tcgen05.mma M128 N256 K16; the accumulator is double-buffered in
+// TMEM (2 x 256 columns), so the epilogue of one tile overlaps the main loop
+// of the next.
+//
+// Warp roles (192 threads): warp 0 TMA producer (one thread), warp 1 TMEM
+// owner and MMA issuer (one thread), warps 2-5 epilogue (thread = output
+// row = TMEM lane; warp w reads lanes 32 (w % 4) ..).
+//
+// Epilogues: store (columns split over up to three destinations, e.g. q, k
+// and v of a fused QKV projection), gated (W = [W_gate; W_up] with 2F rows:
+// per tile two N128 accumulators, output silu(g) * u), residual (y += x W^T).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "hb_internal.h"
+#include "ptx.cuh"
+
+namespace hb {
+
+constexpr int kLinBM = 128;
+constexpr int kLinBN = 256;
+constexpr int kLinBK = 64;
+constexpr int kLinStages = 4;
+constexpr int kLinThreads = 192;
+constexpr int kLinABytes = kLinBM * kLinBK * 2;          // 16 KB
+constexpr int kLinBBytes = kLinBN * kLinBK * 2;          // 32 KB
+constexpr int kLinStageBytes = kLinABytes + kLinBBytes;  // 48 KB
+constexpr int kLinBarOff = kLinStages * kLinStageBytes;
+constexpr int kLinNumBars = 2 * kLinStages + 4 + 1;
+constexpr int kLinMiscOff = kLinBarOff + kLinNumBars * 8;
+constexpr int kLinSmemBytes = kLinMiscOff + 64 + 1024;   // + alignment slack
+static_assert(kLinSmemBytes <= 227 * 1024, "linear smem");
+
+__device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)); }
+
+__global__ void __launch_bounds__(kLinThreads, 1)
+    linear_kernel(const LinearParams p, const __grid_constant__ CUtensorMap xmap,
+                  const __grid_constant__ CUtensorMap wmap) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kLinBarOff);
+  uint64_t* full = bars;                       // [stages]
+  uint64_t* empty = full + kLinStages;         // [stages]
+  uint64_t* acc_full = empty + kLinStages;     // [2]
+  uint64_t* acc_empty = acc_full + 2;          // [2]
+  uint64_t* mma_done = acc_empty + 2;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + kLinMiscOff);
+  int* abort_i = reinterpret_cast<int*>(smem + kLinMiscOff + 16);
+  volatile int* abort_flag = abort_i;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const bool gated = p.epilogue == 1;
+  const int m_tiles = (p.M + kLinBM - 1) / kLinBM;
+  const int n_tiles = gated ? p.F / (kLinBN / 2) : p.N / kLinBN;
+  const int n_tiles_total = m_tiles * n_tiles;
+  const int k_blocks = p.K / kLinBK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kLinStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], 4 * 32);
+    }
+    mbar_init(mma_done, 1);
+    *abort_i = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_holder, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = *tmem_holder;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- producer
+    if (lane == 0) {
+      tma_prefetch_desc(&xmap);
+      tma_prefetch_desc(&wmap);
+      uint32_t g = 0;                  // k-blocks issued by this CTA so far
+      uint32_t issued = 0, par = 0;    // per stage: issued at all / last phase
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < n_tiles_total; t += gridDim.x) {
+        const int m = t % m_tiles, n = t / m_tiles;
+        for (int kb = 0; kb < k_blocks; ++kb, ++g) {
+          const int s = (int)(g % kLinStages);
+          const uint32_t ph = (g / kLinStages) & 1u;
+          if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag)) { ok = false; break; }
+          uint8_t* st = smem + s * kLinStageBytes;
+          mbar_arrive_expect_tx(&full[s], (uint32_t)kLinStageBytes);
+          tma_load_2d(st, &xmap, &full[s], kb * kLinBK, m * kLinBM);
+          if (gated) {
+            tma_load_2d(st + kLinABytes, &wmap, &full[s], kb * kLinBK, n * (kLinBN / 2));
+            tma_load_2d(st + kLinABytes + kLinBBytes / 2, &wmap, &full[s], kb * kLinBK,
+                        p.F + n * (kLinBN / 2));
+          } else {
+            tma_load_2d(st + kLinABytes, &wmap, &full[s], kb * kLinBK, n * kLinBN);
+          }
+          issued |= 1u << s;
+          par = (par & ~(1u << s)) | (ph << s);
+        }
+      }
+      // copies in flight land before the CTA exits
+      for (int s = 0; s < kLinStages; ++s)
+        if (issued & (1u << s)) drain_wait(&full[s], (par >> s) & 1u, abort_flag);
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = gated ? idesc_bf16_f32(kLinBM, kLinBN / 2, false)
+                                   : idesc_bf16_f32(kLinBM, kLinBN, false);
+      uint32_t g = 0;
+      int i = 0;                       // tiles of this CTA so far
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < n_tiles_total; t += gridDim.x, ++i) {
+        const int buf = i & 1;
+        const uint32_t use = (uint32_t)(i >> 1);
+        // the epilogue has drained this accumulator (first use: free)
+        if (!mbar_wait(&acc_empty[buf], (use & 1u) ^ 1u, abort_flag)) break;
+        tc_fence_after_sync();
+        const uint32_t acc = tmem + (uint32_t)(buf * kLinBN);
+        for (int kb = 0; kb < k_blocks; ++kb, ++g) {
+          const int s = (int)(g % kLinStages);
+          if (!mbar_wait(&full[s], (g / kLinStages) & 1u, abort_flag)) { ok = false; break; }
+          tc_fence_after_sync();
+          const uint32_t a = smem_u32(smem + s * kLinStageBytes);
+          const uint32_t b = a + kLinABytes;
+#pragma unroll
+          for (int kk = 0; kk < kLinBK / 16; ++kk) {
+            const uint64_t ad = sdesc_sw128(a + kk * 32, 16, 1024);
+            const uint32_t accum = (kb > 0 || kk > 0) ? 1u : 0u;
+            if (gated) {
+              tc_mma_bf16(acc, ad, sdesc_sw128(b + kk * 32, 16, 1024), idesc, accum);
+              tc_mma_bf16(acc + kLinBN / 2, ad,
+                          sdesc_sw128(b + kLinBBytes / 2 + kk * 32, 16, 1024), idesc, accum);
+            } else {
+              tc_mma_bf16(acc, ad, sdesc_sw128(b + kk * 32, 16, 1024), idesc, accum);
+            }
+          }
+          tc_commit(&empty[s]);         // the stage is free once these MMAs are done
+        }
+        if (ok) tc_commit(&acc_full[buf]);
+      }
+      // every MMA issued must complete before TMEM is freed
+      tc_commit(mma_done);
+      drain_wait(mma_done, 0u, abort_flag);
+    }
+  } else {
+    // ---------------------------------------------------------------- epilogue
+    const int wq = warp & 3;
+    const int row = wq * 32 + lane;
+    const uint32_t t_lane = tmem + ((uint32_t)(wq * 32) << 16);
+    int i = 0;
+    for (int t = blockIdx.x; t < n_tiles_total; t += gridDim.x, ++i) {
+      const int m = t % m_tiles, n = t / m_tiles;
+      const int buf = i & 1;
+      const uint32_t use = (uint32_t)(i >> 1);
+      const bool got = __all_sync(0xffffffffu, mbar_wait(&acc_full[buf], use & 1u, abort_flag));
+      if (!got) break;
+      tc_fence_after_sync();
+      const uint32_t acc = t_lane + (uint32_t)(buf * kLinBN);
+      const int gm = m * kLinBM + row;
+      const bool live = gm < p.M;
+      if (gated) {
+        // silu(gate) * up -> y[0] columns n * 128 ..
+        uint16_t* dst = p.y[0] + (size_t)gm * p.seg_cols[0] + n * (kLinBN / 2);
+#pragma unroll 1
+        for (int c = 0; c < kLinBN / 2 / 32; ++c) {
+          uint32_t gr[32], ur[32];
+          tmem_ld32(acc + c * 32, gr);
+          tmem_ld32(acc + kLinBN / 2 + c * 32, ur);
+          tmem_ld_wait();
+          if (live) {
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              uint32_t w4[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int k = v * 8 + e * 2;
+                w4[e] = pack_bf16x2(silu_f(__uint_as_float(gr[k])) * __uint_as_float(ur[k]),
+                                    silu_f(__uint_as_float(gr[k + 1])) * __uint_as_float(ur[k + 1]));
+              }
+              *reinterpret_cast<uint4*>(dst + c * 32 + v * 8) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+            }
+          }
+        }
+      } else {
+        // the destination segment of this 256-column tile
+        const int col0 = n * kLinBN;
+        int seg = 0, seg_start = 0;
+        while (seg < 2 && col0 >= seg_start + p.seg_cols[seg]) {
+          seg_start += p.seg_cols[seg];
+          ++seg;
+        }
+        uint16_t* dst = p.y[seg] + (size_t)gm * p.seg_cols[seg] + (col0 - seg_start);
+#pragma unroll 1
+        for (int c = 0; c < kLinBN / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld32(acc + c * 32, r);
+          tmem_ld_wait();
+          if (live) {
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32 + v * 8);
+              float f[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(r[v * 8 + e]);
+              if (p.epilogue == 2) {
+                const uint4 old = *d4;
+                const uint32_t o[4] = {old.x, old.y, old.z, old.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  f[2 * e] += bf16lo_to_f32(o[e]);
+                  f[2 * e + 1] += bf16hi_to_f32(o[e]);
+                }
+              }
+              *d4 = make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]),
+                               pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
+            }
+          }
+        }
+      }
+      // this accumulator may be overwritten now
+      tc_fence_before_sync();
+      mbar_arrive(&acc_empty[buf]);
+    }
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, 512);
+  }
+  if (threadIdx.x == 0 && *abort_flag) report_error(p.dev_error, HB_DEVERR_TIMEOUT);
+}
+
+int linear_smem_bytes() { return kLinSmemBytes; }
+
+// Persistent launch: one CTA per SM (at most one per tile).
+cudaError_t launch_linear(const LinearParams& p, const CUtensorMap& xmap, const CUtensorMap& wmap,
+                          int num_sms, cudaStream_t stream) {
+  const int m_tiles = (p.M + kLinBM - 1) / kLinBM;
+  const int n_tiles = p.epilogue == 1 ? p.F / (kLinBN / 2) : p.N / kLinBN;
+  const int tiles = m_tiles * n_tiles;
+  if (tiles == 0) return cudaSuccess;
+  const int grid = tiles < num_sms ? tiles : num_sms;
+  cudaError_t e = cudaFuncSetAttribute(linear_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       kLinSmemBytes);
+  if (e != cudaSuccess) return e;
+  linear_kernel<<<grid, kLinThreads, kLinSmemBytes, stream>>>(p, xmap, wmap);
+  return cudaGetLastError();
+}
+
+}  // namespace hb

@@ -18,8 +18,8 @@ _LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libhb.so")
 _lib = None
 
 HB_OK = 0
-HB_NUM_KERNEL_IDS = 2
-KERNEL_NAMES = ("kv_append", "attention")
+HB_NUM_KERNEL_IDS = 3
+KERNEL_NAMES = ("kv_append", "attention", "linear")
 
 STATUS_NAMES = {
     0: "HB_OK", 1: "HB_ERR_INVALID_ARG", 2: "HB_ERR_SHAPE", 3: "HB_ERR_UNSUPPORTED",
@@ -58,8 +58,14 @@ EXPORTED = (
     "hb_builder_create", "hb_builder_destroy", "hb_builder_add_request",
     "hb_builder_step", "hb_builder_complete", "hb_builder_counts",
     "hb_builder_free_list", "hb_builder_last_error", "hb_decode_attention_noalloc",
-    "hb_selftest_wait_timeout",
+    "hb_selftest_wait_timeout", "hb_linear",
 )
+
+LINEAR_STORE, LINEAR_GATED, LINEAR_RESIDUAL = 0, 1, 2
+
+
+class HbLinearOut(ctypes.Structure):
+    _fields_ = [("y", ctypes.c_void_p * 3), ("cols", ctypes.c_int32 * 3)]
 
 
 def lib_path() -> str:
@@ -93,6 +99,8 @@ def load():
     L.hb_decode_attention_noalloc.restype = ctypes.c_int
     L.hb_decode_attention_noalloc.argtypes = [P(HbBatch), vp, vp, vp, vp, vp, ctypes.c_float,
                                               vp, vp]
+    L.hb_linear.restype = ctypes.c_int
+    L.hb_linear.argtypes = [vp, vp, i32, i32, i32, i32, P(HbLinearOut), vp]
     L.hb_selftest_wait_timeout.restype = ctypes.c_int
     L.hb_selftest_wait_timeout.argtypes = [vp]
     L.hb_check.restype = ctypes.c_int
@@ -383,3 +391,20 @@ class Builder:
         _check(load().hb_builder_free_list(self._h, out.size, ctypes.byref(n), _ptr(out)),
                builder=True)
         return [int(x) for x in out[: n.value]]
+
+
+def hb_linear(x, w, outs, epilogue=LINEAR_STORE, stream=None):
+    """y = x w^T on the tensor cores.  x [M, K], w [N, K] bf16 device tensors;
+    outs: the destination tensors ([M, cols_i] bf16 each; their column
+    counts split N for STORE / RESIDUAL, one [M, N / 2] tensor for GATED)."""
+    if len(outs) > 3:
+        raise ValueError("at most three destinations")
+    o = HbLinearOut()
+    for i, t in enumerate(outs):
+        _bf16(t, "out")
+        if t.dim() != 2 or not t.is_contiguous():
+            raise ValueError("each destination must be a contiguous 2-D tensor")
+        o.y[i] = t.data_ptr()
+        o.cols[i] = t.shape[1]
+    _check(load().hb_linear(_bf16(x, "x"), _bf16(w, "w"), int(x.shape[0]), int(w.shape[0]),
+                            int(x.shape[1]), int(epilogue), ctypes.byref(o), _stream(stream)))

@@ -226,12 +226,51 @@ hb_status hb_check(void* stream);
 hb_status hb_selftest_wait_timeout(void* stream);
 
 /* ---------------------------------------------------------------------------
+ * Linear layer of a hybrid batch on the tensor cores: y = x W^T.  Cited
+ * passage: the first page, §问题背景 (两阶段天然不对称) -- every token of the
+ * batch also passes through the model's linear layers, which take most of
+ * the iteration (compute-bound for prefill tokens, weight-read-bound for
+ * decodes).  One persistent launch.
+ *   x        device, [M, K] bf16 row-major (one row per token), 16-byte aligned
+ *   w        device, [N, K] bf16 row-major (row n: weights of output n)
+ *   M        rows (tokens), >= 0 (0: nothing to do)
+ *   K        multiple of 64
+ *   epilogue HB_LINEAR_STORE: y = x W^T, N a multiple of 256, its columns
+ *              split over out->y[0..2] (out->cols[i] consecutive columns to
+ *              y[i], each a multiple of 256 or 0, summing to N; y[i] is
+ *              [M, cols[i]] row-major) -- e.g. q, k and v of a fused QKV
+ *              projection;
+ *            HB_LINEAR_GATED: w = [W_gate; W_up] with N = 2F rows (F a
+ *              multiple of 128); y[0] [M, F] receives silu(x W_gate^T) *
+ *              (x W_up^T), silu(g) = g / (1 + e^-g); cols[0] = F;
+ *            HB_LINEAR_RESIDUAL: as STORE but y[i] += (its columns of)
+ *              x W^T, in place (a residual connection).
+ * Ownership: all pointers borrowed; nothing is allocated.  Errors:
+ * HB_ERR_INVALID_ARG (NULL or misaligned pointer, unknown epilogue),
+ * HB_ERR_SHAPE (sizes breaking the rules above); a wait that gives up is
+ * reported by hb_check as HB_ERR_TIMEOUT.
+ * ------------------------------------------------------------------------- */
+typedef enum hb_linear_epilogue {
+  HB_LINEAR_STORE = 0,
+  HB_LINEAR_GATED = 1,
+  HB_LINEAR_RESIDUAL = 2
+} hb_linear_epilogue;
+
+typedef struct hb_linear_out {
+  void* y[3];          /* device, bf16; unused entries NULL                     */
+  int32_t cols[3];     /* columns per destination (0 = unused)                 */
+} hb_linear_out;
+
+hb_status hb_linear(const void* x, const void* w, int32_t M, int32_t N, int32_t K,
+                    int32_t epilogue, const hb_linear_out* out, void* stream);
+
+/* ---------------------------------------------------------------------------
  * Instrumentation.  When enabled, every kernel launch of this library is
  * bracketed by CUDA events recorded on its launch stream.
  *   kernel ids: 0 = kv append, 1 = attention (decode and chunk work in one
- *   launch)
+ *   launch), 2 = linear layer
  * ------------------------------------------------------------------------- */
-#define HB_NUM_KERNEL_IDS 2
+#define HB_NUM_KERNEL_IDS 3
 
 /* Start (clearing earlier records) or stop recording.  Not thread-safe with
  * concurrent launches from other threads. */

@@ -267,3 +267,33 @@ def test_plan_splits_short_chunks_at_long_offsets():
     # short key ranges are never split below 4 tiles per piece
     h = _check_plan([(64, 64 + 200)], 8, 8, 64, 148)
     assert h["num_chunk_merges"] == 0
+
+
+def test_linear_argument_checks():
+    """hb_linear's host-side checks (no GPU needed: they come first)."""
+    hb = lib()
+    L = hb.load()
+    buf = (ctypes.c_uint8 * 256)()
+    base = ctypes.cast(buf, ctypes.c_void_p).value
+    a16 = ctypes.c_void_p((base + 15) // 16 * 16)
+    odd = ctypes.c_void_p(a16.value + 2)
+
+    def call(x, w, M, N, K, epi, cols, ys=None):
+        o = hb.HbLinearOut()
+        for i in range(3):
+            o.cols[i] = cols[i]
+            o.y[i] = (ys[i] if ys else a16).value if cols[i] else None
+        return L.hb_linear(x, w, M, N, K, epi, ctypes.byref(o), None)
+
+    assert L.hb_linear(a16, a16, 4, 256, 64, 0, None, None) == 1           # out NULL
+    assert call(a16, a16, 4, 256, 64, 3, (256, 0, 0)) == 1                # unknown epilogue
+    assert call(a16, a16, 4, 256, 96, 0, (256, 0, 0)) == 2                # K % 64
+    assert call(a16, a16, 4, 320, 64, 0, (320, 0, 0)) == 2                # N % 256
+    assert call(a16, a16, 4, 512, 64, 0, (256, 0, 0)) == 2                # cols sum != N
+    assert call(a16, a16, 4, 512, 64, 0, (256, 128, 128)) == 2            # cols % 256
+    assert call(a16, a16, 4, 512, 64, 1, (512, 0, 0)) == 2                # gated: cols = F
+    assert call(odd, a16, 4, 256, 64, 0, (256, 0, 0)) == 1                # misaligned x
+    assert call(a16, a16, 4, 256, 64, 0, (256, 0, 0), ys=[odd, a16, a16]) == 1
+    assert call(a16, a16, -1, 256, 64, 0, (256, 0, 0)) == 2               # M < 0
+    assert call(a16, a16, 0, 768, 64, 0, (256, 512, 0)) == 0              # M = 0: nothing to do
+    assert call(a16, a16, 0, 512, 64, 1, (256, 0, 0)) == 0
