@@ -17,6 +17,8 @@ step's fraction of its roofline, the CPU oracle timed on a bounded sample, and
 the SM clocks sampled during the timed region.
 
 `--impl reference` times the fp64 CPU oracle instead (rank 0 only).
+`--layer` times one whole transformer block of the batch instead (the
+linear layers on synthetic weights around the attention step).
 `--sweep chunk` prefills one 8192-token prompt in chunks of several sizes,
 with and without decode rows beside each chunk, and prints one JSON line per
 chunk size (the chunk-size sweep; not the step benchmark).
@@ -509,6 +511,66 @@ def run_chunk_sweep(args):
         print(json.dumps(r), flush=True)
 
 
+def run_layer(args):
+    """One transformer block of the workload's hybrid batch (linear layers
+    around the attention step, synthetic weights) timed on the device: QKV
+    projection, KV append, attention, output projection, gated MLP and down
+    projection, all in this library's kernels.  One JSON line."""
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    import __graft_entry__
+    __graft_entry__.build()
+    from chunked_prefill_decode_gb300 import hb, layer
+    from chunked_prefill_decode_gb300.device import from_layout
+
+    lay = workloads.WORKLOADS[args.workload]()
+    sh = lay.shape
+    bshape = {32: layer.MISTRAL_7B, 56: layer.YI_34B}.get(sh.num_q_heads)
+    if bshape is None or sh.head_dim != 128:
+        raise SystemExit("--layer supports the Mistral-7B and Yi-34B attention shapes")
+    blk = layer.HybridBlock(bshape, seed=1)
+    ten = workloads.make_tensors(lay, seed=1, device=dev)
+    db = from_layout(lay)
+    T = lay.total_q
+    x = torch.randn(T, bshape.hidden, device=dev).to(torch.bfloat16)
+    bufs = blk.buffers(T)
+    for _ in range(max(args.warmup, 3)):
+        blk.forward(x, db, ten.k_cache, ten.v_cache, bufs=bufs, plan=False)
+    torch.cuda.synchronize(dev)
+    hb.hb_check()
+    steps = max(1, min(args.steps, 500))
+    hb.hb_timing_enable(True)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(0) as clk:
+        ev0.record()
+        for _ in range(steps):
+            blk.forward(x, db, ten.k_cache, ten.v_cache, bufs=bufs, plan=False)
+        ev1.record()
+        torch.cuda.synchronize(dev)
+    kt = hb.hb_timing_read()
+    hb.hb_timing_enable(False)
+    hb.hb_check()
+    ms = ev0.elapsed_time(ev1) / steps
+    peaks = _peaks()
+    lin_ms = kt["linear"][0] / steps
+    lin_flops = blk.flops(T)
+    weight_bytes = 2.0 * bshape.params()
+    line = {
+        "mode": "layer", "workload": args.workload, "tokens_per_step": T, "steps": steps,
+        "ms_per_step": ms, "tokens_per_s": T / (ms * 1e-3),
+        "ms_by_kernel": {k: v[0] / steps for k, v in kt.items()},
+        "launches_per_step": {k: v[1] / steps for k, v in kt.items()},
+        "linear": {"flops": lin_flops, "weight_bytes": weight_bytes,
+                   "tflops": lin_flops / (lin_ms * 1e-3) / 1e12,
+                   "roofline_ms": max(lin_flops / (peaks["bf16_tflops"] * 1e12),
+                                      weight_bytes / (peaks["hbm_gbs"] * 1e9)) * 1e3},
+        "attention_share": (kt["attention"][0] + kt["kv_append"][0]) / steps / ms,
+        "block": {"hidden": bshape.hidden, "ffn": bshape.ffn, "params": bshape.params()},
+        "weights": "synthetic N(0, 1/fan_in)", "data": "synthetic", "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -521,9 +583,14 @@ def main():
                     help="instead of the step benchmark: prefill one 8192-token prompt "
                          "in chunks of 256/257/512/1024/2048/8192 tokens")
     ap.add_argument("--sweep-reps", type=int, default=10)
+    ap.add_argument("--layer", action="store_true",
+                    help="instead of the attention step: one transformer block of the "
+                         "batch (linear layers on synthetic weights around attention)")
     args = ap.parse_args()
     if args.sweep == "chunk":
         run_chunk_sweep(args)
+    elif args.layer:
+        run_layer(args)
     elif args.impl == "reference":
         run_reference(args)
     else:

@@ -21,10 +21,12 @@ What this module does:
     measured device time of each iteration (CUDA events).  Only the attention
     layer is on this path, so an iteration's time is `layers` times that of
     one attention step (`layers` defaults to 1: attention of one layer).
-    Linear layers are not run; optionally (`linear_params` > 0) their time is
-    added as a roofline estimate -- the larger of 2 x params x tokens FLOPs
-    at the dense bf16 peak and one read of the bf16 weights at the HBM rate --
-    clearly a model, not a measurement;
+    With `block` (a layer.BlockShape) the step runs a whole transformer
+    block instead -- the linear layers on synthetic weights around the
+    attention, all measured (`layer.HybridBlock`).  Without it, the linear
+    layers can be added as a roofline estimate (`linear_params` > 0: the
+    larger of 2 x params x tokens FLOPs at the dense bf16 peak and one read
+    of the bf16 weights at the HBM rate) -- a model, not a measurement;
   * `latency_stats` -- TTFT and TBT percentiles from the token times;
   * `select_budget` -- the largest token budget whose P99 TBT stays within a
     multiple of the decode-only iteration time, from measured runs.
@@ -175,7 +177,7 @@ class GpuStep:
 
     def __init__(self, num_pages, num_q_heads=32, num_kv_heads=8, head_dim=128,
                  page_size=16, layers=1, seed=0, device="cuda", sliding_window=0,
-                 linear_params=0.0, peak_tflops=None, hbm_gbs=None):
+                 linear_params=0.0, peak_tflops=None, hbm_gbs=None, block=None):
         import torch
         from . import hb
         self.torch, self.hb = torch, hb
@@ -187,6 +189,13 @@ class GpuStep:
             raise ValueError("the linear-layer model needs peak_tflops and hbm_gbs")
         self.linear_params = linear_params
         self.peak_tflops, self.hbm_gbs = peak_tflops, hbm_gbs
+        self.block = None
+        if block is not None:
+            from .layer import HybridBlock
+            if (block.num_q_heads, block.num_kv_heads, block.head_dim, block.page_size) != \
+                    (num_q_heads, num_kv_heads, head_dim, page_size):
+                raise ValueError("block shape and attention shape differ")
+            self.block = HybridBlock(block, seed=seed, device=device)
         self.num_pages = num_pages
         g = torch.Generator(device=self.dev).manual_seed(seed)
         pool = (num_pages, page_size, num_kv_heads, head_dim)
@@ -213,6 +222,19 @@ class GpuStep:
                           sliding_window=self.window)
         self.plan, self.ws = self.hb.hb_plan(db.batch, db.q_len, db.context_len, self.sms,
                                              workspace=self.ws, plan=self.plan)
+        if self.block is not None:
+            blk = self.block
+            blk._plan, blk._ws = self.plan, self.ws
+            x = torch.randn(T, blk.shape.hidden, generator=self.gen,
+                            device=self.dev).to(torch.bfloat16)
+            torch.cuda.synchronize(self.dev)
+            e0, e1 = self.ev
+            e0.record()
+            blk.forward(x, db, self.k_pool, self.v_pool, plan=False)
+            e1.record()
+            torch.cuda.synchronize(self.dev)
+            self.hb.hb_check()
+            return self.layers * e0.elapsed_time(e1) * 1e-3
         torch.cuda.synchronize(self.dev)
         e0, e1 = self.ev
         e0.record()
@@ -265,6 +287,9 @@ def main(argv=None):
     ap.add_argument("--slo", type=float, default=5.0,
                     help="P99 TBT limit as a multiple of the decode-only iteration")
     ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--block", choices=["none", "mistral"], default="none",
+                    help="run a whole Mistral-7B-shaped block per layer (measured linear "
+                         "layers on synthetic weights) instead of attention alone")
     ap.add_argument("--linear-params", type=float, default=0.0,
                     help="add a roofline estimate of linear layers with this many "
                          "bf16 parameters (Mistral-7B: about 7.1e9); 0 = attention only")
@@ -275,17 +300,21 @@ def main(argv=None):
     args = ap.parse_args(argv)
     reqs = poisson_requests(args.rate, args.requests, seed=args.seed)
     maxp = 8192 // 16
+    block = None
+    if args.block == "mistral":
+        from .layer import MISTRAL_7B
+        block = MISTRAL_7B
     step = GpuStep(args.num_pages, layers=args.layers, seed=args.seed,
                    linear_params=args.linear_params, peak_tflops=args.peak_tflops,
-                   hbm_gbs=args.hbm_gbs)
+                   hbm_gbs=args.hbm_gbs, block=block)
     base_ms = decode_only_iteration_ms(step, 32, 2048, maxp)
     stats = {}
     for bud in [int(x) for x in args.budgets.split(",")]:
         res = run(reqs, bud, step, args.num_pages, maxp)
         stats[bud] = latency_stats(res)
         print(json.dumps({"driver": "poisson", "rate": args.rate, "layers": args.layers,
-                          "linear_params_modelled": args.linear_params, **stats[bud]}),
-              flush=True)
+                          "block": args.block, "linear_params_modelled": args.linear_params,
+                          **stats[bud]}), flush=True)
     print(json.dumps({"decode_only_iter_ms": base_ms, "slo_multiple": args.slo,
                       "selected_budget": select_budget(stats, base_ms, args.slo)}), flush=True)
 

@@ -84,19 +84,18 @@ def test_select_budget():
 @pytest.mark.gpu
 def test_driver_on_the_gpu():
     """A short stream through the real append + attention: all requests finish
-    and the chunked run's worst gap between tokens is below the unchunked one's."""
+    with all their tokens, and the decode-only iteration is timed.  (With
+    attention alone a prefill chunk costs little next to the decode stream,
+    so no ordering of the budgets' gaps is asserted here; see the block test.)"""
     reqs = driver.poisson_requests(rate=400.0, n=24, seed=5, prompt_median=1200,
                                    output_median=12, max_total=4096)
     step = driver.GpuStep(num_pages=8000, layers=1, seed=5)
-    stats = {}
     for bud in (256, 8192):
         res = driver.run(reqs, bud, step, num_pages=8000, max_pages_per_seq=256)
         assert res.unfinished == 0
         assert all(len(res.token_times[r.rid]) == r.max_new for r in reqs)
-        stats[bud] = driver.latency_stats(res)
-    assert stats[256]["tbt_ms_max"] < stats[8192]["tbt_ms_max"]
-    base = driver.decode_only_iteration_ms(step, 8, 1024, 256)
-    assert 0 < base < stats[8192]["tbt_ms_max"]
+        assert min(res.iter_time) > 0
+    assert driver.decode_only_iteration_ms(step, 8, 1024, 256) > 0
 
 
 def test_linear_layer_roofline_estimate():
@@ -111,3 +110,23 @@ def test_linear_layer_roofline_estimate():
     assert s.linear_time(int(crossover) - 1) == pytest.approx(2e-3)
     s.linear_params = 0.0
     assert s.linear_time(4096) == 0.0
+
+
+@pytest.mark.gpu
+def test_driver_with_whole_blocks_on_the_gpu():
+    """With whole transformer blocks per iteration (measured linear layers
+    around the attention step), an iteration's time grows with its tokens, so
+    admitting whole prompts stretches the worst gap between a running
+    request's tokens beyond what a 256-token budget allows."""
+    from chunked_prefill_decode_gb300.layer import BlockShape
+    reqs = driver.poisson_requests(rate=2000.0, n=12, seed=6, prompt_median=1500,
+                                   output_median=8, max_total=4096)
+    blk = BlockShape(hidden=1024, num_q_heads=32, num_kv_heads=8, head_dim=128, ffn=2048)
+    step = driver.GpuStep(num_pages=6000, layers=2, seed=6, block=blk)
+    worst = {}
+    for bud in (256, 8192):
+        res = driver.run(reqs, bud, step, num_pages=6000, max_pages_per_seq=256)
+        assert res.unfinished == 0 and min(res.iter_time) > 0
+        assert all(len(res.token_times[r.rid]) == r.max_new for r in reqs)
+        worst[bud] = driver.latency_stats(res)["tbt_ms_max"]
+    assert worst[256] < worst[8192]
