@@ -8,12 +8,12 @@
 //
 // y = x W^T with x [M, K] (one row per token) and W [N, K], bf16 in, fp32
 // accumulation in tensor memory, bf16 out.  A persistent kernel: one CTA per
-// SM walks output tiles of 128 rows x 256 columns (m fastest, so CTAs that
-// run together share the weight tile through L2); per tile, 64-wide slices of
-// K stream through a 4-stage ring of shared memory by TMA (128-byte swizzle)
-// and feed tcgen05.mma M128 N256 K16; the accumulator is double-buffered in
-// TMEM (2 x 256 columns), so the epilogue of one tile overlaps the main loop
-// of the next.
+// SM walks output tiles of 128 rows x BN columns (m fastest, so CTAs that
+// run together share the weight tile through L2; BN = 256); per
+// tile, 64-wide slices of K stream through a 4-stage ring of shared memory by
+// TMA (128-byte swizzle) and feed tcgen05.mma M128 N(BN) K16; the accumulator
+// is double-buffered in TMEM (2 x BN columns), so the epilogue of one tile
+// overlaps the main loop of the next.
 //
 // Warp roles (192 threads): warp 0 TMA producer (one thread), warp 1 TMEM
 // owner and MMA issuer (one thread), warps 2-5 epilogue (thread = output
@@ -21,7 +21,8 @@
 //
 // Epilogues: store (columns split over up to three destinations, e.g. q, k
 // and v of a fused QKV projection), gated (W = [W_gate; W_up] with 2F rows:
-// per tile two N128 accumulators, output silu(g) * u), residual (y += x W^T).
+// per tile two N(BN/2) accumulators, output silu(g) * u), residual
+// (y += x W^T).
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -31,24 +32,36 @@
 namespace hb {
 
 constexpr int kLinBM = 128;
-constexpr int kLinBN = 256;
 constexpr int kLinBK = 64;
 constexpr int kLinStages = 4;
 constexpr int kLinThreads = 192;
 constexpr int kLinABytes = kLinBM * kLinBK * 2;          // 16 KB
-constexpr int kLinBBytes = kLinBN * kLinBK * 2;          // 32 KB
-constexpr int kLinStageBytes = kLinABytes + kLinBBytes;  // 48 KB
-constexpr int kLinBarOff = kLinStages * kLinStageBytes;
-constexpr int kLinNumBars = 2 * kLinStages + 4 + 1;
-constexpr int kLinMiscOff = kLinBarOff + kLinNumBars * 8;
-constexpr int kLinSmemBytes = kLinMiscOff + 64 + 1024;   // + alignment slack
-static_assert(kLinSmemBytes <= 227 * 1024, "linear smem");
+
+// Tile width BN (output columns per tile); the kernel is built for 256.
+template <int BN>
+struct LinCfg {
+  static constexpr int kBBytes = BN * kLinBK * 2;
+  static constexpr int kStageBytes = kLinABytes + kBBytes;
+  static constexpr int kBarOff = kLinStages * kStageBytes;
+  static constexpr int kNumBars = 2 * kLinStages + 4 + 1;
+  static constexpr int kMiscOff = kBarOff + kNumBars * 8;
+  static constexpr int kSmemBytes = kMiscOff + 64 + 1024;   // + alignment slack
+  static constexpr uint32_t kTmemCols = 2 * BN < 32 ? 32 : 2 * BN;
+};
+static_assert(LinCfg<256>::kSmemBytes <= 227 * 1024, "linear smem");
 
 __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)); }
 
+template <int BN>
 __global__ void __launch_bounds__(kLinThreads, 1)
     linear_kernel(const LinearParams p, const __grid_constant__ CUtensorMap xmap,
                   const __grid_constant__ CUtensorMap wmap) {
+  using C = LinCfg<BN>;
+  constexpr int kLinBN = BN;
+  constexpr int kLinBBytes = C::kBBytes;
+  constexpr int kLinStageBytes = C::kStageBytes;
+  constexpr int kLinBarOff = C::kBarOff;
+  constexpr int kLinMiscOff = C::kMiscOff;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
@@ -84,7 +97,7 @@ __global__ void __launch_bounds__(kLinThreads, 1)
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(tmem_holder, 512);
+    tmem_alloc(tmem_holder, C::kTmemCols);
     tmem_relinquish();
   }
   tc_fence_before_sync();
@@ -249,26 +262,45 @@ __global__ void __launch_bounds__(kLinThreads, 1)
   __syncthreads();
   if (warp == 1) {
     tc_fence_after_sync();
-    tmem_dealloc(tmem, 512);
+    tmem_dealloc(tmem, C::kTmemCols);
   }
   if (threadIdx.x == 0 && *abort_flag) report_error(p.dev_error, HB_DEVERR_TIMEOUT);
 }
 
-int linear_smem_bytes() { return kLinSmemBytes; }
+// Tile width for a problem.  Measured on GB300 (Mistral-7B projections at
+// 512 tokens): 256-column tiles beat 128- and 64-column ones even when they
+// leave SMs idle -- a narrower MMA re-reads its 16 KB activation tile for
+// fewer output columns and becomes bound by shared memory -- so 256 is used.
+int linear_tile_n(int M, int N, int epilogue, int num_sms) {
+  (void)M;
+  (void)N;
+  (void)epilogue;
+  (void)num_sms;
+  return 256;
+}
 
-// Persistent launch: one CTA per SM (at most one per tile).
-cudaError_t launch_linear(const LinearParams& p, const CUtensorMap& xmap, const CUtensorMap& wmap,
-                          int num_sms, cudaStream_t stream) {
+template <int BN>
+static cudaError_t launch_bn(const LinearParams& p, const CUtensorMap& xmap,
+                             const CUtensorMap& wmap, int num_sms, cudaStream_t stream) {
   const int m_tiles = (p.M + kLinBM - 1) / kLinBM;
-  const int n_tiles = p.epilogue == 1 ? p.F / (kLinBN / 2) : p.N / kLinBN;
+  const int n_tiles = p.epilogue == 1 ? p.F / (BN / 2) : p.N / BN;
   const int tiles = m_tiles * n_tiles;
   if (tiles == 0) return cudaSuccess;
   const int grid = tiles < num_sms ? tiles : num_sms;
-  cudaError_t e = cudaFuncSetAttribute(linear_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       kLinSmemBytes);
+  cudaError_t e = cudaFuncSetAttribute(linear_kernel<BN>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       LinCfg<BN>::kSmemBytes);
   if (e != cudaSuccess) return e;
-  linear_kernel<<<grid, kLinThreads, kLinSmemBytes, stream>>>(p, xmap, wmap);
+  linear_kernel<BN><<<grid, kLinThreads, LinCfg<BN>::kSmemBytes, stream>>>(p, xmap, wmap);
   return cudaGetLastError();
+}
+
+// Persistent launch: one CTA per SM (at most one per tile).  `bn` is the
+// tile width the weight map's box was made for (linear_tile_n).
+cudaError_t launch_linear(const LinearParams& p, const CUtensorMap& xmap, const CUtensorMap& wmap,
+                          int bn, int num_sms, cudaStream_t stream) {
+  if (bn != 256) return cudaErrorInvalidValue;
+  return launch_bn<256>(p, xmap, wmap, num_sms, stream);
 }
 
 }  // namespace hb

@@ -40,9 +40,11 @@ def _sentinels_kept(full, M):
     assert (full[M:].view(torch.int16) == SENT).all()
 
 
+# tile counts from 1 to a few waves over the SMs, ragged M everywhere
 @pytest.mark.parametrize("M,cols,K", [
     (1, (256,), 64), (5, (512,), 128), (128, (256,), 4096), (200, (256, 512), 192),
     (513, (4096, 1024, 1024), 512), (2048, (1024,), 256), (130, (256, 256, 256), 64),
+    (1280, (4096,), 128), (1500, (2048, 1024, 1024), 256),
 ])
 def test_store(M, cols, K):
     hb = lib()
@@ -61,7 +63,8 @@ def test_store(M, cols, K):
         c0 += c
 
 
-@pytest.mark.parametrize("M,F,K", [(1, 128, 64), (300, 1024, 256), (512, 2048, 1024)])
+@pytest.mark.parametrize("M,F,K", [(1, 128, 64), (300, 1024, 256), (512, 2048, 1024),
+                                   (1280, 2048, 128)])
 def test_gated(M, F, K):
     hb = lib()
     dev = torch.device("cuda:0")
@@ -75,7 +78,7 @@ def test_gated(M, F, K):
     _sentinels_kept(full, M)
 
 
-@pytest.mark.parametrize("M,N,K", [(77, 512, 128), (640, 256, 2048)])
+@pytest.mark.parametrize("M,N,K", [(77, 512, 128), (640, 256, 2048), (1280, 4096, 64)])
 def test_residual(M, N, K):
     hb = lib()
     dev = torch.device("cuda:0")
