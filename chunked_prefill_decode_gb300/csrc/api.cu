@@ -578,16 +578,22 @@ hb_status hb_plan(const hb_batch* batch, const int32_t* h_q_len,
         ++n_dec_rows;
         dec_pages += (int64_t)((h_context_len[i] + kPageSize - 1) / kPageSize) * n_blocks;
       }
-    const int max_dec_items = (int)std::min<int64_t>(n_dec_rows * n_blocks + num_sms + 1, 1 << 30);
+    // intervals: one static range per decode CTA.  A dynamic tail (short
+    // intervals claimed from a counter) is supported by partition_decode and
+    // the kernel but measured slower on GB300 (Mistral 125 vs 110 us: the
+    // extra pieces and merges cost more than the ragged tail), so it is off.
+    const int max_intervals = std::max(1, decode_ctas) * (1 + kDynamicPerCta) + 1;
+    const int max_dec_items =
+        (int)std::min<int64_t>(n_dec_rows * n_blocks + max_intervals + 1, 1 << 30);
     std::vector<DecodeItem> dec(std::max(1, max_dec_items));
-    std::vector<int32_t> cta_off(num_sms + 1, 0);
+    std::vector<int32_t> cta_off(max_intervals + 1, 0);
     DecodePartition part;
     if (!partition_decode(S, h_q_len, h_context_len, n_blocks, kvhb, std::max(1, decode_ctas), 4,
-                          dec.data(), (int)dec.size(), cta_off.data(), std::max(1, decode_ctas),
-                          &part, W))
+                          dec.data(), (int)dec.size(), cta_off.data(), max_intervals,
+                          &part, W, /*dynamic_tail=*/false))
       return fail(HB_ERR_WORKSPACE, "decode partition overflow");
     dec.resize(part.n_items);
-    cta_off.resize(part.grid + 1);
+    cta_off.resize(part.grid + part.n_dynamic + 1);
     const int n_slots = part.n_slots, n_merge = part.n_merge;
 
     // ---- sizes
@@ -632,6 +638,7 @@ hb_status hb_plan(const hb_batch* batch, const int32_t* h_q_len,
     h.num_partial_slots = n_slots;
     h.num_merge_counters = n_merge;
     h.decode_grid = part.grid;
+    h.num_decode_dynamic = part.n_dynamic;
     h.ws_decode_offsets = offsets_at;
     h.decode_kvh_block = kvhb;
     h.chunk_tokens_per_tile = tpt;
@@ -733,6 +740,8 @@ hb_status hb_attention(const hb_batch* batch, const void* h_plan, const void* q,
       if ((s = encode_map(&dec_v, v_cache, 4, dims, strides, box, "decode V")) != HB_OK) return s;
       dp.items = reinterpret_cast<const DecodeItem*>(ws);
       dp.cta_offsets = reinterpret_cast<const int32_t*>(ws + h.ws_decode_offsets);
+      dp.num_static = h.decode_grid;
+      dp.num_dynamic = h.num_decode_dynamic;
       dp.num_items = h.num_decode_items;
       dp.counters = reinterpret_cast<int32_t*>(ws + h.ws_counters);
       dp.part_o = reinterpret_cast<float*>(ws + h.ws_partial_o);

@@ -8,10 +8,12 @@
 // memory-bound (every step reads the whole KV cache).  So this kernel is
 // built to stream KV pages at HBM speed:
 //
-//  * persistent and statically balanced: the host plan lays the decode
-//    rows' pages end to end and gives each CTA (at most one per SM) an equal
-//    contiguous range, cut at row boundaries into work items (a page range of
-//    one row and one block of <= 8 kv heads);
+//  * persistent and balanced: the host plan lays the decode rows' pages end
+//    to end and gives each CTA (at most one per SM) an equal contiguous
+//    range of ~90 % of them; the rest are short intervals that CTAs claim
+//    from a counter when their own range is done (SMs stream at slightly
+//    different rates); every interval is cut at row boundaries into work
+//    items (a page range of one row and one block of <= 8 kv heads);
 //  * one producer warp streams whole pages (all kv heads of the block, K and
 //    V) into a ring of shared-memory stages with 4-D TMA copies laid out as
 //    [kv head][slot][64 head-dim] rows with the 128-byte swizzle, so the
@@ -135,33 +137,51 @@ __device__ __forceinline__ void decode_cta(const DecodeParams& p, const DecodeLa
     uint32_t issued_mask = 0, last_par_mask = 0;
     const uint32_t page_tx = 2u * (uint32_t)L.half_bytes;
     const uint32_t qbytes = (uint32_t)(kvhb * g * D * 2);
+    // lane l: block-table entry of page base + l of item x, unchecked -- it is
+    // checked where it is used, so no instruction waits on the load earlier
     auto window = [&](const DecodeItem& x, int base) -> int {
       const int lp = base + lane;
-      int phys = p.num_pages;  // out of range: the copy reads zeros
-      if (lp < x.page_end) {
-        phys = (lp < p.max_pages_per_seq)
-                   ? __ldg(&p.block_table[(size_t)x.seq * p.max_pages_per_seq + lp])
-                   : -1;
-        if (phys < 0 || phys >= p.num_pages) {
-          report_error(p.dev_error, HB_DEVERR_INDEX);
-          phys = p.num_pages;
-        }
-      }
-      return phys;
+      if (lp >= x.page_end) return -1;
+      return (lp < p.max_pages_per_seq)
+                 ? __ldg(&p.block_table[(size_t)x.seq * p.max_pages_per_seq + lp])
+                 : -1;
     };
-    const int i0 = p.cta_offsets[cta];
-    const int i1 = p.cta_offsets[cta + 1];
+    // Items: the CTA's own static interval, then dynamic intervals claimed
+    // from the shared counter (lane 0 claims, the warp learns the result by
+    // shuffle).  The item after the current one is found (and its first
+    // block-table window fetched) while the current one streams.
+    auto claim = [&](int& ni, int& ne) -> bool {
+      int c = 0x7fffffff;
+      if (lane == 0 && p.num_dynamic > 0) c = atomicAdd(&p.counters[kCounterWork], 1);
+      c = __shfl_sync(0xffffffffu, c, 0);
+      if (c >= p.num_dynamic) return false;
+      ni = p.cta_offsets[p.num_static + c];
+      ne = p.cta_offsets[p.num_static + c + 1];
+      return true;
+    };
+    auto next_item = [&](int i, int e, int& ni, int& ne) -> bool {
+      if (i + 1 < e) {
+        ni = i + 1;
+        ne = e;
+        return true;
+      }
+      while (claim(ni, ne))
+        if (ni < ne) return true;
+      return false;
+    };
+    int cur_i = p.cta_offsets[cta], cur_e = p.cta_offsets[cta + 1];
+    bool have = cur_i < cur_e || next_item(cur_i, cur_i, cur_i, cur_e);
     bool ok = true;
     DecodeItem it{}, nxt{};
     int win = 0, win_next = 0, nxt_win = 0;
-    if (i0 < i1) {
-      it = p.items[i0];
+    if (have) {
+      it = p.items[cur_i];
       win = window(it, it.page_begin);
       win_next = window(it, it.page_begin + 32);
     }
-    for (int i = i0; ok && i < i1; ++i) {
-      const bool has_next = i + 1 < i1;
-      if (has_next) nxt = p.items[i + 1];
+    while (ok && have) {
+      int ni = 0, ne = 0;
+      bool has_next = false;
       if (lane == 0) {
         ok = mbar_wait(&qempty[qslot], qph[qslot] ^ 1u, abort_flag);
         if (ok) {
@@ -173,15 +193,18 @@ __device__ __forceinline__ void decode_cta(const DecodeParams& p, const DecodeLa
       }
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
       qph[qslot] ^= 1u;
-      const int nxt_at = min(it.page_begin + 1, it.page_end - 1);
       for (int lp = it.page_begin; ok && lp < it.page_end; ++lp) {
         const int k = (lp - it.page_begin) & 31;
         if (k == 0 && lp != it.page_begin) {
           win = win_next;
           win_next = window(it, lp + 32);
         }
-        if (has_next && lp == nxt_at) nxt_win = window(nxt, nxt.page_begin);
-        const int phys = __shfl_sync(0xffffffffu, win, k);
+        int phys = __shfl_sync(0xffffffffu, win, k);
+        if (phys < 0 || phys >= p.num_pages) {
+          // out of range: reported, and fetched out of bounds (zeros)
+          if (lane == 0) report_error(p.dev_error, HB_DEVERR_INDEX);
+          phys = p.num_pages;
+        }
         if (lane == 0) {
           ok = mbar_wait(&empty[st], ph ^ 1u, abort_flag);
           if (ok) {
@@ -209,13 +232,24 @@ __device__ __forceinline__ void decode_cta(const DecodeParams& p, const DecodeLa
           st = 0;
           ph ^= 1u;
         }
+        if (lp == it.page_begin) {
+          // with the item's first page in flight: find the next item (a
+          // claim of a dynamic interval waits on its atomic) and start its
+          // first block-table window
+          has_next = next_item(cur_i, cur_e, ni, ne);
+          if (has_next) {
+            nxt = p.items[ni];
+            nxt_win = window(nxt, nxt.page_begin);
+          }
+        }
       }
       qslot ^= 1;
-      if (has_next) {
-        it = nxt;
-        win = nxt_win;
-        win_next = window(it, it.page_begin + 32);
-      }
+      if (!has_next) break;
+      cur_i = ni;
+      cur_e = ne;
+      it = nxt;
+      win = nxt_win;
+      win_next = window(it, it.page_begin + 32);
     }
     if (lane == 0) {
       if (ok && mbar_wait(&empty[st], ph ^ 1u, abort_flag)) {
@@ -226,6 +260,15 @@ __device__ __forceinline__ void decode_cta(const DecodeParams& p, const DecodeLa
       for (int s2 = 0; s2 < S; ++s2)
         if (issued_mask & (1u << s2))
           drain_wait(&full[s2], (last_par_mask >> s2) & 1u, abort_flag);
+      if (p.num_dynamic > 0) {
+        // this CTA claims no more intervals; the last decode CTA to get here
+        // resets both counters for the next launch
+        __threadfence();
+        if (atomicAdd(&p.counters[kCounterDone], 1) == p.num_static - 1) {
+          p.counters[kCounterWork] = 0;
+          p.counters[kCounterDone] = 0;
+        }
+      }
     }
   } else if (warp < kDecConsumerWarps) {
     // ------------------------------------------------------------ consumers

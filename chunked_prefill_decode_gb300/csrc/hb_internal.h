@@ -22,7 +22,7 @@ constexpr int kChunkKeys = 128;        // keys per tensor-core KV tile
 constexpr int kDecodeKvhBlock = 8;     // kv heads per decode work item (max)
 constexpr int kMaxGroup = 16;          // max q heads per kv head
 constexpr uint32_t kPlanMagic = 0x31504248u;  // "HBP1"
-constexpr uint32_t kPlanVersion = 2;
+constexpr uint32_t kPlanVersion = 3;
 constexpr int kMaxChunkSplits = 16;    // key-range pieces of one query tile (max)
 
 // One decode work item: a range of logical pages of one decode row, for one
@@ -89,6 +89,8 @@ struct PlanHeader {
   int32_t num_chunk_slots;     // partial states of split chunk tiles
   int32_t num_chunk_merges;    // split chunk tiles
   int32_t sliding_window;      // the batch's window (the plan depends on it)
+  int32_t num_decode_dynamic;  // claimable decode intervals after the static ones
+  int32_t pad0;
   uint64_t ws_decode_offsets;  // device offset of the per-CTA item offsets
   uint64_t items_bytes;     // bytes of the item arrays (host and device)
   uint64_t ws_counters;     // device offsets (bytes from workspace start)
@@ -99,19 +101,26 @@ struct PlanHeader {
   uint64_t ws_chunk_counters;   // [num_chunk_merges] arrivals per split tile
   uint64_t ws_chunk_o;          // [num_chunk_slots, D, 128] fp32
   uint64_t ws_chunk_ml;         // [num_chunk_slots, 2, 128] fp32: (m in log2 units, l)
+  uint64_t pad1;
 };
-static_assert(sizeof(PlanHeader) == 160, "header size");
+static_assert(sizeof(PlanHeader) == 176, "header size");
 static_assert(sizeof(PlanHeader) % 16 == 0, "header alignment");
 
-// Workspace counters: [0] decode work counter, [1] decode CTAs done,
+// Workspace counters: [0] decode dynamic intervals claimed, [1] decode CTAs
+// done (the last one resets both for the next launch),
 // [2 .. 2+num_merge_counters) per-(sequence, kv block) split arrivals.
 constexpr int kCounterWork = 0;
 constexpr int kCounterDone = 1;
 constexpr int kCounterMerge0 = 2;
 
 struct DecodeParams {
-  const DecodeItem* items;      // in CTA order
-  const int32_t* cta_offsets;   // [grid + 1]: CTA b takes items [b], [b+1])
+  const DecodeItem* items;      // in interval order
+  // [grid + num_dynamic + 1]: interval k holds items [offsets[k], offsets[k+1]);
+  // CTA b works through interval b, then claims intervals grid + c for
+  // c = counters[kCounterWork]++ while c < num_dynamic
+  const int32_t* cta_offsets;
+  int32_t num_static;           // static intervals = decode CTAs
+  int32_t num_dynamic;
   int32_t num_items;
   int32_t* counters;
   float* part_o;          // [slots, Hq, D]

@@ -154,6 +154,8 @@ extern "C" hb_status hb_decode_attention_noalloc(const hb_batch* batch, const in
     DecodeParams p{};
     p.items = reinterpret_cast<const DecodeItem*>(base);
     p.cta_offsets = reinterpret_cast<const int32_t*>(base + kOffsetsOff);
+    p.num_static = part.grid;
+    p.num_dynamic = 0;
     p.num_items = k;
     p.counters = reinterpret_cast<int32_t*>(base + kCountersOff);
     p.part_o = reinterpret_cast<float*>(base + kPartialOff);

@@ -235,21 +235,22 @@ def hb_plan(batch, q_len, context_len, num_sms, workspace=None, stream=None,
     return plan, workspace
 
 
-HEADER_BYTES = 160
+HEADER_BYTES = 176
 DECODE_ITEM_INTS = 12
 CHUNK_ITEM_INTS = 16
 
 
 def plan_header(plan):
     """Decode the header of a host plan (for tests and reports)."""
-    h = np.frombuffer(plan[:80].tobytes(), dtype=np.int32)
+    h = np.frombuffer(plan[:88].tobytes(), dtype=np.int32)
     keys = ("magic", "version", "num_seqs", "total_q", "num_q_heads", "num_kv_heads",
             "head_dim", "page_size", "max_pages_per_seq", "num_sms",
             "num_decode_items", "num_chunk_items", "num_partial_slots",
             "num_merge_counters", "decode_grid", "decode_kvh_block",
-            "chunk_tokens_per_tile", "num_chunk_slots", "num_chunk_merges", "sliding_window")
+            "chunk_tokens_per_tile", "num_chunk_slots", "num_chunk_merges", "sliding_window",
+            "num_decode_dynamic", "pad0")
     out = {k: int(v) for k, v in zip(keys, h)}
-    u = np.frombuffer(plan[80:HEADER_BYTES].tobytes(), dtype=np.uint64)
+    u = np.frombuffer(plan[88:HEADER_BYTES].tobytes(), dtype=np.uint64)
     for k, v in zip(("ws_decode_offsets", "items_bytes", "ws_counters", "ws_partial_o",
                      "ws_partial_ml", "ws_total", "plan_bytes", "ws_chunk_counters",
                      "ws_chunk_o", "ws_chunk_ml"), u):
@@ -258,8 +259,10 @@ def plan_header(plan):
 
 
 def plan_items(plan):
-    """(decode items [n, 12] int32 in CTA order, chunk items [m, 16] int32,
-    decode CTA offsets [grid + 1]) of a host plan.
+    """(decode items [n, 12] int32 in interval order, chunk items [m, 16]
+    int32, decode interval offsets [grid + num_decode_dynamic + 1]) of a host
+    plan: interval b < grid is decode CTA b's static range, the rest are the
+    dynamic tail.
 
     Chunk item columns: seq, kv_head, tok0, ntok, kv_tiles (end), q0, q_len,
     ctx, kv_begin, split, n_splits, slot, merge_id, 3 x padding."""
@@ -271,9 +274,9 @@ def plan_items(plan):
     dec = ints[: nd * DECODE_ITEM_INTS].reshape(nd, DECODE_ITEM_INTS)
     chk = ints[nd * DECODE_ITEM_INTS: n_int].reshape(nc, CHUNK_ITEM_INTS)
     off = hd["ws_decode_offsets"]
-    grid = hd["decode_grid"]
-    offs = np.frombuffer(body[off: off + 4 * (grid + 1)].tobytes(), dtype=np.int32) \
-        if grid > 0 else np.zeros(1, np.int32)
+    n_int = hd["decode_grid"] + hd["num_decode_dynamic"]
+    offs = np.frombuffer(body[off: off + 4 * (n_int + 1)].tobytes(), dtype=np.int32) \
+        if n_int > 0 else np.zeros(1, np.int32)
     return dec, chk, offs
 
 

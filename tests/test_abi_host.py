@@ -129,15 +129,24 @@ def _check_plan(rows, hq, hkv, d, sms, window=0):
     assert h["decode_kvh_block"] == kvhb
     assert h["chunk_tokens_per_tile"] == 128 // g
     cu = np.concatenate([[0], np.cumsum(ql)])
-    # decode: CTA ranges are contiguous, equal (the last may be shorter),
-    # and together tile every decode row's pages once per kv block
-    grid = h["decode_grid"]
+    # decode: intervals are contiguous and together tile every decode row's
+    # pages once per kv block; the CTAs' static ranges are equal (without a
+    # dynamic tail the last may be shorter); the dynamic tail's intervals hold
+    # at most as many pages as a static range, about 10 % of all pages
+    grid, n_dyn = h["decode_grid"], h["num_decode_dynamic"]
     assert grid <= sms and offs[0] == 0 and offs[-1] == len(dec)
+    assert len(offs) == (grid + n_dyn + 1 if grid else 1)
     assert (np.diff(offs) >= 1).all() if grid else len(dec) == 0
-    per_cta = [int(sum(dec[i, 3] - dec[i, 2] for i in range(offs[c], offs[c + 1])))
-               for c in range(grid)]
+    pages = [int(sum(dec[i, 3] - dec[i, 2] for i in range(offs[c], offs[c + 1])))
+             for c in range(grid + n_dyn)]
     if grid:
-        assert all(x == per_cta[0] for x in per_cta[:-1]) and per_cta[-1] <= per_cta[0]
+        st = pages[:grid]
+        if n_dyn:
+            assert all(x == st[0] for x in st)
+            assert max(pages[grid:]) <= max(4, st[0]) and 4 <= max(pages[grid:])
+            assert sum(pages[grid:]) <= 0.1 * sum(pages) + grid
+        else:
+            assert all(x == st[0] for x in st[:-1]) and st[-1] <= st[0]
     cover = {}
     for seq, kvh0, pb, pe, split, ns, slot, mid, ctx, tok, _, _ in dec:
         assert ql[seq] == 1 and 0 <= pb < pe and kvh0 % kvhb == 0
