@@ -28,6 +28,9 @@ cudaError_t launch_kv_append(const AppendParams& p, int num_sms, cudaStream_t st
 cudaError_t launch_linear(const LinearParams& p, const CUtensorMap& xmap, const CUtensorMap& wmap,
                           int bn, int num_sms, cudaStream_t stream);
 int linear_tile_n(int M, int N, int epilogue, int num_sms);
+int linear_split(int M, int N, int K, int epilogue, int num_sms, int* kb_per_piece);
+size_t linear_workspace_bytes(int M, int N, int K, int epilogue, int num_sms);
+size_t linear_counter_bytes();
 cudaError_t launch_wait_timeout(int* dev_error, cudaStream_t stream);
 cudaError_t launch_attention(const DecodeParams& dec, int decode_grid, const ChunkParams& chk,
                              int head_dim, const CUtensorMap& dec_k, const CUtensorMap& dec_v,
@@ -304,8 +307,17 @@ hb_status hb_kv_append(const hb_batch* batch, const void* k_new, const void* v_n
   }
 }
 
+size_t hb_linear_workspace_size(int32_t M, int32_t N, int32_t K, int32_t epilogue,
+                                int32_t num_sms) {
+  if (M <= 0 || N <= 0 || K <= 0 || K % 64 || N % 256 || num_sms <= 0 ||
+      epilogue < HB_LINEAR_STORE || epilogue > HB_LINEAR_RESIDUAL)
+    return 0;
+  return linear_workspace_bytes(M, N, K, epilogue, num_sms);
+}
+
 hb_status hb_linear(const void* x, const void* w, int32_t M, int32_t N, int32_t K,
-                    int32_t epilogue, const hb_linear_out* out, void* stream) {
+                    int32_t epilogue, const hb_linear_out* out, void* workspace,
+                    size_t workspace_bytes, void* stream) {
   try {
     if (!out) return fail(HB_ERR_INVALID_ARG, "out is NULL");
     if (epilogue < HB_LINEAR_STORE || epilogue > HB_LINEAR_RESIDUAL)
@@ -346,6 +358,18 @@ hb_status hb_linear(const void* x, const void* w, int32_t M, int32_t N, int32_t 
     if ((s = device_state(&dev)) != HB_OK) return s;
     if ((s = get_encoder()) != HB_OK) return s;
     p.dev_error = dev->err;
+    // split-K when the tiles are few and the caller gave room for it
+    p.split = 1;
+    p.kb_per_piece = K / 64;
+    const size_t need = linear_workspace_bytes(M, N, K, epilogue, dev->num_sms);
+    if (need > 0 && workspace != nullptr && workspace_bytes >= need &&
+        (reinterpret_cast<uintptr_t>(workspace) & 255u) == 0) {
+      int kbp = 0;
+      p.split = linear_split(M, N, K, epilogue, dev->num_sms, &kbp);
+      p.kb_per_piece = kbp;
+      p.tile_counters = static_cast<int32_t*>(workspace);
+      p.partial = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + linear_counter_bytes());
+    }
     CUtensorMap xmap, wmap;
     const cuuint64_t xdims[2] = {(cuuint64_t)K, (cuuint64_t)M};
     const cuuint64_t xstr[1] = {(cuuint64_t)K * 2};

@@ -167,6 +167,15 @@ struct LinearParams {
   uint16_t* y[3];
   int32_t seg_cols[3];
   int* dev_error;
+  // split-K: each output tile's K range is cut into `split` pieces of
+  // `kb_per_piece` 64-wide blocks (the last may be shorter); every piece
+  // writes its fp32 partial tile to `partial` ([unit][column][row], unit =
+  // piece * tiles + tile) and the last piece of a tile (counter per tile in
+  // `tile_counters`, reset by that piece) sums them and runs the epilogue.
+  int32_t split;
+  int32_t kb_per_piece;
+  float* partial;
+  int32_t* tile_counters;
 };
 
 struct AppendParams {

@@ -58,7 +58,7 @@ EXPORTED = (
     "hb_builder_create", "hb_builder_destroy", "hb_builder_add_request",
     "hb_builder_step", "hb_builder_complete", "hb_builder_counts",
     "hb_builder_free_list", "hb_builder_last_error", "hb_decode_attention_noalloc",
-    "hb_selftest_wait_timeout", "hb_linear",
+    "hb_selftest_wait_timeout", "hb_linear", "hb_linear_workspace_size",
 )
 
 LINEAR_STORE, LINEAR_GATED, LINEAR_RESIDUAL = 0, 1, 2
@@ -100,7 +100,9 @@ def load():
     L.hb_decode_attention_noalloc.argtypes = [P(HbBatch), vp, vp, vp, vp, vp, ctypes.c_float,
                                               vp, vp]
     L.hb_linear.restype = ctypes.c_int
-    L.hb_linear.argtypes = [vp, vp, i32, i32, i32, i32, P(HbLinearOut), vp]
+    L.hb_linear.argtypes = [vp, vp, i32, i32, i32, i32, P(HbLinearOut), vp, sz, vp]
+    L.hb_linear_workspace_size.restype = sz
+    L.hb_linear_workspace_size.argtypes = [i32, i32, i32, i32, i32]
     L.hb_selftest_wait_timeout.restype = ctypes.c_int
     L.hb_selftest_wait_timeout.argtypes = [vp]
     L.hb_check.restype = ctypes.c_int
@@ -396,10 +398,30 @@ class Builder:
         return [int(x) for x in out[: n.value]]
 
 
-def hb_linear(x, w, outs, epilogue=LINEAR_STORE, stream=None):
+_linear_ws = {}
+
+
+def linear_workspace(M, N, K, epilogue, device=None):
+    """A zero-filled device workspace big enough for hb_linear's split-K on
+    this problem (cached per device and grown as needed), or None."""
+    dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    need = int(load().hb_linear_workspace_size(int(M), int(N), int(K), int(epilogue), sms))
+    if need == 0:
+        return None
+    ws = _linear_ws.get(dev)
+    if ws is None or ws.numel() < need:
+        ws = torch.zeros(need, dtype=torch.uint8, device=dev)
+        _linear_ws[dev] = ws
+    return ws
+
+
+def hb_linear(x, w, outs, epilogue=LINEAR_STORE, stream=None, workspace="auto"):
     """y = x w^T on the tensor cores.  x [M, K], w [N, K] bf16 device tensors;
     outs: the destination tensors ([M, cols_i] bf16 each; their column
-    counts split N for STORE / RESIDUAL, one [M, N / 2] tensor for GATED)."""
+    counts split N for STORE / RESIDUAL, one [M, N / 2] tensor for GATED).
+    workspace: "auto" (a cached zero-filled device buffer for split-K when
+    the problem has few tiles), None (no split), or a uint8 device tensor."""
     if len(outs) > 3:
         raise ValueError("at most three destinations")
     o = HbLinearOut()
@@ -409,5 +431,10 @@ def hb_linear(x, w, outs, epilogue=LINEAR_STORE, stream=None):
             raise ValueError("each destination must be a contiguous 2-D tensor")
         o.y[i] = t.data_ptr()
         o.cols[i] = t.shape[1]
-    _check(load().hb_linear(_bf16(x, "x"), _bf16(w, "w"), int(x.shape[0]), int(w.shape[0]),
-                            int(x.shape[1]), int(epilogue), ctypes.byref(o), _stream(stream)))
+    M, N, K = int(x.shape[0]), int(w.shape[0]), int(x.shape[1])
+    if isinstance(workspace, str):
+        workspace = linear_workspace(M, N, K, epilogue, x.device) if M > 0 else None
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(load().hb_linear(_bf16(x, "x"), _bf16(w, "w"), M, N, K, int(epilogue),
+                            ctypes.byref(o), ws_ptr, ws_bytes, _stream(stream)))

@@ -262,7 +262,19 @@ typedef struct hb_linear_out {
 } hb_linear_out;
 
 hb_status hb_linear(const void* x, const void* w, int32_t M, int32_t N, int32_t K,
-                    int32_t epilogue, const hb_linear_out* out, void* stream);
+                    int32_t epilogue, const hb_linear_out* out, void* workspace,
+                    size_t workspace_bytes, void* stream);
+
+/* Workspace that hb_linear can use for this problem on a device with num_sms
+ * SMs (0: it needs none).  When the output tiles are too few to occupy the
+ * SMs (few tokens), hb_linear splits each tile's K range over several CTAs;
+ * the pieces meet in `workspace` (device, 256-byte aligned, ZERO-FILLED before
+ * its first use; every call leaves it ready for the next, whatever its shape,
+ * so one workspace of the largest size serves all problems).  With a NULL or
+ * smaller workspace hb_linear runs unsplit.  Calls sharing a workspace must
+ * not overlap on the GPU. */
+size_t hb_linear_workspace_size(int32_t M, int32_t N, int32_t K, int32_t epilogue,
+                                int32_t num_sms);
 
 /* ---------------------------------------------------------------------------
  * Instrumentation.  When enabled, every kernel launch of this library is

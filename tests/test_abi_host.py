@@ -292,9 +292,9 @@ def test_linear_argument_checks():
         for i in range(3):
             o.cols[i] = cols[i]
             o.y[i] = (ys[i] if ys else a16).value if cols[i] else None
-        return L.hb_linear(x, w, M, N, K, epi, ctypes.byref(o), None)
+        return L.hb_linear(x, w, M, N, K, epi, ctypes.byref(o), None, 0, None)
 
-    assert L.hb_linear(a16, a16, 4, 256, 64, 0, None, None) == 1           # out NULL
+    assert L.hb_linear(a16, a16, 4, 256, 64, 0, None, None, 0, None) == 1  # out NULL
     assert call(a16, a16, 4, 256, 64, 3, (256, 0, 0)) == 1                # unknown epilogue
     assert call(a16, a16, 4, 256, 96, 0, (256, 0, 0)) == 2                # K % 64
     assert call(a16, a16, 4, 320, 64, 0, (320, 0, 0)) == 2                # N % 256
@@ -306,3 +306,25 @@ def test_linear_argument_checks():
     assert call(a16, a16, -1, 256, 64, 0, (256, 0, 0)) == 2               # M < 0
     assert call(a16, a16, 0, 768, 64, 0, (256, 512, 0)) == 0              # M = 0: nothing to do
     assert call(a16, a16, 0, 512, 64, 1, (256, 0, 0)) == 0
+
+
+def test_linear_workspace_size():
+    """Split-K only when the 128 x 256 tiles cannot fill half the SMs; the
+    workspace holds a fixed 4 KB counter region, then one fp32 tile per
+    (tile, piece)."""
+    hb = lib()
+    L = hb.load()
+    tile = 128 * 256 * 4
+    # 4 x 16 tiles on 152 SMs: 2 pieces
+    assert L.hb_linear_workspace_size(512, 4096, 4096, 0, 152) == 4096 + 2 * 64 * tile
+    # one tile, 64 K blocks: 16 pieces
+    assert L.hb_linear_workspace_size(1, 256, 4096, 0, 152) == 4096 + 16 * tile
+    # enough tiles, or too little K to split: none
+    assert L.hb_linear_workspace_size(8192, 4096, 4096, 0, 152) == 0
+    assert L.hb_linear_workspace_size(256, 28672, 4096, 1, 152) == 0
+    assert L.hb_linear_workspace_size(1, 256, 256, 0, 152) == 0
+    # gated: tiles of 128 output columns from [gate; up]
+    assert L.hb_linear_workspace_size(300, 512, 1024, 1, 152) == 4096 + 3 * 2 * 4 * tile
+    # invalid shapes: 0
+    assert L.hb_linear_workspace_size(4, 300, 64, 0, 152) == 0
+    assert L.hb_linear_workspace_size(4, 256, 100, 0, 152) == 0

@@ -108,3 +108,48 @@ def test_repeated_launches_and_timing():
     assert t["linear"][1] == 5 and t["linear"][0] > 0
     ref = ol.linear(workloads.bf16_bits(x.cpu()), workloads.bf16_bits(w.cpu()))
     _check(y, ref)
+
+
+@pytest.mark.parametrize("M,N,K,epi", [(1, 256, 4096, 0), (200, 512, 4096, 0), (77, 512, 2048, 2),
+                                       (300, 512, 1024, 1), (256, 4096, 14336, 0)])
+def test_split_k_matches_unsplit(M, N, K, epi):
+    """Few tiles: the K range is split over CTAs (workspace given) -- same bar
+    as the unsplit kernel, and repeated calls reuse the workspace."""
+    hb = lib()
+    dev = torch.device("cuda:0")
+    g = torch.Generator().manual_seed(M + N + K)
+    x, w = _rand((M, K), 1.0, g).to(dev), _rand((N, K), K ** -0.5, g).to(dev)
+    cols = N // 2 if epi == 1 else N
+    y0 = _rand((M, cols), 1.0, g).to(dev)
+    assert hb.linear_workspace(M, N, K, epi, dev) is not None
+    outs = {}
+    for ws in ("auto", None):
+        y = y0.clone()
+        for _ in range(2 if epi != 2 else 1):
+            hb.hb_linear(x, w, [y], epilogue=epi, workspace=ws)
+        hb.hb_check()
+        outs[ws] = y
+    xb, wb = workloads.bf16_bits(x.cpu()), workloads.bf16_bits(w.cpu())
+    if epi == 0:
+        ref = ol.linear(xb, wb)
+    elif epi == 1:
+        ref = ol.gated_mlp_up(xb, wb)
+    else:
+        ref = ol.residual(workloads.bf16_bits(y0.cpu()), xb, wb)
+    _check(outs["auto"], ref)
+    _check(outs[None], ref)
+
+
+def test_one_workspace_serves_every_shape():
+    """The cached workspace is shared by problems of different shapes (the
+    counters sit at a fixed place): interleaved calls all meet the bar."""
+    hb = lib()
+    dev = torch.device("cuda:0")
+    g = torch.Generator().manual_seed(99)
+    shapes = [(1, 256, 4096), (300, 1024, 2048), (64, 512, 8192), (1, 256, 4096), (200, 768, 512)]
+    for M, N, K in shapes * 2:
+        x, w = _rand((M, K), 1.0, g).to(dev), _rand((N, K), K ** -0.5, g).to(dev)
+        y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+        hb.hb_linear(x, w, [y])
+        hb.hb_check()
+        _check(y, ol.linear(workloads.bf16_bits(x.cpu()), workloads.bf16_bits(w.cpu())))
