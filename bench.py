@@ -284,6 +284,9 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+TIMING_EVERY = 8   # steps per step with per-kernel CUDA events
+
+
 def run_native(args):
     n, rank, local = _dist()
     torch.cuda.set_device(local)
@@ -318,17 +321,25 @@ def run_native(args):
     _barrier(n)
     torch.cuda.synchronize(dev)
     hb.hb_timing_enable(True)
+    hb.hb_timing_enable(False)
     launches0 = hb.hb_launch_count()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clk:
         ev0.record(stream)
-        for _ in range(args.steps):
+        for i in range(args.steps):
+            # per-kernel events on every TIMING_EVERY-th step only: an event
+            # between two kernels stops the GPU from starting the second
+            # launch under the first one's tail
+            sampled = i % TIMING_EVERY == 0
+            if sampled:
+                hb.hb_timing_enable(True, keep=True)
             step()
+            if sampled:
+                hb.hb_timing_enable(False)
         ev1.record(stream)
         torch.cuda.synchronize(dev)
     launches = hb.hb_launch_count() - launches0
     ktimes = hb.hb_timing_read()
-    hb.hb_timing_enable(False)
     hb.hb_check()
     _barrier(n)
     ms = ev0.elapsed_time(ev1)
@@ -401,6 +412,9 @@ def run_native(args):
     roof["algorithmic"] = {"bytes": att_bytes, "flops": att_flops}
     roof["kernel_roofline_frac"] = max(t_hbm, t_tc) * 1e3 / t_att
     roof["avg_launch_ms"] = {"attention": t_att, "kv_append": t_app}
+    roof["timed_launches"] = {"attention": ktimes["attention"][1],
+                              "kv_append": ktimes["kv_append"][1],
+                              "sample": f"CUDA events around each launch of every {TIMING_EVERY}th timed step"}
     step_roof_s = max(cnt["flops"] / (peaks["bf16_tflops"] * 1e12),
                       cnt["bytes"] / (peaks["hbm_gbs"] * 1e9))
     ms_step = ms_max / args.steps

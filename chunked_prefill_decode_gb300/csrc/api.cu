@@ -866,12 +866,15 @@ hb_status hb_selftest_wait_timeout(void* stream) {
 }
 
 hb_status hb_timing_enable(int32_t enable) {
+  if (enable < 0 || enable > 2) return fail(HB_ERR_INVALID_ARG, "timing mode must be 0, 1 or 2");
   std::lock_guard<std::mutex> lk(g_time_mu);
-  for (auto& r : g_recs) {
-    g_event_pool.push_back(r.a);
-    g_event_pool.push_back(r.b);
+  if (enable == 1) {
+    for (auto& r : g_recs) {
+      g_event_pool.push_back(r.a);
+      g_event_pool.push_back(r.b);
+    }
+    g_recs.clear();
   }
-  g_recs.clear();
   g_timing = enable != 0;
   return ok();
 }

@@ -42,6 +42,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                      const __grid_constant__ CUtensorMap chunk_k,
                      const __grid_constant__ CUtensorMap chunk_v) {
   extern __shared__ uint8_t smem_raw[];
+  griddep_wait();
+  griddep_launch_dependents();
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
   if ((int)blockIdx.x < p.decode_grid)
@@ -81,14 +83,16 @@ cudaError_t launch_attention(const DecodeParams& dec, int decode_grid, const Chu
     e = cudaFuncSetAttribute(attention_kernel<128>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    attention_kernel<128><<<grid, kAttnThreads, smem, stream>>>(p, dec_k, dec_v, chunk_q, chunk_k, chunk_v);
+    e = launch_serialized(attention_kernel<128>, grid, kAttnThreads, smem, stream, p, dec_k, dec_v,
+                          chunk_q, chunk_k, chunk_v);
   } else {
     e = cudaFuncSetAttribute(attention_kernel<64>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    attention_kernel<64><<<grid, kAttnThreads, smem, stream>>>(p, dec_k, dec_v, chunk_q, chunk_k, chunk_v);
+    e = launch_serialized(attention_kernel<64>, grid, kAttnThreads, smem, stream, p, dec_k, dec_v,
+                          chunk_q, chunk_k, chunk_v);
   }
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace hb

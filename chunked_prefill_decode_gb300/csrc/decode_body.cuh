@@ -31,7 +31,10 @@
 // Bytes per decode row: 2 * context * Hkv * D * 2 (K and V read once).
 #pragma once
 
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
+
+#include <type_traits>
 
 #include "hb_internal.h"
 #include "ptx.cuh"
@@ -40,6 +43,7 @@ namespace hb {
 
 constexpr int kDecConsumerWarps = 8;   // warps 0-7; warp 8 is the producer
 constexpr int kDecMaxStages = 8;
+constexpr float kDecRescaleThreshold = 8.0f;   // log2 units
 constexpr int kHdrFirst = 1, kHdrLast = 2, kHdrEnd = 4;
 
 struct StageHeader {
@@ -272,246 +276,316 @@ __device__ __forceinline__ void decode_cta(const DecodeParams& p, const DecodeLa
     }
   } else if (warp < kDecConsumerWarps) {
     // ------------------------------------------------------------ consumers
-    const int w = warp;                  // local kv head of this warp
-    const bool active = w < kvhb;
-    const bool hi_rows = g > 8;          // rows 8..15 of the MMA in use
-    const int r = lane >> 2;             // MMA row (q head in group)
-    const int cq = lane & 3;
-    uint32_t qa[D / 16][4];
-    float o[D / 8][4];
-    float m_run[2], l_run[2];
+    // One warp per kv head of the block.  The products are taken transposed,
+    // so the g <= 16 q heads of the group sit on the MMA's narrow N side
+    // (8 per column tile) instead of padding its 16 rows:
+    //   S^T [16 keys x 8 NQ heads]  = K [16 keys x D] Q^T          (A = K)
+    //   O^T [D x 8 NQ heads]       += V^T [D x 16 keys] P^T         (A = V^T)
+    // which takes D / 8 MMAs per column tile and page instead of D / 4.
+    // P^T leaves the S^T accumulator layout (key = lane / 4) and enters the
+    // B operand layout (key = 2 (lane % 4) ..): one movmatrix.trans per
+    // 8 x 8 quadrant.  The running maximum is raised (and O, l rescaled)
+    // only when it grows by more than 2^8; a stale maximum still bounds
+    // P <= 2^8, which bf16 and the fp32 sums carry exactly as well.
+    auto consume = [&](auto nq_const) {
+      constexpr int NQ = decltype(nq_const)::value;   // 8-head column tiles
+      const int w = warp;                  // local kv head of this warp
+      const bool active = w < kvhb;
+      const int r = lane >> 2;             // accumulator row: key r, r + 8 / dim r, r + 8
+      const int c = lane & 3;              // accumulator columns 2c, 2c + 1 (heads)
+      const int mi = lane >> 3, r8 = lane & 7;   // ldmatrix: matrix, row
+      uint32_t qb[D / 16][NQ][2];          // B operand Q^T (k = head dim, n = head)
+      float o[D / 16][NQ][4];              // O^T: dims 16 jj + r (+8), heads 2c, 2c + 1
+      float m_run[NQ][2], l_part[NQ][2];   // head 8 nq + 2c + e; l summed over this lane's keys
 #pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk)
-      qa[kk][0] = qa[kk][1] = qa[kk][2] = qa[kk][3] = 0u;
+      for (int kk = 0; kk < D / 16; ++kk)
 #pragma unroll
-    for (int nt = 0; nt < D / 8; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
-    m_run[0] = m_run[1] = -INFINITY;
-    l_run[0] = l_run[1] = 0.f;
-
-    int st = 0;
-    uint32_t ph = 0;
-    uint32_t qph[2] = {0u, 0u};
-    while (true) {
-      if (!mbar_wait(&full[st], ph, abort_flag)) break;
-      const StageHeader h = hdr[st];
-      if (h.flags & kHdrEnd) break;
-      if (h.flags & kHdrFirst) {
-        if (!mbar_wait(&qfull[h.qslot], qph[h.qslot], abort_flag)) break;
-        qph[h.qslot] ^= 1u;
-        if (active) {
-          const uint16_t* qs =
-              reinterpret_cast<const uint16_t*>(qbuf + h.qslot * L.qslot_bytes) +
-              (size_t)w * g * D;
+        for (int nq = 0; nq < NQ; ++nq) qb[kk][nq][0] = qb[kk][nq][1] = 0u;
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const int c0 = kk * 16 + cq * 2;
-            qa[kk][0] = (r < g) ? *reinterpret_cast<const uint32_t*>(qs + r * D + c0) : 0u;
-            qa[kk][1] = (r + 8 < g) ? *reinterpret_cast<const uint32_t*>(qs + (r + 8) * D + c0) : 0u;
-            qa[kk][2] = (r < g) ? *reinterpret_cast<const uint32_t*>(qs + r * D + c0 + 8) : 0u;
-            qa[kk][3] = (r + 8 < g) ? *reinterpret_cast<const uint32_t*>(qs + (r + 8) * D + c0 + 8) : 0u;
-          }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&qempty[h.qslot]);
+      for (int jj = 0; jj < D / 16; ++jj)
 #pragma unroll
-        for (int nt = 0; nt < D / 8; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
-        m_run[0] = m_run[1] = -INFINITY;
-        l_run[0] = l_run[1] = 0.f;
+        for (int nq = 0; nq < NQ; ++nq) o[jj][nq][0] = o[jj][nq][1] = o[jj][nq][2] = o[jj][nq][3] = 0.f;
+#pragma unroll
+      for (int nq = 0; nq < NQ; ++nq) {
+        m_run[nq][0] = m_run[nq][1] = -INFINITY;
+        l_part[nq][0] = l_part[nq][1] = 0.f;
       }
 
-      if (active) {
-        uint8_t* kst = stages + st * L.stage_bytes;
-        uint8_t* vst = kst + L.half_bytes;
-        const uint32_t kbase = smem_u32(kst);
-        const uint32_t vbase = smem_u32(vst);
-        const int valid = min(kPageSize, h.item.ctx - h.lpage * kPageSize);
-        // with a sliding window the row sees keys ctx - W .. ctx - 1 only
-        const int lo_valid = p.window > 0 ? h.item.ctx - p.window - h.lpage * kPageSize : 0;
-        if (valid < kPageSize) {
-          // Slots past the context were never written: clear this kv head's
-          // V rows there so that P = 0 never meets a NaN in the PV product.
-          const int nrow = kPageSize - valid;
-          for (int e = lane; e < nrow * CH * 8; e += 32) {
-            const int row = valid + e / (CH * 8);
-            const int rem = e % (CH * 8);
-            const int c = rem / 8, u = rem % 8;
-            uint4* dst = reinterpret_cast<uint4*>(vst + c * L.chunk_bytes +
-                                                  (w * kPageSize + row) * 128 + u * 16);
-            *dst = make_uint4(0u, 0u, 0u, 0u);
+      int st = 0;
+      uint32_t ph = 0;
+      uint32_t qph[2] = {0u, 0u};
+      while (true) {
+        if (!mbar_wait(&full[st], ph, abort_flag)) break;
+        const StageHeader h = hdr[st];
+        if (h.flags & kHdrEnd) break;
+        if (h.flags & kHdrFirst) {
+          if (!mbar_wait(&qfull[h.qslot], qph[h.qslot], abort_flag)) break;
+          qph[h.qslot] ^= 1u;
+          if (active) {
+            const uint16_t* qs =
+                reinterpret_cast<const uint16_t*>(qbuf + h.qslot * L.qslot_bytes) +
+                (size_t)w * g * D;
+#pragma unroll
+            for (int nq = 0; nq < NQ; ++nq) {
+              const int head = nq * 8 + r;
+#pragma unroll
+              for (int kk = 0; kk < D / 16; ++kk) {
+                const int d0 = kk * 16 + c * 2;
+                qb[kk][nq][0] = (head < g) ? *reinterpret_cast<const uint32_t*>(qs + head * D + d0) : 0u;
+                qb[kk][nq][1] = (head < g) ? *reinterpret_cast<const uint32_t*>(qs + head * D + d0 + 8) : 0u;
+              }
+            }
           }
-          fence_async_shared();
           __syncwarp();
-        }
-        // S = Q K^T over the page's 16 tokens (two n8 tiles)
-        float s[2][4];
+          if (lane == 0) mbar_arrive(&qempty[h.qslot]);
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
-        {
-          const int mi = lane >> 3, r8 = lane & 7;
-          const int tokr = ((mi >> 1) << 3) + r8;
-          const uint32_t rowaddr = kbase + (uint32_t)((w * kPageSize + tokr) * 128);
+          for (int jj = 0; jj < D / 16; ++jj)
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const int unit = ((kk & 3) << 1) + (mi & 1);
-            const uint32_t addr = rowaddr + (uint32_t)((kk >> 2) * L.chunk_bytes) +
-                                  (uint32_t)(((unit ^ (tokr & 7)) << 4));
-            uint32_t b0, b1, b2, b3;
-            ldsm_x4(addr, b0, b1, b2, b3);
-            mma_bf16_16816(s[0], qa[kk], b0, b1);
-            mma_bf16_16816(s[1], qa[kk], b2, b3);
+            for (int nq = 0; nq < NQ; ++nq) o[jj][nq][0] = o[jj][nq][1] = o[jj][nq][2] = o[jj][nq][3] = 0.f;
+#pragma unroll
+          for (int nq = 0; nq < NQ; ++nq) {
+            m_run[nq][0] = m_run[nq][1] = -INFINITY;
+            l_part[nq][0] = l_part[nq][1] = 0.f;
           }
         }
-        // scale, mask, online softmax (rows r and r + 8)
-        uint32_t pa[4];
-#pragma unroll
-        for (int hr = 0; hr < 2; ++hr) {
-          if (hr == 1 && !hi_rows) {
-            pa[1] = pa[3] = 0u;
-            continue;
+
+        if (active) {
+          uint8_t* kst = stages + st * L.stage_bytes;
+          uint8_t* vst = kst + L.half_bytes;
+          const uint32_t kbase = smem_u32(kst);
+          const uint32_t vbase = smem_u32(vst);
+          const int valid = min(kPageSize, h.item.ctx - h.lpage * kPageSize);
+          // with a sliding window the row sees keys ctx - W .. ctx - 1 only
+          const int lo_valid = p.window > 0 ? h.item.ctx - p.window - h.lpage * kPageSize : 0;
+          if (valid < kPageSize) {
+            // Slots past the context were never written: clear this kv head's
+            // V rows there so that P = 0 never meets a NaN in the PV product.
+            const int nrow = kPageSize - valid;
+            for (int e = lane; e < nrow * CH * 8; e += 32) {
+              const int row = valid + e / (CH * 8);
+              const int rem = e % (CH * 8);
+              const int cc = rem / 8, u = rem % 8;
+              uint4* dst = reinterpret_cast<uint4*>(vst + cc * L.chunk_bytes +
+                                                    (w * kPageSize + row) * 128 + u * 16);
+              *dst = make_uint4(0u, 0u, 0u, 0u);
+            }
+            fence_async_shared();
+            __syncwarp();
           }
-          float v[4];
+          // S^T = K Q^T: every K fragment is loaded before the first MMA, and
+          // even / odd head-dim steps accumulate apart (two short chains)
+          float s[2][NQ][4];
 #pragma unroll
-          for (int nt = 0; nt < 2; ++nt)
+          for (int x = 0; x < 2; ++x)
+#pragma unroll
+            for (int nq = 0; nq < NQ; ++nq) s[x][nq][0] = s[x][nq][1] = s[x][nq][2] = s[x][nq][3] = 0.f;
+          {
+            // matrix mi: keys 8 (mi & 1) .., head dims 8 (mi >> 1) .. of the step
+            const int tokr = ((mi & 1) << 3) + r8;
+            const uint32_t rowaddr = kbase + (uint32_t)((w * kPageSize + tokr) * 128);
+            uint32_t ka[D / 16][4];
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const int unit = ((kk & 3) << 1) + (mi >> 1);
+              ldsm_x4(rowaddr + (uint32_t)((kk >> 2) * L.chunk_bytes) +
+                          (uint32_t)((unit ^ (tokr & 7)) << 4),
+                      ka[kk][0], ka[kk][1], ka[kk][2], ka[kk][3]);
+            }
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk)
+#pragma unroll
+              for (int nq = 0; nq < NQ; ++nq)
+                mma_bf16_16816(s[kk & 1][nq], ka[kk], qb[kk][nq][0], qb[kk][nq][1]);
+          }
+          // V^T fragments, loaded while the softmax runs; matrix mi: keys
+          // 8 (mi >> 1) .., head dims 8 (mi & 1) .. of the 16-dim block
+          uint32_t va[D / 16][4];
+          {
+            const int tokr = ((mi >> 1) << 3) + r8;
+            const uint32_t rowaddr = vbase + (uint32_t)((w * kPageSize + tokr) * 128);
+#pragma unroll
+            for (int jj = 0; jj < D / 16; ++jj) {
+              const int u = 2 * jj + (mi & 1);   // 8-wide head-dim block
+              ldsm_x4_trans(rowaddr + (uint32_t)((u >> 3) * L.chunk_bytes) +
+                                (uint32_t)((((u & 7) ^ (tokr & 7)) << 4)),
+                            va[jj][0], va[jj][1], va[jj][2], va[jj][3]);
+            }
+          }
+          // softmax over the keys of each head column: keys r and r + 8 here,
+          // the other 14 in the lanes of the same c.  The column maxima are
+          // reduced (xor 4, 8, 16) only when some key of the page exceeds a
+          // running maximum by more than the threshold -- after the first
+          // pages of an item, almost never.
+          const bool ok0 = r < valid && r >= lo_valid;
+          const bool ok1 = r + 8 < valid && r + 8 >= lo_valid;
+          float x0[NQ][2], x1[NQ][2], alpha[NQ][2];
+          bool need = false;
+#pragma unroll
+          for (int nq = 0; nq < NQ; ++nq)
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
-              const int t = nt * 8 + cq * 2 + e;
-              v[nt * 2 + e] = (t < valid && t >= lo_valid) ? s[nt][hr * 2 + e] * p.scale_log2 : -INFINITY;
+              x0[nq][e] = ok0 ? (s[0][nq][e] + s[1][nq][e]) * p.scale_log2 : -INFINITY;
+              x1[nq][e] = ok1 ? (s[0][nq][2 + e] + s[1][nq][2 + e]) * p.scale_log2 : -INFINITY;
+              need |= fmaxf(x0[nq][e], x1[nq][e]) > m_run[nq][e] + kDecRescaleThreshold;
+              alpha[nq][e] = 1.f;
             }
-          float mx = fmaxf(fmaxf(v[0], v[1]), fmaxf(v[2], v[3]));
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-          const float m_new = fmaxf(m_run[hr], mx);
-          const float alpha = fast_exp2(m_run[hr] - m_new);
-          m_run[hr] = m_new;
-          const uint32_t lo = pack_bf16x2(fast_exp2(v[0] - m_new), fast_exp2(v[1] - m_new));
-          const uint32_t hi = pack_bf16x2(fast_exp2(v[2] - m_new), fast_exp2(v[3] - m_new));
-          // the row sum uses the same bf16-rounded P that feeds the MMA
-          l_run[hr] = l_run[hr] * alpha + (bf16lo_to_f32(lo) + bf16hi_to_f32(lo)) +
-                      (bf16lo_to_f32(hi) + bf16hi_to_f32(hi));
+          if (__any_sync(0xffffffffu, need)) {
 #pragma unroll
-          for (int nt = 0; nt < D / 8; ++nt) {
-            o[nt][hr * 2] *= alpha;
-            o[nt][hr * 2 + 1] *= alpha;
-          }
-          pa[hr] = lo;       // A rows r (+8), tokens 0..7
-          pa[hr + 2] = hi;   // tokens 8..15
-        }
-        // O += P V
-        {
-          const int mi = lane >> 3, r8 = lane & 7;
-          const int tokr = ((mi & 1) << 3) + r8;
-          const uint32_t rowaddr = vbase + (uint32_t)((w * kPageSize + tokr) * 128);
+            for (int nq = 0; nq < NQ; ++nq)
 #pragma unroll
-          for (int jj = 0; jj < D / 16; ++jj) {
-            const int u = 2 * jj + (mi >> 1);   // 8-wide head-dim block
-            const uint32_t addr = rowaddr + (uint32_t)((u >> 3) * L.chunk_bytes) +
-                                  (uint32_t)((((u & 7) ^ (tokr & 7)) << 4));
-            uint32_t v0, v1, v2, v3;
-            ldsm_x4_trans(addr, v0, v1, v2, v3);
-            mma_bf16_16816(o[2 * jj], pa, v0, v1);
-            mma_bf16_16816(o[2 * jj + 1], pa, v2, v3);
-          }
-        }
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[st]);
-
-      if (h.flags & kHdrLast) {
-        const DecodeItem& it = h.item;
-        const int Hq = p.num_q_heads;
-        if (active) {
-          float l_tot[2];
-#pragma unroll
-          for (int hr = 0; hr < 2; ++hr) {
-            float t = l_run[hr];
-            t += __shfl_xor_sync(0xffffffffu, t, 1);
-            t += __shfl_xor_sync(0xffffffffu, t, 2);
-            l_tot[hr] = t;
-          }
-          const int head0 = (it.kvh0 + w) * g;
-#pragma unroll
-          for (int hr = 0; hr < 2; ++hr) {
-            const int row = r + 8 * hr;
-            if (row >= g) continue;
-            if (it.n_splits == 1) {
-              const float inv = 1.f / l_tot[hr];
-              uint32_t* dst = reinterpret_cast<uint32_t*>(
-                  p.out + ((size_t)h.item.tok * Hq + head0 + row) * D + cq * 2);
-#pragma unroll
-              for (int nt = 0; nt < D / 8; ++nt)
-                dst[nt * 4] = pack_bf16x2(o[nt][hr * 2] * inv, o[nt][hr * 2 + 1] * inv);
-            } else {
-              const size_t slot = (size_t)(it.slot + it.split);
-              float2* dst = reinterpret_cast<float2*>(
-                  p.part_o + (slot * Hq + head0 + row) * D + cq * 2);
-#pragma unroll
-              for (int nt = 0; nt < D / 8; ++nt)
-                dst[nt * 4] = make_float2(o[nt][hr * 2], o[nt][hr * 2 + 1]);
-              if (cq == 0) {
-                float2* ml = reinterpret_cast<float2*>(p.part_ml) + slot * Hq + head0 + row;
-                *ml = make_float2(m_run[hr], l_tot[hr]);
-              }
-            }
-          }
-        }
-        if (it.n_splits > 1) {
-          // publish this split's partial state: the CTA barrier orders every
-          // consumer's stores before thread 0's device-scope fence + atomic
-          named_bar_sync(1, 32 * kDecConsumerWarps);
-          if (threadIdx.x == 0) {
-            __threadfence();
-            const int old = atomicAdd(&p.counters[kCounterMerge0 + it.merge_id], 1);
-            __threadfence();  // acquire: the other splits' states are visible
-            flags[1] = (old == it.n_splits - 1) ? 1 : 0;
-          }
-          named_bar_sync(1, 32 * kDecConsumerWarps);
-          if (flags[1]) {
-            __threadfence();
-            // one warp per head of the block; each lane owns D/32 head-dim
-            // elements; every split's (m, l) is read once per head
-            constexpr int E = D / 32;
-            const float2* ml = reinterpret_cast<const float2*>(p.part_ml);
-            const int nh = kvhb * g;
-            for (int hl = warp; hl < nh; hl += kDecConsumerWarps) {
-              const int hh = it.kvh0 * g + hl;
-              float mmax = -INFINITY;
-              for (int i = 0; i < it.n_splits; ++i)
-                mmax = fmaxf(mmax, __ldcg(&ml[(size_t)(it.slot + i) * Hq + hh]).x);
-              float acc[E];
-#pragma unroll
-              for (int e = 0; e < E; ++e) acc[e] = 0.f;
-              float lsum = 0.f;
-#pragma unroll 4
-              for (int i = 0; i < it.n_splits; ++i) {
-                const size_t slot = (size_t)(it.slot + i);
-                const float2 st2 = __ldcg(&ml[slot * Hq + hh]);
-                const float wgt = fast_exp2(st2.x - mmax);
-                lsum += wgt * st2.y;
-                const float* po = p.part_o + (slot * Hq + hh) * D + lane * E;
-                if constexpr (E == 4) {
-                  const float4 v = __ldcg(reinterpret_cast<const float4*>(po));
-                  acc[0] += wgt * v.x; acc[1] += wgt * v.y;
-                  acc[2] += wgt * v.z; acc[3] += wgt * v.w;
-                } else {
-                  const float2 v = __ldcg(reinterpret_cast<const float2*>(po));
-                  acc[0] += wgt * v.x; acc[1] += wgt * v.y;
+              for (int e = 0; e < 2; ++e) {
+                float mx = fmaxf(x0[nq][e], x1[nq][e]);
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+                if (mx > m_run[nq][e] + kDecRescaleThreshold) {
+                  alpha[nq][e] = fast_exp2(m_run[nq][e] - mx);
+                  m_run[nq][e] = mx;
                 }
               }
-              const float inv = 1.f / lsum;
-              uint32_t* dst = reinterpret_cast<uint32_t*>(
-                  p.out + ((size_t)h.item.tok * Hq + hh) * D + lane * E);
 #pragma unroll
-              for (int e = 0; e < E; e += 2) dst[e / 2] = pack_bf16x2(acc[e] * inv, acc[e + 1] * inv);
+            for (int jj = 0; jj < D / 16; ++jj)
+#pragma unroll
+              for (int nq = 0; nq < NQ; ++nq)
+#pragma unroll
+                for (int x = 0; x < 4; ++x) o[jj][nq][x] *= alpha[nq][x & 1];
+          }
+          uint32_t pb[NQ][2];
+#pragma unroll
+          for (int nq = 0; nq < NQ; ++nq) {
+            float p0[2], p1[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              // no key seen yet: every x is -inf and so is P's exponent
+              const float mu = m_run[nq][e] == -INFINITY ? 0.f : m_run[nq][e];
+              p0[e] = fast_exp2(x0[nq][e] - mu);
+              p1[e] = fast_exp2(x1[nq][e] - mu);
             }
-            if (threadIdx.x == 0) p.counters[kCounterMerge0 + it.merge_id] = 0;
+            const uint32_t lo = pack_bf16x2(p0[0], p0[1]);   // keys r, heads 2c, 2c + 1
+            const uint32_t hi = pack_bf16x2(p1[0], p1[1]);   // keys r + 8
+            // the row sums use the same bf16-rounded P that feeds the MMA
+            l_part[nq][0] = l_part[nq][0] * alpha[nq][0] + (bf16lo_to_f32(lo) + bf16lo_to_f32(hi));
+            l_part[nq][1] = l_part[nq][1] * alpha[nq][1] + (bf16hi_to_f32(lo) + bf16hi_to_f32(hi));
+            pb[nq][0] = movmatrix_trans(lo);   // B: keys 2c, 2c + 1 of head r
+            pb[nq][1] = movmatrix_trans(hi);   // keys 8 + 2c ..
+          }
+          // O^T += V^T P^T
+#pragma unroll
+          for (int jj = 0; jj < D / 16; ++jj)
+#pragma unroll
+            for (int nq = 0; nq < NQ; ++nq)
+              mma_bf16_16816(o[jj][nq], va[jj], pb[nq][0], pb[nq][1]);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[st]);
+
+        if (h.flags & kHdrLast) {
+          const DecodeItem& it = h.item;
+          const int Hq = p.num_q_heads;
+          if (active) {
+            float l_tot[NQ][2];
+#pragma unroll
+            for (int nq = 0; nq < NQ; ++nq)
+#pragma unroll
+              for (int e = 0; e < 2; ++e) {
+                float t = l_part[nq][e];
+                t += __shfl_xor_sync(0xffffffffu, t, 4);
+                t += __shfl_xor_sync(0xffffffffu, t, 8);
+                t += __shfl_xor_sync(0xffffffffu, t, 16);
+                l_tot[nq][e] = t;
+              }
+            const int head0 = (it.kvh0 + w) * g;
+#pragma unroll
+            for (int nq = 0; nq < NQ; ++nq)
+#pragma unroll
+              for (int e = 0; e < 2; ++e) {
+                const int head = nq * 8 + 2 * c + e;
+                if (head >= g) continue;
+                if (it.n_splits == 1) {
+                  const float inv = 1.f / l_tot[nq][e];
+                  __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(
+                      p.out + ((size_t)it.tok * Hq + head0 + head) * D + r);
+#pragma unroll
+                  for (int jj = 0; jj < D / 16; ++jj) {
+                    dst[jj * 16] = __float2bfloat16_rn(o[jj][nq][e] * inv);
+                    dst[jj * 16 + 8] = __float2bfloat16_rn(o[jj][nq][2 + e] * inv);
+                  }
+                } else {
+                  const size_t slot = (size_t)(it.slot + it.split);
+                  float* dst = p.part_o + (slot * Hq + head0 + head) * D + r;
+#pragma unroll
+                  for (int jj = 0; jj < D / 16; ++jj) {
+                    dst[jj * 16] = o[jj][nq][e];
+                    dst[jj * 16 + 8] = o[jj][nq][2 + e];
+                  }
+                  if (r == 0) {
+                    float2* ml = reinterpret_cast<float2*>(p.part_ml) + slot * Hq + head0 + head;
+                    *ml = make_float2(m_run[nq][e], l_tot[nq][e]);
+                  }
+                }
+              }
+          }
+          if (it.n_splits > 1) {
+            // publish this split's partial state: the CTA barrier orders every
+            // consumer's stores before thread 0's device-scope fence + atomic
+            named_bar_sync(1, 32 * kDecConsumerWarps);
+            if (threadIdx.x == 0) {
+              __threadfence();
+              const int old = atomicAdd(&p.counters[kCounterMerge0 + it.merge_id], 1);
+              __threadfence();  // acquire: the other splits' states are visible
+              flags[1] = (old == it.n_splits - 1) ? 1 : 0;
+            }
+            named_bar_sync(1, 32 * kDecConsumerWarps);
+            if (flags[1]) {
+              __threadfence();
+              // one warp per head of the block; each lane owns D/32 head-dim
+              // elements; every split's (m, l) is read once per head
+              constexpr int E = D / 32;
+              const float2* ml = reinterpret_cast<const float2*>(p.part_ml);
+              const int nh = kvhb * g;
+              for (int hl = warp; hl < nh; hl += kDecConsumerWarps) {
+                const int hh = it.kvh0 * g + hl;
+                float mmax = -INFINITY;
+                for (int i = 0; i < it.n_splits; ++i)
+                  mmax = fmaxf(mmax, __ldcg(&ml[(size_t)(it.slot + i) * Hq + hh]).x);
+                float acc[E];
+#pragma unroll
+                for (int e = 0; e < E; ++e) acc[e] = 0.f;
+                float lsum = 0.f;
+#pragma unroll 4
+                for (int i = 0; i < it.n_splits; ++i) {
+                  const size_t slot = (size_t)(it.slot + i);
+                  const float2 st2 = __ldcg(&ml[slot * Hq + hh]);
+                  const float wgt = fast_exp2(st2.x - mmax);
+                  lsum += wgt * st2.y;
+                  const float* po = p.part_o + (slot * Hq + hh) * D + lane * E;
+                  if constexpr (E == 4) {
+                    const float4 v = __ldcg(reinterpret_cast<const float4*>(po));
+                    acc[0] += wgt * v.x; acc[1] += wgt * v.y;
+                    acc[2] += wgt * v.z; acc[3] += wgt * v.w;
+                  } else {
+                    const float2 v = __ldcg(reinterpret_cast<const float2*>(po));
+                    acc[0] += wgt * v.x; acc[1] += wgt * v.y;
+                  }
+                }
+                const float inv = 1.f / lsum;
+                uint32_t* dst = reinterpret_cast<uint32_t*>(
+                    p.out + ((size_t)h.item.tok * Hq + hh) * D + lane * E);
+#pragma unroll
+                for (int e = 0; e < E; e += 2) dst[e / 2] = pack_bf16x2(acc[e] * inv, acc[e + 1] * inv);
+              }
+              if (threadIdx.x == 0) p.counters[kCounterMerge0 + it.merge_id] = 0;
+            }
           }
         }
+        if (++st == S) {
+          st = 0;
+          ph ^= 1u;
+        }
       }
-      if (++st == S) {
-        st = 0;
-        ph ^= 1u;
-      }
-    }
+    };
+    if (g <= 8) consume(std::integral_constant<int, 1>{});
+    else consume(std::integral_constant<int, 2>{});
   }
   __syncthreads();
   if (threadIdx.x == 0 && *abort_flag) report_error(p.dev_error, HB_DEVERR_TIMEOUT);

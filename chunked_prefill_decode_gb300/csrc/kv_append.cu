@@ -32,6 +32,8 @@ constexpr int kAppendVecsPerLane = 8;
 
 __global__ void __launch_bounds__(256) kv_append_kernel(AppendParams p) {
   extern __shared__ int32_t s_cu[];
+  griddep_wait();
+  griddep_launch_dependents();
   const int lane = threadIdx.x & 31;
   // the row -> sequence search runs on a shared-memory copy of cu_q_len (one
   // coalesced load per CTA instead of a chain of dependent global loads)
@@ -102,8 +104,7 @@ cudaError_t launch_kv_append(const AppendParams& p, int num_sms,
   const long cap = 16L * num_sms;
   if (blocks > cap) blocks = cap;
   const size_t smem = p.num_seqs <= kAppendSmemSeqs ? (size_t)(p.num_seqs + 1) * 4 : 0;
-  kv_append_kernel<<<(unsigned)blocks, 32 * warps_per_block, smem, stream>>>(p);
-  return cudaGetLastError();
+  return launch_serialized(kv_append_kernel, (unsigned)blocks, 32 * warps_per_block, smem, stream, p);
 }
 
 }  // namespace hb

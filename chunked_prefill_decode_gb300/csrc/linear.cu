@@ -65,6 +65,8 @@ __global__ void __launch_bounds__(kLinThreads, 1)
   constexpr int kLinBarOff = C::kBarOff;
   constexpr int kLinMiscOff = C::kMiscOff;
   extern __shared__ uint8_t smem_raw[];
+  griddep_wait();
+  griddep_launch_dependents();
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kLinBarOff);
@@ -407,8 +409,8 @@ static cudaError_t launch_bn(const LinearParams& p, const CUtensorMap& xmap,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        LinCfg<BN>::kSmemBytes);
   if (e != cudaSuccess) return e;
-  linear_kernel<BN><<<grid, kLinThreads, LinCfg<BN>::kSmemBytes, stream>>>(p, xmap, wmap);
-  return cudaGetLastError();
+  return launch_serialized(linear_kernel<BN>, grid, kLinThreads, LinCfg<BN>::kSmemBytes, stream, p,
+                           xmap, wmap);
 }
 
 // Persistent launch: one CTA per SM (at most one per tile).  `bn` is the

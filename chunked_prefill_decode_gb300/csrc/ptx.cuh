@@ -10,12 +10,47 @@
 
 #include <cstdint>
 #include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <utility>
 
 #include "hb_internal.h"
 
 namespace hb {
 
 constexpr uint64_t HB_WAIT_NS = 1000ull * 1000ull * 1000ull;  // 1 s
+
+// ---------------------------------------------------------------- launches
+// Programmatic dependent launch.  Every kernel of the library is launched
+// with programmatic stream serialization: its CTAs may become resident while
+// the previous kernel on the stream is still running, and each kernel's
+// first act, before it touches global memory, is griddep_wait(), which
+// returns once that kernel has completed and its writes are visible.  So
+// the ordering of the stream is unchanged; only the launch latency between
+// two kernels is hidden.  A kernel lets the next one be scheduled with
+// griddep_launch_dependents() (which the next one still waits behind).
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... Params, typename... Args>
+inline cudaError_t launch_serialized(void (*kernel)(Params...), unsigned grid, unsigned block,
+                                     size_t smem, cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -221,6 +256,14 @@ __device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t& r0,
       : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
       : "r"(addr)
       : "memory");
+}
+
+// Transpose of an 8 x 8 b16 matrix held in the warp's fragment layout (lane
+// l holds row l / 4, columns 2 (l % 4) and 2 (l % 4) + 1, low half first).
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t a) {
+  uint32_t d;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+  return d;
 }
 
 // c[16x8] += a[16x16] * b[16x8], bf16 inputs, fp32 accumulate.

@@ -309,8 +309,10 @@ def hb_selftest_wait_timeout(stream=None):
     _check(load().hb_selftest_wait_timeout(_stream(stream)))
 
 
-def hb_timing_enable(on: bool):
-    _check(load().hb_timing_enable(1 if on else 0))
+def hb_timing_enable(on: bool, keep: bool = False):
+    """Start (clearing earlier records; with keep=True resuming) or stop
+    recording launch durations."""
+    _check(load().hb_timing_enable((2 if keep else 1) if on else 0))
 
 
 def hb_timing_read():

@@ -284,8 +284,10 @@ size_t hb_linear_workspace_size(int32_t M, int32_t N, int32_t K, int32_t epilogu
  * ------------------------------------------------------------------------- */
 #define HB_NUM_KERNEL_IDS 3
 
-/* Start (clearing earlier records) or stop recording.  Not thread-safe with
- * concurrent launches from other threads. */
+/* enable = 1: start recording, clearing earlier records; 2: resume
+ * recording, keeping them (to time a sample of the launches); 0: stop (the
+ * records stay readable).  Other values: HB_ERR_INVALID_ARG.  Not
+ * thread-safe with concurrent launches from other threads. */
 hb_status hb_timing_enable(int32_t enable);
 
 /* Synchronise the recorded events and return, per kernel id, the summed

@@ -9,7 +9,7 @@ no code with the CUDA library.
 through the model's linear layers, which take most of the time of both
 phases -- compute-bound for prefill tokens, bound by reading the weights for
 decode tokens.  The pages do not write the layers out; the readings taken
-(listed in the design doc) are the plain ones of a GQA transformer block:
+are the plain ones of a GQA transformer block:
   * a linear layer is y = x W^T, x [M, K] (one row per token of the batch),
     W [N, K] (row n holds the weights of output feature n);
   * the gated MLP multiplies silu(x W_gate^T) with x W_up^T elementwise,

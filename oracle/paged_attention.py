@@ -22,7 +22,7 @@ What the pages fix, and where:
   * "In-flight Batching", §KV Cache 管理的协同优化: fixed 16-token pages, a block
     table maps logical pages to physical ones, which need not be contiguous.
 
-Readings taken where the pages are silent (each is listed in the design doc):
+Readings taken where the pages are silent:
   * attention is standard scaled dot-product attention with a causal mask
     aligned to absolute positions: the new token j of a row with q_len new
     tokens and context_len cached-after-append tokens sits at position

@@ -23,7 +23,7 @@ waiting -> prefill (chunked, repeated until the prompt is done) -> decode
 数据路径 ⑦), so a request enters decode with one generated token whose KV is
 appended by its first decode step.
 
-Readings where the pages are silent (listed in the design doc):
+Readings where the pages are silent:
   * chunk size = min(prompt tokens left, budget left) ("fill the remaining
     budget"); ongoing chunks are also cut to the KV pages that can be had;
   * admission is first-come-first-served in arrival order and stops at the

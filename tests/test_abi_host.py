@@ -26,6 +26,16 @@ def test_status_strings():
         assert L.hb_status_string(code).decode() == name
 
 
+def test_timing_modes():
+    L = lib().load()
+    assert L.hb_timing_enable(3) == 1 and L.hb_timing_enable(-1) == 1   # HB_ERR_INVALID_ARG
+    for mode in (1, 0, 2, 0):
+        assert L.hb_timing_enable(mode) == 0
+    ms = (ctypes.c_double * 3)()
+    n = (ctypes.c_int32 * 3)()
+    assert L.hb_timing_read(ms, n) == 0 and list(n) == [0, 0, 0]
+
+
 @pytest.mark.parametrize("field,value,status", [
     ("page_size", 8, 3), ("head_dim", 96, 3), ("num_kv_heads", 3, 2),
     ("num_q_heads", 0, 2), ("num_pages", 0, 2), ("max_pages_per_seq", 0, 2),

@@ -190,6 +190,17 @@ def test_timing_and_launch_count():
     assert hb.hb_launch_count() - n0 == 2
     for name in ("kv_append", "attention"):
         assert t[name][1] == 1 and t[name][0] > 0
+    # sampling: records survive a pause and a resume adds to them
+    hb.hb_timing_enable(True)
+    gpu_step(lay, ten)
+    hb.hb_timing_enable(False)
+    gpu_step(lay, ten)
+    hb.hb_timing_enable(True, keep=True)
+    gpu_step(lay, ten)
+    hb.hb_timing_enable(False)
+    t = hb.hb_timing_read()
+    for name in ("kv_append", "attention"):
+        assert t[name][1] == 2
 
 
 # ---------------------------------------------------------------- full size
