@@ -10,19 +10,22 @@
 //
 //  * persistent and balanced: the host plan lays the decode rows' pages end
 //    to end and gives each CTA (at most one per SM) an equal contiguous
-//    range of ~90 % of them; the rest are short intervals that CTAs claim
-//    from a counter when their own range is done (SMs stream at slightly
-//    different rates); every interval is cut at row boundaries into work
-//    items (a page range of one row and one block of <= 8 kv heads);
+//    range of them (optionally only ~90 %, the rest as short intervals that
+//    CTAs claim from a counter when their own range is done; the plan
+//    leaves this off, it measured slower); every range is cut at row
+//    boundaries into work items (a page range of one row and one block of
+//    <= 8 kv heads);
 //  * one producer warp streams whole pages (all kv heads of the block, K and
 //    V) into a ring of shared-memory stages with 4-D TMA copies laid out as
 //    [kv head][slot][64 head-dim] rows with the 128-byte swizzle, so the
 //    consumer's ldmatrix reads are bank-conflict free; the q row of each item
 //    arrives by a bulk copy into a two-slot ring;
-//  * eight consumer warps, one per kv head: the GQA group (g <= 16 q heads)
-//    forms the rows of a 16 x 16 x 16 warp MMA, so each K/V element loaded
-//    from shared memory serves all g heads; online softmax in registers with
-//    the exp2 form (scale * log2 e folded in);
+//  * eight consumer warps, one per kv head, with warp MMAs taken transposed
+//    (S^T = K Q^T, O^T += V^T P^T) so the group's g <= 16 q heads sit on
+//    the MMA's N side and each K/V element read from shared memory serves
+//    all g heads; a stage is handed back as soon as its K and V are in
+//    registers; online softmax in registers with the exp2 form (scale *
+//    log2 e folded in);
 //  * a row that straddles ranges leaves one partial state (m, l,
 //    unnormalised o) per piece in the workspace; the last piece of a
 //    (row, kv block) to finish, found with an atomic counter, merges them: m = max m_i, l = sum 2^(m_i - m) l_i, o = sum 2^(m_i - m) o_i
@@ -411,6 +414,10 @@ __device__ __forceinline__ void decode_cta(const DecodeParams& p, const DecodeLa
                             va[jj][0], va[jj][1], va[jj][2], va[jj][3]);
             }
           }
+          // K and V of the page are in registers: the stage goes back to the
+          // producer now, a softmax and a PV ahead of the end of the page
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&empty[st]);
           // softmax over the keys of each head column: keys r and r + 8 here,
           // the other 14 in the lanes of the same c.  The column maxima are
           // reduced (xor 4, 8, 16) only when some key of the page exceeds a
@@ -475,9 +482,10 @@ __device__ __forceinline__ void decode_cta(const DecodeParams& p, const DecodeLa
 #pragma unroll
             for (int nq = 0; nq < NQ; ++nq)
               mma_bf16_16816(o[jj][nq], va[jj], pb[nq][0], pb[nq][1]);
+        } else {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&empty[st]);
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[st]);
 
         if (h.flags & kHdrLast) {
           const DecodeItem& it = h.item;
