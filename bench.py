@@ -554,31 +554,39 @@ def run_layer(args):
     hb.hb_check()
     steps = max(1, min(args.steps, 500))
     hb.hb_timing_enable(True)
+    hb.hb_timing_enable(False)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n_sampled = 0
     with ClockSampler(0) as clk:
         ev0.record()
-        for _ in range(steps):
+        for i in range(steps):
+            sampled = i % TIMING_EVERY == 0
+            if sampled:
+                hb.hb_timing_enable(True, keep=True)
+                n_sampled += 1
             blk.forward(x, db, ten.k_cache, ten.v_cache, bufs=bufs, plan=False)
+            if sampled:
+                hb.hb_timing_enable(False)
         ev1.record()
         torch.cuda.synchronize(dev)
     kt = hb.hb_timing_read()
-    hb.hb_timing_enable(False)
     hb.hb_check()
     ms = ev0.elapsed_time(ev1) / steps
     peaks = _peaks()
-    lin_ms = kt["linear"][0] / steps
+    lin_ms = kt["linear"][0] / n_sampled
     lin_flops = blk.flops(T)
     weight_bytes = 2.0 * bshape.params()
     line = {
         "mode": "layer", "workload": args.workload, "tokens_per_step": T, "steps": steps,
         "ms_per_step": ms, "tokens_per_s": T / (ms * 1e-3),
-        "ms_by_kernel": {k: v[0] / steps for k, v in kt.items()},
-        "launches_per_step": {k: v[1] / steps for k, v in kt.items()},
+        "ms_by_kernel": {k: v[0] / n_sampled for k, v in kt.items()},
+        "launches_per_step": {k: v[1] / n_sampled for k, v in kt.items()},
         "linear": {"flops": lin_flops, "weight_bytes": weight_bytes,
                    "tflops": lin_flops / (lin_ms * 1e-3) / 1e12,
                    "roofline_ms": max(lin_flops / (peaks["bf16_tflops"] * 1e12),
                                       weight_bytes / (peaks["hbm_gbs"] * 1e9)) * 1e3},
-        "attention_share": (kt["attention"][0] + kt["kv_append"][0]) / steps / ms,
+        "attention_share": (kt["attention"][0] + kt["kv_append"][0]) / n_sampled / ms,
+        "kernel_timing": f"CUDA events around each launch of every {TIMING_EVERY}th timed step",
         "block": {"hidden": bshape.hidden, "ffn": bshape.ffn, "params": bshape.params()},
         "weights": "synthetic N(0, 1/fan_in)", "data": "synthetic", "clocks": clk.summary(),
     }
