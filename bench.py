@@ -237,6 +237,51 @@ def oracle_sample_rate(layout, ten_host, budget_s=12.0, rows=None):
                       f"decode rows then every 7th chunk token, cycled, {dt:.1f} s"
 
 
+_ONE_THREAD_ENV = ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS",
+                   "BLIS_NUM_THREADS", "VECLIB_MAXIMUM_THREADS")
+
+
+def oracle_sample_rate_one_thread(workload, budget_s):
+    """The same oracle sample with BLAS held to one thread: a fresh process
+    (the thread count of a BLAS library is fixed when it loads).  Returns
+    (tokens/s, description) or (None, reason)."""
+    import subprocess
+    env = dict(os.environ)
+    for k in _ONE_THREAD_ENV:
+        env[k] = "1"
+    env.pop("RANK", None), env.pop("WORLD_SIZE", None)
+    try:
+        r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-sample",
+                            "--workload", workload, "--cpu-seconds", str(budget_s)],
+                           env=env, capture_output=True, text=True, timeout=300)
+        d = json.loads(r.stdout.strip().splitlines()[-1])
+        return d["value"], d["sample"]
+    except Exception as e:   # reported, not fatal: the GPU numbers stand alone
+        return None, f"one-thread sample failed: {type(e).__name__}"
+
+
+def run_oracle_sample(args):
+    """Print one JSON line with the oracle's sample rate (used by
+    oracle_sample_rate_one_thread in a child process)."""
+    layout = workloads.WORKLOADS[args.workload]()
+    v, desc = oracle_sample_rate(layout, workloads.make_tensors(layout, seed=1),
+                                 budget_s=args.cpu_seconds)
+    print(json.dumps({"value": v, "sample": desc}), flush=True)
+
+
+def plan_host_us(db, layout, sms, reps=20):
+    """Median host time of hb_plan for this batch (the host part only: no
+    upload)."""
+    from chunked_prefill_decode_gb300 import hb
+    plan, _ = hb.hb_plan(db.batch, layout.q_len, layout.context_len, sms, upload=False)
+    ts = []
+    for _ in range(reps):
+        t0 = time.perf_counter()
+        hb.hb_plan(db.batch, layout.q_len, layout.context_len, sms, plan=plan, upload=False)
+        ts.append((time.perf_counter() - t0) * 1e6)
+    return float(np.median(ts))
+
+
 def run_reference(args):
     """The fp64 CPU oracle as the reference arm (rank 0 only)."""
     n, rank, _ = _dist() if int(os.environ.get("WORLD_SIZE", "1")) > 1 else (1, 0, 0)
@@ -420,6 +465,8 @@ def run_native(args):
     ms_step = ms_max / args.steps
     cpu_v, cpu_desc = oracle_sample_rate(layout, workloads.make_tensors(layout, seed=1),
                                          budget_s=args.cpu_seconds)
+    cpu1_v, cpu1_desc = oracle_sample_rate_one_thread(args.workload, args.cpu_seconds / 2)
+    plan_us = plan_host_us(db, layout, sms)
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": n,
         "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms_step,
@@ -442,7 +489,10 @@ def run_native(args):
                           cnt["flops"] / (peaks["bf16_tflops"] * 1e12) else "tensor"},
         "cpu_baseline": {"value": cpu_v, "unit": "tokens/s",
                          "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
-                         "sample": cpu_desc},
+                         "sample": cpu_desc,
+                         "one_thread": {"value": cpu1_v, "unit": "tokens/s", "cores": 1,
+                                        "sample": cpu1_desc}},
+        "plan_host_us": plan_us,
         "e2e": e2e,
         "gpu_launches": int(launches),
         "clocks": clk.summary(),
@@ -608,7 +658,11 @@ def main():
     ap.add_argument("--layer", action="store_true",
                     help="instead of the attention step: one transformer block of the "
                          "batch (linear layers on synthetic weights around attention)")
+    ap.add_argument("--oracle-sample", action="store_true", help=argparse.SUPPRESS)
     args = ap.parse_args()
+    if args.oracle_sample:
+        run_oracle_sample(args)
+        return
     if args.sweep == "chunk":
         run_chunk_sweep(args)
     elif args.layer:

@@ -16,6 +16,8 @@
 // of work end together.  No CTA waits for another.
 #include <cuda_runtime.h>
 
+#include <atomic>
+
 #include "chunk_body.cuh"
 #include "decode_body.cuh"
 #include "hb_internal.h"
@@ -78,6 +80,24 @@ cudaError_t launch_attention(const DecodeParams& dec, int decode_grid, const Chu
   const int grid = p.decode_grid + chk.num_items;
   if (grid == 0) return cudaSuccess;
   const int smem = attention_smem_bytes(head_dim, dec.kvh_block, dec.group);
+  // setmaxnreg.inc waits until the block's register pool holds what it asks
+  // for; the chunk CTAs' split assumes the launch allocation of
+  // kChunkLaunchRegs per thread, so a build that allocated fewer is refused
+  // here instead of launched
+  {
+    static std::atomic<int> regs[2] = {{0}, {0}};   // per head dim, once known
+    std::atomic<int>& known = regs[head_dim == 128 ? 1 : 0];
+    int n = known.load(std::memory_order_relaxed);
+    if (n == 0) {
+      cudaFuncAttributes fa{};
+      const cudaError_t ea = head_dim == 128 ? cudaFuncGetAttributes(&fa, attention_kernel<128>)
+                                             : cudaFuncGetAttributes(&fa, attention_kernel<64>);
+      if (ea != cudaSuccess) return ea;
+      n = fa.numRegs;
+      known.store(n, std::memory_order_relaxed);
+    }
+    if (n < kChunkLaunchRegs) return cudaErrorInvalidConfiguration;
+  }
   cudaError_t e;
   if (head_dim == 128) {
     e = cudaFuncSetAttribute(attention_kernel<128>,

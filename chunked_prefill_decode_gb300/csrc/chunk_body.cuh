@@ -72,6 +72,9 @@ constexpr int kProducerThreads = 32 * kProducerWarps;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr int kSoftmaxRegs = 176;   // per thread, softmax warpgroups (warps 0-7)
 constexpr int kLightRegs = 152;     // per thread, MMA + producer warpgroup (8-11)
+constexpr int kChunkLaunchRegs = 168;   // per thread at launch: 65536 / 384, rounded down
+static_assert(256 * kSoftmaxRegs + 128 * kLightRegs <= 384 * kChunkLaunchRegs,
+              "register split exceeds the launch allocation");
 
 template <int D>
 struct ChunkCfg {
