@@ -161,7 +161,7 @@ __device__ __forceinline__ void chunk_cta(const ChunkParams& p, const CUtensorMa
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&s_full[t], 1);
-      mbar_init(&p_full[t], inter ? 2 * kChunkRows : kChunkRows);   // softmax threads per S tile
+      mbar_init(&p_full[t], inter ? 8 : 4);   // softmax warps per S tile
       mbar_init(&o_done[t], 1);
     }
     mbar_init(mma_done, 1);
@@ -309,15 +309,16 @@ __device__ __forceinline__ void chunk_cta(const ChunkParams& p, const CUtensorMa
                          sdesc_sw128(vb + kk * 2048, 16384, 1024), idesc_pv,
                          (!first || kk > 0) ? 1u : 0u);
       };
+      // K and V arrive by TMA (async proxy, made visible by the barrier's
+      // transaction count); the V rows the softmax zeroes by generic stores
+      // are fenced to the async proxy by their writers before p_full
       auto wait_k = [&](int j) -> bool {
         if (!mbar_wait(&k_full[j % NK], (uint32_t)(j / NK) & 1u, abort_flag)) return false;
-        fence_async_shared();   // gathered K (generic proxy) -> tensor core
         tc_fence_after_sync();
         return true;
       };
       auto wait_v = [&](int j) -> bool {
         if (!mbar_wait(&v_full[j % NV], (uint32_t)(j / NV) & 1u, abort_flag)) return false;
-        fence_async_shared();
         tc_fence_after_sync();
         return true;
       };
@@ -514,7 +515,10 @@ __device__ __forceinline__ void chunk_cta(const ChunkParams& p, const CUtensorMa
       }
       tmem_st_wait();
       tc_fence_before_sync();
-      mbar_arrive(&p_full[t]);
+      // one arrival per warp: the barrier completes after 4 (pair) or 8
+      // (interleaved) arrivals instead of one per thread
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&p_full[t]);
     }
     // epilogue: O / l -> bf16
     if (__all_sync(0xffffffffu, n_t > 0 && ok && mbar_wait(&o_done[t], 0u, abort_flag))) {
@@ -697,7 +701,10 @@ __device__ __forceinline__ void chunk_cta(const ChunkParams& p, const CUtensorMa
       }
       tmem_st_wait();
       tc_fence_before_sync();
-      mbar_arrive(&p_full[t]);
+      // one arrival per warp: the barrier completes after 4 (pair) or 8
+      // (interleaved) arrivals instead of one per thread
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&p_full[t]);
     }
     // ---- epilogue: every MMA is complete once both slots' last PV is (slot
     // 1 is empty with one key tile)
