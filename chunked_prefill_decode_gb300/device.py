@@ -50,3 +50,56 @@ def from_layout(layout, device="cuda") -> DeviceBatch:
                         layout.num_pages, sh.num_q_heads, sh.num_kv_heads,
                         sh.head_dim, sh.page_size, device,
                         sliding_window=sh.sliding_window)
+
+
+class StepStaging:
+    """One step's inputs (q, k_new, v_new and the batch descriptors) and its
+    output, each laid out back to back in one pinned host buffer and one
+    device buffer, so that a step crosses the host link with one copy each
+    way.  Fill the host views (h_q, h_k_new, h_v_new, h_cu_q_len,
+    h_context_len, h_block_table), call upload(stream), run the step on the
+    device views (q, k_new, v_new, out and the hb_batch `batch`), then
+    download(stream) into h_out.  Two instances let one step's copies
+    overlap the neighbouring steps' kernels."""
+
+    _ALIGN = 256
+
+    def __init__(self, num_seqs, total_q, max_pages_per_seq, num_pages, num_q_heads,
+                 num_kv_heads, head_dim, page_size=16, sliding_window=0, device="cuda"):
+        a = self._ALIGN
+        up = lambda n: (n + a - 1) // a * a
+        parts = [("q", (total_q, num_q_heads, head_dim), torch.bfloat16),
+                 ("k_new", (total_q, num_kv_heads, head_dim), torch.bfloat16),
+                 ("v_new", (total_q, num_kv_heads, head_dim), torch.bfloat16),
+                 ("cu_q_len", (num_seqs + 1,), torch.int32),
+                 ("context_len", (num_seqs,), torch.int32),
+                 ("block_table", (num_seqs, max_pages_per_seq), torch.int32)]
+        offs, off = [], 0
+        for name, shape, dt in parts:
+            n = int(np.prod(shape)) * torch.tensor([], dtype=dt).element_size()
+            offs.append((name, shape, dt, off, n))
+            off = up(off + n)
+        self.in_bytes = off
+        self.host = torch.empty(off, dtype=torch.uint8).pin_memory()
+        self.dev = torch.empty(off, dtype=torch.uint8, device=device)
+
+        def view(buf, o, n, shape, dt):
+            return buf[o:o + n].view(dt).view(shape)
+        for name, shape, dt, o, n in offs:
+            setattr(self, "h_" + name, view(self.host, o, n, shape, dt))
+            setattr(self, name, view(self.dev, o, n, shape, dt))
+        self.out = torch.empty(total_q, num_q_heads, head_dim, dtype=torch.bfloat16, device=device)
+        self.h_out = torch.empty(self.out.shape, dtype=torch.bfloat16).pin_memory()
+        self.out_bytes = self.out.numel() * 2
+        self.batch = hb.make_batch(num_seqs, total_q, max(1, max_pages_per_seq), num_pages,
+                                   num_q_heads, num_kv_heads, head_dim, self.cu_q_len,
+                                   self.context_len, self.block_table, page_size=page_size,
+                                   sliding_window=sliding_window)
+
+    def upload(self, stream=None):
+        with torch.cuda.stream(stream or torch.cuda.current_stream()):
+            self.dev.copy_(self.host, non_blocking=True)
+
+    def download(self, stream=None):
+        with torch.cuda.stream(stream or torch.cuda.current_stream()):
+            self.h_out.copy_(self.out, non_blocking=True)

@@ -274,3 +274,39 @@ def test_wait_timeout_is_reported_and_context_survives():
     assert e.value.status == 7
     hb.hb_check()                      # the word was cleared
     _full_check(workloads.tiny(0))     # the context still works
+
+
+def test_staged_step_through_host_buffers():
+    """The packed host staging (one copy in, one out, on side streams) gives
+    the same output as the device-resident step, and matches the oracle."""
+    from chunked_prefill_decode_gb300.device import StepStaging
+    hb = lib()
+    lay = layout_from_rows(Shape(32, 8, 128), [(1, 700), (40, 300), (1, 33), (17, 17)], 21)
+    ten = workloads.make_tensors(lay, 21)
+    sh = lay.shape
+    dev = torch.device("cuda:0")
+    kc0, vc0, ref_out = gpu_step(lay, ten)
+    kc, vc = ten.k_cache.to(dev).clone(), ten.v_cache.to(dev).clone()
+    stg = StepStaging(lay.num_seqs, lay.total_q, lay.block_table.shape[1], lay.num_pages,
+                      sh.num_q_heads, sh.num_kv_heads, sh.head_dim, device=dev)
+    stg.h_q.copy_(ten.q)
+    stg.h_k_new.copy_(ten.k_new)
+    stg.h_v_new.copy_(ten.v_new)
+    stg.h_cu_q_len.copy_(torch.from_numpy(lay.cu_q_len))
+    stg.h_context_len.copy_(torch.from_numpy(lay.context_len))
+    stg.h_block_table.copy_(torch.from_numpy(np.ascontiguousarray(lay.block_table)))
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    main = torch.cuda.current_stream(dev)
+    stg.upload(s_in)
+    main.wait_stream(s_in)
+    plan, ws = hb.hb_plan(stg.batch, lay.q_len, lay.context_len, sms())
+    hb.hb_kv_append(stg.batch, stg.k_new, stg.v_new, kc, vc)
+    hb.hb_attention(stg.batch, plan, stg.q, kc, vc, 1.0 / math.sqrt(sh.head_dim), stg.out, ws)
+    s_out.wait_stream(main)
+    stg.download(s_out)
+    s_out.synchronize()
+    hb.hb_check()
+    assert torch.equal(stg.h_out.view(torch.int16), ref_out.cpu().view(torch.int16))
+    assert torch.equal(kc.view(torch.int16), kc0.view(torch.int16))
+    _, _, ref = oracle_step(lay, ten)
+    compare(stg.h_out, ref)
