@@ -44,7 +44,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                      const __grid_constant__ CUtensorMap chunk_k,
                      const __grid_constant__ CUtensorMap chunk_v) {
   extern __shared__ uint8_t smem_raw[];
-  griddep_wait();
+  // the next kernel may be scheduled now (it waits for this one to finish);
+  // this kernel waits for the previous one only before reading pages that
+  // hold new tokens (decode_body.cuh, chunk_body.cuh producers)
   griddep_launch_dependents();
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);

@@ -221,8 +221,16 @@ __device__ __forceinline__ void chunk_cta(const ChunkParams& p, const CUtensorMa
     const int c_l = lane % CH;
     const bool issuer = lane < my_pages * CH;
     uint32_t issued = 0, par = 0;   // bit s: stage s (K in 0..NK-1, V from NK)
+    // key tiles that hold the chunk's own tokens (from position off on,
+    // written by the append before this launch) are read after griddep_wait
+    bool dep_done = false;
     auto tma_tile = [&](const CUtensorMap* map, uint8_t* stage, uint64_t* full, int batch_reg,
                         int jt, int bit, uint32_t ph) {
+      if (!dep_done && (jb + jt) * kChunkKeys + kChunkKeys - 1 >= off) {
+        griddep_wait();
+        fence_proxy_async_global();
+        dep_done = true;
+      }
       const int raw = __shfl_sync(0xffffffffu, batch_reg,
                                   ((jt % kTilesPerBatch) * kPagesPerTile + (pp_l & 7)) & 31);
       if (lane == 0) mbar_arrive_expect_tx(full, (uint32_t)(my_pages * CH * 2048));

@@ -142,6 +142,7 @@ __device__ __forceinline__ void decode_cta(const DecodeParams& p, const DecodeLa
     int qslot = 0;
     uint32_t qph[2] = {0u, 0u};
     uint32_t issued_mask = 0, last_par_mask = 0;
+    bool dep_done = false;   // griddep_wait done (before the first page with a new token)
     const uint32_t page_tx = 2u * (uint32_t)L.half_bytes;
     const uint32_t qbytes = (uint32_t)(kvhb * g * D * 2);
     // lane l: block-table entry of page base + l of item x, unchecked -- it is
@@ -221,6 +222,13 @@ __device__ __forceinline__ void decode_cta(const DecodeParams& p, const DecodeLa
             h.flags = (lp == it.page_begin ? kHdrFirst : 0) |
                       (lp == it.page_end - 1 ? kHdrLast : 0);
             h.qslot = qslot;
+            // a decode row's new token (position ctx - 1, written by the
+            // append before this launch) is on its last page
+            if (!dep_done && lp >= (it.ctx - 1) / kPageSize) {
+              griddep_wait();
+              fence_proxy_async_global();
+              dep_done = true;
+            }
             mbar_arrive_expect_tx(&full[st], page_tx);
             uint8_t* kd = stages + st * L.stage_bytes;
 #pragma unroll

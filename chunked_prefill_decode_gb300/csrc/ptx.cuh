@@ -23,17 +23,25 @@ constexpr uint64_t HB_WAIT_NS = 1000ull * 1000ull * 1000ull;  // 1 s
 // ---------------------------------------------------------------- launches
 // Programmatic dependent launch.  Every kernel of the library is launched
 // with programmatic stream serialization: its CTAs may become resident while
-// the previous kernel on the stream is still running, and each kernel's
-// first act, before it touches global memory, is griddep_wait(), which
-// returns once that kernel has completed and its writes are visible.  So
-// the ordering of the stream is unchanged; only the launch latency between
-// two kernels is hidden.  A kernel lets the next one be scheduled with
-// griddep_launch_dependents() (which the next one still waits behind).
+// the previous kernel on the stream is still running, and griddep_wait()
+// returns once that kernel has completed and its writes are visible.  The
+// append and linear kernels wait first thing, before they touch global
+// memory, and only then let the next kernel be scheduled
+// (griddep_launch_dependents), so everything before them on the stream is
+// complete once they run.  The attention kernel reads the cache pages the
+// append before it writes (those holding the batch's new tokens) only after
+// its own griddep_wait, and everything else (q, older pages, the plan)
+// without waiting: it overlaps the append.
 __device__ __forceinline__ void griddep_wait() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 __device__ __forceinline__ void griddep_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// After griddep_wait, before TMA (async proxy) reads of global memory that
+// the previous kernel wrote with ordinary stores.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
 template <typename... Params, typename... Args>
