@@ -329,7 +329,7 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
-TIMING_EVERY = 8   # steps per step with per-kernel CUDA events
+TIMING_EVERY = 16   # timed steps per step with per-kernel CUDA events
 
 
 def run_native(args):
