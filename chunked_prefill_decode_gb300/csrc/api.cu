@@ -13,6 +13,7 @@
 #include <cstring>
 #include <functional>
 #include <mutex>
+#include <unordered_map>
 #include <queue>
 #include <string>
 #include <vector>
@@ -36,7 +37,7 @@ cudaError_t launch_attention(const DecodeParams& dec, int decode_grid, const Chu
                              int head_dim, const CUtensorMap& dec_k, const CUtensorMap& dec_v,
                              const CUtensorMap& chunk_q, const CUtensorMap& chunk_k,
                              const CUtensorMap& chunk_v, const void* k_cache,
-                             const void* v_cache, cudaStream_t stream);
+                             const void* v_cache, cudaStream_t stream, bool early);
 }  // namespace hb
 
 using namespace hb;
@@ -247,6 +248,39 @@ hb_status internal_decode_maps(const hb_batch* b, int kvhb, const void* k_cache,
 
 void internal_count_launch() { g_launches.fetch_add(1); }
 
+// ---------------------------------------------------------------- launch order
+// The library's last launch on each stream.  The attention kernel may read
+// the cache pages that hold none of its batch's new tokens before the grid
+// before it has finished (it waits only before the pages with new tokens)
+// when that grid is hb_kv_append of the same batch: that append writes only
+// those tokens.  After any other launch of this library it waits first.
+// Work of other libraries between the two is launched without programmatic
+// serialization, so it starts only after the append has finished and does
+// not release the attention early: a stale record is safe.
+namespace {
+enum LaunchKind { kOtherLaunch = 0, kAppendLaunch = 1 };
+struct LastLaunch {
+  int kind = kOtherLaunch;
+  const void *cu = nullptr, *ctx = nullptr, *bt = nullptr, *kc = nullptr, *vc = nullptr;
+};
+std::mutex g_last_mu;
+std::unordered_map<void*, LastLaunch> g_last;
+void note_launch(void* stream, const LastLaunch& l) {
+  std::lock_guard<std::mutex> lk(g_last_mu);
+  g_last[stream] = l;
+}
+bool follows_own_append(void* stream, const hb_batch* b, const void* kc, const void* vc) {
+  std::lock_guard<std::mutex> lk(g_last_mu);
+  auto it = g_last.find(stream);
+  if (it == g_last.end()) return false;
+  const LastLaunch& l = it->second;
+  return l.kind == kAppendLaunch && l.cu == b->cu_q_len && l.ctx == b->context_len &&
+         l.bt == b->block_table && l.kc == kc && l.vc == vc;
+}
+}  // namespace
+
+void internal_note_other_launch(void* stream) { note_launch(stream, LastLaunch{}); }
+
 }  // namespace hb
 
 // =========================================================================
@@ -300,6 +334,14 @@ hb_status hb_kv_append(const hb_batch* batch, const void* k_new, const void* v_n
     cudaError_t e = launch_kv_append(p, dev->num_sms, st);
     t.done();
     if (e != cudaSuccess) return cuda_fail(e, "kv_append launch");
+    LastLaunch rec;
+    rec.kind = kAppendLaunch;
+    rec.cu = batch->cu_q_len;
+    rec.ctx = batch->context_len;
+    rec.bt = batch->block_table;
+    rec.kc = k_cache;
+    rec.vc = v_cache;
+    note_launch(stream, rec);
     g_launches.fetch_add(1);
     return ok();
   } catch (...) {
@@ -384,6 +426,7 @@ hb_status hb_linear(const void* x, const void* w, int32_t M, int32_t N, int32_t 
     cudaError_t e = launch_linear(p, xmap, wmap, bn, dev->num_sms, st);
     t.done();
     if (e != cudaSuccess) return cuda_fail(e, "linear launch");
+    note_launch(stream, LastLaunch{});
     g_launches.fetch_add(1);
     return ok();
   } catch (...) {
@@ -817,11 +860,13 @@ hb_status hb_attention(const hb_batch* batch, const void* h_plan, const void* q,
       cp.part_ml = reinterpret_cast<float*>(ws + h.ws_chunk_ml);
     }
     if (h.num_decode_items > 0 || h.num_chunk_items > 0) {
+      const bool early = follows_own_append(stream, batch, k_cache, v_cache);
       LaunchTimer t(1, st);
       cudaError_t e = launch_attention(dp, h.decode_grid, cp, D, dec_k, dec_v, chunk_q, chunk_k,
-                                       chunk_v, k_cache, v_cache, st);
+                                       chunk_v, k_cache, v_cache, st, early);
       t.done();
       if (e != cudaSuccess) return cuda_fail(e, "attention launch");
+      note_launch(stream, LastLaunch{});
       g_launches.fetch_add(1);
     }
     return ok();

@@ -34,6 +34,9 @@ struct AttnParams {
   const uint16_t* k_cache;
   const uint16_t* v_cache;
   int32_t decode_grid;
+  // 1: the grid before this one is the append of this batch, which writes
+  // only the pages with new tokens -- read every other page before it ends
+  int32_t early;
 };
 
 template <int D>
@@ -44,9 +47,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                      const __grid_constant__ CUtensorMap chunk_k,
                      const __grid_constant__ CUtensorMap chunk_v) {
   extern __shared__ uint8_t smem_raw[];
-  // the next kernel may be scheduled now (it waits for this one to finish);
-  // this kernel waits for the previous one only before reading pages that
-  // hold new tokens (decode_body.cuh, chunk_body.cuh producers)
+  // the next kernel may be scheduled now (it waits for this one to finish).
+  // After the append of this batch the previous grid is waited for only
+  // before the pages that hold new tokens (decode_body.cuh, chunk_body.cuh
+  // producers); after anything else, first.
+  if (!p.early) griddep_wait();
   griddep_launch_dependents();
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
@@ -70,8 +75,9 @@ cudaError_t launch_attention(const DecodeParams& dec, int decode_grid, const Chu
                              int head_dim, const CUtensorMap& dec_k, const CUtensorMap& dec_v,
                              const CUtensorMap& chunk_q, const CUtensorMap& chunk_k,
                              const CUtensorMap& chunk_v, const void* k_cache,
-                             const void* v_cache, cudaStream_t stream) {
+                             const void* v_cache, cudaStream_t stream, bool early) {
   AttnParams p{};
+  p.early = early ? 1 : 0;
   p.dec = dec;
   p.chk = chk;
   p.decode_grid = dec.num_items > 0 ? decode_grid : 0;

@@ -33,7 +33,7 @@ cudaError_t launch_attention(const DecodeParams& dec, int decode_grid, const Chu
                              int head_dim, const CUtensorMap& dec_k, const CUtensorMap& dec_v,
                              const CUtensorMap& chunk_q, const CUtensorMap& chunk_k,
                              const CUtensorMap& chunk_v, const void* k_cache,
-                             const void* v_cache, cudaStream_t stream);
+                             const void* v_cache, cudaStream_t stream, bool early);
 hb_status internal_fail(hb_status s, const char* msg);
 hb_status internal_ok();
 hb_status internal_check_batch(const hb_batch* b);
@@ -41,6 +41,7 @@ hb_status internal_device(int** err, int* num_sms);
 hb_status internal_decode_maps(const hb_batch* b, int kvhb, const void* k_cache,
                                const void* v_cache, CUtensorMap* kmap, CUtensorMap* vmap);
 void internal_count_launch();
+void internal_note_other_launch(void* stream);
 }  // namespace hb
 
 using namespace hb;
@@ -179,8 +180,9 @@ extern "C" hb_status hb_decode_attention_noalloc(const hb_batch* batch, const in
     CUtensorMap unused;
     std::memset(&unused, 0, sizeof(unused));
     e = launch_attention(p, part.grid, none, D, kmap, vmap, unused, unused, unused, k_cache,
-                         v_cache, st);
+                         v_cache, st, /*early=*/false);
     if (e != cudaSuccess) return internal_fail(HB_ERR_CUDA, "decode launch failed");
+    internal_note_other_launch(stream);
     internal_count_launch();
     return internal_ok();
   } catch (...) {

@@ -35,12 +35,13 @@
  *    must be ordered before attention on the same stream.
  *  - The kernels are launched with programmatic stream serialization: a
  *    kernel of this library may start under the tail of the kernel before
- *    it and waits for that kernel before it depends on it.  hb_attention
- *    waits only before reading the cache pages that hold its batch's new
- *    tokens; pages without one are read at once.  So an hb_kv_append
- *    directly before it must write only that batch's new tokens (as the
- *    append of the same batch does); any other kernel or copy before it is
- *    complete before it starts (they do not release it early).
+ *    it and waits for that kernel before it depends on it.  When the
+ *    library's previous launch on the stream is hb_kv_append of the same
+ *    batch (same descriptors and pools), hb_attention waits for it only
+ *    before reading the cache pages that hold the batch's new tokens and
+ *    reads every other page at once; after anything else it waits first.
+ *    Work of other libraries is complete before a kernel of this library
+ *    starts (it does not release it early).
  *
  * Data layout (bf16 = IEEE bfloat16 stored as uint16)
  *  - q      [total_q, num_q_heads,  head_dim] bf16, rows in batch order

@@ -310,3 +310,52 @@ def test_staged_step_through_host_buffers():
     assert torch.equal(kc.view(torch.int16), kc0.view(torch.int16))
     _, _, ref = oracle_step(lay, ten)
     compare(stg.h_out, ref)
+
+
+def test_attention_right_after_the_kernel_that_writes_q():
+    """hb_attention launched directly after an hb_linear that writes its q (no
+    append in between) waits for that grid before it reads q; and directly
+    after the append of another batch it also waits first."""
+    from chunked_prefill_decode_gb300.device import device_batch
+    hb = lib()
+    lay = layout_from_rows(Shape(32, 8, 128), [(1, 3000)] * 6 + [(1, 700), (40, 300)], 25)
+    ten = workloads.make_tensors(lay, 25)
+    sh = lay.shape
+    dev = torch.device("cuda:0")
+    T = lay.total_q
+    db = device_batch(lay.q_len, lay.context_len, lay.block_table, lay.num_pages,
+                      sh.num_q_heads, sh.num_kv_heads, sh.head_dim, sh.page_size, dev)
+    kc, vc = ten.k_cache.to(dev).clone(), ten.v_cache.to(dev).clone()
+    hb.hb_kv_append(db.batch, ten.k_new.to(dev), ten.v_new.to(dev), kc, vc)
+    plan, ws = hb.hb_plan(db.batch, db.q_len, db.context_len, sms())
+    torch.cuda.synchronize()
+    g = torch.Generator().manual_seed(25)
+    H = sh.num_q_heads * sh.head_dim
+    x = torch.randn(T, 2048, generator=g).to(torch.bfloat16).to(dev)
+    w = (torch.randn(H, 2048, generator=g) / math.sqrt(2048)).to(torch.bfloat16).to(dev)
+    scale = 1.0 / math.sqrt(sh.head_dim)
+    for _ in range(3):
+        q = torch.full((T, H), float("nan"), dtype=torch.bfloat16, device=dev)
+        out = torch.full((T, sh.num_q_heads, sh.head_dim), float("nan"), dtype=torch.bfloat16,
+                         device=dev)
+        hb.hb_linear(x, w, [q])
+        hb.hb_attention(db.batch, plan, q.view(T, sh.num_q_heads, sh.head_dim), kc, vc, scale,
+                        out, ws)
+        torch.cuda.synchronize()
+        hb.hb_check()
+        t2 = workloads.BatchTensors(q.view(T, sh.num_q_heads, sh.head_dim).cpu(), ten.k_new,
+                                    ten.v_new, ten.k_cache, ten.v_cache)
+        _, _, ref = oracle_step(lay, t2)
+        compare(out, ref)
+    # an append of another batch (a copy of the descriptors) right before:
+    # the attention of this batch does not take it for its own
+    db2 = device_batch(lay.q_len, lay.context_len, lay.block_table, lay.num_pages,
+                       sh.num_q_heads, sh.num_kv_heads, sh.head_dim, sh.page_size, dev)
+    q = ten.q.to(dev)
+    out = torch.full_like(q, float("nan"))
+    hb.hb_kv_append(db2.batch, ten.k_new.to(dev), ten.v_new.to(dev), kc, vc)
+    hb.hb_attention(db.batch, plan, q, kc, vc, scale, out, ws)
+    torch.cuda.synchronize()
+    hb.hb_check()
+    _, _, ref = oracle_step(lay, ten)
+    compare(out, ref)
