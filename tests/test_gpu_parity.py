@@ -359,3 +359,40 @@ def test_attention_right_after_the_kernel_that_writes_q():
     hb.hb_check()
     _, _, ref = oracle_step(lay, ten)
     compare(out, ref)
+
+
+def test_step_captured_in_a_cuda_graph():
+    """Append + attention captured once in a CUDA graph (torch.cuda.graph) and
+    replayed: the same output as the direct launches, replay after replay."""
+    from chunked_prefill_decode_gb300.device import device_batch
+    hb = lib()
+    lay = layout_from_rows(Shape(32, 8, 128), [(1, 3000)] * 6 + [(1, 700), (40, 300)], 31)
+    ten = workloads.make_tensors(lay, 31)
+    sh = lay.shape
+    dev = torch.device("cuda:0")
+    db = device_batch(lay.q_len, lay.context_len, lay.block_table, lay.num_pages,
+                      sh.num_q_heads, sh.num_kv_heads, sh.head_dim, sh.page_size, dev)
+    q, kn, vn = (t.to(dev) for t in (ten.q, ten.k_new, ten.v_new))
+    kc, vc = ten.k_cache.to(dev).clone(), ten.v_cache.to(dev).clone()
+    plan, ws = hb.hb_plan(db.batch, db.q_len, db.context_len, sms())
+    scale = 1.0 / math.sqrt(sh.head_dim)
+    out_direct = torch.full_like(q, float("nan"))
+    hb.hb_kv_append(db.batch, kn, vn, kc, vc)
+    hb.hb_attention(db.batch, plan, q, kc, vc, scale, out_direct, ws)
+    torch.cuda.synchronize()
+    hb.hb_check()
+    out = torch.full_like(q, float("nan"))
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(torch.cuda.current_stream(dev))
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        hb.hb_kv_append(db.batch, kn, vn, kc, vc)
+        hb.hb_attention(db.batch, plan, q, kc, vc, scale, out, ws)
+    for _ in range(3):
+        out.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        hb.hb_check()
+        assert torch.equal(out.view(torch.int16), out_direct.view(torch.int16))
+    _, _, ref = oracle_step(lay, ten)
+    compare(out, ref)
