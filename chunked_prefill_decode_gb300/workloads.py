@@ -170,6 +170,13 @@ def yi_b2048(seed: int = 2, offset: int = 6048) -> BatchLayout:
     return layout_from_rows(shape, rows, seed)
 
 
+def yi_b2048_o5043(seed: int = 2) -> BatchLayout:
+    """The Yi-34B batch with its 2016-token chunk at offset 5043: the last
+    full chunk of a 7059-token prompt (the configuration's prompt length),
+    where the default takes the chunk index 3 reading of "offset ~6000"."""
+    return yi_b2048(seed, offset=5043)
+
+
 def decode_only(seed: int = 3) -> BatchLayout:
     """32 q / 8 kv heads, head_dim 128: 256 decode rows, context U[1024, 8192]."""
     rng = np.random.default_rng(seed)
@@ -201,6 +208,7 @@ WORKLOADS = {
     "mistral_b512": mistral_b512,
     "mistral_b512_window": mistral_b512_window,
     "yi_b2048": yi_b2048,
+    "yi_b2048_o5043": yi_b2048_o5043,
     "decode_only": decode_only,
 }
 

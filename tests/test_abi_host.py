@@ -221,7 +221,7 @@ def _check_plan(rows, hq, hkv, d, sms, window=0):
     return h
 
 
-@pytest.mark.parametrize("name", ["tiny", "mistral_b512", "mistral_b512_window", "yi_b2048",
+@pytest.mark.parametrize("name", ["tiny", "mistral_b512", "mistral_b512_window", "yi_b2048", "yi_b2048_o5043",
                                   "decode_only"])
 def test_plan_covers_workloads(name):
     from chunked_prefill_decode_gb300 import workloads

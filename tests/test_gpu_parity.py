@@ -207,7 +207,7 @@ def test_timing_and_launch_count():
 def _full_size(name, n_seq_sample=6, n_chunk_tok=48, seed=None, lay=None):
     if lay is None:
         lay = workloads.WORKLOADS[name]()
-    seed = {"mistral_b512": 1, "mistral_b512_window": 1, "yi_b2048": 2,
+    seed = {"mistral_b512": 1, "mistral_b512_window": 1, "yi_b2048": 2, "yi_b2048_o5043": 2,
             "decode_only": 3}.get(name, 0) if seed is None else seed
     ten = workloads.make_tensors(lay, seed, device="cuda")
     kc, vc, out = gpu_step(lay, ten)
@@ -249,7 +249,8 @@ def _full_size(name, n_seq_sample=6, n_chunk_tok=48, seed=None, lay=None):
 
 
 @pytest.mark.slow
-@pytest.mark.parametrize("name", ["mistral_b512", "mistral_b512_window", "yi_b2048", "decode_only"])
+@pytest.mark.parametrize("name", ["mistral_b512", "mistral_b512_window", "yi_b2048", "yi_b2048_o5043",
+                                  "decode_only"])
 def test_full_size_workloads(name):
     _full_size(name)
 
