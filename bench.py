@@ -520,6 +520,66 @@ def run_native(args):
 SWEEP_CHUNKS = (256, 257, 512, 1024, 2048, 8192)
 
 
+def run_seed_sweep(args):
+    """The workload's batch drawn with seeds 0..4 (lengths, page permutation
+    and tensor contents): tokens/s and the attention launch's roofline
+    fraction per seed (append + attention back to back, inputs larger than
+    L2), one JSON line per seed and a summary line."""
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    import __graft_entry__
+    __graft_entry__.build()
+    from chunked_prefill_decode_gb300 import hb
+    from chunked_prefill_decode_gb300.device import device_batch
+
+    peaks = _peaks()
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    stream = torch.cuda.current_stream(dev)
+    steps = max(10, min(args.steps, 500))
+    rows = []
+    with ClockSampler(0) as clk:
+        for seed in range(5):
+            lay = workloads.WORKLOADS[args.workload](seed)
+            sh = lay.shape
+            ten = workloads.make_tensors(lay, seed=seed, device=dev)
+            db = device_batch(lay.q_len, lay.context_len, lay.block_table, lay.num_pages,
+                              sh.num_q_heads, sh.num_kv_heads, sh.head_dim, sh.page_size, dev,
+                              sliding_window=sh.sliding_window)
+            plan, ws = hb.hb_plan(db.batch, db.q_len, db.context_len, sms)
+            out = torch.empty_like(ten.q)
+            scale = 1.0 / math.sqrt(sh.head_dim)
+
+            def step():
+                hb.hb_kv_append(db.batch, ten.k_new, ten.v_new, ten.k_cache, ten.v_cache)
+                hb.hb_attention(db.batch, plan, ten.q, ten.k_cache, ten.v_cache, scale, out, ws)
+            for _ in range(max(args.warmup, 3)):
+                step()
+            torch.cuda.synchronize(dev)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(steps):
+                step()
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            hb.hb_check()
+            ms = e0.elapsed_time(e1) / steps
+            cnt = algorithmic_counts(lay)
+            step_roof = max(cnt["flops"] / (peaks["bf16_tflops"] * 1e12),
+                            cnt["bytes"] / (peaks["hbm_gbs"] * 1e9)) * 1e3
+            r = {"sweep": "seed", "workload": args.workload, "seed": seed,
+                 "tokens_per_step": lay.total_q, "ms_per_step": ms,
+                 "tokens_per_s": lay.total_q / (ms * 1e-3), "step_roofline_frac": step_roof / ms,
+                 "kv_bytes": cnt["bytes"], "flops": cnt["flops"]}
+            rows.append(r)
+            print(json.dumps(r), flush=True)
+    v = [r["tokens_per_s"] for r in rows]
+    f = [r["step_roofline_frac"] for r in rows]
+    print(json.dumps({"sweep": "seed", "workload": args.workload, "seeds": 5, "steps": steps,
+                      "tokens_per_s": {"mean": statistics.mean(v), "min": min(v), "max": max(v)},
+                      "step_roofline_frac": {"mean": statistics.mean(f), "min": min(f), "max": max(f)},
+                      "clocks": clk.summary()}), flush=True)
+
+
 def run_chunk_sweep(args):
     """Prefill of one 8192-token prompt in chunks of c tokens, each chunk in a
     hybrid batch with 32 decode rows at context 2048, and the same chunks
@@ -668,9 +728,10 @@ def main():
     ap.add_argument("--workload", default="mistral_b512", choices=sorted(workloads.WORKLOADS))
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
-    ap.add_argument("--sweep", choices=["chunk"], default=None,
-                    help="instead of the step benchmark: prefill one 8192-token prompt "
-                         "in chunks of 256/257/512/1024/2048/8192 tokens")
+    ap.add_argument("--sweep", choices=["chunk", "seed"], default=None,
+                    help="instead of the step benchmark: 'chunk' prefills one 8192-token "
+                         "prompt in chunks of 256/257/512/1024/2048/8192 tokens; 'seed' draws "
+                         "the workload's batch with seeds 0..4")
     ap.add_argument("--sweep-reps", type=int, default=10)
     ap.add_argument("--layer", action="store_true",
                     help="instead of the attention step: one transformer block of the "
@@ -682,6 +743,8 @@ def main():
         return
     if args.sweep == "chunk":
         run_chunk_sweep(args)
+    elif args.sweep == "seed":
+        run_seed_sweep(args)
     elif args.layer:
         run_layer(args)
     elif args.impl == "reference":
