@@ -384,10 +384,13 @@ __device__ __forceinline__ void decode_cta(const DecodeParams& p, const DecodeLa
             __syncwarp();
           }
           // S^T = K Q^T: every K fragment is loaded before the first MMA, and
-          // even / odd head-dim steps accumulate apart (two short chains)
-          float s[2][NQ][4];
+          // head-dim steps accumulate in separate sets (short chains)
+          // kQk independent accumulator sets (head-dim steps kk % kQk) keep
+          // the MMA chains short
+          constexpr int kQk = NQ == 1 ? 4 : 2;
+          float s[kQk][NQ][4];
 #pragma unroll
-          for (int x = 0; x < 2; ++x)
+          for (int x = 0; x < kQk; ++x)
 #pragma unroll
             for (int nq = 0; nq < NQ; ++nq) s[x][nq][0] = s[x][nq][1] = s[x][nq][2] = s[x][nq][3] = 0.f;
           {
@@ -406,7 +409,7 @@ __device__ __forceinline__ void decode_cta(const DecodeParams& p, const DecodeLa
             for (int kk = 0; kk < D / 16; ++kk)
 #pragma unroll
               for (int nq = 0; nq < NQ; ++nq)
-                mma_bf16_16816(s[kk & 1][nq], ka[kk], qb[kk][nq][0], qb[kk][nq][1]);
+                mma_bf16_16816(s[kk % kQk][nq], ka[kk], qb[kk][nq][0], qb[kk][nq][1]);
           }
           // V^T fragments, loaded while the softmax runs; matrix mi: keys
           // 8 (mi >> 1) .., head dims 8 (mi & 1) .. of the 16-dim block
@@ -439,8 +442,14 @@ __device__ __forceinline__ void decode_cta(const DecodeParams& p, const DecodeLa
           for (int nq = 0; nq < NQ; ++nq)
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
-              x0[nq][e] = ok0 ? (s[0][nq][e] + s[1][nq][e]) * p.scale_log2 : -INFINITY;
-              x1[nq][e] = ok1 ? (s[0][nq][2 + e] + s[1][nq][2 + e]) * p.scale_log2 : -INFINITY;
+              float a0 = s[0][nq][e], a1 = s[0][nq][2 + e];
+#pragma unroll
+              for (int x = 1; x < kQk; ++x) {
+                a0 += s[x][nq][e];
+                a1 += s[x][nq][2 + e];
+              }
+              x0[nq][e] = ok0 ? a0 * p.scale_log2 : -INFINITY;
+              x1[nq][e] = ok1 ? a1 * p.scale_log2 : -INFINITY;
               need |= fmaxf(x0[nq][e], x1[nq][e]) > m_run[nq][e] + kDecRescaleThreshold;
               alpha[nq][e] = 1.f;
             }
