@@ -338,3 +338,24 @@ def test_linear_workspace_size():
     # invalid shapes: 0
     assert L.hb_linear_workspace_size(4, 300, 64, 0, 152) == 0
     assert L.hb_linear_workspace_size(4, 256, 100, 0, 152) == 0
+
+
+@pytest.mark.parametrize("seed", range(32))
+def test_plan_invariants_on_random_batches(seed):
+    """Seeded random hybrid batches (mixes of decode rows and chunks of every
+    size, several head geometries, SM counts and windows): every plan tiles
+    each decode row's pages and each chunk's (token, kv head) pairs exactly
+    once, with consistent split-KV pieces (the same checks as above)."""
+    rng = np.random.default_rng(1000 + seed)
+    geoms = [(8, 8, 64), (32, 8, 128), (56, 8, 128), (16, 2, 64), (64, 16, 128), (16, 1, 128)]
+    hq, hkv, d = geoms[seed % len(geoms)]
+    n_dec = int(rng.integers(0, 40))
+    n_chk = int(rng.integers(0 if n_dec else 1, 4))
+    rows = [(1, int(rng.integers(1, 9000))) for _ in range(n_dec)]
+    for _ in range(n_chk):
+        q = int(rng.integers(2, 3000))
+        rows.append((q, q + int(rng.integers(0, 6000))))
+    rng.shuffle(rows)
+    sms = int(rng.choice([1, 7, 64, 148, 152]))
+    window = int(rng.choice([0, 0, 0, 1, 37, 1024]))
+    _check_plan([tuple(r) for r in rows], hq, hkv, d, sms, window=window)
