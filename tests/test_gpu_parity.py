@@ -397,3 +397,22 @@ def test_step_captured_in_a_cuda_graph():
         assert torch.equal(out.view(torch.int16), out_direct.view(torch.int16))
     _, _, ref = oracle_step(lay, ten)
     compare(out, ref)
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_random_hybrid_batches(seed):
+    """Seeded random hybrid batches (decode rows and chunks of any size, head
+    geometries, windows): append bit-exact and attention within the bounds,
+    every token checked against the oracle."""
+    rng = np.random.default_rng(2000 + seed)
+    geoms = [(8, 8, 64), (32, 8, 128), (56, 8, 128), (16, 2, 64), (64, 16, 128), (16, 1, 128),
+             (32, 32, 128), (8, 1, 64)]
+    hq, hkv, d = geoms[seed]
+    rows = [(1, int(rng.integers(1, 2500))) for _ in range(int(rng.integers(0, 12)))]
+    for _ in range(int(rng.integers(1, 3))):
+        q = int(rng.integers(2, 400))
+        rows.append((q, q + int(rng.integers(0, 1500))))
+    rng.shuffle(rows)
+    window = int(rng.choice([0, 0, 5, 300]))
+    _full_check(layout_from_rows(Shape(hq, hkv, d, sliding_window=window),
+                                 [tuple(r) for r in rows], 2000 + seed), seed=seed)
