@@ -418,12 +418,16 @@ def run_native(args):
     def e2e_step(i):
         stg = stages[i % 2]
         s_in.wait_event(stg.ev_done)        # step i - 2's kernels are done with these inputs
+        # the plan goes up on the upload stream, ahead of the inputs: a small
+        # copy from pageable memory may first wait for its stream, and this
+        # stream's earlier work is neither the step before's kernels nor
+        # this step's input copy
+        p, _ = hb.hb_plan(stg.batch, layout.q_len, layout.context_len, sms, workspace=stg.ws,
+                          plan=stg.plan, stream=s_in)
         stg.upload(s_in)
         stg.ev_in.record(s_in)
         stream.wait_event(stg.ev_in)
         stream.wait_event(stg.ev_out)       # step i - 2's output has left this buffer
-        p, _ = hb.hb_plan(stg.batch, layout.q_len, layout.context_len, sms, workspace=stg.ws,
-                          plan=stg.plan, stream=stream)
         hb.hb_kv_append(stg.batch, stg.k_new, stg.v_new, kc, vc, stream=stream)
         hb.hb_attention(stg.batch, p, stg.q, kc, vc, scale, stg.out, stg.ws, stream=stream)
         stg.ev_done.record(stream)

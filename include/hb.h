@@ -144,7 +144,11 @@ hb_status hb_kv_append(const hb_batch* batch, const void* k_new,
  * it is also copied into d_workspace and the workspace counters are cleared,
  * asynchronously on `stream` (only this step makes CUDA calls): h_plan must
  * stay unchanged until that copy has completed, and a workspace must not be
- * shared by attention calls in flight at once.
+ * shared by attention calls in flight at once.  From pageable memory the
+ * CUDA driver may wait for `stream` before it stages the copy: a caller
+ * whose host should run ahead of the kernels passes a stream without the
+ * previous step's kernels on it (for example its input-copy stream, ordered
+ * before the kernels by an event).
  * The plan stays valid for any later hb_attention on a batch with the same
  * q_len / context_len / head geometry (block tables and tensors may change).
  * Errors: HB_ERR_SHAPE for rows outside 1 <= q_len <= context_len, or
