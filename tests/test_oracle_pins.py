@@ -326,6 +326,23 @@ def test_pin_catches_transposed_page_index(monkeypatch):
     assert not np.allclose(out, ref)
 
 
+def test_pin_catches_merge_without_rescale(monkeypatch):
+    """A merge that adds the pieces' sums without bringing them to the common
+    maximum (exp(m_i - m)) breaks the split-softmax identity."""
+    def wrong_merge(states):
+        return sum(st[2] for st in states) / sum(st[1] for st in states)
+    monkeypatch.setattr(pa, "merge_partial_states", wrong_merge)
+    with pytest.raises(AssertionError):
+        test_split_softmax_merge_identity()
+
+
+def test_pin_catches_merge_that_drops_a_piece(monkeypatch):
+    real = pa.merge_partial_states
+    monkeypatch.setattr(pa, "merge_partial_states", lambda states: real(states[:-1]))
+    with pytest.raises(AssertionError):
+        test_split_softmax_merge_identity()
+
+
 # --------------------------------------------------------------- sliding window
 @pytest.mark.parametrize("seed,window", [(0, 1), (1, 3), (2, 5), (3, 9)])
 def test_windowed_oracle_matches_bruteforce(seed, window):
