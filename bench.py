@@ -66,23 +66,58 @@ ATTN_SOURCES = ("attention.cu", "decode_body.cuh", "chunk_body.cuh", "ptx.cuh",
                 "hb_internal.h", "decode_plan.h", "api.cu")
 
 
+def source_code_tokens(text):
+    """C/C++/CUDA source with its comments removed and every run of
+    whitespace made one space: what the compiler sees, so that a change to a
+    comment or to the layout of the text does not count as a change of the
+    kernel.  String and character literals are kept as they are."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c == "/" and i + 1 < n and text[i + 1] == "/":
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+            out.append(" ")
+        elif c == "/" and i + 1 < n and text[i + 1] == "*":
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        elif c in "\"'":
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
+def attention_sources_digest(root=None):
+    """First 16 hex digits of the sha256 over the attention launch's sources
+    (comments and layout ignored), as recorded in its ncu summaries."""
+    import hashlib
+    h = hashlib.sha256()
+    for src in ATTN_SOURCES:
+        with open(os.path.join(root or ROOT, "chunked_prefill_decode_gb300", "csrc", src)) as f:
+            h.update(source_code_tokens(f.read()).encode())
+        h.update(b"\0")
+    return h.hexdigest()[:16]
+
+
 def profiled_traffic(workload):
     """DRAM bytes per attention launch from the committed ncu summary of this
-    workload, if the summary was taken on the current kernel sources."""
-    import hashlib
+    workload, if the summary was taken on the current kernel code."""
     path = os.path.join(ROOT, "profiles", f"attention_{workload}.md")
     if not os.path.exists(path):
         return None
     fields = {}
     for line in open(path):
-        if ":" in line and line.split(":")[0] in ("traffic_bytes_per_launch", "sources_sha256"):
+        if ":" in line and line.split(":")[0] in ("traffic_bytes_per_launch", "code_sha256"):
             k, v = line.split(":", 1)
             fields[k.strip()] = v.strip()
-    h = hashlib.sha256()
-    for src in ATTN_SOURCES:
-        with open(os.path.join(ROOT, "chunked_prefill_decode_gb300", "csrc", src), "rb") as f:
-            h.update(f.read())
-    if fields.get("sources_sha256") != h.hexdigest()[:16]:
+    if fields.get("code_sha256") != attention_sources_digest():
         return None
     return int(fields["traffic_bytes_per_launch"])
 

@@ -1,7 +1,7 @@
 """bench.py's host-side accounting, without a GPU: the algorithmic bytes and
 FLOPs the roofline fractions divide by (counted here by hand from the
 definition of attention over a paged cache), the guard that drops a profiled
-DRAM traffic figure once the kernel sources differ from the profiled ones,
+DRAM traffic figure once the kernel code differs from the profiled code,
 and the JSON line of the reference arm (the fp64 oracle on the host)."""
 import json
 import os
@@ -64,20 +64,37 @@ def _copy_tree_for_profiles(dst):
                     os.path.join(dst, "chunked_prefill_decode_gb300", "csrc", src))
 
 
-def test_profiled_traffic_follows_the_sources(tmp_path, monkeypatch):
-    """A committed summary's traffic is used while the attention sources hash
-    to the value it records, and dropped (None) once any of them changes."""
+def test_profiled_traffic_follows_the_code(tmp_path, monkeypatch):
+    """A committed summary's traffic is used while the attention sources'
+    code (comments and layout aside) digests to the value it records, and
+    dropped (None) once the code of any of them changes."""
     dst = str(tmp_path / "repo")
     _copy_tree_for_profiles(dst)
     monkeypatch.setattr(bench, "ROOT", dst)
-    got = {w: bench.profiled_traffic(w) for w in ("mistral_b512", "yi_b2048", "decode_only")}
+    names = ("mistral_b512", "yi_b2048", "decode_only")
+    got = {w: bench.profiled_traffic(w) for w in names}
     for w, v in got.items():
         text = open(os.path.join(dst, "profiles", f"attention_{w}.md")).read()
-        assert f"traffic_bytes_per_launch: {v}" in text
+        assert v is not None and f"traffic_bytes_per_launch: {v}" in text
     assert bench.profiled_traffic("tiny") is None          # no summary for it
-    with open(os.path.join(dst, "chunked_prefill_decode_gb300", "csrc", "decode_plan.h"), "a") as f:
-        f.write("\n")
-    assert all(bench.profiled_traffic(w) is None for w in got)
+    plan_h = os.path.join(dst, "chunked_prefill_decode_gb300", "csrc", "decode_plan.h")
+    with open(plan_h, "a") as f:                           # comments and blank lines
+        f.write("\n// a note\n/* another\n   note */\n\n")
+    assert {w: bench.profiled_traffic(w) for w in names} == got
+    with open(plan_h, "a") as f:                           # code
+        f.write("static const int hb_unused_constant = 1;\n")
+    assert all(bench.profiled_traffic(w) is None for w in names)
+
+
+def test_source_code_tokens():
+    src = ('int a = 1;   // tail comment\n'
+           '/* block\n comment */ const char* s = "x // y /* z */";\n'
+           "char q = '\"'; char e = '\\''; int b;\n")
+    assert bench.source_code_tokens(src) == (
+        'int a = 1; const char* s = "x // y /* z */"; '
+        "char q = '\"'; char e = '\\''; int b;")
+    assert bench.source_code_tokens("a/*x*/b") == "a b"
+    assert bench.source_code_tokens("a  +\n\tb") == bench.source_code_tokens("a + b")
 
 
 def test_reference_arm_prints_the_contract_line():
