@@ -383,10 +383,9 @@ __device__ __forceinline__ void decode_cta(const DecodeParams& p, const DecodeLa
             fence_async_shared();
             __syncwarp();
           }
-          // S^T = K Q^T: every K fragment is loaded before the first MMA, and
-          // head-dim steps accumulate in separate sets (short chains)
-          // kQk independent accumulator sets (head-dim steps kk % kQk) keep
-          // the MMA chains short
+          // S^T = K Q^T: every K fragment is loaded before the first MMA;
+          // head-dim step kk accumulates into set kk % kQk, so kQk short
+          // MMA chains run side by side instead of one long one
           constexpr int kQk = NQ == 1 ? 4 : 2;
           float s[kQk][NQ][4];
 #pragma unroll
