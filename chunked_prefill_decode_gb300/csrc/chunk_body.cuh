@@ -49,10 +49,10 @@
 //              16-token pages, one TMA box per page and 64-column head-dim
 //              chunk (2 KB), coordinates from the block table (read a
 //              batch of four key tiles ahead); the lanes of the three warps
-//              issue the boxes side by side.  Pages past the context are fetched out
-//              of range (zeros); the unwritten tail slots of the last page
-//              are zeroed in V by the softmax group that reads that tile
-//              first.  K runs one tile ahead of V.
+//              issue the boxes side by side.  Pages past the context are
+//              fetched out of range (zeros); the unwritten tail slots of the
+//              last page are zeroed in V by the softmax group that reads that
+//              tile first.  K runs one tile ahead of V.
 // TMEM (512 columns): S_0 0-127, S_1 128-255, O_0 256-(256+D), O_1 after it.
 #pragma once
 

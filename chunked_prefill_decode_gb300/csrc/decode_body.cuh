@@ -28,8 +28,9 @@
 //    log2 e folded in);
 //  * a row that straddles ranges leaves one partial state (m, l,
 //    unnormalised o) per piece in the workspace; the last piece of a
-//    (row, kv block) to finish, found with an atomic counter, merges them: m = max m_i, l = sum 2^(m_i - m) l_i, o = sum 2^(m_i - m) o_i
-//    / l.  Nobody waits on another CTA.
+//    (row, kv block) to finish, found with an atomic counter, merges them:
+//    m = max m_i, l = sum 2^(m_i - m) l_i, o = sum 2^(m_i - m) o_i / l.
+//    Nobody waits on another CTA.
 //
 // Bytes per decode row: 2 * context * Hkv * D * 2 (K and V read once).
 #pragma once
