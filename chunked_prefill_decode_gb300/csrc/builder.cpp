@@ -131,8 +131,12 @@ hb_status hb_builder_step(hb_builder* b, int32_t max_rows, int32_t* num_rows, in
   if (b->pending) return berr(HB_ERR_INVALID_ARG, "complete the previous batch first");
   if (max_rows < 0) return berr(HB_ERR_INVALID_ARG, "max_rows < 0");
 
-  // Work on copies so that a failed step leaves the builder unchanged.
-  std::deque<int32_t> free_pages = b->free_pages;
+  // Pages are taken from the front of the free list as the batch is formed;
+  // a failed step puts them back (front, original order) and shortens the
+  // requests' page lists again, so it leaves the builder unchanged.  The
+  // cost of a step is that of its rows, not of the pool.
+  std::deque<int32_t>& free_pages = b->free_pages;
+  std::vector<int32_t> taken;                    // pages taken, in order
   std::unordered_map<Request*, size_t> grown;   // request -> page count before
   std::vector<Row> rows;
   int64_t tokens = 0;
@@ -142,12 +146,14 @@ hb_status hb_builder_step(hb_builder* b, int32_t max_rows, int32_t* num_rows, in
     if (need > 0 && !grown.count(r)) grown[r] = r->pages.size();
     for (int32_t i = 0; i < need; ++i) {
       r->pages.push_back(free_pages.front());
+      taken.push_back(free_pages.front());
       free_pages.pop_front();
     }
     return true;
   };
   auto rollback = [&]() {
     for (auto& kv : grown) kv.first->pages.resize(kv.second);
+    for (auto it = taken.rbegin(); it != taken.rend(); ++it) free_pages.push_front(*it);
   };
 
   // 1. running decodes
@@ -202,7 +208,6 @@ hb_status hb_builder_step(hb_builder* b, int32_t max_rows, int32_t* num_rows, in
     r->phase = kPrefill;
     b->running.push_back(r);
   }
-  b->free_pages.swap(free_pages);
   const int32_t mp = b->max_pages_per_seq;
   for (size_t i = 0; i < rows.size(); ++i) {
     const Row& w = rows[i];

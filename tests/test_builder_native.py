@@ -103,3 +103,85 @@ def test_native_builder_argument_errors():
         b.add_request(1, 5, 2)
     assert e.value.status == 1
     assert b.counts() == (1, 0, 10)
+
+
+def _raw_step(hb, b, max_rows):
+    import ctypes
+    mp = b.max_pages_per_seq
+    out = {"q_len": np.zeros(max(max_rows, 1), np.int32),
+           "context_len": np.zeros(max(max_rows, 1), np.int32),
+           "block_table": np.zeros((max(max_rows, 1), mp), np.int32),
+           "ids": np.zeros(max(max_rows, 1), np.int64),
+           "kind": np.zeros(max(max_rows, 1), np.int32)}
+    n, over = ctypes.c_int32(0), ctypes.c_int32(0)
+    st = hb.load().hb_builder_step(b._h, max_rows, ctypes.byref(n), hb._ptr(out["q_len"]),
+                                   hb._ptr(out["context_len"]), hb._ptr(out["block_table"]),
+                                   hb._ptr(out["ids"]), hb._ptr(out["kind"]), ctypes.byref(over))
+    return st, n.value
+
+
+def test_failed_step_leaves_the_builder_unchanged():
+    """A step refused for too few output rows puts back every page it took:
+    the free list, the counts and the next batch are those of a twin builder
+    that never failed."""
+    hb = lib()
+    order = np.random.default_rng(5).permutation(200)
+    a = hb.Builder(64, 16, 200, 16, page_order=order)
+    twin = hb.Builder(64, 16, 200, 16, page_order=order)
+    for b in (a, twin):
+        for rid in range(6):
+            b.add_request(rid, 10 + 7 * rid, 3)
+    for _ in range(2):                       # some decodes running, prefills ongoing
+        assert a.step() is not None and twin.step() is not None
+        assert a.complete() == twin.complete()
+    before = (a.free_list(), a.counts())
+    st, need = _raw_step(hb, a, 1)
+    assert st == 4 and need > 1              # HB_ERR_WORKSPACE, rows needed reported
+    assert (a.free_list(), a.counts()) == before
+    x, y = a.step(), twin.step()
+    for k in ("q_len", "context_len", "block_table", "ids", "kind"):
+        assert x[k].tolist() == y[k].tolist()
+    assert a.complete() == twin.complete()
+    assert a.free_list() == twin.free_list()
+
+
+def test_decode_out_of_pages_leaves_the_builder_unchanged():
+    hb = lib()
+    b = hb.Builder(8, 4, 3, 8)
+    b.add_request(1, 4, 10)                  # one 4-token page per prompt
+    b.add_request(2, 4, 10)
+    b.step()
+    b.complete()                             # both prefilled, one page free
+    before = (b.free_list(), b.counts())
+    assert before == ([2], (0, 2, 1))
+    for _ in range(2):
+        # both decode at context 5: request 1 takes the free page, then
+        # request 2 finds none; the step takes nothing in the end
+        with pytest.raises(hb.HbError) as e:
+            b.step()
+        assert e.value.status == 8
+        assert (b.free_list(), b.counts()) == before
+
+
+def test_step_cost_does_not_grow_with_the_pool():
+    """Forming a batch costs what its rows cost: 64 decodes and a chunk
+    take about as long with two million free pages as with two thousand."""
+    import statistics
+    import time
+    hb = lib()
+
+    def median_step_us(num_pages):
+        b = hb.Builder(512, 16, num_pages, 64)
+        for rid in range(64):
+            b.add_request(rid, 16, 200)
+        b.add_request(999, 900, 1)
+        ts = []
+        for _ in range(40):
+            t = time.perf_counter()
+            b.step()
+            b.complete()
+            ts.append(time.perf_counter() - t)
+        return statistics.median(ts[5:]) * 1e6
+
+    small, big = median_step_us(2000), median_step_us(2_000_000)
+    assert big < 20 * small + 200, (small, big)
