@@ -317,6 +317,39 @@ def plan_host_us(db, layout, sms, reps=20):
     return float(np.median(ts))
 
 
+def builder_host_us(layout, reps=60, num_pages=200_000):
+    """Median host time of one stall-free batch build (hb_builder_step and
+    hb_builder_complete through the binding) in a steady state shaped like
+    this batch: its decode rows running and a long prompt chunked into the
+    rest of the budget (budget = the batch's tokens), on a pool of
+    `num_pages` pages."""
+    from chunked_prefill_decode_gb300 import hb
+    n_dec = int((layout.q_len == 1).sum())
+    budget = int(layout.total_q)
+    page = layout.shape.page_size
+    max_pages = max(int(layout.block_table.shape[1]), -(-(reps + 16) // page))
+    b = hb.Builder(budget, page, num_pages, max_pages)
+    for rid in range(n_dec):
+        b.add_request(rid, 1, reps + 16)                  # decodes from the first step on
+    for _ in range(-(-n_dec // budget)):                  # admit them all
+        b.step()
+        b.complete()
+    prompt = max(1, max_pages * page // 2)
+    rid = n_dec
+    b.add_request(rid, prompt, 1)
+    ts = []
+    for _ in range(reps):
+        t0 = time.perf_counter()
+        b.step()
+        fin = b.complete()
+        ts.append((time.perf_counter() - t0) * 1e6)
+        if rid in fin:
+            rid += 1
+            b.add_request(rid, prompt, 1)
+    b.close()
+    return float(np.median(ts[reps // 5:]))
+
+
 def run_reference(args):
     """The fp64 CPU oracle as the reference arm (rank 0 only)."""
     n, rank, _ = _dist() if int(os.environ.get("WORLD_SIZE", "1")) > 1 else (1, 0, 0)
@@ -483,8 +516,9 @@ def run_native(args):
     e2e = {"value": n * T * e2e_steps / e2e_s, "unit": "tokens/s",
            "h2d_bytes_per_step": h2d + plan_bytes, "d2h_bytes_per_step": d2h,
            "copies": "one packed pinned H2D (q, k_new, v_new, descriptors) + the plan upload "
-                     "and one D2H of the output per step, on copy streams overlapping the "
-                     "neighbouring steps' kernels (two staging buffers)"}
+                     "(on the input-copy stream, ahead of the inputs) and one D2H of the output "
+                     "per step, on copy streams overlapping the neighbouring steps' kernels "
+                     "(two staging buffers)"}
 
     if rank != 0:
         return
@@ -523,6 +557,7 @@ def run_native(args):
                                          budget_s=args.cpu_seconds)
     cpu1_v, cpu1_desc = oracle_sample_rate_one_thread(args.workload, args.cpu_seconds / 2)
     plan_us = plan_host_us(db, layout, sms)
+    build_us = builder_host_us(layout)
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": n,
         "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms_step,
@@ -549,6 +584,7 @@ def run_native(args):
                          "one_thread": {"value": cpu1_v, "unit": "tokens/s", "cores": 1,
                                         "sample": cpu1_desc}},
         "plan_host_us": plan_us,
+        "builder_host_us": build_us,
         "e2e": e2e,
         "gpu_launches": int(launches),
         "clocks": clk.summary(),

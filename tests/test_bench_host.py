@@ -116,3 +116,16 @@ def test_reference_arm_prints_the_contract_line():
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"]
     assert d["e2e"] == {"value": d["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}
+
+
+def test_builder_host_time_is_measured_in_steady_state():
+    """The batch-build timing runs the native builder at the batch's shape
+    (its decode rows running, a prompt chunked beside them) and returns a
+    finite positive median."""
+    import math
+    from _hbutil import lib
+    from chunked_prefill_decode_gb300 import workloads
+    lib()
+    for name in ("tiny", "decode_only"):
+        us = bench.builder_host_us(workloads.WORKLOADS[name](), reps=20, num_pages=50_000)
+        assert math.isfinite(us) and us > 0
