@@ -557,7 +557,10 @@ def run_native(args):
                                          budget_s=args.cpu_seconds)
     cpu1_v, cpu1_desc = oracle_sample_rate_one_thread(args.workload, args.cpu_seconds / 2)
     plan_us = plan_host_us(db, layout, sms)
-    build_us = builder_host_us(layout)
+    try:                        # an auxiliary host figure: never costs the line
+        build_us = builder_host_us(layout)
+    except Exception as e:      # noqa: BLE001
+        build_us = f"failed: {e}"
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": n,
         "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms_step,
