@@ -347,7 +347,9 @@ hb_status hb_builder_add_request(hb_builder* b, int64_t id, int32_t prompt_len,
  * rows: q_len, context_len [max_rows], block_table [max_rows *
  * max_pages_per_seq] (unused entries -1), row_ids [max_rows], row_kind
  * [max_rows] (0 decode, 1 prefill).  *num_rows = 0 means nothing to run.
- * HB_ERR_WORKSPACE if max_rows is too small (the builder is then unchanged).
+ * HB_ERR_WORKSPACE if max_rows is too small, HB_ERR_OUT_OF_PAGES if a
+ * decode finds no free page; after any error the builder is unchanged.
+ * A step costs what its rows and their pages cost, whatever the pool size.
  * Call hb_builder_complete before the next step. */
 hb_status hb_builder_step(hb_builder* b, int32_t max_rows, int32_t* num_rows,
                           int32_t* q_len, int32_t* context_len,
