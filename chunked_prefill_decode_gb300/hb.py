@@ -360,11 +360,13 @@ class Builder:
         """Next batch as a dict of numpy arrays, or None when there is nothing to run."""
         while True:
             mr, mp = self._max_rows, self.max_pages_per_seq
-            ql = np.zeros(mr, np.int32)
-            cl = np.zeros(mr, np.int32)
-            bt = np.zeros((mr, mp), np.int32)
-            ids = np.zeros(mr, np.int64)
-            kind = np.zeros(mr, np.int32)
+            # the library writes every entry of the rows it returns (block
+            # table entries past a row's pages as -1); the rest is not read
+            ql = np.empty(mr, np.int32)
+            cl = np.empty(mr, np.int32)
+            bt = np.empty((mr, mp), np.int32)
+            ids = np.empty(mr, np.int64)
+            kind = np.empty(mr, np.int32)
             n, over = ctypes.c_int32(0), ctypes.c_int32(0)
             st = load().hb_builder_step(self._h, mr, ctypes.byref(n), _ptr(ql), _ptr(cl),
                                         _ptr(bt), _ptr(ids), _ptr(kind), ctypes.byref(over))
