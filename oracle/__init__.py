@@ -8,4 +8,6 @@ never do, and nothing here imports them.
                    block table, split-softmax merge
   brute            pure-Python loops of the same attention (tiny shapes)
   stall_free       the stall-free batch builder, step by step
+  linear           fp64 linear layers of the block (projection, gated MLP,
+                   residual) around the attention step
 """
