@@ -7,8 +7,9 @@ A step is one pass of the hot path over one synthetic hybrid batch: the KV
 append of the batch's new tokens and the attention of every new token (decode
 rows and prefill chunks) over the paged cache, through the C ABI.  The batch
 layout (q_len, context_len, block tables) is fixed per workload, so the plan
-is built once.  The default workload is the Mistral-7B attention shape at a
-512-token budget (64 decode rows + one 448-token chunk).
+is built once.  The default workload is the largest single-GPU batch: the
+Yi-34B attention shape at a 2048-token budget (32 decode rows over long
+contexts + one 2016-token chunk at offset 6048).
 
 Printed (rank 0, one JSON line): tokens/s over the timed steps with inputs
 resident in HBM (`value`), the same through host buffers with the copies in
@@ -218,6 +219,34 @@ def _dist(backend="nccl"):
     return n, rank, local
 
 
+def replica_launch(gpus, argv, env=None):
+    """--gpus N against the process's rank environment.  Under a launcher
+    (WORLD_SIZE set) N must equal WORLD_SIZE: a mismatch ends the run with
+    exit code 2 instead of timing the wrong number of GPUs.  Without one, N > 1
+    starts N replica ranks through torch.distributed.run on this node (127.0.0.1)
+    and returns their exit code; N = 1 returns None (run here)."""
+    env = os.environ if env is None else env
+    if gpus < 1:
+        print(f"bench.py: --gpus {gpus} must be >= 1", file=sys.stderr)
+        return 2
+    if "WORLD_SIZE" in env:
+        ws = int(env["WORLD_SIZE"])
+        if ws != gpus:
+            print(f"bench.py: --gpus {gpus} but WORLD_SIZE={ws}", file=sys.stderr)
+            return 2
+        return None
+    if gpus == 1:
+        return None
+    import socket
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes", "1",
+           "--nproc-per-node", str(gpus), "--master-addr", "127.0.0.1",
+           "--master-port", str(port), os.path.abspath(__file__)] + list(argv)
+    return subprocess.run(cmd).returncode
+
+
 def _barrier(n):
     if n > 1:
         torch.distributed.barrier()
@@ -397,7 +426,8 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
-TIMING_EVERY = 16   # timed steps per step with per-kernel CUDA events
+TIMING_EVERY = 16   # --layer: timed steps per step with per-kernel CUDA events
+KERNEL_TIMING_STEPS = 100   # steps of the per-kernel timing pass (>= 50 launches each)
 
 
 def run_native(args):
@@ -433,28 +463,29 @@ def run_native(args):
     # ---- timed region: inputs resident in HBM
     _barrier(n)
     torch.cuda.synchronize(dev)
-    hb.hb_timing_enable(True)
-    hb.hb_timing_enable(False)
     launches0 = hb.hb_launch_count()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clk:
         ev0.record(stream)
-        for i in range(args.steps):
-            # per-kernel events on every TIMING_EVERY-th step only: an event
-            # between two kernels stops the GPU from starting the second
-            # launch under the first one's tail
-            sampled = i % TIMING_EVERY == 0
-            if sampled:
-                hb.hb_timing_enable(True, keep=True)
+        for _ in range(args.steps):
             step()
-            if sampled:
-                hb.hb_timing_enable(False)
         ev1.record(stream)
         torch.cuda.synchronize(dev)
     launches = hb.hb_launch_count() - launches0
-    ktimes = hb.hb_timing_read()
     hb.hb_check()
     _barrier(n)
+    # ---- per-kernel durations, in a pass of their own after the timed
+    # region: CUDA events around every launch of KERNEL_TIMING_STEPS steps
+    # (an event between two kernels stops the second from starting under the
+    # first one's tail, so the headline loop above carries none)
+    k_steps = max(KERNEL_TIMING_STEPS, 1)
+    hb.hb_timing_enable(True)
+    for _ in range(k_steps):
+        step()
+    hb.hb_timing_enable(False)
+    torch.cuda.synchronize(dev)
+    kdur = {k: hb.hb_timing_durations(k) for k in ("kv_append", "attention")}
+    hb.hb_check()
     ms = ev0.elapsed_time(ev1)
     ms_max = max_over_ranks(ms, n)
     value = job_tokens_per_s(T, args.steps, n, ms)
@@ -524,8 +555,8 @@ def run_native(args):
         return
     peaks = _peaks()
     cnt = algorithmic_counts(layout)
-    t_att = ktimes["attention"][0] / max(1, ktimes["attention"][1])
-    t_app = ktimes["kv_append"][0] / max(1, ktimes["kv_append"][1])
+    t_att = float(np.median(kdur["attention"]))
+    t_app = float(np.median(kdur["kv_append"]))
     # the attention launch (decode and chunk CTAs together) is the dominant
     # kernel; its bound is the larger of its two roofline terms
     att_bytes = cnt["decode_bytes"] + cnt["chunk_bytes"]
@@ -546,10 +577,16 @@ def run_native(args):
     roof["traffic"] = profiled_traffic(args.workload)
     roof["algorithmic"] = {"bytes": att_bytes, "flops": att_flops}
     roof["kernel_roofline_frac"] = max(t_hbm, t_tc) * 1e3 / t_att
-    roof["avg_launch_ms"] = {"attention": t_att, "kv_append": t_app}
-    roof["timed_launches"] = {"attention": ktimes["attention"][1],
-                              "kv_append": ktimes["kv_append"][1],
-                              "sample": f"CUDA events around each launch of every {TIMING_EVERY}th timed step"}
+    roof["median_launch_ms"] = {"attention": t_att, "kv_append": t_app}
+    roof["mean_launch_ms"] = {k: float(np.mean(v)) for k, v in kdur.items()}
+    roof["timed_launches"] = {"attention": len(kdur["attention"]),
+                              "kv_append": len(kdur["kv_append"]),
+                              "sample": f"median of CUDA events around each launch of "
+                                        f"{k_steps} steps run after the timed region"}
+    app_bytes = cnt["append_bytes"]
+    roof["kv_append"] = {"bound": "hbm", "algorithmic_bytes": app_bytes,
+                         "achieved": app_bytes / (t_app / 1e3) / 1e9, "unit": "GB/s",
+                         "frac": app_bytes / (t_app / 1e3) / 1e9 / peaks["hbm_gbs"]}
     step_roof_s = max(cnt["flops"] / (peaks["bf16_tflops"] * 1e12),
                       cnt["bytes"] / (peaks["hbm_gbs"] * 1e9))
     ms_step = ms_max / args.steps
@@ -803,7 +840,7 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--workload", default="mistral_b512", choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--workload", default="yi_b2048", choices=sorted(workloads.WORKLOADS))
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--sweep", choices=["chunk", "seed"], default=None,
@@ -819,6 +856,9 @@ def main():
     if args.oracle_sample:
         run_oracle_sample(args)
         return
+    rc = replica_launch(args.gpus, sys.argv[1:])
+    if rc is not None:
+        sys.exit(rc)
     if args.sweep == "chunk":
         run_chunk_sweep(args)
     elif args.sweep == "seed":

@@ -5,6 +5,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <algorithm>
 #include <atomic>
@@ -210,6 +211,15 @@ hb_status check_ptr(const void* p, const char* name) {
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// A named range on the profiler's host timeline around each entry point of
+// the hot path (NVTX; a no-op unless a profiling tool is attached).
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
+
 }  // namespace
 
 // ---------------------------------------------------------------- internal
@@ -305,6 +315,7 @@ const char* hb_status_string(hb_status s) {
 
 hb_status hb_kv_append(const hb_batch* batch, const void* k_new, const void* v_new,
                        void* k_cache, void* v_cache, void* stream) {
+  NvtxRange range("hb_kv_append");
   try {
     hb_status s = check_batch(batch);
     if (s != HB_OK) return s;
@@ -360,6 +371,7 @@ size_t hb_linear_workspace_size(int32_t M, int32_t N, int32_t K, int32_t epilogu
 hb_status hb_linear(const void* x, const void* w, int32_t M, int32_t N, int32_t K,
                     int32_t epilogue, const hb_linear_out* out, void* workspace,
                     size_t workspace_bytes, void* stream) {
+  NvtxRange range("hb_linear");
   try {
     if (!out) return fail(HB_ERR_INVALID_ARG, "out is NULL");
     if (epilogue < HB_LINEAR_STORE || epilogue > HB_LINEAR_RESIDUAL)
@@ -438,6 +450,7 @@ hb_status hb_plan(const hb_batch* batch, const int32_t* h_q_len,
                   const int32_t* h_context_len, int32_t num_sms, void* h_plan,
                   size_t* plan_bytes, void* d_workspace, size_t* workspace_bytes,
                   void* stream) {
+  NvtxRange range("hb_plan");
   try {
     hb_status s = check_batch(batch);
     if (s != HB_OK) return s;
@@ -751,6 +764,7 @@ hb_status hb_plan(const hb_batch* batch, const int32_t* h_q_len,
 hb_status hb_attention(const hb_batch* batch, const void* h_plan, const void* q,
                        const void* k_cache, const void* v_cache, float softmax_scale,
                        void* out, void* d_workspace, void* stream) {
+  NvtxRange range("hb_attention");
   try {
     hb_status s = check_batch(batch);
     if (s != HB_OK) return s;
@@ -942,6 +956,26 @@ hb_status hb_timing_read(double* total_ms, int32_t* launches) {
       launches[r.kernel] += 1;
     }
   }
+  return ok();
+}
+
+hb_status hb_timing_durations(int32_t kernel, float* ms, int32_t max, int32_t* n) {
+  if (!n || (max > 0 && !ms)) return fail(HB_ERR_INVALID_ARG, "NULL output");
+  if (kernel < 0 || kernel >= HB_NUM_KERNEL_IDS)
+    return fail(HB_ERR_INVALID_ARG, "kernel id %d", kernel);
+  std::lock_guard<std::mutex> lk(g_time_mu);
+  int32_t k = 0;
+  for (auto& r : g_recs) {
+    if (r.kernel != kernel) continue;
+    if (k < max) {
+      cudaError_t e = cudaEventSynchronize(r.b);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaEventSynchronize");
+      e = cudaEventElapsedTime(&ms[k], r.a, r.b);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaEventElapsedTime");
+    }
+    ++k;
+  }
+  *n = k;
   return ok();
 }
 

@@ -27,6 +27,8 @@
 #include <unordered_map>
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "hb.h"
 
 namespace {
@@ -69,6 +71,15 @@ struct hb_builder {
   int32_t pages_for(int64_t tokens) const {
     return (int32_t)((tokens + page_size - 1) / page_size);
   }
+};
+
+// A named range on the profiler's host timeline (NVTX; a no-op unless a
+// profiling tool is attached).
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
 };
 
 extern "C" {
@@ -127,6 +138,7 @@ hb_status hb_builder_add_request(hb_builder* b, int64_t id, int32_t prompt_len, 
 hb_status hb_builder_step(hb_builder* b, int32_t max_rows, int32_t* num_rows, int32_t* q_len,
                           int32_t* context_len, int32_t* block_table, int64_t* row_ids,
                           int32_t* row_kind, int32_t* over_budget) {
+  NvtxRange range("hb_builder_step");
   if (!b || !num_rows || !over_budget) return berr(HB_ERR_INVALID_ARG, "NULL argument");
   if (b->pending) return berr(HB_ERR_INVALID_ARG, "complete the previous batch first");
   if (max_rows < 0) return berr(HB_ERR_INVALID_ARG, "max_rows < 0");
@@ -228,6 +240,7 @@ hb_status hb_builder_step(hb_builder* b, int32_t max_rows, int32_t* num_rows, in
 
 hb_status hb_builder_complete(hb_builder* b, int32_t max_finished, int32_t* num_finished,
                               int64_t* finished_ids) {
+  NvtxRange range("hb_builder_complete");
   if (!b || !num_finished) return berr(HB_ERR_INVALID_ARG, "NULL argument");
   if (!b->pending) return berr(HB_ERR_INVALID_ARG, "no batch to complete");
   std::vector<Request*> done;

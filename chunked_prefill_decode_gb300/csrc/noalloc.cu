@@ -111,6 +111,17 @@ extern "C" hb_status hb_decode_attention_noalloc(const hb_batch* batch, const in
     }
     if (batch->total_q != S) return internal_fail(HB_ERR_SHAPE, "total_q must equal num_seqs");
     const int g = Hq / Hkv;
+    // The work list below is copied from this file's static host storage
+    // when the call is made.  A captured copy would read that storage again
+    // at every replay, after later calls have overwritten it, so a call on a
+    // stream that is being captured is refused.
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(static_cast<cudaStream_t>(stream), &cap) != cudaSuccess)
+      return internal_fail(HB_ERR_CUDA, "cudaStreamIsCapturing failed");
+    if (cap != cudaStreamCaptureStatusNone)
+      return internal_fail(HB_ERR_UNSUPPORTED,
+                           "hb_decode_attention_noalloc cannot be called on a stream that is "
+                           "being captured (its work list is copied from host memory at the call)");
 
     // ---- plan into static host storage: the decode partition over at most
     // one CTA per SM; fewer, longer ranges until the partial states fit

@@ -59,6 +59,7 @@ EXPORTED = (
     "hb_builder_step", "hb_builder_complete", "hb_builder_counts",
     "hb_builder_free_list", "hb_builder_last_error", "hb_decode_attention_noalloc",
     "hb_selftest_wait_timeout", "hb_linear", "hb_linear_workspace_size",
+    "hb_timing_durations",
 )
 
 LINEAR_STORE, LINEAR_GATED, LINEAR_RESIDUAL = 0, 1, 2
@@ -111,6 +112,8 @@ def load():
     L.hb_timing_enable.argtypes = [i32]
     L.hb_timing_read.restype = ctypes.c_int
     L.hb_timing_read.argtypes = [P(ctypes.c_double), P(i32)]
+    L.hb_timing_durations.restype = ctypes.c_int
+    L.hb_timing_durations.argtypes = [i32, P(ctypes.c_float), i32, P(i32)]
     L.hb_launch_count.restype = i64
     L.hb_launch_count.argtypes = []
     L.hb_builder_create.restype = ctypes.c_int
@@ -321,6 +324,16 @@ def hb_timing_read():
     n = (ctypes.c_int32 * HB_NUM_KERNEL_IDS)()
     _check(load().hb_timing_read(ms, n))
     return {KERNEL_NAMES[i]: (ms[i], n[i]) for i in range(HB_NUM_KERNEL_IDS)}
+
+
+def hb_timing_durations(kernel):
+    """Per-launch durations (ms, launch order) recorded for one kernel name."""
+    k = KERNEL_NAMES.index(kernel)
+    n = ctypes.c_int32(0)
+    _check(load().hb_timing_durations(k, None, 0, ctypes.byref(n)))
+    buf = (ctypes.c_float * max(1, n.value))()
+    _check(load().hb_timing_durations(k, buf, n.value, ctypes.byref(n)))
+    return [float(buf[i]) for i in range(n.value)]
 
 
 def hb_launch_count() -> int:

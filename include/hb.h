@@ -206,7 +206,10 @@ hb_status hb_attention(const hb_batch* batch, const void* h_plan,
  *     streams or host threads) race and must be serialised by the caller.
  *     Host calls are serialised by a lock inside the library.
  *   - The plan's items are copied from pageable host memory, so the call
- *     returns after the copy is staged.
+ *     returns after the copy is staged.  That storage is the library's own
+ *     and the next call overwrites it, so a call on a stream that is being
+ *     captured into a CUDA graph is refused with HB_ERR_UNSUPPORTED (a
+ *     replayed copy would read a later call's items).
  *   - The work is spread over fewer CTAs when the partial states would not
  *     fit the array; a batch that needs more than 4096 work items (about
  *     num_seqs times ceil(Hkv / 8), plus one per SM) is rejected with
@@ -307,6 +310,11 @@ hb_status hb_timing_enable(int32_t enable);
  * duration in milliseconds and the number of launches recorded.  Both arrays
  * have HB_NUM_KERNEL_IDS entries. */
 hb_status hb_timing_read(double* total_ms, int32_t* launches);
+
+/* Durations in milliseconds of the recorded launches of one kernel id, in
+ * launch order: up to `max` of them go to ms[], *n receives how many were
+ * recorded (which may exceed max).  Synchronises the events it reads. */
+hb_status hb_timing_durations(int32_t kernel, float* ms, int32_t max, int32_t* n);
 
 /* Number of kernels this library has launched in this process so far. */
 int64_t hb_launch_count(void);

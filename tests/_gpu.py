@@ -1,6 +1,7 @@
 """GPU-test helpers: run one hybrid-batch step through the C ABI and compute
 the oracle's answer for the same seeded inputs."""
 import math
+import os
 
 import numpy as np
 import torch
@@ -53,12 +54,20 @@ def oracle_step(layout, ten, scale=None, tokens=None):
     return kp, vp, ref
 
 
+# (test id, max-abs error, mean-abs error) of every compare() in this process,
+# reported at the end of the run (conftest.py) so the margin to the bounds is
+# visible before a regression reaches them
+MARGINS = []
+
+
 def compare(out, ref, tokens=None, max_abs=MAX_ABS, mean_abs=MEAN_ABS):
     got = out.float().cpu().numpy().astype(np.float64)
     if tokens is not None:
         got, ref = got[tokens], ref[tokens]
     assert np.isfinite(got).all(), "non-finite output"
     err = np.abs(got - ref)
+    test = os.environ.get("PYTEST_CURRENT_TEST", "?").split(" ")[0]
+    MARGINS.append((test, float(err.max()), float(err.mean())))
     assert err.max() <= max_abs and err.mean() <= mean_abs, \
         f"max-abs {err.max():.3e} mean-abs {err.mean():.3e}"
     return err.max(), err.mean()

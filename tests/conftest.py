@@ -26,3 +26,29 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+def pytest_terminal_summary(terminalreporter, exitstatus, config):
+    """Margin of the attention parity checks to their bounds (max-abs 1e-2,
+    mean-abs 1e-3): the worst cases, and every case in HB_PARITY_LOG (a JSON
+    lines file) when that variable is set."""
+    mod = sys.modules.get("_gpu")
+    rows = getattr(mod, "MARGINS", None) if mod else None
+    if not rows:
+        return
+    per = {}
+    for test, mx, mean in rows:
+        a, b = per.get(test, (0.0, 0.0))
+        per[test] = (max(a, mx), max(b, mean))
+    tr = terminalreporter
+    tr.write_sep("-", f"attention parity margins ({len(per)} tests, {len(rows)} checks)")
+    worst = sorted(per.items(), key=lambda kv: -kv[1][0] / mod.MAX_ABS)[:10]
+    for test, (mx, mean) in worst:
+        tr.write_line(f"max-abs {mx:.2e} ({100 * mx / mod.MAX_ABS:5.1f}% of bound)  "
+                      f"mean-abs {mean:.2e} ({100 * mean / mod.MEAN_ABS:5.1f}%)  {test}")
+    path = os.environ.get("HB_PARITY_LOG")
+    if path:
+        import json
+        with open(path, "w") as f:
+            for test, (mx, mean) in sorted(per.items()):
+                f.write(json.dumps({"test": test, "max_abs": mx, "mean_abs": mean}) + "\n")

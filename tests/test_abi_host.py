@@ -34,6 +34,14 @@ def test_timing_modes():
     ms = (ctypes.c_double * 3)()
     n = (ctypes.c_int32 * 3)()
     assert L.hb_timing_read(ms, n) == 0 and list(n) == [0, 0, 0]
+    # per-launch durations: no records yet; bad kernel ids and NULLs refused
+    cnt = ctypes.c_int32(-1)
+    buf = (ctypes.c_float * 4)()
+    assert L.hb_timing_durations(1, buf, 4, ctypes.byref(cnt)) == 0 and cnt.value == 0
+    assert L.hb_timing_durations(3, buf, 4, ctypes.byref(cnt)) == 1
+    assert L.hb_timing_durations(-1, buf, 4, ctypes.byref(cnt)) == 1
+    assert L.hb_timing_durations(0, None, 4, ctypes.byref(cnt)) == 1
+    assert L.hb_timing_durations(0, None, 0, ctypes.byref(cnt)) == 0
 
 
 @pytest.mark.parametrize("field,value,status", [

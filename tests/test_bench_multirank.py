@@ -43,3 +43,17 @@ def test_single_rank_needs_no_process_group():
     import bench
     assert bench.max_over_ranks(3.5, 1) == 3.5
     assert bench.job_tokens_per_s(10, 4, 1, 2.0) == pytest.approx(10 * 4 / 0.002)
+
+
+def test_gpus_flag_against_the_rank_environment():
+    """--gpus N must agree with a launcher's WORLD_SIZE (else exit code 2);
+    without a launcher N = 1 runs in place and N > 1 starts N ranks itself."""
+    import bench
+    assert bench.replica_launch(2, [], env={"WORLD_SIZE": "1"}) == 2
+    assert bench.replica_launch(1, [], env={"WORLD_SIZE": "4"}) == 2
+    assert bench.replica_launch(4, [], env={"WORLD_SIZE": "4"}) is None
+    assert bench.replica_launch(1, [], env={}) is None
+    assert bench.replica_launch(0, [], env={}) == 2
+    # two ranks started through torch.distributed.run; each parses --help
+    # and exits 0 before touching a device
+    assert bench.replica_launch(2, ["--help"], env={}) == 0

@@ -98,6 +98,19 @@ def test_sliding_window(window, geom):
                 seed=15, repeats=2)
 
 
+@pytest.mark.parametrize("seed", [15, 17])
+@pytest.mark.parametrize("window", [1, 7, 16, 100])
+@pytest.mark.parametrize("geom", [(8, 8, 64), (32, 8, 128), (56, 8, 128)])
+def test_sliding_window_keeps_headroom(window, geom, seed):
+    """Short windows leave each row few keys, where the bf16 rounding of the
+    softmax weights counts most: the error stays at or below 80 % of both
+    bounds."""
+    hq, hkv, d = geom
+    mx, mean = _full_check(layout_from_rows(Shape(hq, hkv, d, sliding_window=window),
+                                            WINDOW_ROWS, seed), seed=seed)
+    assert mx <= 0.8 * MAX_ABS and mean <= 0.8 * MEAN_ABS, (mx, mean)
+
+
 @pytest.mark.parametrize("window", [16, 100, 1000])
 def test_sliding_window_never_reads_pages_below_it(window):
     """Block-table entries of pages below every window of their row are set
