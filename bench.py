@@ -333,17 +333,31 @@ def run_oracle_sample(args):
     print(json.dumps({"value": v, "sample": desc}), flush=True)
 
 
-def plan_host_us(db, layout, sms, reps=20):
-    """Median host time of hb_plan for this batch (the host part only: no
-    upload)."""
+def plan_host_us(db, layout, sms, reps=200):
+    """Median host time of hb_plan for this batch, the host part only (no
+    upload): (the C call with its arguments marshalled once, the same call
+    through the Python binding)."""
+    import ctypes
     from chunked_prefill_decode_gb300 import hb
     plan, _ = hb.hb_plan(db.batch, layout.q_len, layout.context_len, sms, upload=False)
-    ts = []
+    ql = np.ascontiguousarray(layout.q_len, dtype=np.int32)
+    cl = np.ascontiguousarray(layout.context_len, dtype=np.int32)
+    L = hb.load()
+    pb, wb = ctypes.c_size_t(plan.nbytes), ctypes.c_size_t(0)
+    args = (ctypes.byref(db.batch), ql.ctypes.data_as(ctypes.c_void_p),
+            cl.ctypes.data_as(ctypes.c_void_p), int(sms), plan.ctypes.data_as(ctypes.c_void_p),
+            ctypes.byref(pb), None, ctypes.byref(wb), None)
+    c_ts, py_ts = [], []
     for _ in range(reps):
         t0 = time.perf_counter()
+        st = L.hb_plan(*args)
+        c_ts.append((time.perf_counter() - t0) * 1e6)
+        if st != 0:
+            raise RuntimeError(f"hb_plan failed ({st})")
+        t0 = time.perf_counter()
         hb.hb_plan(db.batch, layout.q_len, layout.context_len, sms, plan=plan, upload=False)
-        ts.append((time.perf_counter() - t0) * 1e6)
-    return float(np.median(ts))
+        py_ts.append((time.perf_counter() - t0) * 1e6)
+    return float(np.median(c_ts)), float(np.median(py_ts))
 
 
 def builder_host_us(layout, reps=60, num_pages=200_000):
@@ -593,7 +607,7 @@ def run_native(args):
     cpu_v, cpu_desc = oracle_sample_rate(layout, workloads.make_tensors(layout, seed=1),
                                          budget_s=args.cpu_seconds)
     cpu1_v, cpu1_desc = oracle_sample_rate_one_thread(args.workload, args.cpu_seconds / 2)
-    plan_us = plan_host_us(db, layout, sms)
+    plan_us, plan_binding_us = plan_host_us(db, layout, sms)
     try:                        # an auxiliary host figure: never costs the line
         build_us = builder_host_us(layout)
     except Exception as e:      # noqa: BLE001
@@ -624,6 +638,7 @@ def run_native(args):
                          "one_thread": {"value": cpu1_v, "unit": "tokens/s", "cores": 1,
                                         "sample": cpu1_desc}},
         "plan_host_us": plan_us,
+        "plan_binding_us": plan_binding_us,
         "builder_host_us": build_us,
         "e2e": e2e,
         "gpu_launches": int(launches),

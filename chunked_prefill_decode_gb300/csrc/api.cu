@@ -15,7 +15,6 @@
 #include <functional>
 #include <mutex>
 #include <unordered_map>
-#include <queue>
 #include <string>
 #include <vector>
 
@@ -220,6 +219,98 @@ struct NvtxRange {
   NvtxRange& operator=(const NvtxRange&) = delete;
 };
 
+
+// ---------------------------------------------------------------- plan scratch
+struct DurGroup {
+  double d;       // duration of each piece (us)
+  int32_t count;  // pieces of that duration
+};
+struct FreeAt {
+  double t;       // an SM frees up at t
+  int32_t count;  // SMs that free up then
+};
+
+// Working arrays of hb_plan, kept per host thread so that their capacity
+// carries over from call to call.
+struct PlanScratch {
+  std::vector<ChunkItem> raw, chk;
+  std::vector<int32_t> count;
+  std::vector<int32_t> dur_count;
+  std::vector<DurGroup> groups;
+  std::vector<FreeAt> free_at, next, fresh;
+  std::vector<DecodeItem> dec;
+  std::vector<int32_t> cta_off;
+  std::vector<double> t_end;
+};
+
+PlanScratch& plan_scratch() {
+  thread_local PlanScratch ps;
+  return ps;
+}
+
+// Stable sort of `in` into `out` by key(x) in 0..kmax, largest key first.
+template <class T, class Key>
+void counting_sort_desc(const std::vector<T>& in, std::vector<T>& out, std::vector<int32_t>& cnt,
+                        int kmax, Key key) {
+  cnt.assign((size_t)kmax + 2, 0);
+  for (const T& x : in) ++cnt[key(x)];
+  int32_t run = 0;
+  for (int k = kmax; k >= 0; --k) {
+    const int32_t c = cnt[k];
+    cnt[k] = run;
+    run += c;
+  }
+  out.resize(in.size());
+  for (const T& x : in) out[cnt[key(x)]++] = x;
+}
+
+// End time of a launch whose pieces (ps.groups: durations, longest first,
+// with their counts) start one after another, each on the SM that frees up
+// first; G of the num_sms SMs are busy until td, the others free at 0.  The
+// same end as placing the pieces one by one with a heap of SM free times,
+// computed on (time, count) runs: within a run of equal durations the next
+// piece takes the earlier of the oldest free time left and the oldest time
+// freed by the run itself, both of which come in ascending order.
+double simulate_dispatch(PlanScratch& ps, int num_sms, int G, double td) {
+  std::vector<FreeAt>& F = ps.free_at;
+  F.clear();
+  if (G < num_sms) F.push_back({0.0, num_sms - G});
+  if (G > 0) F.push_back({td, G});
+  double end = td;
+  for (const DurGroup& grp : ps.groups) {
+    std::vector<FreeAt>& Q = ps.fresh;   // times freed by this run, ascending
+    Q.clear();
+    size_t i1 = 0, i2 = 0;
+    int32_t left = grp.count;
+    double last = 0.0;
+    while (left > 0) {
+      const bool from_f = i1 < F.size() && (i2 >= Q.size() || F[i1].t <= Q[i2].t);
+      FreeAt* src = from_f ? &F[i1] : &Q[i2];
+      const int32_t k = std::min(src->count, left);
+      const double t = src->t;
+      src->count -= k;               // (before the push below can move Q)
+      if (src->count == 0) {
+        if (from_f) ++i1; else ++i2;
+      }
+      last = t;
+      left -= k;
+      Q.push_back({t + grp.d, k});
+    }
+    end = std::max(end, last + grp.d);
+    // the free times left: the rest of F merged with the rest of Q
+    std::vector<FreeAt>& M = ps.next;
+    M.clear();
+    while (i1 < F.size() || i2 < Q.size()) {
+      const bool from_f = i1 < F.size() && (i2 >= Q.size() || F[i1].t <= Q[i2].t);
+      const FreeAt x = from_f ? F[i1++] : Q[i2++];
+      if (x.count == 0) continue;
+      if (!M.empty() && M.back().t == x.t) M.back().count += x.count;
+      else M.push_back(x);
+    }
+    F.swap(M);
+  }
+  return end;
+}
 }  // namespace
 
 // ---------------------------------------------------------------- internal
@@ -479,8 +570,10 @@ hb_status hb_plan(const hb_batch* batch, const int32_t* h_q_len,
 
     const int kvhb = std::min(Hkv, kDecodeKvhBlock);
     const int n_blocks = Hkv / kvhb;
-    std::vector<int32_t> cu(S + 1, 0);
-    for (int i = 0; i < S; ++i) cu[i + 1] = cu[i] + h_q_len[i];
+    // all working arrays live in per-thread storage that keeps its capacity
+    // from call to call: a plan of a batch shaped like the last one
+    // allocates nothing
+    PlanScratch& ps = plan_scratch();
 
     // ---- chunk items: rows with q_len > 1, (kv head, query tile)
     const int tpt = kChunkRows / g;
@@ -488,34 +581,43 @@ hb_status hb_plan(const hb_batch* batch, const int32_t* h_q_len,
     for (int i = 0; i < S; ++i)
       if (h_q_len[i] > 1) n_tiles_total += (int64_t)((h_q_len[i] + tpt - 1) / tpt) * Hkv;
     const int tiles_per_item = (n_tiles_total >= 2LL * num_sms) ? 2 : 1;
-    std::vector<ChunkItem> chk;
-    for (int i = 0; i < S; ++i) {
-      if (h_q_len[i] == 1) continue;
-      const int off = h_context_len[i] - h_q_len[i];
-      // an item is a pair of query tiles (2 * tokens_per_tile tokens) that
-      // share every K/V tile when there are enough of them to fill the GPU,
-      // else a single tile (more CTAs); the last item of a row may be short
-      for (int kvh = 0; kvh < Hkv; ++kvh)
-        for (int t0 = 0; t0 < h_q_len[i]; t0 += tiles_per_item * tpt) {
-          ChunkItem c{};
-          c.seq = i;
-          c.kv_head = kvh;
-          c.tok0 = t0;
-          c.ntok = std::min(tiles_per_item * tpt, h_q_len[i] - t0);
-          c.kv_tiles = (off + t0 + c.ntok + kChunkKeys - 1) / kChunkKeys;
-          // with a sliding window the first row sees keys from off+t0-W+1 on
-          c.kv_begin = W > 0 ? std::max(0, off + t0 - W + 1) / kChunkKeys : 0;
-          c.n_splits = 1;
-          c.q0 = cu[i];
-          c.q_len = h_q_len[i];
-          c.ctx = h_context_len[i];
-          chk.push_back(c);
-        }
-    }
+    const int item_tokens = tiles_per_item * tpt;
+    size_t n_raw = 0;
+    for (int i = 0; i < S; ++i)
+      if (h_q_len[i] > 1) n_raw += (size_t)((h_q_len[i] + item_tokens - 1) / item_tokens) * Hkv;
+    ps.raw.resize(n_raw);
     auto key_tiles = [](const ChunkItem& c) { return c.kv_tiles - c.kv_begin; };
-    std::stable_sort(chk.begin(), chk.end(), [&](const ChunkItem& a, const ChunkItem& b) {
-      return key_tiles(a) > key_tiles(b);
-    });
+    int key_max = 0;
+    {
+      size_t k = 0;
+      int32_t q0 = 0;
+      for (int i = 0; i < S; q0 += h_q_len[i], ++i) {
+        if (h_q_len[i] == 1) continue;
+        const int off = h_context_len[i] - h_q_len[i];
+        // an item is a pair of query tiles (2 * tokens_per_tile tokens) that
+        // share every K/V tile when there are enough of them to fill the GPU,
+        // else a single tile (more CTAs); the last item of a row may be short
+        for (int kvh = 0; kvh < Hkv; ++kvh)
+          for (int t0 = 0; t0 < h_q_len[i]; t0 += item_tokens) {
+            ChunkItem c{};
+            c.seq = i;
+            c.kv_head = kvh;
+            c.tok0 = t0;
+            c.ntok = std::min(item_tokens, h_q_len[i] - t0);
+            c.kv_tiles = (off + t0 + c.ntok + kChunkKeys - 1) / kChunkKeys;
+            // with a sliding window the first row sees keys from off+t0-W+1 on
+            c.kv_begin = W > 0 ? std::max(0, off + t0 - W + 1) / kChunkKeys : 0;
+            c.n_splits = 1;
+            c.q0 = q0;
+            c.q_len = h_q_len[i];
+            c.ctx = h_context_len[i];
+            key_max = std::max(key_max, key_tiles(c));
+            ps.raw[k++] = c;
+          }
+      }
+    }
+    // longest first (a stable counting sort on the key-tile count)
+    counting_sort_desc(ps.raw, ps.chk, ps.count, key_max, key_tiles);
 
     // ---- cost model, in microseconds, from rates measured on GB300.  The
     // attention kernel runs decode CTAs and chunk CTAs side by side (one CTA
@@ -542,7 +644,8 @@ hb_status hb_plan(const hb_batch* batch, const int32_t* h_q_len,
     auto pick_decode = [&](double chunk_us, double max_item_us) -> int {
       if (decode_bytes <= 0.0) return 0;
       if (chunk_us <= 0.0) return num_sms;
-      std::vector<double> t(num_sms + 1, 0.0);
+      std::vector<double>& t = ps.t_end;
+      t.resize((size_t)num_sms + 1);
       double best = 1e300;
       for (int G = 1; G <= num_sms; ++G) {
         const double td = t_decode(G);
@@ -562,53 +665,51 @@ hb_status hb_plan(const hb_batch* batch, const int32_t* h_q_len,
       int n = std::min(kMaxChunkSplits, (kv + L - 1) / L);
       return std::max(1, std::min(n, kv / kMinPieceTiles));
     };
-    // end time of the launch: CTAs start in index order on the SM that frees
-    // up first; the G decode CTAs come first and hold their SMs for the
-    // decode time
-    auto simulate = [&](const std::vector<double>& durs, int G) {
-      std::priority_queue<double, std::vector<double>, std::greater<double>> free_at;
-      const double td = G > 0 ? t_decode(G) : 0.0;
-      for (int i = 0; i < num_sms; ++i) free_at.push(i < G ? td : 0.0);
-      double end = td;
-      for (double d : durs) {
-        const double t0 = free_at.top();
-        free_at.pop();
-        free_at.push(t0 + d);
-        end = std::max(end, t0 + d);
-      }
-      return end;
-    };
 
     // ---- split-KV: when single query tiles are too few to fill the SMs, a
     // tile's key range may be cut into up to kMaxChunkSplits pieces (each its
     // own CTA, merged by the last to finish).  The piece length is the one
     // with the earliest estimated end among a few candidates (no split
-    // included).
+    // included); the end is that of CTAs started in index order on the SM
+    // that frees up first, the G decode CTAs first, holding their SMs for
+    // the decode time (simulate_dispatch).
     int best_L = 0;   // 0: no split
-    if (tiles_per_item == 1 && !chk.empty()) {
-      const int kmax = key_tiles(chk.front());
+    if (tiles_per_item == 1 && !ps.chk.empty()) {
+      const int kmax = key_tiles(ps.chk.front());
       double best_t = 1e300;
       int prev_L = -1;
       for (int n = 1; n <= kMaxChunkSplits; ++n) {
         const int L = (kmax + n - 1) / n;
         if (L == prev_L || (n > 1 && L < kMinPieceTiles)) continue;
         prev_L = L;
-        std::vector<double> durs;
+        // pieces counted per (length, split) class; the sums run in item
+        // order
+        ps.dur_count.assign(2 * (size_t)(kmax + 1), 0);
+        size_t n_pieces = 0;
         double sum = 0.0, mx = 0.0;
-        for (const ChunkItem& c : chk) {
+        for (const ChunkItem& c : ps.chk) {
           const int kv = key_tiles(c);
           const int np = pieces_of(kv, L);
           for (int k = 0; k < np; ++k) {
             const int len = (k + 1) * kv / np - k * kv / np;
             const double d = len * tile_us + (np > 1 ? kPieceUs : 0.0);
-            durs.push_back(d);
+            ++ps.dur_count[2 * (size_t)len + (np > 1 ? 1 : 0)];
+            ++n_pieces;
             sum += d;
             mx = std::max(mx, d);
           }
         }
-        if (n > 1 && durs.size() > (size_t)(2 * num_sms)) break;   // at most two waves
-        std::sort(durs.begin(), durs.end(), std::greater<double>());
-        const double t = simulate(durs, pick_decode(sum, mx));
+        if (n > 1 && n_pieces > (size_t)(2 * num_sms)) break;   // at most two waves
+        ps.groups.clear();
+        for (int len = 0; len <= kmax; ++len)
+          for (int sp = 0; sp < 2; ++sp) {
+            const int32_t cnt = ps.dur_count[2 * (size_t)len + sp];
+            if (cnt) ps.groups.push_back({len * tile_us + (sp ? kPieceUs : 0.0), cnt});
+          }
+        std::sort(ps.groups.begin(), ps.groups.end(),
+                  [](const DurGroup& a, const DurGroup& b) { return a.d > b.d; });
+        const int G = pick_decode(sum, mx);
+        const double t = simulate_dispatch(ps, num_sms, G, G > 0 ? t_decode(G) : 0.0);
         if (t < 0.97 * best_t) {   // a split has to pay for itself clearly
           best_t = t;
           best_L = n == 1 ? 0 : L;
@@ -616,12 +717,13 @@ hb_status hb_plan(const hb_batch* batch, const int32_t* h_q_len,
       }
     }
     int n_cslots = 0, n_cmerge = 0;
-    {
-      std::vector<ChunkItem> out;
-      for (ChunkItem c : chk) {
+    if (best_L > 0) {
+      ps.raw.clear();
+      int piece_max = 0;
+      for (ChunkItem c : ps.chk) {
         const int kv = key_tiles(c);
         const int kb0 = c.kv_begin;
-        const int np = best_L > 0 ? pieces_of(kv, best_L) : 1;
+        const int np = pieces_of(kv, best_L);
         c.n_splits = np;
         c.slot = np > 1 ? n_cslots : 0;
         c.merge_id = np > 1 ? n_cmerge : 0;
@@ -629,7 +731,8 @@ hb_status hb_plan(const hb_batch* batch, const int32_t* h_q_len,
           c.split = k;
           c.kv_begin = kb0 + k * kv / np;
           c.kv_tiles = kb0 + (k + 1) * kv / np;
-          out.push_back(c);
+          piece_max = std::max(piece_max, key_tiles(c));
+          ps.raw.push_back(c);
         }
         if (np > 1) {
           n_cslots += np;
@@ -637,13 +740,11 @@ hb_status hb_plan(const hb_batch* batch, const int32_t* h_q_len,
         }
       }
       // longest first, so that short pieces fill the end of the launch
-      std::stable_sort(out.begin(), out.end(), [](const ChunkItem& a, const ChunkItem& b) {
-        return a.kv_tiles - a.kv_begin > b.kv_tiles - b.kv_begin;
-      });
-      chk.swap(out);
+      counting_sort_desc(ps.raw, ps.chk, ps.count, piece_max, key_tiles);
     }
+    // (without a split every item is one piece and the order stands)
     double chunk_us = 0.0, max_item_us = 0.0;
-    for (const ChunkItem& c : chk) {
+    for (const ChunkItem& c : ps.chk) {
       const double us = (c.kv_tiles - c.kv_begin) * tile_us + (c.n_splits > 1 ? kPieceUs : 0.0);
       chunk_us += us;
       max_item_us = std::max(max_item_us, us);
@@ -652,12 +753,9 @@ hb_status hb_plan(const hb_batch* batch, const int32_t* h_q_len,
 
     // ---- decode items: the decode rows' pages, end to end, cut into one
     // equal contiguous range per CTA, each range cut at row boundaries
-    int64_t n_dec_rows = 0, dec_pages = 0;
+    int64_t n_dec_rows = 0;
     for (int i = 0; i < S; ++i)
-      if (h_q_len[i] == 1) {
-        ++n_dec_rows;
-        dec_pages += (int64_t)((h_context_len[i] + kPageSize - 1) / kPageSize) * n_blocks;
-      }
+      if (h_q_len[i] == 1) ++n_dec_rows;
     // intervals: one static range per decode CTA.  A dynamic tail (short
     // intervals claimed from a counter) is supported by partition_decode and
     // the kernel but measured slower on GB300 (Mistral 125 vs 110 us: the
@@ -665,20 +763,22 @@ hb_status hb_plan(const hb_batch* batch, const int32_t* h_q_len,
     const int max_intervals = std::max(1, decode_ctas) * (1 + kDynamicPerCta) + 1;
     const int max_dec_items =
         (int)std::min<int64_t>(n_dec_rows * n_blocks + max_intervals + 1, 1 << 30);
-    std::vector<DecodeItem> dec(std::max(1, max_dec_items));
-    std::vector<int32_t> cta_off(max_intervals + 1, 0);
+    ps.dec.resize(std::max(1, max_dec_items));
+    ps.cta_off.resize(max_intervals + 1);
+    ps.cta_off[0] = 0;
     DecodePartition part;
     if (!partition_decode(S, h_q_len, h_context_len, n_blocks, kvhb, std::max(1, decode_ctas), 4,
-                          dec.data(), (int)dec.size(), cta_off.data(), max_intervals,
+                          ps.dec.data(), (int)ps.dec.size(), ps.cta_off.data(), max_intervals,
                           &part, W, /*dynamic_tail=*/false))
       return fail(HB_ERR_WORKSPACE, "decode partition overflow");
-    dec.resize(part.n_items);
-    cta_off.resize(part.grid + part.n_dynamic + 1);
+    const size_t n_dec = (size_t)part.n_items;
+    const size_t n_chk = ps.chk.size();
+    const size_t n_off = (size_t)(part.grid + part.n_dynamic + 1);
     const int n_slots = part.n_slots, n_merge = part.n_merge;
 
     // ---- sizes
-    const size_t offsets_at = dec.size() * sizeof(DecodeItem) + chk.size() * sizeof(ChunkItem);
-    const size_t items_bytes = align_up(offsets_at + cta_off.size() * sizeof(int32_t), 256);
+    const size_t offsets_at = n_dec * sizeof(DecodeItem) + n_chk * sizeof(ChunkItem);
+    const size_t items_bytes = align_up(offsets_at + n_off * sizeof(int32_t), 256);
     const size_t need_plan = sizeof(PlanHeader) + items_bytes;
     const size_t ws_counters = items_bytes;
     const size_t ws_partial_o = align_up(ws_counters + (size_t)(kCounterMerge0 + n_merge) * 4, 256);
@@ -713,8 +813,8 @@ hb_status hb_plan(const hb_batch* batch, const int32_t* h_q_len,
     h.page_size = batch->page_size;
     h.max_pages_per_seq = batch->max_pages_per_seq;
     h.num_sms = num_sms;
-    h.num_decode_items = (int32_t)dec.size();
-    h.num_chunk_items = (int32_t)chk.size();
+    h.num_decode_items = (int32_t)n_dec;
+    h.num_chunk_items = (int32_t)n_chk;
     h.num_partial_slots = n_slots;
     h.num_merge_counters = n_merge;
     h.decode_grid = part.grid;
@@ -735,13 +835,13 @@ hb_status hb_plan(const hb_batch* batch, const int32_t* h_q_len,
     h.ws_total = ws_total;
     h.plan_bytes = need_plan;
     uint8_t* hp = static_cast<uint8_t*>(h_plan);
-    std::memset(hp, 0, need_plan);
     std::memcpy(hp, &h, sizeof(h));
     uint8_t* items = hp + sizeof(PlanHeader);
-    if (!dec.empty()) std::memcpy(items, dec.data(), dec.size() * sizeof(DecodeItem));
-    if (!chk.empty())
-      std::memcpy(items + dec.size() * sizeof(DecodeItem), chk.data(), chk.size() * sizeof(ChunkItem));
-    std::memcpy(items + offsets_at, cta_off.data(), cta_off.size() * sizeof(int32_t));
+    if (n_dec) std::memcpy(items, ps.dec.data(), n_dec * sizeof(DecodeItem));
+    if (n_chk) std::memcpy(items + n_dec * sizeof(DecodeItem), ps.chk.data(), n_chk * sizeof(ChunkItem));
+    std::memcpy(items + offsets_at, ps.cta_off.data(), n_off * sizeof(int32_t));
+    const size_t used = offsets_at + n_off * sizeof(int32_t);
+    std::memset(items + used, 0, items_bytes - used);   // alignment padding
 
     if (d_workspace == nullptr) return ok();  // host plan only
     cudaStream_t st = static_cast<cudaStream_t>(stream);

@@ -81,13 +81,13 @@ inline bool partition_decode(int S, const int32_t* q_len, const int32_t* ctx, in
   r.pages_per_cta = per;
   r.pages_per_dynamic = n_dyn ? q : 0;
   const int64_t n_int = grid + n_dyn;
-  auto interval_of = [&](int64_t x) { return x < static_end ? x / per : grid + (x - static_end) / q; };
   auto ibegin = [&](int64_t c) { return c < grid ? c * per : static_end + (c - grid) * q; };
   auto iend = [&](int64_t c) {
     return std::min(total, c < grid ? (c + 1) * per : static_end + (c - grid + 1) * q);
   };
   for (int64_t b = 0; b <= n_int; ++b) offsets[b] = 0;
   int64_t pos = 0;   // start of the current row in the concatenation
+  int64_t c_pos = 0;  // the interval holding pos (intervals are consecutive and ascending)
   int k = 0;
   for (int i = 0; i < S; ++i) {
     const int32_t this_tok = tok;
@@ -97,7 +97,10 @@ inline bool partition_decode(int S, const int32_t* q_len, const int32_t* ctx, in
     const int64_t np = (ctx[i] + kPageSize - 1) / kPageSize - first;
     for (int blk = 0; blk < n_blocks; ++blk) {
       const int64_t a = pos, e = pos + np;
-      const int64_t c0 = interval_of(a), c1 = interval_of(e - 1);
+      while (iend(c_pos) <= a) ++c_pos;
+      int64_t c_last = c_pos;
+      while (iend(c_last) < e) ++c_last;
+      const int64_t c0 = c_pos, c1 = c_last;
       const int pieces = (int)(c1 - c0 + 1);
       const int slot = pieces > 1 ? r.n_slots : 0;
       const int merge_id = pieces > 1 ? r.n_merge : 0;

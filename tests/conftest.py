@@ -37,18 +37,22 @@ def pytest_terminal_summary(terminalreporter, exitstatus, config):
     if not rows:
         return
     per = {}
-    for test, mx, mean in rows:
-        a, b = per.get(test, (0.0, 0.0))
-        per[test] = (max(a, mx), max(b, mean))
+    for test, mx, mean, xmx, xmean in rows:
+        a = per.get(test, (0.0, 0.0, 0.0, 0.0))
+        per[test] = (max(a[0], mx), max(a[1], mean), max(a[2], xmx), max(a[3], xmean))
     tr = terminalreporter
     tr.write_sep("-", f"attention parity margins ({len(per)} tests, {len(rows)} checks)")
-    worst = sorted(per.items(), key=lambda kv: -kv[1][0] / mod.MAX_ABS)[:10]
-    for test, (mx, mean) in worst:
-        tr.write_line(f"max-abs {mx:.2e} ({100 * mx / mod.MAX_ABS:5.1f}% of bound)  "
-                      f"mean-abs {mean:.2e} ({100 * mean / mod.MEAN_ABS:5.1f}%)  {test}")
+    tr.write_line("of the bounds; in brackets the part beyond the exact answer's own bf16 rounding")
+    worst = sorted(per.items(), key=lambda kv: -kv[1][0])[:10]
+    for test, (mx, mean, xmx, xmean) in worst:
+        tr.write_line(f"max-abs {mx:.2e} {100 * mx / mod.MAX_ABS:5.1f}% [{100 * xmx / mod.MAX_ABS:5.1f}%]  "
+                      f"mean-abs {mean:.2e} {100 * mean / mod.MEAN_ABS:5.1f}% "
+                      f"[{100 * xmean / mod.MEAN_ABS:5.1f}%]  {test}")
     path = os.environ.get("HB_PARITY_LOG")
     if path:
         import json
         with open(path, "w") as f:
-            for test, (mx, mean) in sorted(per.items()):
-                f.write(json.dumps({"test": test, "max_abs": mx, "mean_abs": mean}) + "\n")
+            for test, (mx, mean, xmx, xmean) in sorted(per.items()):
+                f.write(json.dumps({"test": test, "max_abs": mx, "mean_abs": mean,
+                                    "max_abs_beyond_rounding": xmx,
+                                    "mean_abs_beyond_rounding": xmean}) + "\n")
