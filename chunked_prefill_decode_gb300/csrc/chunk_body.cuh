@@ -558,17 +558,17 @@ __device__ __forceinline__ void chunk_cta(const ChunkParams& p, const CUtensorMa
     // tiles, S_0/O_0 and S_1/O_1).  Every S tile passes through all eight
     // warps: warp w serves TMEM lanes 32 (w % 4) .. (its query rows) and
     // column half h = w / 4 (keys 64 h .. 64 h + 63 and head-dim columns
-    // h D / 2 ..).  Both halves read the whole row for its maximum, and warps
-    // w and w + 4 meet at named barrier 4 + w % 4 before either writes its P
-    // over the S columns.  P of keys 0-63 goes to S columns 0-31 and of keys
-    // 64-127 to columns 64-95.
+    // h D / 2 ..).  Each warp reads only its half of the row; warps w and
+    // w + 4 exchange their halves' maxima through shared memory at named
+    // barrier 4 + w % 4.  P of keys 0-63 goes to S columns 0-31 and of keys
+    // 64-127 to columns 64-95, each within the half that computed it.
     const int h = warp >> 2;
     const int wq = warp & 3;
     const int row = wq * 32 + lane;
     const uint32_t bar_pair = 4u + (uint32_t)wq;
     const uint32_t t_lane = tmem + ((uint32_t)(wq * 32) << 16);
     const float sl2 = p.scale_log2;
-    const int c_own = h * 64, c_oth = (1 - h) * 64;   // S columns: exponentiated / max only
+    const int c_own = h * 64;                         // this warp's S columns
     const int o_c0 = h * (D / 2);                     // head-dim columns of O
     constexpr int o_nc = D / 2;
     const int tok_local = row / g;
@@ -596,42 +596,63 @@ __device__ __forceinline__ void chunk_cta(const ChunkParams& p, const CUtensorMa
       const int lo_lim = win_lo == INT_MIN ? INT_MIN : win_lo - kbase;   // .. and lo_lim..
       const uint32_t s_col = t_lane + t * kChunkKeys;
       // tcgen05.ld / tcgen05.st are warp-collective: every lane executes
-      // each of them; rows that hold no query only change the arithmetic
-      uint32_t own[64], oth[64];
+      // each of them; rows that hold no query only change the arithmetic.
+      // This warp reads, and later overwrites with P, only its own 64
+      // columns of the row.
+      uint32_t own[64];
       tmem_ld32(s_col + c_own, own);
       tmem_ld32(s_col + c_own + 32, own + 32);
-      tmem_ld32(s_col + c_oth, oth);
-      tmem_ld32(s_col + c_oth + 32, oth + 32);
       tmem_ld_wait();
-      // both halves hold the row before either overwrites it; a failed wait
-      // ends the loop for both
-      if (!named_bar_and(bar_pair, 64, got_s)) { ok = false; break; }
       if (masked) {
-        const int lim_own = lim - c_own, lim_oth = lim - c_oth;
+        const int lim_own = lim - c_own;
         const int lo_own = lo_lim == INT_MIN ? INT_MIN : lo_lim - c_own;
-        const int lo_oth = lo_lim == INT_MIN ? INT_MIN : lo_lim - c_oth;
 #pragma unroll
-        for (int i = 0; i < 64; ++i) {
+        for (int i = 0; i < 64; ++i)
           if (i > lim_own || i < lo_own) own[i] = __float_as_uint(-INFINITY);
-          if (i > lim_oth || i < lo_oth) oth[i] = __float_as_uint(-INFINITY);
-        }
       }
-      float mxp[8];
+      // P = 2^(s c - m) as bf16 for this half's 64 keys, written over its
+      // first 32 columns.  It is computed with the running maximum m as it
+      // stands while the half's maximum is reduced in the same loop (a stale
+      // maximum is exact as long as it bounds s c - m by the threshold);
+      // dead rows and rows that have seen no key yet get P = 0.
+      const uint64_t c2 = pack_f32x2(sl2, sl2);
+      uint64_t lsum2[2];
+      float mxp[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+      auto half_exps = [&](float m_use, bool with_max) {
+        const float neg_m = (valid_row && m_use != -INFINITY) ? -m_use : -INFINITY;
+        const uint64_t nm2 = pack_f32x2(neg_m, neg_m);
+        lsum2[0] = lsum2[1] = pack_f32x2(0.f, 0.f);
 #pragma unroll
-      for (int e = 0; e < 8; ++e) mxp[e] = -INFINITY;
+        for (int q = 0; q < 2; ++q) {
+          uint32_t pk[16];
 #pragma unroll
-      for (int i = 0; i < 64; i += 8) {
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          mxp[e] = fmax3(mxp[e], __uint_as_float(own[i + 2 * e]), __uint_as_float(own[i + 2 * e + 1]));
-          mxp[4 + e] = fmax3(mxp[4 + e], __uint_as_float(oth[i + 2 * e]), __uint_as_float(oth[i + 2 * e + 1]));
+          for (int i = 0; i < 16; ++i) {
+            const int k = q * 32 + 2 * i;
+            if (with_max)
+              mxp[i & 3] = fmax3(mxp[i & 3], __uint_as_float(own[k]), __uint_as_float(own[k + 1]));
+            float x0, x1;
+            unpack_f32x2(fma_f32x2(pack_f32x2(__uint_as_float(own[k]), __uint_as_float(own[k + 1])),
+                                   c2, nm2), x0, x1);
+            const float e0 = fast_exp2(x0), e1 = fast_exp2(x1);
+            pk[i] = pack_bf16x2(e0, e1);
+            lsum2[i & 1] = add_f32x2(lsum2[i & 1], pack_f32x2(e0, e1));
+          }
+          tmem_st16(s_col + c_own + q * 16, pk);
         }
-      }
+      };
+      half_exps(m_run, true);
+      // the row's maximum: this half's and the partner warp's, exchanged
+      // through shared memory (two buffers, by key-tile parity, so that a
+      // warp running ahead never overwrites a value its partner has yet to
+      // read); a failed wait ends the loop for both warps
+      const float mx_own = fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3]));
+      float* xm = reinterpret_cast<float*>(sQ + C::kTileBytes + 4096) + (j & 1) * 2 * kChunkRows;
+      xm[h * kChunkRows + row] = mx_own;
+      if (!named_bar_and(bar_pair, 64, got_s)) { ok = false; break; }
+      const float mx = fmaxf(mx_own, xm[(1 - h) * kChunkRows + row]);
       float alpha = 1.f;
       bool resc = false;
       if (valid_row) {
-        const float mx = fmaxf(fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3])),
-                               fmaxf(fmaxf(mxp[4], mxp[5]), fmaxf(mxp[6], mxp[7])));
         const float m_new = fmaxf(m_run, mx * sl2);
         if (m_new > m_run + kRescaleThreshold) {
           alpha = fast_exp2(m_run - m_new);
@@ -639,26 +660,13 @@ __device__ __forceinline__ void chunk_cta(const ChunkParams& p, const CUtensorMa
           resc = true;
         }
       }
-      // P = 2^(s c - m) as bf16 for this half's 64 keys; dead rows and rows
-      // that have seen no key yet get P = 0
-      const float neg_m = (valid_row && m_run != -INFINITY) ? -m_run : -INFINITY;
-      const uint64_t c2 = pack_f32x2(sl2, sl2);
-      const uint64_t nm2 = pack_f32x2(neg_m, neg_m);
-      uint64_t lsum2[2] = {pack_f32x2(0.f, 0.f), pack_f32x2(0.f, 0.f)};
-#pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int k = q * 32 + 2 * i;
-          float x0, x1;
-          unpack_f32x2(fma_f32x2(pack_f32x2(__uint_as_float(own[k]), __uint_as_float(own[k + 1])),
-                                 c2, nm2), x0, x1);
-          const float e0 = fast_exp2(x0), e1 = fast_exp2(x1);
-          pk[i] = pack_bf16x2(e0, e1);
-          lsum2[i & 1] = add_f32x2(lsum2[i & 1], pack_f32x2(e0, e1));
-        }
-        tmem_st16(s_col + c_own + q * 16, pk);
+      // a row whose maximum moved past the threshold (every row on its
+      // first key tile, rarely later) needs P again from its new maximum:
+      // the warp recomputes all its rows (the others get the same values)
+      // once the first stores have landed
+      if (__any_sync(0xffffffffu, resc)) {
+        tmem_st_wait();
+        half_exps(m_run, false);
       }
       float lsp[4];
       unpack_f32x2(lsum2[0], lsp[0], lsp[1]);

