@@ -161,7 +161,7 @@ __device__ __forceinline__ void chunk_cta(const ChunkParams& p, const CUtensorMa
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&s_full[t], 1);
-      mbar_init(&p_full[t], inter ? 8 : 4);   // softmax warps per S tile
+      mbar_init(&p_full[t], 4);   // softmax warps per S tile (one arrival each)
       mbar_init(&o_done[t], 1);
     }
     mbar_init(mma_done, 1);
@@ -554,22 +554,24 @@ __device__ __forceinline__ void chunk_cta(const ChunkParams& p, const CUtensorMa
     }
   } else {
     // ------------------------------------------------------------ softmax (interleaved)
-    // One query tile; its S tiles come in two slots (the even and odd key
-    // tiles, S_0/O_0 and S_1/O_1).  Every S tile passes through all eight
-    // warps: warp w serves TMEM lanes 32 (w % 4) .. (its query rows) and
-    // column half h = w / 4 (keys 64 h .. 64 h + 63 and head-dim columns
-    // h D / 2 ..).  Each warp reads only its half of the row; warps w and
-    // w + 4 exchange their halves' maxima through shared memory at named
-    // barrier 4 + w % 4.  P of keys 0-63 goes to S columns 0-31 and of keys
-    // 64-127 to columns 64-95, each within the half that computed it.
-    const int h = warp >> 2;
+    // One query tile; its key tiles alternate between two slots: the even
+    // ones go to S_0/O_0 and warps 0-3, the odd ones to S_1/O_1 and warps
+    // 4-7, so the two slots' softmaxes run side by side while the tensor
+    // cores work on the other slot.  As in pair mode, thread = query row =
+    // TMEM lane and one thread holds the whole 128-column S row (one TMEM
+    // load wait per key tile); each slot keeps its own running maximum and
+    // row sum.  At the end warps w and w + 4 exchange their slots' (m, l)
+    // through shared memory and each writes half the head-dim columns of the
+    // merged O.  P of keys 0-63 goes to S columns 0-31 and of keys 64-127 to
+    // columns 64-95.
+    const int t = warp >> 2;                          // slot (and head-dim half at the end)
+    const int h = t;
     const int wq = warp & 3;
     const int row = wq * 32 + lane;
     const uint32_t bar_pair = 4u + (uint32_t)wq;
     const uint32_t t_lane = tmem + ((uint32_t)(wq * 32) << 16);
     const float sl2 = p.scale_log2;
-    const int c_own = h * 64;                         // this warp's S columns
-    const int o_c0 = h * (D / 2);                     // head-dim columns of O
+    const int o_c0 = h * (D / 2);                     // head-dim columns written at the end
     constexpr int o_nc = D / 2;
     const int tok_local = row / g;
     const bool valid_row = (row < g * tpt) && (tok_local < ntokA);
@@ -579,80 +581,44 @@ __device__ __forceinline__ void chunk_cta(const ChunkParams& p, const CUtensorMa
     // sliding window: row sees keys pos - W + 1 .. pos
     const int win_lo = p.window > 0 ? pos - p.window + 1 : INT_MIN;
     const int tile_lo = p.window > 0 ? off + it.tok0 + ntokA - p.window : INT_MIN;
-    // per slot: running maximum (scaled log2 units) and this half's row sum
-    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-    const int zero_slot = (n_all - 1) & 1;
+    const uint32_t s_col = t_lane + t * kChunkKeys;
+    const uint32_t o_col = t_lane + C::kOCol + t * D;
+    float m_run = -INFINITY;   // this slot's running maximum, scaled log2 units
+    float l_run = 0.f;
     bool ok = true;
-    for (int j = 0; j < n_all; ++j) {   // key tile jb + j, slot j & 1
-      const int t = j & 1;
-      const uint32_t u = (uint32_t)j >> 1;      // S tiles of slot t before this one
-      float m_run = t ? m1 : m0;
-      float l_run = t ? l1 : l0;
-      const bool got_s = mbar_wait(&s_full[t], u & 1u, abort_flag);
+    for (int j = t; j < n_all; j += 2) {   // key tile jb + j, this slot's u-th
+      const uint32_t u = (uint32_t)j >> 1;
+      // waits are made warp-uniform: a lane that gave up must not leave its
+      // warp's collective TMEM accesses
+      if (!__all_sync(0xffffffffu, mbar_wait(&s_full[t], u & 1u, abort_flag))) { ok = false; break; }
       tc_fence_after_sync();
       const int kbase = (jb + j) * kChunkKeys;
       const bool masked = kbase + kChunkKeys - 1 > min_pos || kbase < tile_lo;
       const int lim = pos - kbase;   // keys 0..lim of this tile are visible
       const int lo_lim = win_lo == INT_MIN ? INT_MIN : win_lo - kbase;   // .. and lo_lim..
-      const uint32_t s_col = t_lane + t * kChunkKeys;
-      // tcgen05.ld / tcgen05.st are warp-collective: every lane executes
-      // each of them; rows that hold no query only change the arithmetic.
-      // This warp reads, and later overwrites with P, only its own 64
-      // columns of the row.
-      uint32_t own[64];
-      tmem_ld32(s_col + c_own, own);
-      tmem_ld32(s_col + c_own + 32, own + 32);
+      uint32_t sr[kChunkKeys];
+#pragma unroll
+      for (int q = 0; q < kChunkKeys / 32; ++q) tmem_ld32(s_col + q * 32, sr + q * 32);
       tmem_ld_wait();
       if (masked) {
-        const int lim_own = lim - c_own;
-        const int lo_own = lo_lim == INT_MIN ? INT_MIN : lo_lim - c_own;
 #pragma unroll
-        for (int i = 0; i < 64; ++i)
-          if (i > lim_own || i < lo_own) own[i] = __float_as_uint(-INFINITY);
+        for (int i = 0; i < kChunkKeys; ++i)
+          if (i > lim || i < lo_lim) sr[i] = __float_as_uint(-INFINITY);
       }
-      // P = 2^(s c - m) as bf16 for this half's 64 keys, written over its
-      // first 32 columns.  It is computed with the running maximum m as it
-      // stands while the half's maximum is reduced in the same loop (a stale
-      // maximum is exact as long as it bounds s c - m by the threshold);
-      // dead rows and rows that have seen no key yet get P = 0.
-      const uint64_t c2 = pack_f32x2(sl2, sl2);
-      uint64_t lsum2[2];
-      float mxp[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-      auto half_exps = [&](float m_use, bool with_max) {
-        const float neg_m = (valid_row && m_use != -INFINITY) ? -m_use : -INFINITY;
-        const uint64_t nm2 = pack_f32x2(neg_m, neg_m);
-        lsum2[0] = lsum2[1] = pack_f32x2(0.f, 0.f);
+      float mxp[8];
 #pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          uint32_t pk[16];
+      for (int e = 0; e < 8; ++e) mxp[e] = -INFINITY;
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int k = q * 32 + 2 * i;
-            if (with_max)
-              mxp[i & 3] = fmax3(mxp[i & 3], __uint_as_float(own[k]), __uint_as_float(own[k + 1]));
-            float x0, x1;
-            unpack_f32x2(fma_f32x2(pack_f32x2(__uint_as_float(own[k]), __uint_as_float(own[k + 1])),
-                                   c2, nm2), x0, x1);
-            const float e0 = fast_exp2(x0), e1 = fast_exp2(x1);
-            pk[i] = pack_bf16x2(e0, e1);
-            lsum2[i & 1] = add_f32x2(lsum2[i & 1], pack_f32x2(e0, e1));
-          }
-          tmem_st16(s_col + c_own + q * 16, pk);
-        }
-      };
-      half_exps(m_run, true);
-      // the row's maximum: this half's and the partner warp's, exchanged
-      // through shared memory (two buffers, by key-tile parity, so that a
-      // warp running ahead never overwrites a value its partner has yet to
-      // read); a failed wait ends the loop for both warps
-      const float mx_own = fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3]));
-      float* xm = reinterpret_cast<float*>(sQ + C::kTileBytes + 4096) + (j & 1) * 2 * kChunkRows;
-      xm[h * kChunkRows + row] = mx_own;
-      if (!named_bar_and(bar_pair, 64, got_s)) { ok = false; break; }
-      const float mx = fmaxf(mx_own, xm[(1 - h) * kChunkRows + row]);
+      for (int i = 0; i < kChunkKeys; i += 16) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          mxp[e] = fmax3(mxp[e], __uint_as_float(sr[i + 2 * e]), __uint_as_float(sr[i + 2 * e + 1]));
+      }
       float alpha = 1.f;
       bool resc = false;
       if (valid_row) {
+        const float mx = fmaxf(fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3])),
+                               fmaxf(fmaxf(mxp[4], mxp[5]), fmaxf(mxp[6], mxp[7])));
         const float m_new = fmaxf(m_run, mx * sl2);
         if (m_new > m_run + kRescaleThreshold) {
           alpha = fast_exp2(m_run - m_new);
@@ -660,26 +626,32 @@ __device__ __forceinline__ void chunk_cta(const ChunkParams& p, const CUtensorMa
           resc = true;
         }
       }
-      // a row whose maximum moved past the threshold (every row on its
-      // first key tile, rarely later) needs P again from its new maximum:
-      // the warp recomputes all its rows (the others get the same values)
-      // once the first stores have landed
-      if (__any_sync(0xffffffffu, resc)) {
-        tmem_st_wait();
-        half_exps(m_run, false);
+      // P = 2^(s c - m) as bf16; dead rows and rows that have seen no key
+      // yet get P = 0
+      const float neg_m = (valid_row && m_run != -INFINITY) ? -m_run : -INFINITY;
+      const uint64_t c2 = pack_f32x2(sl2, sl2);
+      const uint64_t nm2 = pack_f32x2(neg_m, neg_m);
+      uint64_t lsum2[2] = {pack_f32x2(0.f, 0.f), pack_f32x2(0.f, 0.f)};
+#pragma unroll
+      for (int q = 0; q < kChunkKeys / 32; ++q) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          float x0, x1;
+          unpack_f32x2(fma_f32x2(pack_f32x2(__uint_as_float(sr[q * 32 + 2 * i]),
+                                            __uint_as_float(sr[q * 32 + 2 * i + 1])),
+                                 c2, nm2), x0, x1);
+          const float e0 = fast_exp2(x0), e1 = fast_exp2(x1);
+          pk[i] = pack_bf16x2(e0, e1);
+          lsum2[i & 1] = add_f32x2(lsum2[i & 1], pack_f32x2(e0, e1));
+        }
+        tmem_st16(s_col + (q >> 1) * 64 + (q & 1) * 16, pk);
       }
       float lsp[4];
       unpack_f32x2(lsum2[0], lsp[0], lsp[1]);
       unpack_f32x2(lsum2[1], lsp[2], lsp[3]);
       if (valid_row) l_run = l_run * alpha + ((lsp[0] + lsp[1]) + (lsp[2] + lsp[3]));
-      if (t) {
-        m1 = m_run;
-        l1 = l_run;
-      } else {
-        m0 = m_run;
-        l0 = l_run;
-      }
-      if (jb + j == T - 1 && t == zero_slot) {
+      if (jb + j == T - 1) {
         // the last page's slots past the context were never written (its
         // TMA box brings them in as they are): clear those V rows before
         // the first PV that reads this tile, so that P = 0 never meets a NaN
@@ -687,11 +659,10 @@ __device__ __forceinline__ void chunk_cta(const ChunkParams& p, const CUtensorMa
         const int end_bad = min(kChunkKeys, ((ctx + kPageSize - 1) / kPageSize) * kPageSize - kbase);
         if (first_bad < end_bad) {
           const int s = j % NV;
-          const bool got_v = mbar_wait(&v_full[s], (uint32_t)(j / NV) & 1u, abort_flag);
-          if (!named_bar_and(bar_pair, 64, got_v)) { ok = false; break; }
+          if (!__all_sync(0xffffffffu, mbar_wait(&v_full[s], (uint32_t)(j / NV) & 1u, abort_flag))) { ok = false; break; }
           uint8_t* vt = sV + s * C::kTileBytes;
           const int n_units = (end_bad - first_bad) * CH * 8;
-          for (int e = (int)threadIdx.x; e < n_units; e += 2 * kChunkRows) {
+          for (int e = row; e < n_units; e += kChunkRows) {
             const int key = first_bad + e / (CH * 8);
             const int rem = e % (CH * 8);
             *reinterpret_cast<uint4*>(vt + (rem >> 3) * 16384 + key * 128 + (rem & 7) * 16) =
@@ -701,24 +672,22 @@ __device__ __forceinline__ void chunk_cta(const ChunkParams& p, const CUtensorMa
         }
       }
       // O_t is stable here (slot t's previous PV completed before its S was
-      // ready); each half rescales its own head-dim columns
+      // ready)
       if (u > 0 && __any_sync(0xffffffffu, resc)) {
         const float f = resc ? alpha : 1.f;
-        const uint32_t oc = t_lane + C::kOCol + t * D + o_c0;
 #pragma unroll 1
-        for (int q = 0; q < o_nc / 32; ++q) {
+        for (int q = 0; q < D / 32; ++q) {
           uint32_t orow[32];
-          tmem_ld32(oc + q * 32, orow);
+          tmem_ld32(o_col + q * 32, orow);
           tmem_ld_wait();
 #pragma unroll
           for (int i = 0; i < 32; ++i) orow[i] = __float_as_uint(__uint_as_float(orow[i]) * f);
-          tmem_st32(oc + q * 32, orow);
+          tmem_st32(o_col + q * 32, orow);
         }
       }
       tmem_st_wait();
       tc_fence_before_sync();
-      // one arrival per warp: the barrier completes after 4 (pair) or 8
-      // (interleaved) arrivals instead of one per thread
+      // one arrival per warp: the barrier completes after the slot's 4
       __syncwarp();
       if (lane == 0) mbar_arrive(&p_full[t]);
     }
@@ -727,23 +696,23 @@ __device__ __forceinline__ void chunk_cta(const ChunkParams& p, const CUtensorMa
     bool have_o = ok && mbar_wait(&o_done[0], 0u, abort_flag);
     if (n_all > 1) have_o = have_o && mbar_wait(&o_done[1], 0u, abort_flag);
     tc_fence_after_sync();
-    // row sums over both column halves, through the second Q tile's room
+    // the slots' (m, l) of every row, through the second Q tile's room
     // (unused with one query tile)
     float* xl = reinterpret_cast<float*>(sQ + C::kTileBytes);
-    xl[(h * 2 + 0) * kChunkRows + row] = l0;
-    xl[(h * 2 + 1) * kChunkRows + row] = l1;
+    xl[(t * 2 + 0) * kChunkRows + row] = m_run;
+    xl[(t * 2 + 1) * kChunkRows + row] = l_run;
     have_o = named_bar_and(bar_pair, 64, have_o);
-    const float l_tot0 = l0 + xl[((1 - h) * 2 + 0) * kChunkRows + row];
-    const float l_tot1 = l1 + xl[((1 - h) * 2 + 1) * kChunkRows + row];
+    const float m0 = xl[0 * kChunkRows + row], l0 = xl[1 * kChunkRows + row];
+    const float m1 = xl[2 * kChunkRows + row], l1 = xl[3 * kChunkRows + row];
     // the two slots merge: O = w0 O_0 + w1 O_1 relative to 2^m_fin, l_fin
     // likewise
     const bool merge_slots = n_all > 1;
-    float m_fin = m0, l_fin = l_tot0, w0 = 1.f, w1 = 0.f;
+    float m_fin = m0, l_fin = l0, w0 = 1.f, w1 = 0.f;
     if (merge_slots) {
       m_fin = fmaxf(m0, m1);
       w0 = (m0 == -INFINITY) ? 0.f : fast_exp2(m0 - m_fin);
       w1 = (m1 == -INFINITY) ? 0.f : fast_exp2(m1 - m_fin);
-      l_fin = w0 * l_tot0 + w1 * l_tot1;
+      l_fin = w0 * l0 + w1 * l1;
     }
     // 32 head-dim columns c0 .. c0 + 31 of the final O (warp-collective)
     auto load_o = [&](int c0, uint32_t (&o)[32]) {
