@@ -37,7 +37,8 @@ cudaError_t launch_attention(const DecodeParams& dec, int decode_grid, const Chu
                              int head_dim, const CUtensorMap& dec_k, const CUtensorMap& dec_v,
                              const CUtensorMap& chunk_q, const CUtensorMap& chunk_k,
                              const CUtensorMap& chunk_v, const void* k_cache,
-                             const void* v_cache, cudaStream_t stream, bool early);
+                             const void* v_cache, cudaStream_t stream, bool early,
+                             bool pairs_only);
 }  // namespace hb
 
 using namespace hb;
@@ -575,28 +576,29 @@ hb_status hb_plan(const hb_batch* batch, const int32_t* h_q_len,
     // allocates nothing
     PlanScratch& ps = plan_scratch();
 
-    // ---- chunk items: rows with q_len > 1, (kv head, query tile)
+    // ---- chunk items: rows with q_len > 1, (kv head, query tile or pair of
+    // query tiles)
     const int tpt = kChunkRows / g;
     int64_t n_tiles_total = 0;
     for (int i = 0; i < S; ++i)
       if (h_q_len[i] > 1) n_tiles_total += (int64_t)((h_q_len[i] + tpt - 1) / tpt) * Hkv;
-    const int tiles_per_item = (n_tiles_total >= 2LL * num_sms) ? 2 : 1;
-    const int item_tokens = tiles_per_item * tpt;
-    size_t n_raw = 0;
-    for (int i = 0; i < S; ++i)
-      if (h_q_len[i] > 1) n_raw += (size_t)((h_q_len[i] + item_tokens - 1) / item_tokens) * Hkv;
-    ps.raw.resize(n_raw);
     auto key_tiles = [](const ChunkItem& c) { return c.kv_tiles - c.kv_begin; };
-    int key_max = 0;
-    {
+    // the items of one layout (tpi query tiles per item) into ps.chk,
+    // longest first
+    auto build_items = [&](int tpi) {
+      const int item_tokens = tpi * tpt;
+      size_t n_raw = 0;
+      for (int i = 0; i < S; ++i)
+        if (h_q_len[i] > 1) n_raw += (size_t)((h_q_len[i] + item_tokens - 1) / item_tokens) * Hkv;
+      ps.raw.resize(n_raw);
+      int key_max = 0;
       size_t k = 0;
       int32_t q0 = 0;
       for (int i = 0; i < S; q0 += h_q_len[i], ++i) {
         if (h_q_len[i] == 1) continue;
         const int off = h_context_len[i] - h_q_len[i];
-        // an item is a pair of query tiles (2 * tokens_per_tile tokens) that
-        // share every K/V tile when there are enough of them to fill the GPU,
-        // else a single tile (more CTAs); the last item of a row may be short
+        // the last item of a row may be short (a pair's second tile short
+        // or empty)
         for (int kvh = 0; kvh < Hkv; ++kvh)
           for (int t0 = 0; t0 < h_q_len[i]; t0 += item_tokens) {
             ChunkItem c{};
@@ -615,9 +617,9 @@ hb_status hb_plan(const hb_batch* batch, const int32_t* h_q_len,
             ps.raw[k++] = c;
           }
       }
-    }
-    // longest first (a stable counting sort on the key-tile count)
-    counting_sort_desc(ps.raw, ps.chk, ps.count, key_max, key_tiles);
+      // longest first (a stable counting sort on the key-tile count)
+      counting_sort_desc(ps.raw, ps.chk, ps.count, key_max, key_tiles);
+    };
 
     // ---- cost model, in microseconds, from rates measured on GB300.  The
     // attention kernel runs decode CTAs and chunk CTAs side by side (one CTA
@@ -626,14 +628,14 @@ hb_status hb_plan(const hb_batch* batch, const int32_t* h_q_len,
     // stream rate); everything ends no earlier than (chunk work + G x decode
     // time) / SMs, nor before the longest chunk item.  That estimate is flat
     // over a range of G whose ends it knows only roughly, so the middle of
-    // the range within 2% of the best is taken.
+    // the range within 2% of the best is taken.  A pair of query tiles
+    // shares its page gather, so it costs 1.6x one tile, not 2x.
     constexpr double kHbmBytesPerUs = 7.0e6;      // whole-GPU HBM stream
     constexpr double kSmBytesPerUs = 8.5e4;       // one SM's stream ceiling
     constexpr double kPairTileUs = 2.0;           // 2-tile item x one key tile
-    constexpr double kSingleTileUs = 1.1;         // 1-tile item x one key tile
+    constexpr double kSingleTileUs = 1.25;        // 1-tile item x one key tile
     constexpr double kPieceUs = 3.0;              // extra cost of one split piece
     constexpr int kMinPieceTiles = 4;             // key tiles per split piece (min)
-    const double tile_us = tiles_per_item == 2 ? kPairTileUs : kSingleTileUs;
     double decode_bytes = 0.0;
     for (int i = 0; i < S; ++i)
       if (h_q_len[i] == 1)
@@ -666,15 +668,16 @@ hb_status hb_plan(const hb_batch* batch, const int32_t* h_q_len,
       return std::max(1, std::min(n, kv / kMinPieceTiles));
     };
 
-    // ---- split-KV: when single query tiles are too few to fill the SMs, a
-    // tile's key range may be cut into up to kMaxChunkSplits pieces (each its
-    // own CTA, merged by the last to finish).  The piece length is the one
-    // with the earliest estimated end among a few candidates (no split
-    // included); the end is that of CTAs started in index order on the SM
-    // that frees up first, the G decode CTAs first, holding their SMs for
-    // the decode time (simulate_dispatch).
-    int best_L = 0;   // 0: no split
-    if (tiles_per_item == 1 && !ps.chk.empty()) {
+    // ---- split-KV: when the items are too few to fill the SMs, an item's
+    // key range may be cut into up to kMaxChunkSplits pieces (each its own
+    // CTA, merged by the last to finish).  The piece length is the one with
+    // the earliest estimated end among a few candidates (no split included);
+    // the end is that of CTAs started in index order on the SM that frees up
+    // first, the G decode CTAs first, holding their SMs for the decode time
+    // (simulate_dispatch).  Returns that end; *out_L = 0 for no split.
+    auto search_split = [&](double tile_us, int* out_L) -> double {
+      *out_L = 0;
+      if (ps.chk.empty()) return 0.0;
       const int kmax = key_tiles(ps.chk.front());
       double best_t = 1e300;
       int prev_L = -1;
@@ -689,7 +692,7 @@ hb_status hb_plan(const hb_batch* batch, const int32_t* h_q_len,
         double sum = 0.0, mx = 0.0;
         for (const ChunkItem& c : ps.chk) {
           const int kv = key_tiles(c);
-          const int np = pieces_of(kv, L);
+          const int np = n == 1 ? 1 : pieces_of(kv, L);
           for (int k = 0; k < np; ++k) {
             const int len = (k + 1) * kv / np - k * kv / np;
             const double d = len * tile_us + (np > 1 ? kPieceUs : 0.0);
@@ -712,10 +715,35 @@ hb_status hb_plan(const hb_batch* batch, const int32_t* h_q_len,
         const double t = simulate_dispatch(ps, num_sms, G, G > 0 ? t_decode(G) : 0.0);
         if (t < 0.97 * best_t) {   // a split has to pay for itself clearly
           best_t = t;
-          best_L = n == 1 ? 0 : L;
+          *out_L = n == 1 ? 0 : L;
         }
       }
+      return best_t;
+    };
+    // Layout: pairs of query tiles, which share every K/V tile they gather,
+    // or -- when the tiles are too few to fill the GPU twice -- whichever of
+    // pairs and single tiles (each with its best split) ends earlier.
+    int tiles_per_item = 2, best_L = 0;
+    ps.chk.clear();
+    if (n_tiles_total > 0) {
+      double t_single = 1e300;
+      int L_single = 0;
+      if (n_tiles_total < 2LL * num_sms) {
+        build_items(1);
+        t_single = search_split(kSingleTileUs, &L_single);
+      }
+      build_items(2);
+      int L_pair = 0;
+      const double t_pair = search_split(kPairTileUs, &L_pair);
+      if (t_single < t_pair) {
+        tiles_per_item = 1;
+        best_L = L_single;
+        build_items(1);
+      } else {
+        best_L = L_pair;
+      }
     }
+    const double tile_us = tiles_per_item == 2 ? kPairTileUs : kSingleTileUs;
     int n_cslots = 0, n_cmerge = 0;
     if (best_L > 0) {
       ps.raw.clear();
@@ -724,6 +752,8 @@ hb_status hb_plan(const hb_batch* batch, const int32_t* h_q_len,
         const int kv = key_tiles(c);
         const int kb0 = c.kv_begin;
         const int np = pieces_of(kv, best_L);
+        // a split pair keeps one partial state per tile and piece
+        const int tiles = c.ntok > tpt ? 2 : 1;
         c.n_splits = np;
         c.slot = np > 1 ? n_cslots : 0;
         c.merge_id = np > 1 ? n_cmerge : 0;
@@ -735,7 +765,7 @@ hb_status hb_plan(const hb_batch* batch, const int32_t* h_q_len,
           ps.raw.push_back(c);
         }
         if (np > 1) {
-          n_cslots += np;
+          n_cslots += np * tiles;
           n_cmerge += 1;
         }
       }
@@ -819,6 +849,12 @@ hb_status hb_plan(const hb_batch* batch, const int32_t* h_q_len,
     h.num_merge_counters = n_merge;
     h.decode_grid = part.grid;
     h.num_decode_dynamic = part.n_dynamic;
+    {
+      bool pairs = n_chk > 0;
+      for (size_t i = 0; pairs && i < n_chk; ++i)
+        pairs = ps.chk[i].ntok > tpt && ps.chk[i].n_splits == 1;
+      h.chunk_pairs_only = pairs ? 1 : 0;
+    }
     h.ws_decode_offsets = offsets_at;
     h.decode_kvh_block = kvhb;
     h.chunk_tokens_per_tile = tpt;
@@ -977,7 +1013,8 @@ hb_status hb_attention(const hb_batch* batch, const void* h_plan, const void* q,
       const bool early = follows_own_append(stream, batch, k_cache, v_cache);
       LaunchTimer t(1, st);
       cudaError_t e = launch_attention(dp, h.decode_grid, cp, D, dec_k, dec_v, chunk_q, chunk_k,
-                                       chunk_v, k_cache, v_cache, st, early);
+                                       chunk_v, k_cache, v_cache, st, early,
+                                       h.chunk_pairs_only != 0);
       t.done();
       if (e != cudaSuccess) return cuda_fail(e, "attention launch");
       note_launch(stream, LastLaunch{});

@@ -39,7 +39,7 @@ struct AttnParams {
   int32_t early;
 };
 
-template <int D>
+template <int D, bool kPairs>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     attention_kernel(const AttnParams p, const __grid_constant__ CUtensorMap dec_k,
                      const __grid_constant__ CUtensorMap dec_v,
@@ -58,7 +58,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   if ((int)blockIdx.x < p.decode_grid)
     decode_cta<D>(p.dec, p.dl, dec_k, dec_v, smem, blockIdx.x);
   else
-    chunk_cta<D>(p.chk, chunk_q, chunk_k, chunk_v, p.k_cache, p.v_cache, smem, blockIdx.x - p.decode_grid);
+    chunk_cta<D, kPairs>(p.chk, chunk_q, chunk_k, chunk_v, p.k_cache, p.v_cache, smem,
+                         blockIdx.x - p.decode_grid);
 }
 
 // Dynamic shared memory of the attention kernel for this geometry.
@@ -71,11 +72,15 @@ int attention_smem_bytes(int head_dim, int kvh_block, int group) {
 // Launch decode_grid decode CTAs followed by one CTA per chunk item.  Either
 // part may be empty (dec.num_items == 0: no decode CTA).  dec.kvh_block and
 // dec.group must be set in every case (they size the shared memory).
+// pairs_only: every chunk item is an unsplit pair of query tiles, and the
+// kernel instantiation without the single-tile and split paths runs (the
+// pair loop compiles to faster code on its own).
 cudaError_t launch_attention(const DecodeParams& dec, int decode_grid, const ChunkParams& chk,
                              int head_dim, const CUtensorMap& dec_k, const CUtensorMap& dec_v,
                              const CUtensorMap& chunk_q, const CUtensorMap& chunk_k,
                              const CUtensorMap& chunk_v, const void* k_cache,
-                             const void* v_cache, cudaStream_t stream, bool early) {
+                             const void* v_cache, cudaStream_t stream, bool early,
+                             bool pairs_only) {
   AttnParams p{};
   p.early = early ? 1 : 0;
   p.dec = dec;
@@ -88,39 +93,33 @@ cudaError_t launch_attention(const DecodeParams& dec, int decode_grid, const Chu
   const int grid = p.decode_grid + chk.num_items;
   if (grid == 0) return cudaSuccess;
   const int smem = attention_smem_bytes(head_dim, dec.kvh_block, dec.group);
+  using Kernel = void (*)(const AttnParams, const __grid_constant__ CUtensorMap,
+                          const __grid_constant__ CUtensorMap, const __grid_constant__ CUtensorMap,
+                          const __grid_constant__ CUtensorMap, const __grid_constant__ CUtensorMap);
+  const int which = (head_dim == 128 ? 2 : 0) + (pairs_only ? 1 : 0);
+  const Kernel kernels[4] = {attention_kernel<64, false>, attention_kernel<64, true>,
+                             attention_kernel<128, false>, attention_kernel<128, true>};
+  const Kernel kernel = kernels[which];
   // setmaxnreg.inc waits until the block's register pool holds what it asks
   // for; the chunk CTAs' split assumes the launch allocation of
   // kChunkLaunchRegs per thread, so a build that allocated fewer is refused
   // here instead of launched
   {
-    static std::atomic<int> regs[2] = {{0}, {0}};   // per head dim, once known
-    std::atomic<int>& known = regs[head_dim == 128 ? 1 : 0];
-    int n = known.load(std::memory_order_relaxed);
+    static std::atomic<int> regs[4] = {{0}, {0}, {0}, {0}};   // per instantiation, once known
+    int n = regs[which].load(std::memory_order_relaxed);
     if (n == 0) {
       cudaFuncAttributes fa{};
-      const cudaError_t ea = head_dim == 128 ? cudaFuncGetAttributes(&fa, attention_kernel<128>)
-                                             : cudaFuncGetAttributes(&fa, attention_kernel<64>);
+      const cudaError_t ea = cudaFuncGetAttributes(&fa, kernel);
       if (ea != cudaSuccess) return ea;
       n = fa.numRegs;
-      known.store(n, std::memory_order_relaxed);
+      regs[which].store(n, std::memory_order_relaxed);
     }
     if (n < kChunkLaunchRegs) return cudaErrorInvalidConfiguration;
   }
-  cudaError_t e;
-  if (head_dim == 128) {
-    e = cudaFuncSetAttribute(attention_kernel<128>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    e = launch_serialized(attention_kernel<128>, grid, kAttnThreads, smem, stream, p, dec_k, dec_v,
-                          chunk_q, chunk_k, chunk_v);
-  } else {
-    e = cudaFuncSetAttribute(attention_kernel<64>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    e = launch_serialized(attention_kernel<64>, grid, kAttnThreads, smem, stream, p, dec_k, dec_v,
-                          chunk_q, chunk_k, chunk_v);
-  }
-  return e;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  return launch_serialized(kernel, grid, kAttnThreads, smem, stream, p, dec_k, dec_v, chunk_q,
+                           chunk_k, chunk_v);
 }
 
 }  // namespace hb

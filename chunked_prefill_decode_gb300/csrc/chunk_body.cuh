@@ -98,9 +98,71 @@ struct ChunkCfg {
 static_assert(ChunkCfg<128>::kSmemBytes <= 227 * 1024, "chunk smem (D=128)");
 static_assert(ChunkCfg<64>::kSmemBytes <= 227 * 1024, "chunk smem (D=64)");
 
+// The last piece of a split key range merges the pieces' partial states of
+// one query row: o = sum_k 2^(m_k - M) o_k / sum_k 2^(m_k - M) l_k over the
+// ns pieces (M their largest m), for head-dim columns c0 .. c0 + nc - 1, and
+// stores the row (if it holds a query) as bf16 at out_row.  o0 / ml0 point at
+// this row in the first piece's slot of part_o ([slot][D][128 rows]) and
+// part_ml ([slot][2][128 rows]).  A piece that saw no key of the row has
+// m = -inf and weight 0 (its O is not read).  The partial states were
+// written by other CTAs: read through L2.  Each piece's block of BW columns
+// is loaded in one round (BW loads in flight per thread), so the merge costs
+// about one L2 round trip per piece and block.
+template <int D, int BW>
+__device__ __forceinline__ void merge_pieces(const float* o0, const float* ml0, int ns, int c0,
+                                             int nc, bool valid_row, uint16_t* out_row) {
+  static_assert(BW % 8 == 0 && BW <= 64, "merge block width");
+  float mk[kMaxChunkSplits];
+  float mmax = -INFINITY;
+#pragma unroll
+  for (int k = 0; k < kMaxChunkSplits; ++k) {
+    mk[k] = k < ns ? __ldcg(ml0 + (size_t)k * 2 * kChunkRows) : -INFINITY;
+    mmax = fmaxf(mmax, mk[k]);
+  }
+  float lsum = 0.f;
+#pragma unroll
+  for (int k = 0; k < kMaxChunkSplits; ++k) {
+    mk[k] = (mk[k] == -INFINITY) ? 0.f : fast_exp2(mk[k] - mmax);   // now the weight
+    if (mk[k] != 0.f) lsum += mk[k] * __ldcg(ml0 + (size_t)k * 2 * kChunkRows + kChunkRows);
+  }
+  const float inv = (lsum > 0.f) ? 1.f / lsum : 0.f;
+  for (int cb = c0; cb < c0 + nc; cb += BW) {
+    float acc[BW];
+#pragma unroll
+    for (int i = 0; i < BW; ++i) acc[i] = 0.f;
+#pragma unroll 1
+    for (int k = 0; k < ns; ++k) {
+      float wk = 0.f;
+#pragma unroll
+      for (int x = 0; x < kMaxChunkSplits; ++x)
+        if (x == k) wk = mk[x];
+      if (wk == 0.f) continue;
+      const float* src = o0 + ((size_t)k * D + cb) * kChunkRows;
+      float v[BW];
+#pragma unroll
+      for (int i = 0; i < BW; ++i) v[i] = __ldcg(src + (size_t)i * kChunkRows);
+#pragma unroll
+      for (int i = 0; i < BW; ++i) acc[i] += wk * v[i];
+    }
+    if (valid_row) {
+#pragma unroll
+      for (int i = 0; i < BW; i += 8) {
+        uint4 pk4;
+        pk4.x = pack_bf16x2(acc[i + 0] * inv, acc[i + 1] * inv);
+        pk4.y = pack_bf16x2(acc[i + 2] * inv, acc[i + 3] * inv);
+        pk4.z = pack_bf16x2(acc[i + 4] * inv, acc[i + 5] * inv);
+        pk4.w = pack_bf16x2(acc[i + 6] * inv, acc[i + 7] * inv);
+        *reinterpret_cast<uint4*>(out_row + cb + i) = pk4;
+      }
+    }
+  }
+}
+
 // Body of one chunk CTA working on item `item`; `smem` is the 1024-byte-
-// aligned dynamic shared memory.
-template <int D>
+// aligned dynamic shared memory.  kPairs: the launch holds only unsplit
+// pairs of query tiles (the plan says so), and the single-tile and split
+// paths are left out of this instantiation.
+template <int D, bool kPairs>
 __device__ __forceinline__ void chunk_cta(const ChunkParams& p, const CUtensorMap& qmap,
                                           const CUtensorMap& kmap, const CUtensorMap& vmap,
                                           const uint16_t* __restrict__ k_cache,
@@ -147,7 +209,7 @@ __device__ __forceinline__ void chunk_cta(const ChunkParams& p, const CUtensorMa
   const int nA = TA - jb;
   // one query tile: the two softmax groups take alternate key tiles of it
   // (even: S_0/O_0, odd: S_1/O_1) and merge their states at the end
-  const bool inter = !hasB;
+  const bool inter = !kPairs && !hasB;
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
@@ -528,27 +590,83 @@ __device__ __forceinline__ void chunk_cta(const ChunkParams& p, const CUtensorMa
       __syncwarp();
       if (lane == 0) mbar_arrive(&p_full[t]);
     }
-    // epilogue: O / l -> bf16
-    if (__all_sync(0xffffffffu, n_t > 0 && ok && mbar_wait(&o_done[t], 0u, abort_flag))) {
-      tc_fence_after_sync();
-      const float inv = (l_run > 0.f) ? 1.f / l_run : 0.f;
-      uint16_t* dst = p.out + ((size_t)(q0 + tok_rel) * p.num_q_heads +
-                               (size_t)it.kv_head * g + (row % g)) * D;
+    // epilogue.  t_ok: this tile's waits held (a tile with no key tile in
+    // this item -- tile A of a split piece past its own last key -- has
+    // nothing to wait for); have_o: its O is complete
+    const bool t_ok =
+        __all_sync(0xffffffffu, ok && (n_t <= 0 || mbar_wait(&o_done[t], 0u, abort_flag)));
+    const bool have_o = t_ok && n_t > 0;
+    if (have_o) tc_fence_after_sync();
+    if (kPairs || it.n_splits == 1) {
+      // O / l -> bf16
+      if (have_o) {
+        const float inv = (l_run > 0.f) ? 1.f / l_run : 0.f;
+        uint16_t* dst = p.out + ((size_t)(q0 + tok_rel) * p.num_q_heads +
+                                 (size_t)it.kv_head * g + (row % g)) * D;
 #pragma unroll 1
-      for (int q = 0; q < D / 32; ++q) {
-        uint32_t orow[32];
-        tmem_ld32(o_col + q * 32, orow);
-        tmem_ld_wait();
-        if (valid_row) {
+        for (int q = 0; q < D / 32; ++q) {
+          uint32_t orow[32];
+          tmem_ld32(o_col + q * 32, orow);
+          tmem_ld_wait();
+          if (valid_row) {
 #pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            uint4 pk4;
-            pk4.x = pack_bf16x2(__uint_as_float(orow[v * 8 + 0]) * inv, __uint_as_float(orow[v * 8 + 1]) * inv);
-            pk4.y = pack_bf16x2(__uint_as_float(orow[v * 8 + 2]) * inv, __uint_as_float(orow[v * 8 + 3]) * inv);
-            pk4.z = pack_bf16x2(__uint_as_float(orow[v * 8 + 4]) * inv, __uint_as_float(orow[v * 8 + 5]) * inv);
-            pk4.w = pack_bf16x2(__uint_as_float(orow[v * 8 + 6]) * inv, __uint_as_float(orow[v * 8 + 7]) * inv);
-            *reinterpret_cast<uint4*>(dst + q * 32 + v * 8) = pk4;
+            for (int v = 0; v < 4; ++v) {
+              uint4 pk4;
+              pk4.x = pack_bf16x2(__uint_as_float(orow[v * 8 + 0]) * inv, __uint_as_float(orow[v * 8 + 1]) * inv);
+              pk4.y = pack_bf16x2(__uint_as_float(orow[v * 8 + 2]) * inv, __uint_as_float(orow[v * 8 + 3]) * inv);
+              pk4.z = pack_bf16x2(__uint_as_float(orow[v * 8 + 4]) * inv, __uint_as_float(orow[v * 8 + 5]) * inv);
+              pk4.w = pack_bf16x2(__uint_as_float(orow[v * 8 + 6]) * inv, __uint_as_float(orow[v * 8 + 7]) * inv);
+              *reinterpret_cast<uint4*>(dst + q * 32 + v * 8) = pk4;
+            }
           }
+        }
+      }
+    } else {
+      // one piece of a split key range of the pair: each tile publishes its
+      // unnormalised O and (m, l) to its own slot (tile A's pieces first,
+      // then tile B's; a tile with no key tile here publishes m = -inf), and
+      // the last piece to arrive merges every piece of both tiles,
+      // o = sum_k 2^(m_k - M) o_k / sum_k 2^(m_k - M) l_k
+      const int ns = it.n_splits;
+      const size_t tile_slot0 = (size_t)it.slot + (size_t)t * ns;
+      const size_t slot = tile_slot0 + it.split;
+      float* po = p.part_o + slot * D * kChunkRows + row;
+      float* pml = p.part_ml + slot * 2 * kChunkRows + row;
+      if (have_o) {
+#pragma unroll 1
+        for (int q = 0; q < D / 32; ++q) {
+          uint32_t orow[32];
+          tmem_ld32(o_col + q * 32, orow);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) po[(size_t)(q * 32 + i) * kChunkRows] = __uint_as_float(orow[i]);
+        }
+        pml[0] = m_run;
+        pml[kChunkRows] = l_run;
+      } else {
+        pml[0] = -INFINITY;
+        pml[kChunkRows] = 0.f;
+      }
+      __threadfence();
+      // all 256 softmax threads reach these barriers; a piece whose waits
+      // gave up does not arrive (the error word reports it)
+      volatile int* last_flag = reinterpret_cast<volatile int*>(smem + C::kMiscOff + 32);
+      if (named_bar_and(2, 2 * kChunkRows, t_ok)) {
+        if (threadIdx.x == 0) {
+          __threadfence();
+          const int old = atomicAdd(&p.counters[it.merge_id], 1);
+          __threadfence();
+          *last_flag = (old == ns - 1) ? 1 : 0;
+        }
+        named_bar_sync(2, 2 * kChunkRows);
+        if (*last_flag) {
+          __threadfence();
+          const float* o0 = p.part_o + tile_slot0 * D * kChunkRows + row;
+          const float* ml0 = p.part_ml + tile_slot0 * 2 * kChunkRows + row;
+          merge_pieces<D, 64>(o0, ml0, ns, 0, D, valid_row,
+                          p.out + ((size_t)(q0 + tok_rel) * p.num_q_heads +
+                                   (size_t)it.kv_head * g + (row % g)) * D);
+          if (threadIdx.x == 0) p.counters[it.merge_id] = 0;   // ready for the next launch
         }
       }
     }
@@ -789,44 +907,9 @@ __device__ __forceinline__ void chunk_cta(const ChunkParams& p, const CUtensorMa
           const int ns = it.n_splits;
           const float* o0 = p.part_o + (size_t)it.slot * D * kChunkRows + row;
           const float* ml0 = p.part_ml + (size_t)it.slot * 2 * kChunkRows + row;
-          float mk[kMaxChunkSplits], w[kMaxChunkSplits];
-          float mmax = -INFINITY;
-#pragma unroll
-          for (int k = 0; k < kMaxChunkSplits; ++k) {
-            mk[k] = k < ns ? __ldcg(ml0 + (size_t)k * 2 * kChunkRows) : -INFINITY;
-            mmax = fmaxf(mmax, mk[k]);
-          }
-          float lsum = 0.f;
-#pragma unroll
-          for (int k = 0; k < kMaxChunkSplits; ++k) {
-            w[k] = (mk[k] == -INFINITY) ? 0.f : fast_exp2(mk[k] - mmax);
-            if (k < ns) lsum += w[k] * __ldcg(ml0 + (size_t)k * 2 * kChunkRows + kChunkRows);
-          }
-          const float inv = (lsum > 0.f) ? 1.f / lsum : 0.f;
-          if (valid_row) {
-            uint16_t* dst = p.out + ((size_t)(q0 + tok_rel) * p.num_q_heads +
-                                     (size_t)it.kv_head * g + (row % g)) * D;
-#pragma unroll 1
-            for (int d0 = o_c0; d0 < o_c0 + o_nc; d0 += 8) {
-              float acc[8];
-#pragma unroll
-              for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-#pragma unroll
-              for (int k = 0; k < kMaxChunkSplits; ++k) {
-                if (k < ns) {
-                  const float* src = o0 + ((size_t)k * D + d0) * kChunkRows;
-#pragma unroll
-                  for (int i = 0; i < 8; ++i) acc[i] += w[k] * __ldcg(src + (size_t)i * kChunkRows);
-                }
-              }
-              uint4 pk4;
-              pk4.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
-              pk4.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
-              pk4.z = pack_bf16x2(acc[4] * inv, acc[5] * inv);
-              pk4.w = pack_bf16x2(acc[6] * inv, acc[7] * inv);
-              *reinterpret_cast<uint4*>(dst + d0) = pk4;
-            }
-          }
+          merge_pieces<D, D / 2>(o0, ml0, ns, o_c0, o_nc, valid_row,
+                          p.out + ((size_t)(q0 + tok_rel) * p.num_q_heads +
+                                   (size_t)it.kv_head * g + (row % g)) * D);
           if (threadIdx.x == 0) p.counters[it.merge_id] = 0;   // ready for the next launch
         }
       }

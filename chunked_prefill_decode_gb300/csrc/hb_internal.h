@@ -22,7 +22,7 @@ constexpr int kChunkKeys = 128;        // keys per tensor-core KV tile
 constexpr int kDecodeKvhBlock = 8;     // kv heads per decode work item (max)
 constexpr int kMaxGroup = 16;          // max q heads per kv head
 constexpr uint32_t kPlanMagic = 0x31504248u;  // "HBP1"
-constexpr uint32_t kPlanVersion = 3;
+constexpr uint32_t kPlanVersion = 4;
 constexpr int kMaxChunkSplits = 16;    // key-range pieces of one query tile (max)
 
 // One decode work item: a range of logical pages of one decode row, for one
@@ -90,7 +90,7 @@ struct PlanHeader {
   int32_t num_chunk_merges;    // split chunk tiles
   int32_t sliding_window;      // the batch's window (the plan depends on it)
   int32_t num_decode_dynamic;  // claimable decode intervals after the static ones
-  int32_t pad0;
+  int32_t chunk_pairs_only;    // 1: chunk items exist and all are unsplit pairs
   uint64_t ws_decode_offsets;  // device offset of the per-CTA item offsets
   uint64_t items_bytes;     // bytes of the item arrays (host and device)
   uint64_t ws_counters;     // device offsets (bytes from workspace start)

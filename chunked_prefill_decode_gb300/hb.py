@@ -253,7 +253,7 @@ def plan_header(plan):
             "num_decode_items", "num_chunk_items", "num_partial_slots",
             "num_merge_counters", "decode_grid", "decode_kvh_block",
             "chunk_tokens_per_tile", "num_chunk_slots", "num_chunk_merges", "sliding_window",
-            "num_decode_dynamic", "pad0")
+            "num_decode_dynamic", "chunk_pairs_only")
     out = {k: int(v) for k, v in zip(keys, h)}
     u = np.frombuffer(plan[88:HEADER_BYTES].tobytes(), dtype=np.uint64)
     for k, v in zip(("ws_decode_offsets", "items_bytes", "ws_counters", "ws_partial_o",

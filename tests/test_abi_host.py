@@ -188,9 +188,11 @@ def _check_plan(rows, hq, hkv, d, sms, window=0):
                 slots.add(parts[0][4])
     # chunk items cover every (token, kv head) of every chunk row once; an
     # item holds two query tiles when there are enough tiles to fill the SMs
+    # twice, and otherwise whichever of pairs and single tiles the plan
+    # estimates to end first
     tpt = 128 // g
     n_tiles = sum(-(-int(q) // tpt) * hkv for q in ql if q > 1)
-    tpi = 2 if n_tiles >= 2 * sms else 1
+    tpi = 2 if n_tiles >= 2 * sms or any(int(c[3]) > tpt for c in chk) else 1
     seen = set()
     groups = {}
     for seq, kvh, t0, nt, end, q0, qn, ctx, kb, split, ns, slot, mid, *_ in chk:
@@ -198,7 +200,7 @@ def _check_plan(rows, hq, hkv, d, sms, window=0):
         assert q0 == cu[seq] and qn == ql[seq] and ctx == cl[seq]
         assert 1 <= ns <= 16 and 0 <= split < ns and 0 <= kb < end
         if ns > 1:
-            assert tpi == 1 and end - kb >= 4      # only single tiles are split
+            assert end - kb >= 4                   # no piece below 4 key tiles
         groups.setdefault((seq, kvh, t0), []).append((split, kb, end, ns, slot, mid, nt))
     slots, merges = set(), set()
     for (seq, kvh, t0), parts in groups.items():
@@ -215,7 +217,9 @@ def _check_plan(rows, hq, hkv, d, sms, window=0):
         if ns > 1:
             assert parts[0][5] not in merges
             merges.add(parts[0][5])
-            rng_ = set(range(parts[0][4], parts[0][4] + ns))
+            # one partial state per piece and query tile (a pair has two)
+            tiles = 2 if nt > tpt else 1
+            rng_ = set(range(parts[0][4], parts[0][4] + ns * tiles))
             assert not (rng_ & slots)
             slots |= rng_
         for t in range(t0, t0 + nt):
@@ -226,6 +230,10 @@ def _check_plan(rows, hq, hkv, d, sms, window=0):
     assert slots == set(range(len(slots))) and merges == set(range(len(merges)))
     lengths = [c[4] - c[8] for c in chk]
     assert lengths == sorted(lengths, reverse=True)
+    # the launch takes the pairs-only kernel when every chunk item is an
+    # unsplit pair of query tiles
+    pairs_only = len(chk) > 0 and all(int(c[3]) > tpt and int(c[10]) == 1 for c in chk)
+    assert h["chunk_pairs_only"] == int(pairs_only)
     return h
 
 
@@ -238,6 +246,19 @@ def test_plan_covers_workloads(name):
     rows = list(zip(lay.q_len.tolist(), lay.context_len.tolist()))
     h = _check_plan(rows, sh.num_q_heads, sh.num_kv_heads, sh.head_dim, 152,
                     window=sh.sliding_window)
+
+
+def test_plan_of_a_decode_batch_after_a_chunk_batch():
+    """The plan's working arrays are reused from call to call on a thread: a
+    batch without chunk rows planned after one with many has no chunk item."""
+    from chunked_prefill_decode_gb300 import workloads
+    for name in ("yi_b2048", "decode_only", "mistral_b512", "decode_only"):
+        lay = workloads.WORKLOADS[name]()
+        sh = lay.shape
+        rows = list(zip(lay.q_len.tolist(), lay.context_len.tolist()))
+        h = _check_plan(rows, sh.num_q_heads, sh.num_kv_heads, sh.head_dim, 152)
+        if name == "decode_only":
+            assert h["num_chunk_items"] == 0
 
 
 def test_plan_edge_shapes():
@@ -286,7 +307,7 @@ def test_plan_splits_short_chunks_at_long_offsets():
     fill 148 SMs as whole tiles: its key ranges are split; a chunk with enough
     tiles to pair is not."""
     h = _check_plan([(256, 8192)], 32, 8, 128, 148)
-    assert h["num_chunk_merges"] == 64 and h["num_chunk_slots"] >= 128
+    assert h["num_chunk_merges"] > 0 and h["num_chunk_slots"] >= 2 * h["num_chunk_merges"]
     h = _check_plan([(1, 2048)] * 32 + [(256, 8192)], 32, 8, 128, 148)
     assert h["num_chunk_merges"] > 0
     h = _check_plan([(4096, 8192)], 32, 8, 128, 148)

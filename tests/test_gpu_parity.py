@@ -84,6 +84,32 @@ def test_split_key_ranges(geom, rows):
     _full_check(layout_from_rows(Shape(hq, hkv, d), rows, 14), seed=14, repeats=3)
 
 
+@pytest.mark.parametrize("geom,rows,window", [
+    ((32, 8, 128), [(512, 8192)], 0),
+    ((56, 8, 128), [(252, 8000)], 0),
+    ((32, 8, 128), [(1, 2048)] * 8 + [(512, 7000)], 0),
+    ((16, 1, 128), [(600, 9000)], 0),
+    ((32, 8, 128), [(200, 5000), (300, 6000)], 0),
+    ((32, 8, 128), [(512, 8192)], 3000),
+])
+def test_split_pairs(geom, rows, window):
+    """Pairs of query tiles whose key range is cut into pieces (with single
+    tiles split alongside in the mixed batch): each piece publishes both
+    tiles' partial states, a tile past its own last key publishes none, and
+    the last piece merges them.  Sampled rows of every chunk against the
+    oracle, three launches on one plan."""
+    from _hbutil import host_batch
+    hq, hkv, d = geom
+    hb = lib()
+    b, ql, cl = host_batch(hb, rows, hq=hq, hkv=hkv, d=d, window=window)
+    plan, _ = hb.hb_plan(b, ql, cl, sms(), upload=False)
+    tpt = hb.plan_header(plan)["chunk_tokens_per_tile"]
+    _, chk, _ = hb.plan_items(plan)
+    assert ((chk[:, 3] > tpt) & (chk[:, 10] > 1)).any()
+    lay = layout_from_rows(Shape(hq, hkv, d, sliding_window=window), rows, 19)
+    _full_size(None, seed=19, lay=lay, repeats=3)
+
+
 WINDOW_ROWS = [(1, 1), (1, 17), (1, 700), (1, 3000), (5, 37), (130, 700), (64, 4160),
                (257, 2000), (1, 129)]
 
@@ -255,13 +281,13 @@ def test_timing_and_launch_count():
 
 
 # ---------------------------------------------------------------- full size
-def _full_size(name, n_seq_sample=6, n_chunk_tok=48, seed=None, lay=None):
+def _full_size(name, n_seq_sample=6, n_chunk_tok=48, seed=None, lay=None, repeats=1):
     if lay is None:
         lay = workloads.WORKLOADS[name]()
     seed = {"mistral_b512": 1, "mistral_b512_window": 1, "yi_b2048": 2, "yi_b2048_o5043": 2,
             "decode_only": 3}.get(name, 0) if seed is None else seed
     ten = workloads.make_tensors(lay, seed, device="cuda")
-    kc, vc, out = gpu_step(lay, ten)
+    kc, vc, out = gpu_step(lay, ten, repeats=repeats)
     rng = np.random.default_rng(seed)
     dec = [s for s in range(lay.num_seqs) if lay.q_len[s] == 1]
     chk = [s for s in range(lay.num_seqs) if lay.q_len[s] > 1]
