@@ -504,16 +504,19 @@ def run_native(args):
     ms_max = max_over_ranks(ms, n)
     value = job_tokens_per_s(T, args.steps, n, ms)
 
-    # ---- end to end through the public API with host buffers.  Every step
-    # copies its inputs (q, k_new, v_new, descriptors: one packed pinned
-    # buffer) to the device, plans, runs append + attention and copies the
-    # output back.  Two staging buffers and a copy stream each way let a
-    # step's copies overlap the neighbouring steps' kernels, as a serving
-    # loop would run them; the kernels stay in order on one stream.
+    # ---- end to end through the public API with host buffers: hb_step, one
+    # library call per step that plans, copies the step's inputs (q, k_new,
+    # v_new, descriptors: one packed page-locked block) to the device, runs
+    # append + attention and copies the output back.  Its slots order an
+    # input-copy stream, the kernels' stream and an output-copy stream, so
+    # a step's copies overlap the neighbouring steps' kernels, as a serving
+    # loop would run them.
     from chunked_prefill_decode_gb300.device import StepStaging
     stages = [StepStaging(layout.num_seqs, T, layout.block_table.shape[1], layout.num_pages,
                           sh.num_q_heads, sh.num_kv_heads, sh.head_dim, sh.page_size,
-                          sh.sliding_window, dev) for _ in range(2)]
+                          sh.sliding_window, dev) for _ in range(args.e2e_stages)]
+    q_len_h = np.ascontiguousarray(layout.q_len, dtype=np.int32)
+    ctx_h = np.ascontiguousarray(layout.context_len, dtype=np.int32)
     for stg in stages:
         stg.h_q.copy_(ten.q.cpu())
         stg.h_k_new.copy_(ten.k_new.cpu())
@@ -522,31 +525,17 @@ def run_native(args):
         stg.h_context_len.copy_(torch.from_numpy(layout.context_len))
         stg.h_block_table.copy_(torch.from_numpy(np.ascontiguousarray(layout.block_table)))
         stg.plan, stg.ws = hb.hb_plan(stg.batch, layout.q_len, layout.context_len, sms)
-        stg.ev_in, stg.ev_done, stg.ev_out = (torch.cuda.Event() for _ in range(3))
+        stg.slot = hb.StepSlot()
+        stg.bufs = stg.step_buffers(stg.plan, stg.ws)
     s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     e2e_steps = max(1, min(args.steps, 200))
     h2d = stages[0].in_bytes
     d2h = stages[0].out_bytes
 
     def e2e_step(i):
-        stg = stages[i % 2]
-        s_in.wait_event(stg.ev_done)        # step i - 2's kernels are done with these inputs
-        # the plan goes up on the upload stream, ahead of the inputs: a small
-        # copy from pageable memory may first wait for its stream, and this
-        # stream's earlier work is neither the step before's kernels nor
-        # this step's input copy
-        p, _ = hb.hb_plan(stg.batch, layout.q_len, layout.context_len, sms, workspace=stg.ws,
-                          plan=stg.plan, stream=s_in)
-        stg.upload(s_in)
-        stg.ev_in.record(s_in)
-        stream.wait_event(stg.ev_in)
-        stream.wait_event(stg.ev_out)       # step i - 2's output has left this buffer
-        hb.hb_kv_append(stg.batch, stg.k_new, stg.v_new, kc, vc, stream=stream)
-        hb.hb_attention(stg.batch, p, stg.q, kc, vc, scale, stg.out, stg.ws, stream=stream)
-        stg.ev_done.record(stream)
-        s_out.wait_event(stg.ev_done)
-        stg.download(s_out)
-        stg.ev_out.record(s_out)
+        stg = stages[i % len(stages)]
+        hb.hb_step(stg.batch, q_len_h, ctx_h, sms, stg.slot, stg.bufs, kc, vc, scale,
+                   s_in, stream, s_out)
 
     for i in range(4):
         e2e_step(i)
@@ -557,13 +546,15 @@ def run_native(args):
         e2e_step(i)
     torch.cuda.synchronize(dev)
     e2e_s = max_over_ranks(time.perf_counter() - t0, n)
+    hb.hb_check()
     plan_bytes = int(hb.plan_header(plan)["items_bytes"])
     e2e = {"value": n * T * e2e_steps / e2e_s, "unit": "tokens/s",
            "h2d_bytes_per_step": h2d + plan_bytes, "d2h_bytes_per_step": d2h,
-           "copies": "one packed pinned H2D (q, k_new, v_new, descriptors) + the plan upload "
-                     "(on the input-copy stream, ahead of the inputs) and one D2H of the output "
-                     "per step, on copy streams overlapping the neighbouring steps' kernels "
-                     "(two staging buffers)"}
+           "api": "hb_step (one C call per step)",
+           "copies": "per step: the plan and one packed page-locked block (q, k_new, v_new, "
+                     "descriptors) up on an input-copy stream, the output down on an "
+                     "output-copy stream, ordered against the kernels' stream by events; "
+                     f"{len(stages)} staging buffers in flight"}
 
     if rank != 0:
         return
@@ -863,6 +854,9 @@ def main():
                          "prompt in chunks of 256/257/512/1024/2048/8192 tokens; 'seed' draws "
                          "the workload's batch with seeds 0..4")
     ap.add_argument("--sweep-reps", type=int, default=10)
+    ap.add_argument("--e2e-stages", type=int, default=2,
+                    help="staging buffers of the end-to-end loop (steps whose copies may be "
+                         "in flight at once)")
     ap.add_argument("--layer", action="store_true",
                     help="instead of the attention step: one transformer block of the "
                          "batch (linear layers on synthetic weights around attention)")

@@ -21,7 +21,7 @@ BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libhb.so")
 
 SOURCES = ["api.cu", "kv_append.cu", "attention.cu", "linear.cu", "noalloc.cu", "selftest.cu",
-           "builder.cpp"]
+           "step.cu", "builder.cpp"]
 HEADERS = ["hb_internal.h", "ptx.cuh", "decode_body.cuh", "chunk_body.cuh", "decode_plan.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-O2",

@@ -237,6 +237,7 @@ struct PlanScratch {
   std::vector<ChunkItem> raw, chk;
   std::vector<int32_t> count;
   std::vector<int32_t> dur_count;
+  std::vector<int32_t> hist;
   std::vector<DurGroup> groups;
   std::vector<FreeAt> free_at, next, fresh;
   std::vector<DecodeItem> dec;
@@ -643,23 +644,41 @@ hb_status hb_plan(const hb_batch* batch, const int32_t* h_q_len,
     auto t_decode = [&](int G) {
       return decode_bytes / std::min(kHbmBytesPerUs, G * kSmBytesPerUs);
     };
+    // t(G) falls while G SMs cannot stream at the HBM rate (G x one SM's
+    // rate below it: t_decode shrinks, G x t_decode stays) and rises after
+    // (t_decode fixed, G x t_decode grows), so each side is searched by
+    // bisection instead of evaluating every G
     auto pick_decode = [&](double chunk_us, double max_item_us) -> int {
       if (decode_bytes <= 0.0) return 0;
       if (chunk_us <= 0.0) return num_sms;
-      std::vector<double>& t = ps.t_end;
-      t.resize((size_t)num_sms + 1);
-      double best = 1e300;
-      for (int G = 1; G <= num_sms; ++G) {
+      auto t_of = [&](int G) {
         const double td = t_decode(G);
-        t[G] = std::max({td, (chunk_us + G * td) / num_sms, max_item_us});
-        best = std::min(best, t[G]);
+        return std::max({td, (chunk_us + G * td) / num_sms, max_item_us});
+      };
+      // the last G whose SMs together stream below the HBM rate
+      int gs = std::min(num_sms, std::max(1, (int)(kHbmBytesPerUs / kSmBytesPerUs)));
+      while (gs > 1 && gs * kSmBytesPerUs >= kHbmBytesPerUs) --gs;
+      while (gs < num_sms && (gs + 1) * kSmBytesPerUs < kHbmBytesPerUs) ++gs;
+      const double best = std::min(t_of(gs), gs < num_sms ? t_of(gs + 1) : 1e300);
+      const double lim = 1.02 * best;
+      // lo: the first G in 1..gs with t(G) <= lim (t non-increasing there)
+      int a = 1, b = gs;
+      if (t_of(gs) > lim) a = gs + 1;   // none on this side
+      while (a < b) {
+        const int m = (a + b) / 2;
+        if (t_of(m) <= lim) b = m; else a = m + 1;
       }
-      int lo = 0, hi = 0;
-      for (int G = 1; G <= num_sms; ++G)
-        if (t[G] <= 1.02 * best) {
-          if (!lo) lo = G;
-          hi = G;
+      const int lo = a;
+      // hi: the last G in gs+1..num_sms with t(G) <= lim (t non-decreasing)
+      int hi = lo <= gs ? gs : lo;
+      if (gs < num_sms && t_of(gs + 1) <= lim) {
+        int c = gs + 1, d = num_sms;
+        while (c < d) {
+          const int m = (c + d + 1) / 2;
+          if (t_of(m) <= lim) c = m; else d = m - 1;
         }
+        hi = c;
+      }
       return (lo + hi) / 2;
     };
     // pieces per item when each piece holds about L key tiles
@@ -679,30 +698,36 @@ hb_status hb_plan(const hb_batch* batch, const int32_t* h_q_len,
       *out_L = 0;
       if (ps.chk.empty()) return 0.0;
       const int kmax = key_tiles(ps.chk.front());
+      // items by key-tile count: a candidate costs what the distinct counts
+      // cost, not what the items do
+      ps.hist.assign((size_t)kmax + 1, 0);
+      for (const ChunkItem& c : ps.chk) ++ps.hist[key_tiles(c)];
       double best_t = 1e300;
       int prev_L = -1;
       for (int n = 1; n <= kMaxChunkSplits; ++n) {
         const int L = (kmax + n - 1) / n;
         if (L == prev_L || (n > 1 && L < kMinPieceTiles)) continue;
         prev_L = L;
-        // pieces counted per (length, split) class; the sums run in item
-        // order
+        // pieces counted per (length, split) class
         ps.dur_count.assign(2 * (size_t)(kmax + 1), 0);
-        size_t n_pieces = 0;
+        int64_t n_pieces = 0;
         double sum = 0.0, mx = 0.0;
-        for (const ChunkItem& c : ps.chk) {
-          const int kv = key_tiles(c);
+        bool too_many = false;
+        for (int kv = kmax; kv >= 0 && !too_many; --kv) {
+          const int32_t items = ps.hist[kv];
+          if (!items) continue;
           const int np = n == 1 ? 1 : pieces_of(kv, L);
           for (int k = 0; k < np; ++k) {
             const int len = (k + 1) * kv / np - k * kv / np;
             const double d = len * tile_us + (np > 1 ? kPieceUs : 0.0);
-            ++ps.dur_count[2 * (size_t)len + (np > 1 ? 1 : 0)];
-            ++n_pieces;
-            sum += d;
+            ps.dur_count[2 * (size_t)len + (np > 1 ? 1 : 0)] += items;
+            sum += items * d;
             mx = std::max(mx, d);
           }
+          n_pieces += (int64_t)np * items;
+          too_many = n > 1 && n_pieces > 2LL * num_sms;
         }
-        if (n > 1 && n_pieces > (size_t)(2 * num_sms)) break;   // at most two waves
+        if (too_many) break;   // at most two waves
         ps.groups.clear();
         for (int len = 0; len <= kmax; ++len)
           for (int sp = 0; sp < 2; ++sp) {

@@ -663,7 +663,7 @@ __device__ __forceinline__ void chunk_cta(const ChunkParams& p, const CUtensorMa
           __threadfence();
           const float* o0 = p.part_o + tile_slot0 * D * kChunkRows + row;
           const float* ml0 = p.part_ml + tile_slot0 * 2 * kChunkRows + row;
-          merge_pieces<D, 64>(o0, ml0, ns, 0, D, valid_row,
+          merge_pieces<D, 32>(o0, ml0, ns, 0, D, valid_row,
                           p.out + ((size_t)(q0 + tok_rel) * p.num_q_heads +
                                    (size_t)it.kv_head * g + (row % g)) * D);
           if (threadIdx.x == 0) p.counters[it.merge_id] = 0;   // ready for the next launch
@@ -907,7 +907,7 @@ __device__ __forceinline__ void chunk_cta(const ChunkParams& p, const CUtensorMa
           const int ns = it.n_splits;
           const float* o0 = p.part_o + (size_t)it.slot * D * kChunkRows + row;
           const float* ml0 = p.part_ml + (size_t)it.slot * 2 * kChunkRows + row;
-          merge_pieces<D, D / 2>(o0, ml0, ns, o_c0, o_nc, valid_row,
+          merge_pieces<D, 32>(o0, ml0, ns, o_c0, o_nc, valid_row,
                           p.out + ((size_t)(q0 + tok_rel) * p.num_q_heads +
                                    (size_t)it.kv_head * g + (row % g)) * D);
           if (threadIdx.x == 0) p.counters[it.merge_id] = 0;   // ready for the next launch

@@ -11,15 +11,17 @@
 //
 // One warp moves one segment of up to 2 KB of one row (4 x 16 bytes per
 // lane), so every segment is in flight at once: the grid is one warp per
-// segment and the register budget (<= 64 per thread) lets eight 128-thread
-// CTAs share an SM, i.e. a batch of up to 152 x 8 x 4 segments (19 MB of
-// K and V at 2 KB rows) runs in a single wave; small CTAs spread a small
-// batch over many SMs.  A warp issues its data loads
+// segment; with <= 64 registers per thread two 512-thread CTAs share an SM,
+// so a batch of up to 152 x 2 x 16 segments (19 MB of K and V at 2 KB rows)
+// runs in a single wave, and the CTA size shrinks with the batch so that a
+// small batch still spreads over many SMs.  A warp issues its data loads
 // first; the row -> sequence search (over a shared-memory copy of
 // cu_q_len), the context length and the block-table entry are looked up
 // while the data is on its way, so the dependent index chain overlaps the
 // copy instead of preceding it.
 #include <cuda_runtime.h>
+
+#include <algorithm>
 
 #include "hb_internal.h"
 #include "ptx.cuh"
@@ -38,11 +40,11 @@ __device__ __forceinline__ uint4 ld_stream(const uint4* p) {
 // many sequences (at most 48 KB, the dynamic shared memory a launch gets
 // without opting in)
 constexpr int kAppendSmemSeqs = 6143;
-constexpr int kAppendWarps = 4;                 // warps per CTA
+constexpr int kAppendMaxWarps = 16;             // warps per CTA (at most)
 constexpr int kSegVecsPerLane = 4;              // 16-byte vectors per lane
 constexpr int kSegVecs = 32 * kSegVecsPerLane;  // vectors per segment (2 KB)
 
-__global__ void __launch_bounds__(32 * kAppendWarps, 8) kv_append_kernel(AppendParams p) {
+__global__ void __launch_bounds__(32 * kAppendMaxWarps, 2) kv_append_kernel(AppendParams p) {
   extern __shared__ int32_t s_cu[];
   // k_new / v_new may come from the kernel before this one, and the pages
   // written here may be read by it: wait for it first
@@ -51,7 +53,7 @@ __global__ void __launch_bounds__(32 * kAppendWarps, 8) kv_append_kernel(AppendP
   const int lane = threadIdx.x & 31;
   const int spr = (p.row_vec16 + kSegVecs - 1) / kSegVecs;   // segments per row
   const int64_t n_k = (int64_t)p.total_q * spr;              // segments of the K rows
-  const int64_t seg = (int64_t)blockIdx.x * kAppendWarps + (threadIdx.x >> 5);
+  const int64_t seg = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const bool live = seg < 2 * n_k;
   const bool is_v = seg >= n_k;
   const int64_t sk = is_v ? seg - n_k : seg;
@@ -109,14 +111,19 @@ __global__ void __launch_bounds__(32 * kAppendWarps, 8) kv_append_kernel(AppendP
 }
 
 cudaError_t launch_kv_append(const AppendParams& p, int num_sms, cudaStream_t stream) {
-  (void)num_sms;
   if (p.total_q == 0) return cudaSuccess;
   const int64_t spr = (p.row_vec16 + kSegVecs - 1) / kSegVecs;
   const int64_t segs = 2LL * p.total_q * spr;
-  const int64_t blocks = (segs + kAppendWarps - 1) / kAppendWarps;
+  // CTAs of 4 to 16 warps: about two per SM when the batch is large (few
+  // CTAs to schedule, one wave), smaller ones spread a small batch over more
+  // SMs
+  int64_t warps = (segs + 2LL * num_sms - 1) / (2LL * num_sms);
+  warps = std::min<int64_t>(kAppendMaxWarps, std::max<int64_t>(4, warps));
+  const int64_t blocks = (segs + warps - 1) / warps;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   const size_t smem = p.num_seqs <= kAppendSmemSeqs ? (size_t)(2 * p.num_seqs + 1) * 4 : 0;
-  return launch_serialized(kv_append_kernel, (unsigned)blocks, 32 * kAppendWarps, smem, stream, p);
+  return launch_serialized(kv_append_kernel, (unsigned)blocks, (unsigned)(32 * warps), smem,
+                           stream, p);
 }
 
 }  // namespace hb

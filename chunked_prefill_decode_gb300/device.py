@@ -64,10 +64,11 @@ class StepStaging:
 
     _ALIGN = 256
 
-    def __init__(self, num_seqs, total_q, max_pages_per_seq, num_pages, num_q_heads,
-                 num_kv_heads, head_dim, page_size=16, sliding_window=0, device="cuda"):
-        a = self._ALIGN
-        up = lambda n: (n + a - 1) // a * a
+    @staticmethod
+    def layout(num_seqs, total_q, max_pages_per_seq, num_q_heads, num_kv_heads, head_dim):
+        """[(name, shape, dtype, offset, bytes)] of the packed input block (the
+        same as hb_step_layout's: 256-byte aligned sections), and its size."""
+        a = StepStaging._ALIGN
         parts = [("q", (total_q, num_q_heads, head_dim), torch.bfloat16),
                  ("k_new", (total_q, num_kv_heads, head_dim), torch.bfloat16),
                  ("v_new", (total_q, num_kv_heads, head_dim), torch.bfloat16),
@@ -78,7 +79,13 @@ class StepStaging:
         for name, shape, dt in parts:
             n = int(np.prod(shape)) * torch.tensor([], dtype=dt).element_size()
             offs.append((name, shape, dt, off, n))
-            off = up(off + n)
+            off = (off + n + a - 1) // a * a
+        return offs, off
+
+    def __init__(self, num_seqs, total_q, max_pages_per_seq, num_pages, num_q_heads,
+                 num_kv_heads, head_dim, page_size=16, sliding_window=0, device="cuda"):
+        offs, off = self.layout(num_seqs, total_q, max_pages_per_seq, num_q_heads,
+                                num_kv_heads, head_dim)
         self.in_bytes = off
         self.host = torch.empty(off, dtype=torch.uint8).pin_memory()
         self.dev = torch.empty(off, dtype=torch.uint8, device=device)
@@ -95,6 +102,16 @@ class StepStaging:
                                    num_q_heads, num_kv_heads, head_dim, self.cu_q_len,
                                    self.context_len, self.block_table, page_size=page_size,
                                    sliding_window=sliding_window)
+
+    def step_buffers(self, plan, workspace):
+        """hb_step's buffers over this staging (plan: host uint8 array,
+        workspace: device uint8 tensor, both sized by hb_plan)."""
+        b = hb.HbStepBuffers()
+        b.h_in, b.d_in = self.host.data_ptr(), self.dev.data_ptr()
+        b.h_out, b.d_out = self.h_out.data_ptr(), self.out.data_ptr()
+        b.h_plan, b.plan_bytes = plan.ctypes.data, plan.nbytes
+        b.d_workspace, b.workspace_bytes = workspace.data_ptr(), workspace.numel()
+        return b
 
     def upload(self, stream=None):
         with torch.cuda.stream(stream or torch.cuda.current_stream()):

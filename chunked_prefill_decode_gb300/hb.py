@@ -59,10 +59,21 @@ EXPORTED = (
     "hb_builder_step", "hb_builder_complete", "hb_builder_counts",
     "hb_builder_free_list", "hb_builder_last_error", "hb_decode_attention_noalloc",
     "hb_selftest_wait_timeout", "hb_linear", "hb_linear_workspace_size",
-    "hb_timing_durations",
+    "hb_timing_durations", "hb_step_layout", "hb_step_slot_create", "hb_step_slot_destroy",
+    "hb_step_slot_sync", "hb_step",
 )
 
 LINEAR_STORE, LINEAR_GATED, LINEAR_RESIDUAL = 0, 1, 2
+
+
+class HbStepBuffers(ctypes.Structure):
+    _fields_ = [("h_in", ctypes.c_void_p), ("d_in", ctypes.c_void_p),
+                ("h_out", ctypes.c_void_p), ("d_out", ctypes.c_void_p),
+                ("h_plan", ctypes.c_void_p), ("plan_bytes", ctypes.c_size_t),
+                ("d_workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t)]
+
+
+HB_STEP_SECTIONS = 6
 
 
 class HbLinearOut(ctypes.Structure):
@@ -114,6 +125,17 @@ def load():
     L.hb_timing_read.argtypes = [P(ctypes.c_double), P(i32)]
     L.hb_timing_durations.restype = ctypes.c_int
     L.hb_timing_durations.argtypes = [i32, P(ctypes.c_float), i32, P(i32)]
+    L.hb_step_layout.restype = ctypes.c_int
+    L.hb_step_layout.argtypes = [P(HbBatch), P(sz), P(sz)]
+    L.hb_step_slot_create.restype = ctypes.c_int
+    L.hb_step_slot_create.argtypes = [P(vp)]
+    L.hb_step_slot_destroy.restype = None
+    L.hb_step_slot_destroy.argtypes = [vp]
+    L.hb_step_slot_sync.restype = ctypes.c_int
+    L.hb_step_slot_sync.argtypes = [vp]
+    L.hb_step.restype = ctypes.c_int
+    L.hb_step.argtypes = [P(HbBatch), vp, vp, i32, vp, P(HbStepBuffers), vp, vp,
+                          ctypes.c_float, vp, vp, vp]
     L.hb_launch_count.restype = i64
     L.hb_launch_count.argtypes = []
     L.hb_builder_create.restype = ctypes.c_int
@@ -334,6 +356,50 @@ def hb_timing_durations(kernel):
     buf = (ctypes.c_float * max(1, n.value))()
     _check(load().hb_timing_durations(k, buf, n.value, ctypes.byref(n)))
     return [float(buf[i]) for i in range(n.value)]
+
+
+def hb_step_layout(batch):
+    """(section offsets [q, k_new, v_new, cu_q_len, context_len, block_table],
+    total bytes) of hb_step's packed input block for this batch's sizes."""
+    offs = (ctypes.c_size_t * HB_STEP_SECTIONS)()
+    n = ctypes.c_size_t(0)
+    _check(load().hb_step_layout(ctypes.byref(batch), offs, ctypes.byref(n)))
+    return list(offs), n.value
+
+
+class StepSlot:
+    """hb_step_slot: the events that order one set of staging buffers' copies
+    and kernels (created on the current device)."""
+
+    def __init__(self):
+        h = ctypes.c_void_p()
+        _check(load().hb_step_slot_create(ctypes.byref(h)))
+        self._h = h
+
+    def sync(self):
+        _check(load().hb_step_slot_sync(self._h))
+
+    def close(self):
+        if self._h:
+            load().hb_step_slot_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def hb_step(batch, q_len, context_len, num_sms, slot, buffers, k_cache, v_cache, scale,
+            copy_in_stream, stream, copy_out_stream):
+    """One step from host memory (see hb.h).  `buffers` is an HbStepBuffers;
+    q_len / context_len are host int32 arrays (kept contiguous by the
+    caller for repeated calls)."""
+    _check(load().hb_step(ctypes.byref(batch), _ptr(q_len), _ptr(context_len), int(num_sms),
+                          slot._h, ctypes.byref(buffers), _bf16(k_cache, "k_cache"),
+                          _bf16(v_cache, "v_cache"), ctypes.c_float(scale),
+                          _stream(copy_in_stream), _stream(stream), _stream(copy_out_stream)))
 
 
 def hb_launch_count() -> int:

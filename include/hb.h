@@ -225,6 +225,68 @@ hb_status hb_decode_attention_noalloc(const hb_batch* batch,
                                       const void* v_cache, float softmax_scale,
                                       void* out, void* stream);
 
+/* ---------------------------------------------------------------------------
+ * One step from host memory.  For a serving loop that keeps a few steps in
+ * flight: the step's inputs cross the host link as one packed block, the
+ * plan goes up ahead of them on the input-copy stream, hb_kv_append and
+ * hb_attention run on the compute stream, the output comes back on the
+ * output-copy stream, and the step's slot (a set of CUDA events) orders the
+ * three streams against the previous step that used the same buffers.  The
+ * host does not wait, so one step's copies overlap the neighbouring steps'
+ * kernels.  The operation is that of hb_kv_append then hb_attention (same
+ * citations); only the copies and their ordering are added.
+ *
+ * Packed input block (host and device alike): q [total_q, Hq, D] bf16 |
+ * k_new | v_new [total_q, Hkv, D] bf16 | cu_q_len [num_seqs+1] | context_len
+ * [num_seqs] | block_table [num_seqs, max_pages_per_seq] int32, each section
+ * starting on a 256-byte boundary.  hb_step_layout writes the six section
+ * offsets and the block's size; it checks only the sizes it reads.
+ * ------------------------------------------------------------------------- */
+#define HB_STEP_SECTIONS 6
+
+hb_status hb_step_layout(const hb_batch* shape, size_t offsets[HB_STEP_SECTIONS],
+                         size_t* in_bytes);
+
+/* Events of one set of staging buffers, on the current device. */
+typedef struct hb_step_slot hb_step_slot;
+hb_status hb_step_slot_create(hb_step_slot** out);
+void hb_step_slot_destroy(hb_step_slot* slot);
+/* Blocks until the slot's last step has completed (inputs consumed, output on
+ * the host): call it before refilling the slot's host inputs or reading its
+ * output. */
+hb_status hb_step_slot_sync(hb_step_slot* slot);
+
+typedef struct hb_step_buffers {
+  const void* h_in;        /* host packed inputs (page-locked, for the copy to overlap) */
+  void* d_in;              /* device packed inputs, 256-byte aligned                      */
+  void* h_out;             /* host output [total_q, Hq, D] bf16                           */
+  void* d_out;             /* device output, 16-byte aligned                              */
+  void* h_plan;            /* host plan buffer (hb_plan's plan_bytes)                     */
+  size_t plan_bytes;
+  void* d_workspace;       /* device workspace (hb_plan's workspace_bytes), 256-aligned   */
+  size_t workspace_bytes;
+} hb_step_buffers;
+
+/*
+ * The step.  `shape` gives the sizes (its three device pointers are ignored:
+ * the descriptors are read from d_in); h_q_len / h_context_len are the host
+ * copies hb_plan needs.  On copy_in_stream: wait for the slot's last kernels,
+ * plan + upload (hb_plan), copy h_in -> d_in.  On stream: wait for the
+ * inputs and for the slot's last output copy, hb_kv_append, hb_attention.  On
+ * copy_out_stream: wait for the kernels, copy d_out -> h_out.  The buffers
+ * belong to the slot until hb_step_slot_sync says its step is over; a slot's
+ * buffers must not be shared with another slot.  The host blocks only if the
+ * slot's previous input copy has not yet run (its plan buffer is rewritten
+ * here).  Errors: as hb_plan, hb_kv_append and hb_attention;
+ * HB_ERR_INVALID_ARG for NULL or misaligned buffers or a slot of another
+ * device; HB_ERR_CUDA if an event or copy call fails.
+ */
+hb_status hb_step(const hb_batch* shape, const int32_t* h_q_len,
+                  const int32_t* h_context_len, int32_t num_sms, hb_step_slot* slot,
+                  const hb_step_buffers* buf, void* k_cache, void* v_cache,
+                  float softmax_scale, void* copy_in_stream, void* stream,
+                  void* copy_out_stream);
+
 /*
  * Synchronise `stream`, then read and clear the device error word of the
  * current device: HB_OK, HB_ERR_DEVICE_INDEX or HB_ERR_TIMEOUT (or

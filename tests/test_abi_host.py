@@ -388,3 +388,35 @@ def test_plan_invariants_on_random_batches(seed):
     sms = int(rng.choice([1, 7, 64, 148, 152]))
     window = int(rng.choice([0, 0, 0, 1, 37, 1024]))
     _check_plan([tuple(r) for r in rows], hq, hkv, d, sms, window=window)
+
+
+@pytest.mark.parametrize("rows,geom", [([(1, 40), (64, 500), (1, 3000)], (32, 8, 128)),
+                                       ([(7, 7)], (8, 8, 64)), ([(1, 1)] * 33, (56, 8, 128))])
+def test_step_layout_matches_the_staging_buffers(rows, geom):
+    """hb_step's packed input block has the layout the Python staging
+    buffers fill: q, k_new, v_new, cu_q_len, context_len, block_table, each
+    on a 256-byte boundary."""
+    from chunked_prefill_decode_gb300.device import StepStaging
+    hb = lib()
+    hq, hkv, d = geom
+    b, ql, cl = host_batch(hb, rows, hq=hq, hkv=hkv, d=d)
+    offs, total = hb.hb_step_layout(b)
+    parts, want = StepStaging.layout(b.num_seqs, b.total_q, b.max_pages_per_seq, hq, hkv, d)
+    assert offs == [p[3] for p in parts] and total == want
+    assert all(o % 256 == 0 for o in offs)
+
+
+def test_step_argument_errors_need_no_gpu():
+    hb = lib()
+    L = hb.load()
+    b, ql, cl = host_batch(hb, [(1, 40)])
+    bufs = hb.HbStepBuffers()
+    assert L.hb_step(ctypes.byref(b), hb._ptr(ql), hb._ptr(cl), 148, None, ctypes.byref(bufs),
+                     None, None, 1.0, None, None, None) == 1       # NULL slot
+    assert L.hb_step_slot_sync(None) == 1
+    L.hb_step_slot_destroy(None)                                   # a no-op
+    offs = (ctypes.c_size_t * 6)()
+    n = ctypes.c_size_t(0)
+    b.num_q_heads = 0
+    assert L.hb_step_layout(ctypes.byref(b), offs, ctypes.byref(n)) == 2
+    assert L.hb_step_layout(None, offs, ctypes.byref(n)) == 1

@@ -390,6 +390,53 @@ def test_staged_step_through_host_buffers():
     compare(stg.h_out, ref)
 
 
+def test_hb_step_with_slots_in_flight():
+    """hb_step: three slots, each with its own inputs (other q, k_new and
+    v_new values over the same batch layout), stepped round-robin without
+    the host waiting; after each slot's sync its output equals the
+    device-resident append + attention on that slot's inputs, bit for bit,
+    and matches the oracle."""
+    from chunked_prefill_decode_gb300.device import StepStaging
+    hb = lib()
+    lay = layout_from_rows(Shape(32, 8, 128), [(1, 700), (40, 300), (1, 33), (17, 17), (1, 2000)], 22)
+    sh = lay.shape
+    dev = torch.device("cuda:0")
+    base = workloads.make_tensors(lay, 22)
+    kc, vc = base.k_cache.to(dev).clone(), base.v_cache.to(dev).clone()
+    scale = 1.0 / math.sqrt(sh.head_dim)
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    main = torch.cuda.current_stream(dev)
+    ql = np.ascontiguousarray(lay.q_len, dtype=np.int32)
+    cl = np.ascontiguousarray(lay.context_len, dtype=np.int32)
+    slots, tens = [], []
+    for k in range(3):
+        ten = workloads.make_tensors(lay, 100 + k)
+        ten = workloads.BatchTensors(ten.q, ten.k_new, ten.v_new, base.k_cache, base.v_cache)
+        stg = StepStaging(lay.num_seqs, lay.total_q, lay.block_table.shape[1], lay.num_pages,
+                          sh.num_q_heads, sh.num_kv_heads, sh.head_dim, device=dev)
+        stg.h_q.copy_(ten.q)
+        stg.h_k_new.copy_(ten.k_new)
+        stg.h_v_new.copy_(ten.v_new)
+        stg.h_cu_q_len.copy_(torch.from_numpy(lay.cu_q_len))
+        stg.h_context_len.copy_(torch.from_numpy(lay.context_len))
+        stg.h_block_table.copy_(torch.from_numpy(np.ascontiguousarray(lay.block_table)))
+        stg.plan, stg.ws = hb.hb_plan(stg.batch, lay.q_len, lay.context_len, sms())
+        stg.slot = hb.StepSlot()
+        stg.bufs = stg.step_buffers(stg.plan, stg.ws)
+        slots.append(stg)
+        tens.append(ten)
+    for i in range(9):
+        stg = slots[i % 3]
+        hb.hb_step(stg.batch, ql, cl, sms(), stg.slot, stg.bufs, kc, vc, scale, s_in, main, s_out)
+    for k, stg in enumerate(slots):
+        stg.slot.sync()
+        _, _, ref_out = gpu_step(lay, tens[k])
+        assert torch.equal(stg.h_out.view(torch.int16), ref_out.cpu().view(torch.int16))
+        _, _, ref = oracle_step(lay, tens[k])
+        compare(stg.h_out, ref)
+    hb.hb_check()
+
+
 def test_attention_right_after_the_kernel_that_writes_q():
     """hb_attention launched directly after an hb_linear that writes its q (no
     append in between) waits for that grid before it reads q; and directly
