@@ -742,18 +742,27 @@ def run_chunk_sweep(args):
         return statistics.median(e0.elapsed_time(e1) for e0, e1 in evs[3:])
 
     rows = []
+    chunks = SWEEP_CHUNKS if not args.sweep_chunks else tuple(args.sweep_chunks)
     with ClockSampler(0) as clk:
-        for c in SWEEP_CHUNKS:
+        for c in chunks:
             n_chunks = -(-8192 // c)
+            iters = range(n_chunks) if args.sweep_iters is None else \
+                [i for i in args.sweep_iters if i < n_chunks]
             r = {"sweep": "chunk", "chunk": c, "n_chunks": n_chunks, "prefill_ms_with_decodes": 0.0,
-                 "prefill_ms_chunk_only": 0.0, "chunk_flops": 0, "chunk_kv_bytes": 0}
-            for i in range(n_chunks):
+                 "prefill_ms_chunk_only": 0.0, "chunk_flops": 0, "chunk_kv_bytes": 0,
+                 "iterations": []}
+            for i in iters:
                 alone = workloads.chunk_sweep(c, i, n_decode=0)
                 cnt = algorithmic_counts(alone)
+                t_alone = time_layout(alone)
+                t_dec = time_layout(workloads.chunk_sweep(c, i)) if not args.sweep_chunk_only else 0.0
                 r["chunk_flops"] += cnt["chunk_flops"]
                 r["chunk_kv_bytes"] += cnt["chunk_bytes"]
-                r["prefill_ms_chunk_only"] += time_layout(alone)
-                r["prefill_ms_with_decodes"] += time_layout(workloads.chunk_sweep(c, i))
+                r["prefill_ms_chunk_only"] += t_alone
+                r["prefill_ms_with_decodes"] += t_dec
+                r["iterations"].append({"index": i, "ms_chunk_only": t_alone, "ms_with_decodes": t_dec,
+                                        "chunk_kv_bytes": cnt["chunk_bytes"],
+                                        "chunk_flops": cnt["chunk_flops"]})
             t = r["prefill_ms_chunk_only"] * 1e-3
             r["chunk_only_tflops"] = r["chunk_flops"] / t / 1e12
             r["chunk_only_tc_frac"] = r["chunk_only_tflops"] / peaks["bf16_tflops"]
@@ -763,9 +772,9 @@ def run_chunk_sweep(args):
     base = rows[-1]
     clocks = clk.summary()
     for r in rows:
-        r["chunk_only_vs_unchunked"] = r["prefill_ms_chunk_only"] / base["prefill_ms_chunk_only"]
+        r["chunk_only_vs_unchunked"] = r["prefill_ms_chunk_only"] / max(base["prefill_ms_chunk_only"], 1e-12)
         r["with_decodes_vs_unchunked"] = (r["prefill_ms_with_decodes"] /
-                                          base["prefill_ms_with_decodes"])
+                                          max(base["prefill_ms_with_decodes"], 1e-12))
         r["peak"] = {"bf16_tflops": peaks["bf16_tflops"], "source": peaks["source"]}
         r["l2"] = "flushed before every timed step (%d MB written)" % (flush.numel() >> 20)
         r["reps"] = reps
@@ -854,6 +863,13 @@ def main():
                          "prompt in chunks of 256/257/512/1024/2048/8192 tokens; 'seed' draws "
                          "the workload's batch with seeds 0..4")
     ap.add_argument("--sweep-reps", type=int, default=10)
+    ap.add_argument("--sweep-chunks", type=int, nargs="+", default=None,
+                    help="chunk sweep: only these chunk sizes (the ratios are then relative "
+                         "to the last size given)")
+    ap.add_argument("--sweep-iters", type=int, nargs="+", default=None,
+                    help="chunk sweep: only these iterations (chunk indices) of each size")
+    ap.add_argument("--sweep-chunk-only", action="store_true",
+                    help="chunk sweep: skip the iterations with decode rows beside the chunk")
     ap.add_argument("--e2e-stages", type=int, default=2,
                     help="staging buffers of the end-to-end loop (steps whose copies may be "
                          "in flight at once)")
