@@ -27,8 +27,8 @@ __device__ int g_hb_device_error = 0;
 namespace hb {
 cudaError_t launch_kv_append(const AppendParams& p, int num_sms, cudaStream_t stream);
 cudaError_t launch_linear(const LinearParams& p, const CUtensorMap& xmap, const CUtensorMap& wmap,
-                          int bn, int num_sms, cudaStream_t stream);
-int linear_tile_n(int M, int N, int epilogue, int num_sms);
+                          int num_sms, cudaStream_t stream);
+int linear_w_box_rows();
 int linear_split(int M, int N, int K, int epilogue, int num_sms, int* kb_per_piece);
 size_t linear_workspace_bytes(int M, int N, int K, int epilogue, int num_sms);
 size_t linear_counter_bytes();
@@ -522,13 +522,12 @@ hb_status hb_linear(const void* x, const void* w, int32_t M, int32_t N, int32_t 
     const cuuint64_t xstr[1] = {(cuuint64_t)K * 2};
     const cuuint32_t xbox[2] = {64, 128};
     if ((s = encode_map(&xmap, x, 2, xdims, xstr, xbox, "linear x")) != HB_OK) return s;
-    const int bn = linear_tile_n(M, N, epilogue, dev->num_sms);
     const cuuint64_t wdims[2] = {(cuuint64_t)K, (cuuint64_t)N};
-    const cuuint32_t wbox[2] = {64, (cuuint32_t)(epilogue == HB_LINEAR_GATED ? bn / 2 : bn)};
+    const cuuint32_t wbox[2] = {64, (cuuint32_t)linear_w_box_rows()};
     if ((s = encode_map(&wmap, w, 2, wdims, xstr, wbox, "linear w")) != HB_OK) return s;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     LaunchTimer t(2, st);
-    cudaError_t e = launch_linear(p, xmap, wmap, bn, dev->num_sms, st);
+    cudaError_t e = launch_linear(p, xmap, wmap, dev->num_sms, st);
     t.done();
     if (e != cudaSuccess) return cuda_fail(e, "linear launch");
     note_launch(stream, LastLaunch{});

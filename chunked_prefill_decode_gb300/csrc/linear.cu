@@ -7,73 +7,79 @@
 // compute-bound for prefill tokens, bound by the weight read for decodes.
 //
 // y = x W^T with x [M, K] (one row per token) and W [N, K], bf16 in, fp32
-// accumulation in tensor memory, bf16 out.  A persistent kernel: one CTA per
-// SM walks output tiles of 128 rows x BN columns (m fastest, so CTAs that
-// run together share the weight tile through L2; BN = 256); per
-// tile, 64-wide slices of K stream through a 4-stage ring of shared memory by
-// TMA (128-byte swizzle) and feed tcgen05.mma M128 N(BN) K16; the accumulator
-// is double-buffered in TMEM (2 x BN columns), so the epilogue of one tile
-// overlaps the main loop of the next.
+// accumulation in tensor memory, bf16 out.  A persistent kernel of CTA pairs
+// (clusters of two CTAs on two SMs): each pair walks output tiles of 256 rows
+// x 256 columns (m fastest, so pairs that run together share the weight tile
+// through L2) and computes each with tcgen05.mma.cta_group::2 M256 N256 K16.
+// Each CTA stages its own 128 rows of x and 128 of the tile's 256 weight rows
+// -- per 64-wide K block 32 KB by TMA into a 6-stage ring -- and keeps its
+// 128 output rows in its own TMEM.  The odd CTA's copies complete on the even
+// CTA's barrier (TMA .cta_group::2), which counts both CTAs' bytes: a thread
+// relaying each landing with a remote mbarrier arrive (release at cluster
+// scope) measured ~1 us per stage on GB300 and held the pair to a third of
+// its MMA rate.  Against one CTA per 128 x 256 tile (x 16
+// KB + W 32 KB per K block and SM) this moves a third less through shared
+// memory per FLOP, which is what bounds an SS MMA at this size (the TMA
+// writes and the tensor cores' operand reads share the SM's shared-memory
+// bandwidth).  The accumulator is double-buffered in TMEM (2 x 256 columns),
+// so the epilogue of one tile overlaps the main loop of the next.
 //
-// Warp roles (192 threads): warp 0 TMA producer (one thread), warp 1 TMEM
-// owner and MMA issuer (one thread), warps 2-5 epilogue (thread = output
-// row = TMEM lane; warp w reads lanes 32 (w % 4) ..).
+// Warp roles (192 threads per CTA): warp 0 TMA producer (one thread); warp 1
+// TMEM owner, and in the even CTA (rank 0) the MMA issuer (one thread); warps
+// 2-5 epilogue (thread = output row = TMEM lane; warp w reads lanes 32 (w % 4)
+// ..).
 //
 // Epilogues: store (columns split over up to three destinations, e.g. q, k
 // and v of a fused QKV projection), gated (W = [W_gate; W_up] with 2F rows:
-// per tile two N(BN/2) accumulators, output silu(g) * u), residual
-// (y += x W^T).
+// the even CTA stages 128 gate rows and the odd CTA the matching 128 up rows,
+// so accumulator columns 0-127 hold x W_gate^T and 128-255 x W_up^T; output
+// silu(g) * u), residual (y += x W^T).
 #include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <mutex>
 
 #include "hb_internal.h"
 #include "ptx.cuh"
 
 namespace hb {
 
-constexpr int kLinBM = 128;
+constexpr int kLinBM = 128;                               // output rows per CTA
+constexpr int kLinPairBM = 2 * kLinBM;                    // output rows per tile (pair)
+constexpr int kLinBN = 256;                               // output columns per tile
 constexpr int kLinBK = 64;
-constexpr int kLinStages = 4;
+constexpr int kLinStages = 6;
 constexpr int kLinThreads = 192;
-constexpr int kLinABytes = kLinBM * kLinBK * 2;          // 16 KB
-
-// Tile width BN (output columns per tile); the kernel is built for 256.
-template <int BN>
-struct LinCfg {
-  static constexpr int kBBytes = BN * kLinBK * 2;
-  static constexpr int kStageBytes = kLinABytes + kBBytes;
-  static constexpr int kBarOff = kLinStages * kStageBytes;
-  static constexpr int kNumBars = 2 * kLinStages + 4 + 1;
-  static constexpr int kMiscOff = kBarOff + kNumBars * 8;
-  static constexpr int kSmemBytes = kMiscOff + 64 + 1024;   // + alignment slack
-  static constexpr uint32_t kTmemCols = 2 * BN < 32 ? 32 : 2 * BN;
-};
-static_assert(LinCfg<256>::kSmemBytes <= 227 * 1024, "linear smem");
+constexpr int kLinABytes = kLinBM * kLinBK * 2;          // 16 KB: this CTA's x rows
+constexpr int kLinBBytes = (kLinBN / 2) * kLinBK * 2;    // 16 KB: this CTA's W rows
+constexpr int kLinStageBytes = kLinABytes + kLinBBytes;
+constexpr int kLinBarOff = kLinStages * kLinStageBytes;
+constexpr int kLinNumBars = 2 * kLinStages + 2 + 2 + 1;
+constexpr int kLinMiscOff = kLinBarOff + kLinNumBars * 8;
+constexpr int kLinSmemBytes = kLinMiscOff + 64 + 1024;    // + alignment slack
+constexpr uint32_t kLinTmemCols = 2 * kLinBN;
+static_assert(kLinSmemBytes <= 227 * 1024, "linear smem");
+// epilogue warps of both CTAs release an accumulator, one arrival per warp
+constexpr uint32_t kLinAccEmptyArrivals = 2 * 4;
 
 __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)); }
 
-template <int BN>
-__global__ void __launch_bounds__(kLinThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kLinThreads, 1)
     linear_kernel(const LinearParams p, const __grid_constant__ CUtensorMap xmap,
                   const __grid_constant__ CUtensorMap wmap) {
-  using C = LinCfg<BN>;
-  constexpr int kLinBN = BN;
-  constexpr int kLinBBytes = C::kBBytes;
-  constexpr int kLinStageBytes = C::kStageBytes;
-  constexpr int kLinBarOff = C::kBarOff;
-  constexpr int kLinMiscOff = C::kMiscOff;
   extern __shared__ uint8_t smem_raw[];
   griddep_wait();
   griddep_launch_dependents();
+  // the same offset in both CTAs: the leader's MMAs address the peer's
+  // stages at this CTA's offsets
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kLinBarOff);
-  uint64_t* full = bars;                       // [stages]
-  uint64_t* empty = full + kLinStages;         // [stages]
+  uint64_t* full = bars;                       // [stages] leader: both CTAs' TMA bytes
+  uint64_t* empty = full + kLinStages;         // [stages] leader's MMAs done with it
   uint64_t* acc_full = empty + kLinStages;     // [2]
-  uint64_t* acc_empty = acc_full + 2;          // [2]
+  uint64_t* acc_empty = acc_full + 2;          // [2] leader: both epilogues drained it
   uint64_t* mma_done = acc_empty + 2;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + kLinMiscOff);
   int* abort_i = reinterpret_cast<int*>(smem + kLinMiscOff + 16);
@@ -81,8 +87,11 @@ __global__ void __launch_bounds__(kLinThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();     // 0: leader (issues the MMAs)
+  const int pair = blockIdx.x >> 1;
+  const int n_pairs = gridDim.x >> 1;
   const bool gated = p.epilogue == 1;
-  const int m_tiles = (p.M + kLinBM - 1) / kLinBM;
+  const int m_tiles = (p.M + kLinPairBM - 1) / kLinPairBM;
   const int n_tiles = gated ? p.F / (kLinBN / 2) : p.N / kLinBN;
   const int tiles = m_tiles * n_tiles;
   const int n_units = tiles * p.split;    // (tile, K piece) pairs
@@ -101,18 +110,19 @@ __global__ void __launch_bounds__(kLinThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], 1);
-      mbar_init(&acc_empty[b], 4 * 32);
+      mbar_init(&acc_empty[b], kLinAccEmptyArrivals);
     }
     mbar_init(mma_done, 1);
     *abort_i = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(tmem_holder, C::kTmemCols);
-    tmem_relinquish();
+    tmem_alloc_pair(tmem_holder, kLinTmemCols);
+    tmem_relinquish_pair();
   }
+  // both CTAs' barriers are initialised before either touches the other's
   tc_fence_before_sync();
-  __syncthreads();
+  cluster_sync_all();
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_holder;
 
@@ -122,76 +132,76 @@ __global__ void __launch_bounds__(kLinThreads, 1)
       tma_prefetch_desc(&xmap);
       tma_prefetch_desc(&wmap);
       uint32_t g = 0;                  // k-blocks issued by this CTA so far
-      uint32_t issued = 0, par = 0;    // per stage: issued at all / last phase
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < n_units; u += gridDim.x) {
+      for (int u = pair; ok && u < n_units; u += n_pairs) {
         const int t = u % tiles;
         const int m = t % m_tiles, n = t / m_tiles;
         int kb_lo, kb_hi;
         k_range(u, kb_lo, kb_hi);
+        // this CTA's 128 rows of x and 128 weight rows of the tile
+        const int x_row = m * kLinPairBM + (int)rank * kLinBM;
+        const int w_row = gated ? (int)rank * p.F + n * (kLinBN / 2)
+                                : n * kLinBN + (int)rank * (kLinBN / 2);
         for (int kb = kb_lo; kb < kb_hi; ++kb, ++g) {
           const int s = (int)(g % kLinStages);
           const uint32_t ph = (g / kLinStages) & 1u;
-          if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag)) { ok = false; break; }
+          if (!mbar_wait_cluster(&empty[s], ph ^ 1u, abort_flag)) { ok = false; break; }
           uint8_t* st = smem + s * kLinStageBytes;
-          mbar_arrive_expect_tx(&full[s], (uint32_t)kLinStageBytes);
-          tma_load_2d(st, &xmap, &full[s], kb * kLinBK, m * kLinBM);
-          if (gated) {
-            tma_load_2d(st + kLinABytes, &wmap, &full[s], kb * kLinBK, n * (kLinBN / 2));
-            tma_load_2d(st + kLinABytes + kLinBBytes / 2, &wmap, &full[s], kb * kLinBK,
-                        p.F + n * (kLinBN / 2));
+          if (rank == 0) {
+            mbar_arrive_expect_tx(&full[s], (uint32_t)(2 * kLinStageBytes));
+            tma_load_2d(st, &xmap, &full[s], kb * kLinBK, x_row);
+            tma_load_2d(st + kLinABytes, &wmap, &full[s], kb * kLinBK, w_row);
           } else {
-            tma_load_2d(st + kLinABytes, &wmap, &full[s], kb * kLinBK, n * kLinBN);
+            const uint32_t bar0 = mapa_shared(smem_u32(&full[s]), 0);
+            tma_load_2d_to_leader(st, &xmap, bar0, kb * kLinBK, x_row);
+            tma_load_2d_to_leader(st + kLinABytes, &wmap, bar0, kb * kLinBK, w_row);
           }
-          issued |= 1u << s;
-          par = (par & ~(1u << s)) | (ph << s);
         }
       }
-      // copies in flight land before the CTA exits
-      for (int s = 0; s < kLinStages; ++s)
-        if (issued & (1u << s)) drain_wait(&full[s], (par >> s) & 1u, abort_flag);
+      // before the CTA exits: the leader's releases of every stage
+      // (multicast arrivals on this CTA's barriers) have arrived, so the
+      // leader's MMAs have read the stage and its copies have landed
+      for (int s = 0; s < kLinStages && (uint32_t)s < g; ++s) {
+        const uint32_t last = (g - 1 - (uint32_t)s) / kLinStages;   // last round of stage s
+        if (rank == 0) drain_wait(&full[s], last & 1u, abort_flag);
+        drain_wait_cluster(&empty[s], last & 1u, abort_flag);
+      }
     }
   } else if (warp == 1) {
-    // ---------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      const uint32_t idesc = gated ? idesc_bf16_f32(kLinBM, kLinBN / 2, false)
-                                   : idesc_bf16_f32(kLinBM, kLinBN, false);
+    if (rank == 0 && lane == 0) {
+      // ------------------------------------------------------------ MMA issuer
+      const uint32_t idesc = idesc_bf16_f32(kLinPairBM, kLinBN, false);
       uint32_t g = 0;
-      int i = 0;                       // tiles of this CTA so far
+      int i = 0;                       // tiles of this pair so far
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < n_units; u += gridDim.x, ++i) {
+      for (int u = pair; ok && u < n_units; u += n_pairs, ++i) {
         const int buf = i & 1;
         const uint32_t use = (uint32_t)(i >> 1);
-        // the epilogue has drained this accumulator (first use: free)
-        if (!mbar_wait(&acc_empty[buf], (use & 1u) ^ 1u, abort_flag)) break;
+        // both CTAs' epilogues have drained this accumulator (first use: free)
+        if (!mbar_wait_cluster(&acc_empty[buf], (use & 1u) ^ 1u, abort_flag)) break;
         tc_fence_after_sync();
         const uint32_t acc = tmem + (uint32_t)(buf * kLinBN);
         int kb_lo, kb_hi;
         k_range(u, kb_lo, kb_hi);
         for (int kb = kb_lo; kb < kb_hi; ++kb, ++g) {
           const int s = (int)(g % kLinStages);
-          if (!mbar_wait(&full[s], (g / kLinStages) & 1u, abort_flag)) { ok = false; break; }
+          const uint32_t ph = (g / kLinStages) & 1u;
+          if (!mbar_wait_cluster(&full[s], ph, abort_flag)) { ok = false; break; }
           tc_fence_after_sync();
           const uint32_t a = smem_u32(smem + s * kLinStageBytes);
           const uint32_t b = a + kLinABytes;
 #pragma unroll
-          for (int kk = 0; kk < kLinBK / 16; ++kk) {
-            const uint64_t ad = sdesc_sw128(a + kk * 32, 16, 1024);
-            const uint32_t accum = (kb > kb_lo || kk > 0) ? 1u : 0u;
-            if (gated) {
-              tc_mma_bf16(acc, ad, sdesc_sw128(b + kk * 32, 16, 1024), idesc, accum);
-              tc_mma_bf16(acc + kLinBN / 2, ad,
-                          sdesc_sw128(b + kLinBBytes / 2 + kk * 32, 16, 1024), idesc, accum);
-            } else {
-              tc_mma_bf16(acc, ad, sdesc_sw128(b + kk * 32, 16, 1024), idesc, accum);
-            }
-          }
-          tc_commit(&empty[s]);         // the stage is free once these MMAs are done
+          for (int kk = 0; kk < kLinBK / 16; ++kk)
+            tc_mma_bf16_pair(acc, sdesc_sw128(a + kk * 32, 16, 1024),
+                             sdesc_sw128(b + kk * 32, 16, 1024), idesc,
+                             (kb > kb_lo || kk > 0) ? 1u : 0u);
+          // the stage is free in both CTAs once these MMAs are done
+          tc_commit_pair_mc(&empty[s], 0x3);
         }
-        if (ok) tc_commit(&acc_full[buf]);
+        if (ok) tc_commit_pair_mc(&acc_full[buf], 0x3);
       }
       // every MMA issued must complete before TMEM is freed
-      tc_commit(mma_done);
+      tc_commit_pair(mma_done);
       drain_wait(mma_done, 0u, abort_flag);
     }
   } else {
@@ -200,19 +210,21 @@ __global__ void __launch_bounds__(kLinThreads, 1)
     const int row = wq * 32 + lane;
     const int etid = threadIdx.x - 64;          // 0..127 over the epilogue warps
     const uint32_t t_lane = tmem + ((uint32_t)(wq * 32) << 16);
+    const uint32_t acc_empty0 = mapa_shared(smem_u32(acc_empty), 0);
     volatile int* last_flag = reinterpret_cast<volatile int*>(smem + kLinMiscOff + 32);
     // y columns of 32 accumulator columns c0 .. c0 + 31 of tile (m, n) for
     // this thread's row; gated: g / u are the gate and up sums
+    auto out_row = [&](int m) { return m * kLinPairBM + (int)rank * kLinBM + row; };
     auto store_plain = [&](int m, int n, int c0, const float* v) {
-      const int gm = m * kLinBM + row;
-      if (gm >= p.M) return;
+      const int r = out_row(m);
+      if (r >= p.M) return;
       const int col0 = n * kLinBN;
       int seg = 0, seg_start = 0;
       while (seg < 2 && col0 >= seg_start + p.seg_cols[seg]) {
         seg_start += p.seg_cols[seg];
         ++seg;
       }
-      uint16_t* dst = p.y[seg] + (size_t)gm * p.seg_cols[seg] + (col0 - seg_start) + c0;
+      uint16_t* dst = p.y[seg] + (size_t)r * p.seg_cols[seg] + (col0 - seg_start) + c0;
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         uint4* d4 = reinterpret_cast<uint4*>(dst + q * 8);
@@ -233,9 +245,9 @@ __global__ void __launch_bounds__(kLinThreads, 1)
       }
     };
     auto store_gated = [&](int m, int n, int c0, const float* gv, const float* uv) {
-      const int gm = m * kLinBM + row;
-      if (gm >= p.M) return;
-      uint16_t* dst = p.y[0] + (size_t)gm * p.seg_cols[0] + n * (kLinBN / 2) + c0;
+      const int r = out_row(m);
+      if (r >= p.M) return;
+      uint16_t* dst = p.y[0] + (size_t)r * p.seg_cols[0] + n * (kLinBN / 2) + c0;
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         uint32_t w4[4];
@@ -247,13 +259,20 @@ __global__ void __launch_bounds__(kLinThreads, 1)
         *reinterpret_cast<uint4*>(dst + q * 8) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
       }
     };
+    // this warp is done reading accumulator buf: one arrival on the leader's
+    // barrier
+    auto release = [&](int buf) {
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(acc_empty0 + (uint32_t)buf * 8u);
+    };
     int i = 0;
-    for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++i) {
+    for (int u = pair; u < n_units; u += n_pairs, ++i) {
       const int t = u % tiles;
       const int m = t % m_tiles, n = t / m_tiles;
       const int buf = i & 1;
       const uint32_t use = (uint32_t)(i >> 1);
-      bool got = __all_sync(0xffffffffu, mbar_wait(&acc_full[buf], use & 1u, abort_flag));
+      bool got = __all_sync(0xffffffffu, mbar_wait_cluster(&acc_full[buf], use & 1u, abort_flag));
       // with split-K the four epilogue warps meet at barriers below, so they
       // leave together
       if (p.split > 1) got = named_bar_and(3, 128, got);
@@ -281,12 +300,12 @@ __global__ void __launch_bounds__(kLinThreads, 1)
           }
         }
         // this accumulator may be overwritten now
-        tc_fence_before_sync();
-        mbar_arrive(&acc_empty[buf]);
+        release(buf);
         continue;
       }
-      // split-K: publish this piece's fp32 tile, release the accumulator
-      float* part = p.partial + (size_t)u * kLinBN * kLinBM + row;
+      // split-K: publish this CTA's half of the piece's fp32 tile ([unit][rank]
+      // blocks of 256 columns x 128 rows), release the accumulator
+      float* part = p.partial + ((size_t)u * 2 + rank) * kLinBN * kLinBM + row;
 #pragma unroll 1
       for (int c = 0; c < kLinBN / 32; ++c) {
         uint32_t r[32];
@@ -295,23 +314,23 @@ __global__ void __launch_bounds__(kLinThreads, 1)
 #pragma unroll
         for (int e = 0; e < 32; ++e) part[(size_t)(c * 32 + e) * kLinBM] = __uint_as_float(r[e]);
       }
-      tc_fence_before_sync();
-      mbar_arrive(&acc_empty[buf]);
+      release(buf);
       __threadfence();
-      // the last piece of the tile to get here sums all pieces (the 128
+      // the last piece of the tile half to get here sums all pieces (the 128
       // epilogue threads all reach these barriers)
       named_bar_sync(2, 128);
+      const int counter = t * 2 + (int)rank;
       if (etid == 0) {
         __threadfence();
-        const int old = atomicAdd(&p.tile_counters[t], 1);
+        const int old = atomicAdd(&p.tile_counters[counter], 1);
         __threadfence();
         *last_flag = (old == p.split - 1) ? 1 : 0;
       }
       named_bar_sync(2, 128);
       if (*last_flag) {
         __threadfence();
-        const float* src0 = p.partial + (size_t)t * kLinBN * kLinBM + row;   // piece 0
-        const size_t piece_stride = (size_t)tiles * kLinBN * kLinBM;
+        const float* src0 = p.partial + ((size_t)t * 2 + rank) * kLinBN * kLinBM + row;  // piece 0
+        const size_t piece_stride = (size_t)tiles * 2 * kLinBN * kLinBM;
         auto sum_cols = [&](int c0, float* v) {
 #pragma unroll
           for (int e = 0; e < 32; ++e) v[e] = 0.f;
@@ -337,43 +356,40 @@ __global__ void __launch_bounds__(kLinThreads, 1)
             store_plain(m, n, c * 32, v);
           }
         }
-        if (etid == 0) p.tile_counters[t] = 0;   // ready for the next launch
+        if (etid == 0) p.tile_counters[counter] = 0;   // ready for the next launch
       }
     }
   }
+  if (rank == 1 && threadIdx.x == 0 && *abort_flag) {
+    // after an abort the odd CTA cannot see its own copies land (they
+    // complete on the leader's barrier): give any in flight time to land
+    const uint64_t t0 = global_ns();
+    while (global_ns() - t0 < 20000ull) {}
+  }
+  // neither CTA leaves while the other may still arrive on its barriers or
+  // (the leader's MMAs) read its shared memory and write its TMEM
   tc_fence_before_sync();
-  __syncthreads();
+  cluster_sync_all();
   if (warp == 1) {
     tc_fence_after_sync();
-    tmem_dealloc(tmem, C::kTmemCols);
+    tmem_dealloc_pair(tmem, kLinTmemCols);
   }
   if (threadIdx.x == 0 && *abort_flag) report_error(p.dev_error, HB_DEVERR_TIMEOUT);
 }
 
-// Tile width for a problem.  Measured on GB300 (Mistral-7B projections at
-// 512 tokens): 256-column tiles beat 128- and 64-column ones even when they
-// leave SMs idle -- a narrower MMA re-reads its 16 KB activation tile for
-// fewer output columns and becomes bound by shared memory -- so 256 is used.
-int linear_tile_n(int M, int N, int epilogue, int num_sms) {
-  (void)M;
-  (void)N;
-  (void)epilogue;
-  (void)num_sms;
-  return 256;
-}
-
-// Split-K for few tiles: when the 128 x 256 tiles cannot fill half the SMs,
-// each tile's K range is cut into up to 16 pieces of at least four 64-wide
-// blocks, so that tiles x pieces ~ SMs.  Returns the pieces (1: no split)
-// and the K blocks per piece.
+// Split-K for few tiles: when the 256 x 256 tiles cannot fill half the CTA
+// pairs, each tile's K range is cut into up to 16 pieces of at least four
+// 64-wide blocks, so that tiles x pieces ~ pairs.  Returns the pieces (1: no
+// split) and the K blocks per piece.
 int linear_split(int M, int N, int K, int epilogue, int num_sms, int* kb_per_piece) {
-  const int m_tiles = (M + kLinBM - 1) / kLinBM;
-  const int n_tiles = epilogue == 1 ? (N / 2) / 128 : N / 256;
+  const int pairs = num_sms / 2;
+  const int m_tiles = (M + kLinPairBM - 1) / kLinPairBM;
+  const int n_tiles = epilogue == 1 ? (N / 2) / (kLinBN / 2) : N / kLinBN;
   const long long tiles = (long long)m_tiles * n_tiles;
   const int k_blocks = K / kLinBK;
   *kb_per_piece = k_blocks;
-  if (tiles == 0 || 2 * tiles > num_sms) return 1;
-  int s = (int)std::min<long long>(16, std::min<long long>(num_sms / tiles, k_blocks / 4));
+  if (tiles == 0 || 2 * tiles > pairs) return 1;
+  int s = (int)std::min<long long>(16, std::min<long long>(pairs / tiles, k_blocks / 4));
   if (s < 2) return 1;
   const int kbp = (k_blocks + s - 1) / s;
   *kb_per_piece = kbp;
@@ -381,44 +397,57 @@ int linear_split(int M, int N, int K, int epilogue, int num_sms, int* kb_per_pie
 }
 
 // Workspace of the split-K path: a fixed region of kLinCounterBytes for the
-// per-tile counters at the start (the same place for every problem, so that
-// a workspace shared by calls of different shapes keeps zeroed counters --
-// split-K runs with at most num_sms / 2 tiles), then the fp32 partial tiles.
+// per-tile-half counters at the start (the same place for every problem, so
+// that a workspace shared by calls of different shapes keeps zeroed counters
+// -- split-K runs with at most num_sms / 4 tiles), then the fp32 partial
+// tiles, two 128-row halves per tile and piece.
 constexpr size_t kLinCounterBytes = 4096;
 
 size_t linear_workspace_bytes(int M, int N, int K, int epilogue, int num_sms) {
   int kbp = 0;
   const int split = linear_split(M, N, K, epilogue, num_sms, &kbp);
   if (split == 1) return 0;
-  const long long tiles = (long long)((M + kLinBM - 1) / kLinBM) * (N / 256);   // gated: F / 128
-  if (tiles * 4 > (long long)kLinCounterBytes) return 0;
-  return kLinCounterBytes + (size_t)split * tiles * 256 * kLinBM * 4;
+  const long long tiles = (long long)((M + kLinPairBM - 1) / kLinPairBM) * (N / kLinBN);
+  if (tiles * 2 * 4 > (long long)kLinCounterBytes) return 0;
+  return kLinCounterBytes + (size_t)split * tiles * 2 * kLinBN * kLinBM * 4;
 }
 
 size_t linear_counter_bytes() { return kLinCounterBytes; }
 
-template <int BN>
-static cudaError_t launch_bn(const LinearParams& p, const CUtensorMap& xmap,
-                             const CUtensorMap& wmap, int num_sms, cudaStream_t stream) {
-  const int m_tiles = (p.M + kLinBM - 1) / kLinBM;
-  const int n_tiles = p.epilogue == 1 ? p.F / (BN / 2) : p.N / BN;
+// Rows of the weight tensor map's box: the weight rows one CTA stages.
+int linear_w_box_rows() { return kLinBN / 2; }
+
+// Persistent launch: CTA pairs, at most as many as can be resident at once
+// (and at most one per tile).
+cudaError_t launch_linear(const LinearParams& p, const CUtensorMap& xmap, const CUtensorMap& wmap,
+                          int num_sms, cudaStream_t stream) {
+  const int m_tiles = (p.M + kLinPairBM - 1) / kLinPairBM;
+  const int n_tiles = p.epilogue == 1 ? p.F / (kLinBN / 2) : p.N / kLinBN;
   const int units = m_tiles * n_tiles * p.split;
   if (units == 0) return cudaSuccess;
-  const int grid = units < num_sms ? units : num_sms;
-  cudaError_t e = cudaFuncSetAttribute(linear_kernel<BN>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       LinCfg<BN>::kSmemBytes);
+  cudaError_t e = cudaFuncSetAttribute(linear_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       kLinSmemBytes);
   if (e != cudaSuccess) return e;
-  return launch_serialized(linear_kernel<BN>, grid, kLinThreads, LinCfg<BN>::kSmemBytes, stream, p,
-                           xmap, wmap);
-}
-
-// Persistent launch: one CTA per SM (at most one per tile).  `bn` is the
-// tile width the weight map's box was made for (linear_tile_n).
-cudaError_t launch_linear(const LinearParams& p, const CUtensorMap& xmap, const CUtensorMap& wmap,
-                          int bn, int num_sms, cudaStream_t stream) {
-  if (bn != 256) return cudaErrorInvalidValue;
-  return launch_bn<256>(p, xmap, wmap, num_sms, stream);
+  // resident pairs, found once per SM count
+  static std::mutex mu;
+  static int cached_sms = -1, max_pairs = 1;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (cached_sms != num_sms) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(2 * (num_sms / 2));
+      cfg.blockDim = dim3(kLinThreads);
+      cfg.dynamicSmemBytes = kLinSmemBytes;
+      int n = 0;
+      e = cudaOccupancyMaxActiveClusters(&n, linear_kernel, &cfg);
+      if (e != cudaSuccess) return e;
+      max_pairs = std::max(1, std::min(n, num_sms / 2));
+      cached_sms = num_sms;
+    }
+  }
+  const int pairs = std::min(units, max_pairs);
+  return launch_serialized(linear_kernel, 2 * pairs, kLinThreads, kLinSmemBytes, stream, p, xmap,
+                           wmap);
 }
 
 }  // namespace hb

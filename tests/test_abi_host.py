@@ -348,22 +348,27 @@ def test_linear_argument_checks():
 
 
 def test_linear_workspace_size():
-    """Split-K only when the 128 x 256 tiles cannot fill half the SMs; the
-    workspace holds a fixed 4 KB counter region, then one fp32 tile per
-    (tile, piece)."""
+    """Split-K only when the 256 x 256 tiles (one per pair of CTAs) cannot
+    fill half the 76 pairs of 152 SMs: then up to 16 pieces of at least four
+    K blocks, about one piece per pair; the workspace holds a fixed 4 KB
+    counter region, then one fp32 half tile (128 rows x 256 columns) per
+    (tile, CTA of the pair, piece)."""
     hb = lib()
     L = hb.load()
-    tile = 128 * 256 * 4
-    # 4 x 16 tiles on 152 SMs: 2 pieces
-    assert L.hb_linear_workspace_size(512, 4096, 4096, 0, 152) == 4096 + 2 * 64 * tile
+    half = 128 * 256 * 4
+    # 2 x 16 tiles on 76 pairs: 2 pieces of 32 K blocks
+    assert L.hb_linear_workspace_size(512, 4096, 4096, 0, 152) == 4096 + 2 * 32 * 2 * half
+    assert L.hb_linear_workspace_size(512, 4096, 14336, 0, 152) == 4096 + 2 * 32 * 2 * half
     # one tile, 64 K blocks: 16 pieces
-    assert L.hb_linear_workspace_size(1, 256, 4096, 0, 152) == 4096 + 16 * tile
-    # enough tiles, or too little K to split: none
+    assert L.hb_linear_workspace_size(1, 256, 4096, 0, 152) == 4096 + 16 * 1 * 2 * half
+    # enough tiles (2 x 24 = 48 > 76 / 2), or too little K to split: none
+    assert L.hb_linear_workspace_size(512, 6144, 4096, 0, 152) == 0
     assert L.hb_linear_workspace_size(8192, 4096, 4096, 0, 152) == 0
     assert L.hb_linear_workspace_size(256, 28672, 4096, 1, 152) == 0
     assert L.hb_linear_workspace_size(1, 256, 256, 0, 152) == 0
-    # gated: tiles of 128 output columns from [gate; up]
-    assert L.hb_linear_workspace_size(300, 512, 1024, 1, 152) == 4096 + 3 * 2 * 4 * tile
+    # gated: tiles of 128 output columns from [gate; up]; 2 x 2 tiles, 16 K
+    # blocks: 4 pieces of 4
+    assert L.hb_linear_workspace_size(300, 512, 1024, 1, 152) == 4096 + 4 * 4 * 2 * half
     # invalid shapes: 0
     assert L.hb_linear_workspace_size(4, 300, 64, 0, 152) == 0
     assert L.hb_linear_workspace_size(4, 256, 100, 0, 152) == 0
