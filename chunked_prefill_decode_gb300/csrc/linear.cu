@@ -303,16 +303,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kLinThreads, 1)
         release(buf);
         continue;
       }
-      // split-K: publish this CTA's half of the piece's fp32 tile ([unit][rank]
-      // blocks of 256 columns x 128 rows), release the accumulator
-      float* part = p.partial + ((size_t)u * 2 + rank) * kLinBN * kLinBM + row;
+      // split-K: publish this CTA's half of the piece's fp32 tile as 64
+      // groups of 4 columns, each group [128 rows][4] (a thread stores and
+      // later loads its row's 4 columns as one float4; a warp's accesses to a
+      // group are contiguous), release the accumulator
+      float4* part = reinterpret_cast<float4*>(p.partial + ((size_t)u * 2 + rank) * kLinBN * kLinBM) + row;
 #pragma unroll 1
       for (int c = 0; c < kLinBN / 32; ++c) {
         uint32_t r[32];
         tmem_ld32(acc + c * 32, r);
         tmem_ld_wait();
 #pragma unroll
-        for (int e = 0; e < 32; ++e) part[(size_t)(c * 32 + e) * kLinBM] = __uint_as_float(r[e]);
+        for (int g4 = 0; g4 < 8; ++g4)
+          __stcg(part + (size_t)(c * 8 + g4) * kLinBM,
+                 make_float4(__uint_as_float(r[4 * g4]), __uint_as_float(r[4 * g4 + 1]),
+                             __uint_as_float(r[4 * g4 + 2]), __uint_as_float(r[4 * g4 + 3])));
       }
       release(buf);
       __threadfence();
@@ -329,31 +334,41 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kLinThreads, 1)
       named_bar_sync(2, 128);
       if (*last_flag) {
         __threadfence();
-        const float* src0 = p.partial + ((size_t)t * 2 + rank) * kLinBN * kLinBM + row;  // piece 0
-        const size_t piece_stride = (size_t)tiles * 2 * kLinBN * kLinBM;
-        auto sum_cols = [&](int c0, float* v) {
-#pragma unroll
-          for (int e = 0; e < 32; ++e) v[e] = 0.f;
-          for (int pc = 0; pc < p.split; ++pc) {
-            const float* src = src0 + pc * piece_stride + (size_t)c0 * kLinBM;
-#pragma unroll
-            for (int e = 0; e < 32; ++e) v[e] += __ldcg(src + (size_t)e * kLinBM);
-          }
-        };
-        if (gated) {
+        // four rounds of 16 groups (plain: 64 columns; gated: 32 gate and
+        // the matching 32 up columns), two pieces' loads in flight at once:
+        // each round costs about one L2 round trip per two pieces
+        const float4* src0 =
+            reinterpret_cast<const float4*>(p.partial + ((size_t)t * 2 + rank) * kLinBN * kLinBM) + row;
+        const size_t piece_stride = (size_t)tiles * 2 * kLinBN * kLinBM / 4;   // float4s
 #pragma unroll 1
-          for (int c = 0; c < kLinBN / 2 / 32; ++c) {
-            float gv[32], uv[32];
-            sum_cols(c * 32, gv);
-            sum_cols(kLinBN / 2 + c * 32, uv);
-            store_gated(m, n, c * 32, gv, uv);
-          }
-        } else {
+        for (int rd = 0; rd < 4; ++rd) {
+          float v[64];
+#pragma unroll
+          for (int e = 0; e < 64; ++e) v[e] = 0.f;
 #pragma unroll 1
-          for (int c = 0; c < kLinBN / 32; ++c) {
-            float v[32];
-            sum_cols(c * 32, v);
-            store_plain(m, n, c * 32, v);
+          for (int pc = 0; pc < p.split; pc += 2) {
+            const bool two = pc + 1 < p.split;
+            float4 a4[16], b4[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const int grp = gated ? (i < 8 ? 8 * rd + i : 32 + 8 * rd + (i - 8)) : 16 * rd + i;
+              a4[i] = __ldcg(src0 + (size_t)pc * piece_stride + (size_t)grp * kLinBM);
+              b4[i] = two ? __ldcg(src0 + (size_t)(pc + 1) * piece_stride + (size_t)grp * kLinBM)
+                          : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              v[4 * i] += a4[i].x + b4[i].x;
+              v[4 * i + 1] += a4[i].y + b4[i].y;
+              v[4 * i + 2] += a4[i].z + b4[i].z;
+              v[4 * i + 3] += a4[i].w + b4[i].w;
+            }
+          }
+          if (gated) {
+            store_gated(m, n, 32 * rd, v, v + 32);
+          } else {
+            store_plain(m, n, 64 * rd, v);
+            store_plain(m, n, 64 * rd + 32, v + 32);
           }
         }
         if (etid == 0) p.tile_counters[counter] = 0;   // ready for the next launch
