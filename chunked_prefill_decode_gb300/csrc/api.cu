@@ -584,41 +584,59 @@ hb_status hb_plan(const hb_batch* batch, const int32_t* h_q_len,
       if (h_q_len[i] > 1) n_tiles_total += (int64_t)((h_q_len[i] + tpt - 1) / tpt) * Hkv;
     auto key_tiles = [](const ChunkItem& c) { return c.kv_tiles - c.kv_begin; };
     // the items of one layout (tpi query tiles per item) into ps.chk,
-    // longest first
+    // longest first (stable: ties keep the order row, kv head, t0).  An
+    // item's key-tile count depends on its row and t0 only, so the counts
+    // are taken once per (row, t0), Hkv items each, and every item is then
+    // written once, straight into its place.
     auto build_items = [&](int tpi) {
       const int item_tokens = tpi * tpt;
-      size_t n_raw = 0;
-      for (int i = 0; i < S; ++i)
-        if (h_q_len[i] > 1) n_raw += (size_t)((h_q_len[i] + item_tokens - 1) / item_tokens) * Hkv;
-      ps.raw.resize(n_raw);
+      // key-tile range [*kb, return) of the item of row i starting at t0
+      auto range_of = [&](int i, int t0, int* kb) {
+        const int off = h_context_len[i] - h_q_len[i];
+        const int ntok = std::min(item_tokens, h_q_len[i] - t0);
+        // with a sliding window the first row sees keys from off+t0-W+1 on
+        *kb = W > 0 ? std::max(0, off + t0 - W + 1) / kChunkKeys : 0;
+        return (off + t0 + ntok + kChunkKeys - 1) / kChunkKeys;
+      };
       int key_max = 0;
-      size_t k = 0;
+      size_t n = 0;
+      for (int i = 0; i < S; ++i) {
+        if (h_q_len[i] == 1) continue;
+        for (int t0 = 0; t0 < h_q_len[i]; t0 += item_tokens) {
+          int kb;
+          key_max = std::max(key_max, range_of(i, t0, &kb) - kb);
+          n += (size_t)Hkv;
+        }
+      }
+      ps.count.assign((size_t)key_max + 2, 0);
+      for (int i = 0; i < S; ++i) {
+        if (h_q_len[i] == 1) continue;
+        for (int t0 = 0; t0 < h_q_len[i]; t0 += item_tokens) {
+          int kb;
+          ps.count[range_of(i, t0, &kb) - kb] += Hkv;
+        }
+      }
+      int32_t run = 0;
+      for (int k = key_max; k >= 0; --k) {
+        const int32_t c = ps.count[k];
+        ps.count[k] = run;
+        run += c;
+      }
+      ps.chk.resize(n);
       int32_t q0 = 0;
       for (int i = 0; i < S; q0 += h_q_len[i], ++i) {
         if (h_q_len[i] == 1) continue;
-        const int off = h_context_len[i] - h_q_len[i];
         // the last item of a row may be short (a pair's second tile short
         // or empty)
         for (int kvh = 0; kvh < Hkv; ++kvh)
           for (int t0 = 0; t0 < h_q_len[i]; t0 += item_tokens) {
-            ChunkItem c{};
-            c.seq = i;
-            c.kv_head = kvh;
-            c.tok0 = t0;
-            c.ntok = std::min(item_tokens, h_q_len[i] - t0);
-            c.kv_tiles = (off + t0 + c.ntok + kChunkKeys - 1) / kChunkKeys;
-            // with a sliding window the first row sees keys from off+t0-W+1 on
-            c.kv_begin = W > 0 ? std::max(0, off + t0 - W + 1) / kChunkKeys : 0;
-            c.n_splits = 1;
-            c.q0 = q0;
-            c.q_len = h_q_len[i];
-            c.ctx = h_context_len[i];
-            key_max = std::max(key_max, key_tiles(c));
-            ps.raw[k++] = c;
+            int kb;
+            const int kt = range_of(i, t0, &kb);
+            ps.chk[ps.count[kt - kb]++] =
+                ChunkItem{i, kvh, t0, std::min(item_tokens, h_q_len[i] - t0), kt, q0, h_q_len[i],
+                          h_context_len[i], kb, 0, 1, 0, 0, 0, 0, 0};
           }
       }
-      // longest first (a stable counting sort on the key-tile count)
-      counting_sort_desc(ps.raw, ps.chk, ps.count, key_max, key_tiles);
     };
 
     // ---- cost model, in microseconds, from rates measured on GB300.  The
@@ -696,6 +714,10 @@ hb_status hb_plan(const hb_batch* batch, const int32_t* h_q_len,
     auto search_split = [&](double tile_us, int* out_L) -> double {
       *out_L = 0;
       if (ps.chk.empty()) return 0.0;
+      // more items than two waves: no split is allowed (every candidate
+      // below gives up at once), and the pair layout is taken without a
+      // comparison, so the end time is not needed
+      if ((int64_t)ps.chk.size() > 2LL * num_sms) return 0.0;
       const int kmax = key_tiles(ps.chk.front());
       // items by key-tile count: a candidate costs what the distinct counts
       // cost, not what the items do
