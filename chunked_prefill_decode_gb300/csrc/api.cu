@@ -384,6 +384,12 @@ bool follows_own_append(void* stream, const hb_batch* b, const void* kc, const v
 
 void internal_note_other_launch(void* stream) { note_launch(stream, LastLaunch{}); }
 
+// hb_kv_append, optionally gated on a flag raised by a copy on another
+// stream (defined below)
+hb_status internal_kv_append(const hb_batch* batch, const void* k_new, const void* v_new,
+                             void* k_cache, void* v_cache, void* stream,
+                             const uint32_t* ready_flag, uint32_t ready_value);
+
 }  // namespace hb
 
 // =========================================================================
@@ -408,6 +414,14 @@ const char* hb_status_string(hb_status s) {
 
 hb_status hb_kv_append(const hb_batch* batch, const void* k_new, const void* v_new,
                        void* k_cache, void* v_cache, void* stream) {
+  return hb::internal_kv_append(batch, k_new, v_new, k_cache, v_cache, stream, nullptr, 0);
+}
+
+}  // extern "C"
+
+hb_status hb::internal_kv_append(const hb_batch* batch, const void* k_new, const void* v_new,
+                                 void* k_cache, void* v_cache, void* stream,
+                                 const uint32_t* ready_flag, uint32_t ready_value) {
   NvtxRange range("hb_kv_append");
   try {
     hb_status s = check_batch(batch);
@@ -433,6 +447,8 @@ hb_status hb_kv_append(const hb_batch* batch, const void* k_new, const void* v_n
     p.k_cache = static_cast<uint16_t*>(k_cache);
     p.v_cache = static_cast<uint16_t*>(v_cache);
     p.dev_error = dev->err;
+    p.ready_flag = ready_flag;
+    p.ready_value = ready_value;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     LaunchTimer t(0, st);
     cudaError_t e = launch_kv_append(p, dev->num_sms, st);
@@ -452,6 +468,8 @@ hb_status hb_kv_append(const hb_batch* batch, const void* k_new, const void* v_n
     return fail(HB_ERR_CUDA, "unexpected exception in hb_kv_append");
   }
 }
+
+extern "C" {
 
 size_t hb_linear_workspace_size(int32_t M, int32_t N, int32_t K, int32_t epilogue,
                                 int32_t num_sms) {

@@ -189,6 +189,11 @@ struct AppendParams {
   uint16_t* k_cache;
   uint16_t* v_cache;
   int* dev_error;
+  // optional: k_new / v_new (and the next kernel's inputs) are copied in on
+  // another stream, which then writes ready_value (or later) to *ready_flag;
+  // the kernel reads nothing and starts the next kernel only after that
+  const uint32_t* ready_flag;
+  uint32_t ready_value;
 };
 
 }  // namespace hb

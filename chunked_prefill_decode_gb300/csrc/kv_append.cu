@@ -49,6 +49,31 @@ __global__ void __launch_bounds__(32 * kAppendMaxWarps, 2) kv_append_kernel(Appe
   // k_new / v_new may come from the kernel before this one, and the pages
   // written here may be read by it: wait for it first
   griddep_wait();
+  if (p.ready_flag) {
+    // the inputs come from a copy on another stream, which then raises the
+    // flag; the next kernel (which reads more of what that stream copied)
+    // is let in only after it.  One lane per warp polls; the CTA goes on
+    // only if every warp saw the flag (a barrier reduction, so the CTA
+    // decides as one and no shared memory is taken from the staging).  The
+    // wait is bounded: a flag that never comes is reported as a timeout and
+    // the batch is left unwritten.
+    int ready = 1;
+    if ((threadIdx.x & 31) == 0) {
+      const uint64_t t0 = global_ns();
+      while ((int32_t)(ld_acquire_u32(p.ready_flag) - p.ready_value) < 0) {
+        if (global_ns() - t0 > HB_WAIT_NS) {
+          report_error(p.dev_error, HB_DEVERR_TIMEOUT);
+          ready = 0;
+          break;
+        }
+        __nanosleep(128);
+      }
+    }
+    if (!__syncthreads_and(__shfl_sync(0xffffffffu, ready, 0))) {
+      griddep_launch_dependents();
+      return;
+    }
+  }
   griddep_launch_dependents();
   const int lane = threadIdx.x & 31;
   const int spr = (p.row_vec16 + kSegVecs - 1) / kSegVecs;   // segments per row

@@ -499,6 +499,13 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N,
          ((b_mn_major ? 1u : 0u) << 16) | ((N >> 3) << 17) | ((M >> 4) << 24);
 }
 
+// Load with acquire semantics at GPU scope (a flag another agent writes).
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
 // ---------------------------------------------------------------- CTA pairs
 // A cluster of two CTAs on two SMs sharing one tcgen05.mma.cta_group::2: the
 // even CTA (rank 0) issues the MMAs, each CTA holds half of A (M / 2 rows),

@@ -230,8 +230,12 @@ hb_status hb_decode_attention_noalloc(const hb_batch* batch,
  * flight: the step's inputs cross the host link as one packed block, the
  * plan goes up ahead of them on the input-copy stream, hb_kv_append and
  * hb_attention run on the compute stream, the output comes back on the
- * output-copy stream, and the step's slot (a set of CUDA events) orders the
- * three streams against the previous step that used the same buffers.  The
+ * output-copy stream, and the step's slot (CUDA events and a device flag)
+ * orders the three streams against the previous step that used the same
+ * buffers.  The input copy is followed by a write of the step's sequence
+ * number to the slot's flag, which the append kernel polls before it reads
+ * its inputs (so the compute stream carries no wait between two steps and
+ * each step's append launches under the previous attention's tail).  The
  * host does not wait, so one step's copies overlap the neighbouring steps'
  * kernels.  The operation is that of hb_kv_append then hb_attention (same
  * citations); only the copies and their ordering are added.
@@ -247,7 +251,9 @@ hb_status hb_decode_attention_noalloc(const hb_batch* batch,
 hb_status hb_step_layout(const hb_batch* shape, size_t offsets[HB_STEP_SECTIONS],
                          size_t* in_bytes);
 
-/* Events of one set of staging buffers, on the current device. */
+/* Events and a 4-byte device flag of one set of staging buffers, on the
+ * current device (creating a slot allocates the flag; destroying it frees
+ * it, which synchronises the device). */
 typedef struct hb_step_slot hb_step_slot;
 hb_status hb_step_slot_create(hb_step_slot** out);
 void hb_step_slot_destroy(hb_step_slot* slot);
@@ -271,9 +277,13 @@ typedef struct hb_step_buffers {
  * The step.  `shape` gives the sizes (its three device pointers are ignored:
  * the descriptors are read from d_in); h_q_len / h_context_len are the host
  * copies hb_plan needs.  On copy_in_stream: wait for the slot's last kernels,
- * plan + upload (hb_plan), copy h_in -> d_in.  On stream: wait for the
- * inputs and for the slot's last output copy, hb_kv_append, hb_attention.  On
- * copy_out_stream: wait for the kernels, copy d_out -> h_out.  The buffers
+ * plan + upload (hb_plan), copy h_in -> d_in, raise the slot's flag.  On
+ * stream: wait for the slot's last output copy if it is still pending when
+ * the step is issued, hb_kv_append (which waits for the flag on the device,
+ * bounded: a flag that does not come within about a second is reported as
+ * HB_ERR_TIMEOUT by hb_check and the step's output is undefined),
+ * hb_attention.  On copy_out_stream: wait for the kernels, copy d_out ->
+ * h_out.  The buffers
  * belong to the slot until hb_step_slot_sync says its step is over; a slot's
  * buffers must not be shared with another slot.  The host blocks only if the
  * slot's previous input copy has not yet run (its plan buffer is rewritten
