@@ -33,6 +33,7 @@ int linear_split(int M, int N, int K, int epilogue, int num_sms, int* kb_per_pie
 size_t linear_workspace_bytes(int M, int N, int K, int epilogue, int num_sms);
 size_t linear_counter_bytes();
 cudaError_t launch_wait_timeout(int* dev_error, cudaStream_t stream);
+cudaError_t launch_flag_timeout(int* dev_error, cudaStream_t stream);
 cudaError_t launch_attention(const DecodeParams& dec, int decode_grid, const ChunkParams& chk,
                              int head_dim, const CUtensorMap& dec_k, const CUtensorMap& dec_v,
                              const CUtensorMap& chunk_q, const CUtensorMap& chunk_k,
@@ -1122,6 +1123,20 @@ hb_status hb_selftest_wait_timeout(void* stream) {
     return ok();
   } catch (...) {
     return fail(HB_ERR_CUDA, "unexpected exception in hb_selftest_wait_timeout");
+  }
+}
+
+hb_status hb_selftest_flag_timeout(void* stream) {
+  try {
+    DevState* dev = nullptr;
+    hb_status s = device_state(&dev);
+    if (s != HB_OK) return s;
+    cudaError_t e = launch_flag_timeout(dev->err, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "self-test launch");
+    g_launches.fetch_add(1);
+    return ok();
+  } catch (...) {
+    return fail(HB_ERR_CUDA, "unexpected exception in hb_selftest_flag_timeout");
   }
 }
 

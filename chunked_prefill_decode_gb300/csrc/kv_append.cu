@@ -57,19 +57,7 @@ __global__ void __launch_bounds__(32 * kAppendMaxWarps, 2) kv_append_kernel(Appe
     // decides as one and no shared memory is taken from the staging).  The
     // wait is bounded: a flag that never comes is reported as a timeout and
     // the batch is left unwritten.
-    int ready = 1;
-    if ((threadIdx.x & 31) == 0) {
-      const uint64_t t0 = global_ns();
-      while ((int32_t)(ld_acquire_u32(p.ready_flag) - p.ready_value) < 0) {
-        if (global_ns() - t0 > HB_WAIT_NS) {
-          report_error(p.dev_error, HB_DEVERR_TIMEOUT);
-          ready = 0;
-          break;
-        }
-        __nanosleep(128);
-      }
-    }
-    if (!__syncthreads_and(__shfl_sync(0xffffffffu, ready, 0))) {
+    if (!__syncthreads_and(warp_wait_flag(p.ready_flag, p.ready_value, p.dev_error))) {
       griddep_launch_dependents();
       return;
     }

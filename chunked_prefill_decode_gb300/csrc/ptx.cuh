@@ -506,6 +506,27 @@ __device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
   return v;
 }
 
+// Wait until *flag (a counter another agent -- a copy engine, the host --
+// only raises) has reached `value`; lane 0 of each warp polls, the warp gets
+// its answer.  Bounded: after HB_WAIT_NS it reports HB_DEVERR_TIMEOUT in
+// dev_error and returns false.
+__device__ __forceinline__ bool warp_wait_flag(const uint32_t* flag, uint32_t value,
+                                               int* dev_error) {
+  int ready = 1;
+  if ((threadIdx.x & 31) == 0) {
+    const uint64_t t0 = global_ns();
+    while ((int32_t)(ld_acquire_u32(flag) - value) < 0) {
+      if (global_ns() - t0 > HB_WAIT_NS) {
+        report_error(dev_error, HB_DEVERR_TIMEOUT);
+        ready = 0;
+        break;
+      }
+      __nanosleep(128);
+    }
+  }
+  return __shfl_sync(0xffffffffu, ready, 0) != 0;
+}
+
 // ---------------------------------------------------------------- CTA pairs
 // A cluster of two CTAs on two SMs sharing one tcgen05.mma.cta_group::2: the
 // even CTA (rank 0) issues the MMAs, each CTA holds half of A (M / 2 rows),

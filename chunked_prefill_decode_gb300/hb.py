@@ -58,7 +58,7 @@ EXPORTED = (
     "hb_builder_create", "hb_builder_destroy", "hb_builder_add_request",
     "hb_builder_step", "hb_builder_complete", "hb_builder_counts",
     "hb_builder_free_list", "hb_builder_last_error", "hb_decode_attention_noalloc",
-    "hb_selftest_wait_timeout", "hb_linear", "hb_linear_workspace_size",
+    "hb_selftest_wait_timeout", "hb_selftest_flag_timeout", "hb_linear", "hb_linear_workspace_size",
     "hb_timing_durations", "hb_step_layout", "hb_step_slot_create", "hb_step_slot_destroy",
     "hb_step_slot_sync", "hb_step",
 )
@@ -117,6 +117,8 @@ def load():
     L.hb_linear_workspace_size.argtypes = [i32, i32, i32, i32, i32]
     L.hb_selftest_wait_timeout.restype = ctypes.c_int
     L.hb_selftest_wait_timeout.argtypes = [vp]
+    L.hb_selftest_flag_timeout.restype = ctypes.c_int
+    L.hb_selftest_flag_timeout.argtypes = [vp]
     L.hb_check.restype = ctypes.c_int
     L.hb_check.argtypes = [vp]
     L.hb_timing_enable.restype = ctypes.c_int
@@ -332,6 +334,10 @@ def hb_check(stream=None):
 
 def hb_selftest_wait_timeout(stream=None):
     _check(load().hb_selftest_wait_timeout(_stream(stream)))
+
+
+def hb_selftest_flag_timeout(stream=None):
+    _check(load().hb_selftest_flag_timeout(_stream(stream)))
 
 
 def hb_timing_enable(on: bool, keep: bool = False):

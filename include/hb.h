@@ -313,6 +313,15 @@ hb_status hb_check(void* stream);
  */
 hb_status hb_selftest_wait_timeout(void* stream);
 
+/*
+ * The same for the flag wait of hb_step's append kernel (a device counter
+ * that the input-copy stream raises): one CTA of two warps waits for a
+ * device word that nothing raises; after the time limit each warp gives up,
+ * the kernel records a timeout and returns, and hb_check() gives
+ * HB_ERR_TIMEOUT.  No fault or hang.
+ */
+hb_status hb_selftest_flag_timeout(void* stream);
+
 /* ---------------------------------------------------------------------------
  * Linear layer of a hybrid batch on the tensor cores: y = x W^T.  Cited
  * passage: the first page, §问题背景 (两阶段天然不对称) -- every token of the

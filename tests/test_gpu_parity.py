@@ -354,6 +354,18 @@ def test_wait_timeout_is_reported_and_context_survives():
     _full_check(workloads.tiny(0))     # the context still works
 
 
+def test_flag_wait_timeout_is_reported_and_context_survives():
+    """hb_step's append waits for its slot's flag with the same bounded wait:
+    on a flag that is never raised it ends with a status, not a hang."""
+    hb = lib()
+    hb.hb_selftest_flag_timeout()
+    with pytest.raises(hb.HbError) as e:
+        hb.hb_check()
+    assert e.value.status == 7
+    hb.hb_check()
+    _full_check(workloads.tiny(0))
+
+
 def test_staged_step_through_host_buffers():
     """The packed host staging (one copy in, one out, on side streams) gives
     the same output as the device-resident step, and matches the oracle."""
