@@ -469,7 +469,7 @@ def run_native(args):
 
     def step():
         hb.hb_kv_append(db.batch, ten.k_new, ten.v_new, kc, vc)
-        hb.hb_attention(db.batch, plan, ten.q, kc, vc, scale, out, ws)
+        hb.hb_attention_new_kv(db.batch, plan, ten.q, ten.k_new, ten.v_new, kc, vc, scale, out, ws)
 
     for _ in range(max(args.warmup, 3)):
         step()
@@ -672,7 +672,8 @@ def run_seed_sweep(args):
 
             def step():
                 hb.hb_kv_append(db.batch, ten.k_new, ten.v_new, ten.k_cache, ten.v_cache)
-                hb.hb_attention(db.batch, plan, ten.q, ten.k_cache, ten.v_cache, scale, out, ws)
+                hb.hb_attention_new_kv(db.batch, plan, ten.q, ten.k_new, ten.v_new, ten.k_cache,
+                                       ten.v_cache, scale, out, ws)
             for _ in range(max(args.warmup, 3)):
                 step()
             torch.cuda.synchronize(dev)
@@ -735,7 +736,8 @@ def run_chunk_sweep(args):
             flush.fill_(1)
             e0.record(stream)
             hb.hb_kv_append(db.batch, ten.k_new, ten.v_new, ten.k_cache, ten.v_cache)
-            hb.hb_attention(db.batch, plan, ten.q, ten.k_cache, ten.v_cache, scale, out, ws)
+            hb.hb_attention_new_kv(db.batch, plan, ten.q, ten.k_new, ten.v_new, ten.k_cache,
+                                   ten.v_cache, scale, out, ws)
             e1.record(stream)
         torch.cuda.synchronize(dev)
         hb.hb_check()

@@ -37,7 +37,8 @@ cudaError_t launch_flag_timeout(int* dev_error, cudaStream_t stream);
 cudaError_t launch_attention(const DecodeParams& dec, int decode_grid, const ChunkParams& chk,
                              int head_dim, const CUtensorMap& dec_k, const CUtensorMap& dec_v,
                              const CUtensorMap& chunk_q, const CUtensorMap& chunk_k,
-                             const CUtensorMap& chunk_v, const void* k_cache,
+                             const CUtensorMap& chunk_v, const CUtensorMap& chunk_knew,
+                             const CUtensorMap& chunk_vnew, const void* k_cache,
                              const void* v_cache, cudaStream_t stream, bool early,
                              bool pairs_only);
 }  // namespace hb
@@ -390,6 +391,13 @@ void internal_note_other_launch(void* stream) { note_launch(stream, LastLaunch{}
 hb_status internal_kv_append(const hb_batch* batch, const void* k_new, const void* v_new,
                              void* k_cache, void* v_cache, void* stream,
                              const uint32_t* ready_flag, uint32_t ready_value);
+
+// hb_attention, optionally reading the new tokens' K/V from k_new / v_new
+// (defined below)
+hb_status internal_attention(const hb_batch* batch, const void* h_plan, const void* q,
+                             const void* k_new, const void* v_new, const void* k_cache,
+                             const void* v_cache, float softmax_scale, void* out,
+                             void* d_workspace, void* stream);
 
 }  // namespace hb
 
@@ -965,6 +973,27 @@ hb_status hb_plan(const hb_batch* batch, const int32_t* h_q_len,
 hb_status hb_attention(const hb_batch* batch, const void* h_plan, const void* q,
                        const void* k_cache, const void* v_cache, float softmax_scale,
                        void* out, void* d_workspace, void* stream) {
+  return hb::internal_attention(batch, h_plan, q, nullptr, nullptr, k_cache, v_cache,
+                                softmax_scale, out, d_workspace, stream);
+}
+
+hb_status hb_attention_new_kv(const hb_batch* batch, const void* h_plan, const void* q,
+                              const void* k_new, const void* v_new, const void* k_cache,
+                              const void* v_cache, float softmax_scale, void* out,
+                              void* d_workspace, void* stream) {
+  if (!k_new || !v_new) return fail(HB_ERR_INVALID_ARG, "k_new and v_new must be non-NULL");
+  return hb::internal_attention(batch, h_plan, q, k_new, v_new, k_cache, v_cache,
+                                softmax_scale, out, d_workspace, stream);
+}
+
+}  // extern "C"
+
+// hb_attention; with k_new / v_new (the append's inputs) the chunk CTAs read
+// the pages that hold only new tokens from there
+hb_status hb::internal_attention(const hb_batch* batch, const void* h_plan, const void* q,
+                                 const void* k_new, const void* v_new, const void* k_cache,
+                                 const void* v_cache, float softmax_scale, void* out,
+                                 void* d_workspace, void* stream) {
   NvtxRange range("hb_attention");
   try {
     hb_status s = check_batch(batch);
@@ -987,6 +1016,8 @@ hb_status hb_attention(const hb_batch* batch, const void* h_plan, const void* q,
     if ((s = check_ptr(out, "out")) != HB_OK) return s;
     if ((s = check_ptr(k_cache, "k_cache")) != HB_OK) return s;
     if ((s = check_ptr(v_cache, "v_cache")) != HB_OK) return s;
+    if (k_new && (s = check_ptr(k_new, "k_new")) != HB_OK) return s;
+    if (v_new && (s = check_ptr(v_new, "v_new")) != HB_OK) return s;
     if (!d_workspace || (reinterpret_cast<uintptr_t>(d_workspace) & 255u))
       return fail(HB_ERR_INVALID_ARG, "d_workspace must be non-NULL and 256-byte aligned");
     DevState* dev = nullptr;
@@ -1000,7 +1031,9 @@ hb_status hb_attention(const hb_batch* batch, const void* h_plan, const void* q,
     cudaStream_t st = static_cast<cudaStream_t>(stream);
 
     // one launch: decode CTAs first, then one CTA per chunk item
-    CUtensorMap dec_k, dec_v, chunk_q, chunk_k, chunk_v;
+    CUtensorMap dec_k, dec_v, chunk_q, chunk_k, chunk_v, chunk_knew, chunk_vnew;
+    std::memset(&chunk_knew, 0, sizeof(chunk_knew));
+    std::memset(&chunk_vnew, 0, sizeof(chunk_vnew));
     std::memset(&chunk_k, 0, sizeof(chunk_k));
     std::memset(&chunk_v, 0, sizeof(chunk_v));
     std::memset(&dec_k, 0, sizeof(dec_k));
@@ -1056,6 +1089,19 @@ hb_status hb_attention(const hb_batch* batch, const void* h_plan, const void* q,
       const cuuint32_t kbox[3] = {64, 1, (cuuint32_t)kPageSize};
       if ((s = encode_map(&chunk_k, k_cache, 3, kdims, kstr, kbox, "chunk K")) != HB_OK) return s;
       if ((s = encode_map(&chunk_v, v_cache, 3, kdims, kstr, kbox, "chunk V")) != HB_OK) return s;
+      if (k_new && v_new) {
+        // the new rows [total_q, Hkv, D] viewed as (D, kv head, token), the
+        // same 16-token boxes as a page
+        const cuuint64_t ndims[3] = {(cuuint64_t)D, (cuuint64_t)Hkv, (cuuint64_t)batch->total_q};
+        if ((s = encode_map(&chunk_knew, k_new, 3, ndims, kstr, kbox, "chunk K (new rows)")) != HB_OK)
+          return s;
+        if ((s = encode_map(&chunk_vnew, v_new, 3, ndims, kstr, kbox, "chunk V (new rows)")) != HB_OK)
+          return s;
+        cp.has_new = 1;
+      } else {
+        chunk_knew = chunk_k;
+        chunk_vnew = chunk_v;
+      }
       cp.items = reinterpret_cast<const ChunkItem*>(ws + (size_t)h.num_decode_items * sizeof(DecodeItem));
       cp.num_items = h.num_chunk_items;
       cp.cu_q_len = batch->cu_q_len;
@@ -1078,8 +1124,8 @@ hb_status hb_attention(const hb_batch* batch, const void* h_plan, const void* q,
       const bool early = follows_own_append(stream, batch, k_cache, v_cache);
       LaunchTimer t(1, st);
       cudaError_t e = launch_attention(dp, h.decode_grid, cp, D, dec_k, dec_v, chunk_q, chunk_k,
-                                       chunk_v, k_cache, v_cache, st, early,
-                                       h.chunk_pairs_only != 0);
+                                       chunk_v, chunk_knew, chunk_vnew, k_cache, v_cache, st,
+                                       early, h.chunk_pairs_only != 0);
       t.done();
       if (e != cudaSuccess) return cuda_fail(e, "attention launch");
       note_launch(stream, LastLaunch{});
@@ -1090,6 +1136,8 @@ hb_status hb_attention(const hb_batch* batch, const void* h_plan, const void* q,
     return fail(HB_ERR_CUDA, "unexpected exception in hb_attention");
   }
 }
+
+extern "C" {
 
 hb_status hb_check(void* stream) {
   try {

@@ -45,7 +45,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                      const __grid_constant__ CUtensorMap dec_v,
                      const __grid_constant__ CUtensorMap chunk_q,
                      const __grid_constant__ CUtensorMap chunk_k,
-                     const __grid_constant__ CUtensorMap chunk_v) {
+                     const __grid_constant__ CUtensorMap chunk_v,
+                     const __grid_constant__ CUtensorMap chunk_knew,
+                     const __grid_constant__ CUtensorMap chunk_vnew) {
   extern __shared__ uint8_t smem_raw[];
   // the next kernel may be scheduled now (it waits for this one to finish).
   // After the append of this batch the previous grid is waited for only
@@ -58,8 +60,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   if ((int)blockIdx.x < p.decode_grid)
     decode_cta<D>(p.dec, p.dl, dec_k, dec_v, smem, blockIdx.x);
   else
-    chunk_cta<D, kPairs>(p.chk, chunk_q, chunk_k, chunk_v, p.k_cache, p.v_cache, smem,
-                         blockIdx.x - p.decode_grid);
+    chunk_cta<D, kPairs>(p.chk, chunk_q, chunk_k, chunk_v, chunk_knew, chunk_vnew, p.k_cache,
+                         p.v_cache, smem, blockIdx.x - p.decode_grid);
 }
 
 // Dynamic shared memory of the attention kernel for this geometry.
@@ -72,13 +74,15 @@ int attention_smem_bytes(int head_dim, int kvh_block, int group) {
 // Launch decode_grid decode CTAs followed by one CTA per chunk item.  Either
 // part may be empty (dec.num_items == 0: no decode CTA).  dec.kvh_block and
 // dec.group must be set in every case (they size the shared memory).
+// chunk_knew / chunk_vnew map k_new / v_new when chk.has_new (else any map).
 // pairs_only: every chunk item is an unsplit pair of query tiles, and the
 // kernel instantiation without the single-tile and split paths runs (the
 // pair loop compiles to faster code on its own).
 cudaError_t launch_attention(const DecodeParams& dec, int decode_grid, const ChunkParams& chk,
                              int head_dim, const CUtensorMap& dec_k, const CUtensorMap& dec_v,
                              const CUtensorMap& chunk_q, const CUtensorMap& chunk_k,
-                             const CUtensorMap& chunk_v, const void* k_cache,
+                             const CUtensorMap& chunk_v, const CUtensorMap& chunk_knew,
+                             const CUtensorMap& chunk_vnew, const void* k_cache,
                              const void* v_cache, cudaStream_t stream, bool early,
                              bool pairs_only) {
   AttnParams p{};
@@ -94,6 +98,7 @@ cudaError_t launch_attention(const DecodeParams& dec, int decode_grid, const Chu
   if (grid == 0) return cudaSuccess;
   const int smem = attention_smem_bytes(head_dim, dec.kvh_block, dec.group);
   using Kernel = void (*)(const AttnParams, const __grid_constant__ CUtensorMap,
+                          const __grid_constant__ CUtensorMap, const __grid_constant__ CUtensorMap,
                           const __grid_constant__ CUtensorMap, const __grid_constant__ CUtensorMap,
                           const __grid_constant__ CUtensorMap, const __grid_constant__ CUtensorMap);
   const int which = (head_dim == 128 ? 2 : 0) + (pairs_only ? 1 : 0);
@@ -119,7 +124,7 @@ cudaError_t launch_attention(const DecodeParams& dec, int decode_grid, const Chu
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   return launch_serialized(kernel, grid, kAttnThreads, smem, stream, p, dec_k, dec_v, chunk_q,
-                           chunk_k, chunk_v);
+                           chunk_k, chunk_v, chunk_knew, chunk_vnew);
 }
 
 }  // namespace hb

@@ -165,6 +165,7 @@ __device__ __forceinline__ void merge_pieces(const float* o0, const float* ml0, 
 template <int D, bool kPairs>
 __device__ __forceinline__ void chunk_cta(const ChunkParams& p, const CUtensorMap& qmap,
                                           const CUtensorMap& kmap, const CUtensorMap& vmap,
+                                          const CUtensorMap& knewmap, const CUtensorMap& vnewmap,
                                           const uint16_t* __restrict__ k_cache,
                                           const uint16_t* __restrict__ v_cache,
                                           uint8_t* smem, int item) {
@@ -283,12 +284,22 @@ __device__ __forceinline__ void chunk_cta(const ChunkParams& p, const CUtensorMa
     const int c_l = lane % CH;
     const bool issuer = lane < my_pages * CH;
     uint32_t issued = 0, par = 0;   // bit s: stage s (K in 0..NK-1, V from NK)
-    // key tiles that hold the chunk's own tokens (from position off on,
-    // written by the append before this launch) are read after griddep_wait
+    // The chunk's own tokens (positions off .. ctx-1) are written into their
+    // pages by the append before this launch.  With the append's inputs at
+    // hand (p.has_new), the pages from the first page boundary at or after
+    // off on are read from k_new / v_new instead (token q0 + position - off)
+    // and need no wait; what is left for after griddep_wait is the one page
+    // that holds position off when off is not page-aligned -- and, without
+    // k_new / v_new, every page from off on.
+    const int new_from = p.has_new ? (off + kPageSize - 1) / kPageSize * kPageSize : INT_MAX;
     bool dep_done = false;
-    auto tma_tile = [&](const CUtensorMap* map, uint8_t* stage, uint64_t* full, int batch_reg,
-                        int jt, int bit, uint32_t ph) {
-      if (!dep_done && (jb + jt) * kChunkKeys + kChunkKeys - 1 >= off) {
+    auto tma_tile = [&](const CUtensorMap* map, const CUtensorMap* new_map, uint8_t* stage,
+                        uint64_t* full, int batch_reg, int jt, int bit, uint32_t ph) {
+      const int tpos = (jb + jt) * kChunkKeys;
+      const bool needs_append = p.has_new ? (off % kPageSize != 0 && tpos <= off &&
+                                             off < tpos + kChunkKeys)
+                                          : tpos + kChunkKeys - 1 >= off;
+      if (!dep_done && needs_append) {
         griddep_wait();
         fence_proxy_async_global();
         dep_done = true;
@@ -297,9 +308,15 @@ __device__ __forceinline__ void chunk_cta(const ChunkParams& p, const CUtensorMa
                                   ((jt % kTilesPerBatch) * kPagesPerTile + (pp_l & 7)) & 31);
       if (lane == 0) mbar_arrive_expect_tx(full, (uint32_t)(my_pages * CH * 2048));
       __syncwarp();
-      if (issuer)
-        tma_load_3d(stage + c_l * 16384 + pp_l * 2048, map, full, c_l * 64, it.kv_head,
-                    phys_of(raw) * kPageSize);
+      if (issuer) {
+        const int page_pos = tpos + pp_l * kPageSize;
+        if (page_pos >= new_from && page_pos < ctx)
+          tma_load_3d(stage + c_l * 16384 + pp_l * 2048, new_map, full, c_l * 64, it.kv_head,
+                      q0 + (page_pos - off));
+        else
+          tma_load_3d(stage + c_l * 16384 + pp_l * 2048, map, full, c_l * 64, it.kv_head,
+                      phys_of(raw) * kPageSize);
+      }
       if (lane == 0) {
         issued |= 1u << bit;
         par = (par & ~(1u << bit)) | (ph << bit);
@@ -319,7 +336,7 @@ __device__ __forceinline__ void chunk_cta(const ChunkParams& p, const CUtensorMa
         ok = lane != 0 || mbar_wait(&k_empty[s], ph ^ 1u, abort_flag);
         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
         if (!ok) break;
-        tma_tile(&kmap, sK + s * C::kTileBytes, &k_full[s], bt_cur, j, s, ph);
+        tma_tile(&kmap, &knewmap, sK + s * C::kTileBytes, &k_full[s], bt_cur, j, s, ph);
       }
       if (j >= 1) {
         const int jv = j - 1;
@@ -329,7 +346,7 @@ __device__ __forceinline__ void chunk_cta(const ChunkParams& p, const CUtensorMa
         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
         if (!ok) break;
         const int breg = (jv / kTilesPerBatch == j / kTilesPerBatch) ? bt_cur : bt_prev;
-        tma_tile(&vmap, sV + s * C::kTileBytes, &v_full[s], breg, jv, NK + s, ph);
+        tma_tile(&vmap, &vnewmap, sV + s * C::kTileBytes, &v_full[s], breg, jv, NK + s, ph);
       }
     }
     if (lane == 0) {

@@ -154,6 +154,10 @@ struct ChunkParams {
   float* part_o;          // [slots, D, 128]: unnormalised O, row fastest
   float* part_ml;         // [slots, 2, 128]: row maximum (log2 units), row sum
   int32_t window;         // sliding window in tokens, 0 = none
+  // 1: the batch's new K/V rows are also given as k_new / v_new (the append's
+  // inputs, [total_q, Hkv, D]): pages that hold only new tokens are read from
+  // there, so the chunk does not wait for the append that writes them
+  int32_t has_new;
 };
 
 // Linear layer y = x W^T (linear.cu).  epilogue: 0 store, 1 gated (W has

@@ -32,7 +32,8 @@ namespace hb {
 cudaError_t launch_attention(const DecodeParams& dec, int decode_grid, const ChunkParams& chk,
                              int head_dim, const CUtensorMap& dec_k, const CUtensorMap& dec_v,
                              const CUtensorMap& chunk_q, const CUtensorMap& chunk_k,
-                             const CUtensorMap& chunk_v, const void* k_cache,
+                             const CUtensorMap& chunk_v, const CUtensorMap& chunk_knew,
+                             const CUtensorMap& chunk_vnew, const void* k_cache,
                              const void* v_cache, cudaStream_t stream, bool early,
                              bool pairs_only);
 hb_status internal_fail(hb_status s, const char* msg);
@@ -191,8 +192,8 @@ extern "C" hb_status hb_decode_attention_noalloc(const hb_batch* batch, const in
     none.group = g;
     CUtensorMap unused;
     std::memset(&unused, 0, sizeof(unused));
-    e = launch_attention(p, part.grid, none, D, kmap, vmap, unused, unused, unused, k_cache,
-                         v_cache, st, /*early=*/false, /*pairs_only=*/false);
+    e = launch_attention(p, part.grid, none, D, kmap, vmap, unused, unused, unused, unused,
+                         unused, k_cache, v_cache, st, /*early=*/false, /*pairs_only=*/false);
     if (e != cudaSuccess) return internal_fail(HB_ERR_CUDA, "decode launch failed");
     internal_note_other_launch(stream);
     internal_count_launch();

@@ -16,7 +16,8 @@
 // a 106 us step).  The output copy is ordered by the slot's events, and the
 // kernels wait for the slot's previous output copy only if it has not
 // finished by the time the step is issued.  The kernels are those of
-// hb_kv_append and hb_attention.
+// hb_kv_append and hb_attention_new_kv (the chunks read their new K/V rows
+// from the packed block rather than after the append).
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -208,8 +209,9 @@ hb_status hb_step(const hb_batch* shape, const int32_t* h_q_len, const int32_t* 
     s = hb::internal_kv_append(&b, d_in + off[1], d_in + off[2], k_cache, v_cache, stream,
                                slot->flag, seq);
     if (s != HB_OK) return s;
-    s = hb_attention(&b, buf->h_plan, d_in + off[0], k_cache, v_cache, softmax_scale, buf->d_out,
-                     buf->d_workspace, stream);
+    // the chunks read their new rows from d_in, not after the append
+    s = hb_attention_new_kv(&b, buf->h_plan, d_in + off[0], d_in + off[1], d_in + off[2], k_cache,
+                            v_cache, softmax_scale, buf->d_out, buf->d_workspace, stream);
     if (s != HB_OK) return s;
     if (cudaEventRecord(slot->done, s_run) != cudaSuccess)
       return step_fail(HB_ERR_CUDA, "recording the kernels' end failed");

@@ -239,8 +239,8 @@ class GpuStep:
         e0, e1 = self.ev
         e0.record()
         self.hb.hb_kv_append(db.batch, kn, vn, self.k_pool, self.v_pool)
-        self.hb.hb_attention(db.batch, self.plan, q, self.k_pool, self.v_pool, self.scale,
-                             out, self.ws)
+        self.hb.hb_attention_new_kv(db.batch, self.plan, q, kn, vn, self.k_pool, self.v_pool,
+                                    self.scale, out, self.ws)
         e1.record()
         torch.cuda.synchronize(self.dev)
         self.hb.hb_check()

@@ -54,6 +54,7 @@ class HbBatch(ctypes.Structure):
 
 EXPORTED = (
     "hb_last_error", "hb_status_string", "hb_kv_append", "hb_plan", "hb_attention",
+    "hb_attention_new_kv",
     "hb_check", "hb_timing_enable", "hb_timing_read", "hb_launch_count",
     "hb_builder_create", "hb_builder_destroy", "hb_builder_add_request",
     "hb_builder_step", "hb_builder_complete", "hb_builder_counts",
@@ -108,6 +109,9 @@ def load():
     L.hb_plan.argtypes = [P(HbBatch), vp, vp, i32, vp, P(sz), vp, P(sz), vp]
     L.hb_attention.restype = ctypes.c_int
     L.hb_attention.argtypes = [P(HbBatch), vp, vp, vp, vp, ctypes.c_float, vp, vp, vp]
+    L.hb_attention_new_kv.restype = ctypes.c_int
+    L.hb_attention_new_kv.argtypes = [P(HbBatch), vp, vp, vp, vp, vp, vp, ctypes.c_float, vp,
+                                      vp, vp]
     L.hb_decode_attention_noalloc.restype = ctypes.c_int
     L.hb_decode_attention_noalloc.argtypes = [P(HbBatch), vp, vp, vp, vp, vp, ctypes.c_float,
                                               vp, vp]
@@ -314,6 +318,17 @@ def hb_attention(batch, plan, q, k_cache, v_cache, scale, out, workspace, stream
                                _bf16(k_cache, "k_cache"), _bf16(v_cache, "v_cache"),
                                ctypes.c_float(scale), _bf16(out, "out"), _ptr(workspace),
                                _stream(stream)))
+
+
+def hb_attention_new_kv(batch, plan, q, k_new, v_new, k_cache, v_cache, scale, out, workspace,
+                        stream=None):
+    """hb_attention that reads the chunks' new K/V rows from k_new / v_new (the
+    append's inputs) instead of waiting for the append to write them."""
+    _check(load().hb_attention_new_kv(ctypes.byref(batch), _ptr(plan), _bf16(q, "q"),
+                                      _bf16(k_new, "k_new"), _bf16(v_new, "v_new"),
+                                      _bf16(k_cache, "k_cache"), _bf16(v_cache, "v_cache"),
+                                      ctypes.c_float(scale), _bf16(out, "out"), _ptr(workspace),
+                                      _stream(stream)))
 
 
 def hb_decode_attention_noalloc(batch, q_len, context_len, q, k_cache, v_cache, scale,

@@ -11,7 +11,7 @@ are elementwise and outside the pages, are left out):
 
     q, k, v = split(x Wqkv^T)                    hb_linear, split epilogue
     append k, v to the paged cache               hb_kv_append
-    a = attention(q, cache)                       hb_plan + hb_attention
+    a = attention(q, cache)                       hb_plan + hb_attention_new_kv
     x = x + a Wo^T                                hb_linear, residual epilogue
     m = silu(x Wg^T) * (x Wu^T)                   hb_linear, gated epilogue
     x = x + m Wd^T                                hb_linear, residual epilogue
@@ -104,8 +104,8 @@ class HybridBlock:
         if plan or self._plan is None:
             self._plan, self._ws = hb.hb_plan(batch.batch, batch.q_len, batch.context_len,
                                               self._sms, workspace=self._ws, plan=self._plan)
-        hb.hb_attention(batch.batch, self._plan, b["q"], k_cache, v_cache, self.scale, b["a"],
-                        self._ws)
+        hb.hb_attention_new_kv(batch.batch, self._plan, b["q"], b["k"], b["v"], k_cache, v_cache,
+                               self.scale, b["a"], self._ws)
         hb.hb_linear(b["a"], self.w_o, [x], epilogue=hb.LINEAR_RESIDUAL)
         if snapshot:
             b["h"] = x.clone()

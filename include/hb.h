@@ -184,6 +184,24 @@ hb_status hb_attention(const hb_batch* batch, const void* h_plan,
                        void* d_workspace, void* stream);
 
 /*
+ * hb_attention, with the batch's new K/V rows also given as k_new / v_new
+ * (the arrays passed to hb_kv_append for this batch, [total_q, Hkv, D] bf16,
+ * 16-byte aligned).  The result is the same; the chunk rows read the pages
+ * that hold only their sequence's new tokens from k_new / v_new instead of
+ * from the caches, so they do not wait for the append kernel that writes
+ * those pages (the one page holding a chunk's first token, when that token
+ * does not start a page, and the decode rows' last pages are still read
+ * from the caches after the append).  The caches must receive the new rows
+ * by hb_kv_append as usual, queued before this call on the same stream.
+ * Same passages as hb_attention.  Errors: as hb_attention;
+ * HB_ERR_INVALID_ARG for a NULL or misaligned k_new / v_new.
+ */
+hb_status hb_attention_new_kv(const hb_batch* batch, const void* h_plan, const void* q,
+                              const void* k_new, const void* v_new, const void* k_cache,
+                              const void* v_cache, float softmax_scale, void* out,
+                              void* d_workspace, void* stream);
+
+/*
  * Decode attention without a workspace, for callers that cannot allocate
  * device memory.  (The pages have no counterpart of this call: it exists for
  * callers such as a serving engine that gives nearly all free HBM to its

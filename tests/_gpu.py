@@ -19,9 +19,10 @@ def sms():
     return torch.cuda.get_device_properties(0).multi_processor_count
 
 
-def gpu_step(layout, ten, scale=None, repeats=1, check=True):
-    """Append + plan + attention on cuda:0.  Returns (k_cache, v_cache, out)
-    as device tensors (the caches after append)."""
+def gpu_step(layout, ten, scale=None, repeats=1, check=True, new_kv=False):
+    """Append + plan + attention on cuda:0 (new_kv: hb_attention_new_kv, which
+    reads the chunks' new rows from k_new / v_new).  Returns (k_cache,
+    v_cache, out) as device tensors (the caches after append)."""
     hb = lib()
     sh = layout.shape
     scale = scale if scale is not None else 1.0 / math.sqrt(sh.head_dim)
@@ -35,7 +36,10 @@ def gpu_step(layout, ten, scale=None, repeats=1, check=True):
     hb.hb_kv_append(db.batch, kn, vn, kc, vc)
     plan, ws = hb.hb_plan(db.batch, db.q_len, db.context_len, sms())
     for _ in range(repeats):
-        hb.hb_attention(db.batch, plan, q, kc, vc, scale, out, ws)
+        if new_kv:
+            hb.hb_attention_new_kv(db.batch, plan, q, kn, vn, kc, vc, scale, out, ws)
+        else:
+            hb.hb_attention(db.batch, plan, q, kc, vc, scale, out, ws)
     if check:
         hb.hb_check()
     torch.cuda.synchronize()

@@ -63,6 +63,33 @@ def test_other_head_geometries(geom):
     _full_check(layout_from_rows(Shape(hq, hkv, d), rows, 12), seed=12)
 
 
+@pytest.mark.parametrize("geom,rows,window", [
+    ((32, 8, 128), [(512, 1024)], 0),                    # chunk at offset 512: page-aligned
+    ((32, 8, 128), [(257, 1000)], 0),                    # offset 743: its first page straddles
+    ((32, 8, 128), [(100, 100)], 0),                     # offset 0: every page is new
+    ((56, 8, 128), [(1, 3000)] * 4 + [(2016, 7059)], 0),  # pairs, offset 5043
+    ((56, 8, 128), [(1, 2000)] * 2 + [(48, 6048)], 0),
+    ((8, 8, 64), [(300, 3000), (1, 50), (33, 33)], 0),
+    ((16, 1, 128), [(300, 9000)], 0),                    # split pieces
+    ((32, 8, 128), [(448, 4000), (1, 3000)], 1024),      # sliding window
+    ((32, 8, 128), [(130, 700), (5, 37), (1, 3)], 7),
+])
+def test_attention_with_new_rows(geom, rows, window):
+    """hb_attention_new_kv reads the chunks' pages of new tokens from k_new /
+    v_new instead of the caches: with the same plan the products are the same
+    on the same bf16 values, so the output equals hb_attention's bit for bit,
+    and it meets the oracle's bars."""
+    hq, hkv, d = geom
+    lay = layout_from_rows(Shape(hq, hkv, d, sliding_window=window), rows, 21)
+    ten = workloads.make_tensors(lay, 21)
+    _, _, out_cache = gpu_step(lay, ten)
+    kc, vc, out_new = gpu_step(lay, ten, new_kv=True)
+    assert torch.equal(out_cache.view(torch.int16), out_new.view(torch.int16))
+    kp, vp, ref = oracle_step(lay, ten)
+    assert np.array_equal(bits(kc), kp) and np.array_equal(bits(vc), vp)
+    compare(out_new, ref)
+
+
 @pytest.mark.parametrize("geom,rows", [
     ((32, 8, 128), [(64, 4160)]),
     ((32, 8, 128), [(1, 2048)] * 8 + [(96, 6000)]),
