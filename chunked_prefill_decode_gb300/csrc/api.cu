@@ -674,12 +674,19 @@ hb_status hb_plan(const hb_batch* batch, const int32_t* h_q_len,
     // time) / SMs, nor before the longest chunk item.  That estimate is flat
     // over a range of G whose ends it knows only roughly, so the middle of
     // the range within 2% of the best is taken.  A pair of query tiles
-    // shares its page gather, so it costs 1.6x one tile, not 2x.
+    // shares its page gather, so it costs 1.6x one tile, not 2x.  A split
+    // piece pays its own setup (barriers, Q load, pipeline fill) and its
+    // publish-and-merge: per-CTA timelines show split pair pieces at 1.9-2.2
+    // us per key tile against 1.56 for whole pairs, and on the chunk-only
+    // sweep (8192-token prompt, chunks of 256 / 512 / 1024) a piece cost of
+    // 10 us gave 1.310 / 0.804 / 0.584 ms against 1.376 / 0.833 / 0.637 ms
+    // at 3 us (6: 1.311 / 0.814 / 0.586, 15: 1.298 / 0.824 / 0.585), the
+    // batches with decode rows unchanged.
     constexpr double kHbmBytesPerUs = 7.0e6;      // whole-GPU HBM stream
     constexpr double kSmBytesPerUs = 8.5e4;       // one SM's stream ceiling
     constexpr double kPairTileUs = 2.0;           // 2-tile item x one key tile
     constexpr double kSingleTileUs = 1.25;        // 1-tile item x one key tile
-    constexpr double kPieceUs = 3.0;              // extra cost of one split piece
+    constexpr double kPieceUs = 10.0;             // extra cost of one split piece
     constexpr int kMinPieceTiles = 4;             // key tiles per split piece (min)
     double decode_bytes = 0.0;
     for (int i = 0; i < S; ++i)

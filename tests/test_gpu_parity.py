@@ -117,7 +117,7 @@ def test_split_key_ranges(geom, rows):
     ((32, 8, 128), [(1, 2048)] * 8 + [(512, 7000)], 0),
     ((16, 1, 128), [(600, 9000)], 0),
     ((32, 8, 128), [(200, 5000), (300, 6000)], 0),
-    ((32, 8, 128), [(512, 8192)], 3000),
+    ((32, 8, 128), [(256, 8192)], 3000),
 ])
 def test_split_pairs(geom, rows, window):
     """Pairs of query tiles whose key range is cut into pieces (with single
