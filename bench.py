@@ -524,7 +524,11 @@ def run_native(args):
         stg.h_cu_q_len.copy_(torch.from_numpy(layout.cu_q_len))
         stg.h_context_len.copy_(torch.from_numpy(layout.context_len))
         stg.h_block_table.copy_(torch.from_numpy(np.ascontiguousarray(layout.block_table)))
-        stg.plan, stg.ws = hb.hb_plan(stg.batch, layout.q_len, layout.context_len, sms)
+        plan_h, stg.ws = hb.hb_plan(stg.batch, layout.q_len, layout.context_len, sms)
+        # the plan buffer hb_step rewrites and uploads every step, page-locked
+        # so that its copy is asynchronous like the inputs'
+        stg.plan = torch.empty(plan_h.nbytes, dtype=torch.uint8, pin_memory=True).numpy()
+        stg.plan[:] = plan_h
         stg.slot = hb.StepSlot()
         stg.bufs = stg.step_buffers(stg.plan, stg.ws)
     s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
@@ -551,9 +555,10 @@ def run_native(args):
     e2e = {"value": n * T * e2e_steps / e2e_s, "unit": "tokens/s",
            "h2d_bytes_per_step": h2d + plan_bytes, "d2h_bytes_per_step": d2h,
            "api": "hb_step (one C call per step)",
-           "copies": "per step: the plan and one packed page-locked block (q, k_new, v_new, "
-                     "descriptors) up on an input-copy stream, the output down on an "
-                     "output-copy stream, ordered against the kernels' stream by events; "
+           "copies": "per step: the plan (page-locked) and one packed page-locked block (q, "
+                     "k_new, v_new, descriptors) up on an input-copy stream, which then raises "
+                     "the slot's flag for the append kernel; the output down on an "
+                     "output-copy stream, ordered by the slot's events; "
                      f"{len(stages)} staging buffers in flight"}
 
     if rank != 0:

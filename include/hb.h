@@ -285,7 +285,8 @@ typedef struct hb_step_buffers {
   void* d_in;              /* device packed inputs, 256-byte aligned                      */
   void* h_out;             /* host output [total_q, Hq, D] bf16                           */
   void* d_out;             /* device output, 16-byte aligned                              */
-  void* h_plan;            /* host plan buffer (hb_plan's plan_bytes)                     */
+  void* h_plan;            /* host plan buffer (hb_plan's plan_bytes; page-locked makes   */
+                           /* its upload asynchronous like the inputs')                    */
   size_t plan_bytes;
   void* d_workspace;       /* device workspace (hb_plan's workspace_bytes), 256-aligned   */
   size_t workspace_bytes;
