@@ -40,7 +40,7 @@ cudaError_t launch_attention(const DecodeParams& dec, int decode_grid, const Chu
                              const CUtensorMap& chunk_v, const CUtensorMap& chunk_knew,
                              const CUtensorMap& chunk_vnew, const void* k_cache,
                              const void* v_cache, cudaStream_t stream, bool early,
-                             bool pairs_only);
+                             int pairs_mode);
 }  // namespace hb
 
 using namespace hb;
@@ -930,10 +930,16 @@ hb_status hb_plan(const hb_batch* batch, const int32_t* h_q_len,
     h.decode_grid = part.grid;
     h.num_decode_dynamic = part.n_dynamic;
     {
-      bool pairs = n_chk > 0;
-      for (size_t i = 0; pairs && i < n_chk; ++i)
-        pairs = ps.chk[i].ntok > tpt && ps.chk[i].n_splits == 1;
-      h.chunk_pairs_only = pairs ? 1 : 0;
+      // bit 0: every item an unsplit pair; bit 1: some item's first row sees
+      // few keys (its P is written in two terms)
+      bool pairs = n_chk > 0, few = false;
+      for (size_t i = 0; i < n_chk; ++i) {
+        const ChunkItem& c = ps.chk[i];
+        const int first_keys = c.ctx - c.q_len + c.tok0 + 1;
+        pairs = pairs && c.ntok > tpt && c.n_splits == 1;
+        few = few || (W > 0 ? std::min(W, first_keys) : first_keys) <= kChunkFewKeys;
+      }
+      h.chunk_pairs_only = (pairs ? 1 : 0) | (few ? 2 : 0);
     }
     h.ws_decode_offsets = offsets_at;
     h.decode_kvh_block = kvhb;
@@ -1132,7 +1138,7 @@ hb_status hb::internal_attention(const hb_batch* batch, const void* h_plan, cons
       LaunchTimer t(1, st);
       cudaError_t e = launch_attention(dp, h.decode_grid, cp, D, dec_k, dec_v, chunk_q, chunk_k,
                                        chunk_v, chunk_knew, chunk_vnew, k_cache, v_cache, st,
-                                       early, h.chunk_pairs_only != 0);
+                                       early, h.chunk_pairs_only);
       t.done();
       if (e != cudaSuccess) return cuda_fail(e, "attention launch");
       note_launch(stream, LastLaunch{});

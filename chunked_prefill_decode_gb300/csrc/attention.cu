@@ -39,7 +39,7 @@ struct AttnParams {
   int32_t early;
 };
 
-template <int D, bool kPairs>
+template <int D, bool kPairs, bool kFew>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     attention_kernel(const AttnParams p, const __grid_constant__ CUtensorMap dec_k,
                      const __grid_constant__ CUtensorMap dec_v,
@@ -60,7 +60,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   if ((int)blockIdx.x < p.decode_grid)
     decode_cta<D>(p.dec, p.dl, dec_k, dec_v, smem, blockIdx.x);
   else
-    chunk_cta<D, kPairs>(p.chk, chunk_q, chunk_k, chunk_v, chunk_knew, chunk_vnew, p.k_cache,
+    chunk_cta<D, kPairs, kFew>(p.chk, chunk_q, chunk_k, chunk_v, chunk_knew, chunk_vnew, p.k_cache,
                          p.v_cache, smem, blockIdx.x - p.decode_grid);
 }
 
@@ -75,16 +75,18 @@ int attention_smem_bytes(int head_dim, int kvh_block, int group) {
 // part may be empty (dec.num_items == 0: no decode CTA).  dec.kvh_block and
 // dec.group must be set in every case (they size the shared memory).
 // chunk_knew / chunk_vnew map k_new / v_new when chk.has_new (else any map).
-// pairs_only: every chunk item is an unsplit pair of query tiles, and the
-// kernel instantiation without the single-tile and split paths runs (the
-// pair loop compiles to faster code on its own).
+// pairs_mode bit 0: every chunk item is an unsplit pair of query tiles, and
+// the kernel instantiation without the single-tile and split paths runs (the
+// pair loop compiles to faster code on its own); bit 1: some item's first
+// row sees few keys (its P is written in two terms), and the instantiation
+// that can do so runs.
 cudaError_t launch_attention(const DecodeParams& dec, int decode_grid, const ChunkParams& chk,
                              int head_dim, const CUtensorMap& dec_k, const CUtensorMap& dec_v,
                              const CUtensorMap& chunk_q, const CUtensorMap& chunk_k,
                              const CUtensorMap& chunk_v, const CUtensorMap& chunk_knew,
                              const CUtensorMap& chunk_vnew, const void* k_cache,
                              const void* v_cache, cudaStream_t stream, bool early,
-                             bool pairs_only) {
+                             int pairs_mode) {
   AttnParams p{};
   p.early = early ? 1 : 0;
   p.dec = dec;
@@ -101,16 +103,19 @@ cudaError_t launch_attention(const DecodeParams& dec, int decode_grid, const Chu
                           const __grid_constant__ CUtensorMap, const __grid_constant__ CUtensorMap,
                           const __grid_constant__ CUtensorMap, const __grid_constant__ CUtensorMap,
                           const __grid_constant__ CUtensorMap, const __grid_constant__ CUtensorMap);
-  const int which = (head_dim == 128 ? 2 : 0) + (pairs_only ? 1 : 0);
-  const Kernel kernels[4] = {attention_kernel<64, false>, attention_kernel<64, true>,
-                             attention_kernel<128, false>, attention_kernel<128, true>};
+  if (pairs_mode < 0 || pairs_mode > 3) return cudaErrorInvalidValue;
+  const int which = (head_dim == 128 ? 4 : 0) + pairs_mode;
+  const Kernel kernels[8] = {attention_kernel<64, false, false>,  attention_kernel<64, true, false>,
+                             attention_kernel<64, false, true>,   attention_kernel<64, true, true>,
+                             attention_kernel<128, false, false>, attention_kernel<128, true, false>,
+                             attention_kernel<128, false, true>,  attention_kernel<128, true, true>};
   const Kernel kernel = kernels[which];
   // setmaxnreg.inc waits until the block's register pool holds what it asks
   // for; the chunk CTAs' split assumes the launch allocation of
   // kChunkLaunchRegs per thread, so a build that allocated fewer is refused
   // here instead of launched
   {
-    static std::atomic<int> regs[4] = {{0}, {0}, {0}, {0}};   // per instantiation, once known
+    static std::atomic<int> regs[8] = {};   // registers per instantiation, once known
     int n = regs[which].load(std::memory_order_relaxed);
     if (n == 0) {
       cudaFuncAttributes fa{};

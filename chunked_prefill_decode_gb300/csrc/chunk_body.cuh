@@ -32,7 +32,11 @@
 //              that cross the diagonal, reduced to its maximum, and turned
 //              into p = 2^(s c - m) with one FFMA + EX2 (c = scale * log2 e),
 //              rounded to bf16 and written over the S columns (tcgen05.st);
-//              the row sum uses the same rounded P.  O is rescaled in TMEM
+//              the row sum adds p in fp32.  An item whose first row
+//              sees at most 256 keys (a prompt's first tokens, short windows)
+//              also writes the bf16 remainder of P into the S columns P
+//              leaves free, and its PV runs a second pass over it (P to
+//              ~2^-17; write_p32).  O is rescaled in TMEM
 //              only when a row maximum grows by more than 2^8 (a stale
 //              maximum stays exact while it bounds P, and P <= 2^8 is safe);
 //              epilogue O / l to bf16.  These warps hold 176 registers (the
@@ -59,6 +63,7 @@
 #include <cuda_runtime.h>
 
 #include <climits>
+#include <type_traits>
 
 #include "hb_internal.h"
 #include "ptx.cuh"
@@ -70,6 +75,10 @@ constexpr int kProducerWarp0 = 9;
 constexpr int kProducerWarps = 3;
 constexpr int kProducerThreads = 32 * kProducerWarps;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
+// (kChunkFewKeys, hb_internal.h: an item whose first query row sees at most
+// that many keys carries P as two bf16 terms, see write_p32: with few keys a
+// row's output leans on a few weights, whose bf16 rounding alone, 2^-9
+// relative, can move it by more than half a bf16 step of an output near 2.)
 constexpr int kSoftmaxRegs = 176;   // per thread, softmax warpgroups (warps 0-7)
 constexpr int kLightRegs = 152;     // per thread, MMA + producer warpgroup (8-11)
 constexpr int kChunkLaunchRegs = 168;   // per thread at launch: 65536 / 384, rounded down
@@ -158,11 +167,59 @@ __device__ __forceinline__ void merge_pieces(const float* o0, const float* ml0, 
   }
 }
 
+// p = 2^(s c - m) for 32 keys of one row (s = sr[0..31]; c2 / nm2 hold c
+// and -m twice), written as 16 columns of bf16 pairs at TMEM address `col`.
+// With kSplit the remainder p - bf16(p), rounded to bf16, goes to the 16
+// columns at col + 32 as well, and the PV runs over both terms, so P enters
+// the products to about 2^-17 relative; otherwise P is the bf16 value alone.
+// lsum2 receives p in fp32 (two lanes, alternating): what the two passes
+// read, to 2^-17; with bf16 P alone it differs from the rounded weights by
+// 2^-9 relative, which a row over many keys averages away (the few-key rows
+// that it would not are the ones that take the split).
+template <bool kSplit>
+__device__ __forceinline__ void write_p32(const uint32_t* sr, uint64_t c2, uint64_t nm2,
+                                          uint32_t col, uint64_t (&lsum2)[2]) {
+  if constexpr (kSplit) {
+    // 16 keys at a time, so that the two terms of only 8 pairs are live
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      uint32_t ph[8], pl[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int k = 16 * h + 2 * i;
+        float x0, x1;
+        unpack_f32x2(fma_f32x2(pack_f32x2(__uint_as_float(sr[k]), __uint_as_float(sr[k + 1])), c2, nm2),
+                     x0, x1);
+        const float e0 = fast_exp2(x0), e1 = fast_exp2(x1);
+        ph[i] = pack_bf16x2(e0, e1);
+        pl[i] = pack_bf16x2(e0 - bf16lo_to_f32(ph[i]), e1 - bf16hi_to_f32(ph[i]));
+        lsum2[i & 1] = add_f32x2(lsum2[i & 1], pack_f32x2(e0, e1));
+      }
+      tmem_st8(col + 8 * h, ph);
+      tmem_st8(col + 32 + 8 * h, pl);
+    }
+  } else {
+    uint32_t pk[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      float x0, x1;
+      unpack_f32x2(fma_f32x2(pack_f32x2(__uint_as_float(sr[2 * i]), __uint_as_float(sr[2 * i + 1])),
+                             c2, nm2), x0, x1);
+      const float e0 = fast_exp2(x0), e1 = fast_exp2(x1);
+      pk[i] = pack_bf16x2(e0, e1);
+      lsum2[i & 1] = add_f32x2(lsum2[i & 1], pack_f32x2(e0, e1));
+    }
+    tmem_st16(col, pk);
+  }
+}
+
 // Body of one chunk CTA working on item `item`; `smem` is the 1024-byte-
 // aligned dynamic shared memory.  kPairs: the launch holds only unsplit
 // pairs of query tiles (the plan says so), and the single-tile and split
-// paths are left out of this instantiation.
-template <int D, bool kPairs>
+// paths are left out of this instantiation.  kFew: items whose first row sees
+// at most kChunkFewKeys keys may occur (their P is written in two terms; the
+// plan says so).
+template <int D, bool kPairs, bool kFew>
 __device__ __forceinline__ void chunk_cta(const ChunkParams& p, const CUtensorMap& qmap,
                                           const CUtensorMap& kmap, const CUtensorMap& vmap,
                                           const CUtensorMap& knewmap, const CUtensorMap& vnewmap,
@@ -211,6 +268,10 @@ __device__ __forceinline__ void chunk_cta(const ChunkParams& p, const CUtensorMa
   // one query tile: the two softmax groups take alternate key tiles of it
   // (even: S_0/O_0, odd: S_1/O_1) and merge their states at the end
   const bool inter = !kPairs && !hasB;
+  // the item's first row sees the fewest keys (P in two terms, write_p32;
+  // kFew: the launch may hold such items, which the plan says)
+  const bool few = kFew && (p.window > 0 ? min(p.window, off + it.tok0 + 1)
+                                         : off + it.tok0 + 1) <= kChunkFewKeys;
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
@@ -386,7 +447,8 @@ __device__ __forceinline__ void chunk_cta(const ChunkParams& p, const CUtensorMa
         }
         tc_commit(&s_full[t]);
       };
-      // O_t (+)= P_t V(j); `first` starts O_t
+      // O_t (+)= P_t V(j); `first` starts O_t.  With P in two terms a
+      // second pass adds the remainder (S columns 32-63 and 96-127).
       auto pv = [&](int t, int j, bool first) {
         const uint32_t vb = aV + (j % NV) * C::kTileBytes;
         const uint32_t ocol = C::kOCol + t * D;
@@ -395,6 +457,12 @@ __device__ __forceinline__ void chunk_cta(const ChunkParams& p, const CUtensorMa
           tc_mma_bf16_ts(tmem + ocol, tmem + t * kChunkKeys + (kk >> 2) * 64 + (kk & 3) * 8,
                          sdesc_sw128(vb + kk * 2048, 16384, 1024), idesc_pv,
                          (!first || kk > 0) ? 1u : 0u);
+        if (few) {
+#pragma unroll
+          for (int kk = 0; kk < kChunkKeys / 16; ++kk)
+            tc_mma_bf16_ts(tmem + ocol, tmem + t * kChunkKeys + (kk >> 2) * 64 + 32 + (kk & 3) * 8,
+                           sdesc_sw128(vb + kk * 2048, 16384, 1024), idesc_pv, 1u);
+        }
       };
       // K and V arrive by TMA (async proxy, made visible by the barrier's
       // transaction count); the V rows the softmax zeroes by generic stores
@@ -502,111 +570,106 @@ __device__ __forceinline__ void chunk_cta(const ChunkParams& p, const CUtensorMa
     float m_run = -INFINITY;   // running maximum, scaled log2 units
     float l_run = 0.f;
     bool ok = true;
-    for (int j = 0; j < n_t; ++j) {   // key tile jb + j
-      // waits are made warp-uniform: a lane that gave up must not leave its
-      // warp's collective TMEM accesses
-      if (!__all_sync(0xffffffffu, mbar_wait(&s_full[t], (uint32_t)j & 1u, abort_flag))) { ok = false; break; }
-      tc_fence_after_sync();
-      const int kbase = (jb + j) * kChunkKeys;
-      const bool masked = kbase + kChunkKeys - 1 > min_pos || kbase < tile_lo;
-      const int lim = pos - kbase;   // keys 0..lim of this tile are visible
-      const int lo_lim = win_lo == INT_MIN ? INT_MIN : win_lo - kbase;   // .. and lo_lim..
-      uint32_t sr[kChunkKeys];
+    // the loop once per way of writing P (write_p32), so that the
+    // common one keeps its own register allocation
+    auto pair_loop = [&](auto split_c) {
+      constexpr bool kSplit = decltype(split_c)::value;
+      for (int j = 0; j < n_t; ++j) {   // key tile jb + j
+        // waits are made warp-uniform: a lane that gave up must not leave its
+        // warp's collective TMEM accesses
+        if (!__all_sync(0xffffffffu, mbar_wait(&s_full[t], (uint32_t)j & 1u, abort_flag))) { ok = false; break; }
+        tc_fence_after_sync();
+        const int kbase = (jb + j) * kChunkKeys;
+        const bool masked = kbase + kChunkKeys - 1 > min_pos || kbase < tile_lo;
+        const int lim = pos - kbase;   // keys 0..lim of this tile are visible
+        const int lo_lim = win_lo == INT_MIN ? INT_MIN : win_lo - kbase;   // .. and lo_lim..
+        uint32_t sr[kChunkKeys];
 #pragma unroll
-      for (int q = 0; q < kChunkKeys / 32; ++q) tmem_ld32(s_col + q * 32, sr + q * 32);
-      tmem_ld_wait();
-      if (masked) {
+        for (int q = 0; q < kChunkKeys / 32; ++q) tmem_ld32(s_col + q * 32, sr + q * 32);
+        tmem_ld_wait();
+        if (masked) {
 #pragma unroll
-        for (int i = 0; i < kChunkKeys; ++i)
-          if (i > lim || i < lo_lim) sr[i] = __float_as_uint(-INFINITY);
-      }
-      float mxp[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) mxp[e] = -INFINITY;
-#pragma unroll
-      for (int i = 0; i < kChunkKeys; i += 16) {
-#pragma unroll
-        for (int e = 0; e < 8; ++e)
-          mxp[e] = fmax3(mxp[e], __uint_as_float(sr[i + 2 * e]), __uint_as_float(sr[i + 2 * e + 1]));
-      }
-      float alpha = 1.f;
-      bool resc = false;
-      if (valid_row) {
-        const float mx = fmaxf(fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3])),
-                               fmaxf(fmaxf(mxp[4], mxp[5]), fmaxf(mxp[6], mxp[7])));
-        const float m_new = fmaxf(m_run, mx * sl2);
-        if (m_new > m_run + kRescaleThreshold) {
-          alpha = fast_exp2(m_run - m_new);
-          m_run = m_new;
-          resc = true;
+          for (int i = 0; i < kChunkKeys; ++i)
+            if (i > lim || i < lo_lim) sr[i] = __float_as_uint(-INFINITY);
         }
-      }
-      // P = 2^(s c - m) as bf16; dead rows and rows that have seen no key
-      // yet get P = 0
-      const float neg_m = (valid_row && m_run != -INFINITY) ? -m_run : -INFINITY;
-      const uint64_t c2 = pack_f32x2(sl2, sl2);
-      const uint64_t nm2 = pack_f32x2(neg_m, neg_m);
-      uint64_t lsum2[2] = {pack_f32x2(0.f, 0.f), pack_f32x2(0.f, 0.f)};
+        float mxp[8];
 #pragma unroll
-      for (int q = 0; q < kChunkKeys / 32; ++q) {
-        uint32_t pk[16];
+        for (int e = 0; e < 8; ++e) mxp[e] = -INFINITY;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          float x0, x1;
-          unpack_f32x2(fma_f32x2(pack_f32x2(__uint_as_float(sr[q * 32 + 2 * i]),
-                                            __uint_as_float(sr[q * 32 + 2 * i + 1])),
-                                 c2, nm2), x0, x1);
-          const float e0 = fast_exp2(x0), e1 = fast_exp2(x1);
-          pk[i] = pack_bf16x2(e0, e1);
-          lsum2[i & 1] = add_f32x2(lsum2[i & 1], pack_f32x2(e0, e1));
+        for (int i = 0; i < kChunkKeys; i += 16) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            mxp[e] = fmax3(mxp[e], __uint_as_float(sr[i + 2 * e]), __uint_as_float(sr[i + 2 * e + 1]));
         }
-        tmem_st16(s_col + (q >> 1) * 64 + (q & 1) * 16, pk);
-      }
-      float lsp[4];
-      unpack_f32x2(lsum2[0], lsp[0], lsp[1]);
-      unpack_f32x2(lsum2[1], lsp[2], lsp[3]);
-      if (valid_row) l_run = l_run * alpha + ((lsp[0] + lsp[1]) + (lsp[2] + lsp[3]));
-      if (jb + j == T - 1 && t == zero_t) {
-        // the last page's slots past the context were never written (its TMA
-        // box brings them in as they are): clear those V rows before the
-        // first PV that reads this tile, so that P = 0 never meets a NaN
-        const int first_bad = ctx - kbase;
-        const int end_bad = min(kChunkKeys, ((ctx + kPageSize - 1) / kPageSize) * kPageSize - kbase);
-        if (first_bad < end_bad) {
-          const int s = j % NV;
-          if (!__all_sync(0xffffffffu, mbar_wait(&v_full[s], (uint32_t)(j / NV) & 1u, abort_flag))) { ok = false; break; }
-          uint8_t* vt = sV + s * C::kTileBytes;
-          const int n_units = (end_bad - first_bad) * CH * 8;
-          for (int e = row; e < n_units; e += kChunkRows) {
-            const int key = first_bad + e / (CH * 8);
-            const int rem = e % (CH * 8);
-            *reinterpret_cast<uint4*>(vt + (rem >> 3) * 16384 + key * 128 + (rem & 7) * 16) =
-                make_uint4(0u, 0u, 0u, 0u);
+        float alpha = 1.f;
+        bool resc = false;
+        if (valid_row) {
+          const float mx = fmaxf(fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3])),
+                                 fmaxf(fmaxf(mxp[4], mxp[5]), fmaxf(mxp[6], mxp[7])));
+          const float m_new = fmaxf(m_run, mx * sl2);
+          if (m_new > m_run + kRescaleThreshold) {
+            alpha = fast_exp2(m_run - m_new);
+            m_run = m_new;
+            resc = true;
           }
-          fence_async_shared();
         }
-      }
-      // O_t is stable here (PV_t of the previous key tile completed before
-      // S_t was ready)
-      if (j > 0 && __any_sync(0xffffffffu, resc)) {
-        const float f = resc ? alpha : 1.f;
-#pragma unroll 1
-        for (int q = 0; q < D / 32; ++q) {
-          uint32_t orow[32];
-          tmem_ld32(o_col + q * 32, orow);
-          tmem_ld_wait();
+        // P = 2^(s c - m) as bf16; dead rows and rows that have seen no key
+        // yet get P = 0
+        const float neg_m = (valid_row && m_run != -INFINITY) ? -m_run : -INFINITY;
+        const uint64_t c2 = pack_f32x2(sl2, sl2);
+        const uint64_t nm2 = pack_f32x2(neg_m, neg_m);
+        uint64_t lsum2[2] = {pack_f32x2(0.f, 0.f), pack_f32x2(0.f, 0.f)};
 #pragma unroll
-          for (int i = 0; i < 32; ++i) orow[i] = __float_as_uint(__uint_as_float(orow[i]) * f);
-          tmem_st32(o_col + q * 32, orow);
+        for (int q = 0; q < kChunkKeys / 32; ++q)
+          write_p32<kSplit>(sr + q * 32, c2, nm2, s_col + (q >> 1) * 64 + (q & 1) * 16, lsum2);
+        float lsp[4];
+        unpack_f32x2(lsum2[0], lsp[0], lsp[1]);
+        unpack_f32x2(lsum2[1], lsp[2], lsp[3]);
+        if (valid_row) l_run = l_run * alpha + ((lsp[0] + lsp[1]) + (lsp[2] + lsp[3]));
+        if (jb + j == T - 1 && t == zero_t) {
+          // the last page's slots past the context were never written (its TMA
+          // box brings them in as they are): clear those V rows before the
+          // first PV that reads this tile, so that P = 0 never meets a NaN
+          const int first_bad = ctx - kbase;
+          const int end_bad = min(kChunkKeys, ((ctx + kPageSize - 1) / kPageSize) * kPageSize - kbase);
+          if (first_bad < end_bad) {
+            const int s = j % NV;
+            if (!__all_sync(0xffffffffu, mbar_wait(&v_full[s], (uint32_t)(j / NV) & 1u, abort_flag))) { ok = false; break; }
+            uint8_t* vt = sV + s * C::kTileBytes;
+            const int n_units = (end_bad - first_bad) * CH * 8;
+            for (int e = row; e < n_units; e += kChunkRows) {
+              const int key = first_bad + e / (CH * 8);
+              const int rem = e % (CH * 8);
+              *reinterpret_cast<uint4*>(vt + (rem >> 3) * 16384 + key * 128 + (rem & 7) * 16) =
+                  make_uint4(0u, 0u, 0u, 0u);
+            }
+            fence_async_shared();
+          }
         }
+        // O_t is stable here (PV_t of the previous key tile completed before
+        // S_t was ready)
+        if (j > 0 && __any_sync(0xffffffffu, resc)) {
+          const float f = resc ? alpha : 1.f;
+#pragma unroll 1
+          for (int q = 0; q < D / 32; ++q) {
+            uint32_t orow[32];
+            tmem_ld32(o_col + q * 32, orow);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) orow[i] = __float_as_uint(__uint_as_float(orow[i]) * f);
+            tmem_st32(o_col + q * 32, orow);
+          }
+        }
+        tmem_st_wait();
+        tc_fence_before_sync();
+        // one arrival per warp: the barrier completes after 4 (pair) or 8
+        // (interleaved) arrivals instead of one per thread
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&p_full[t]);
       }
-      tmem_st_wait();
-      tc_fence_before_sync();
-      // one arrival per warp: the barrier completes after 4 (pair) or 8
-      // (interleaved) arrivals instead of one per thread
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&p_full[t]);
-    }
+    };
+    if (few) pair_loop(std::true_type{});
+    else pair_loop(std::false_type{});
     // epilogue.  t_ok: this tile's waits held (a tile with no key tile in
     // this item -- tile A of a split piece past its own last key -- has
     // nothing to wait for); have_o: its O is complete
@@ -721,111 +784,106 @@ __device__ __forceinline__ void chunk_cta(const ChunkParams& p, const CUtensorMa
     float m_run = -INFINITY;   // this slot's running maximum, scaled log2 units
     float l_run = 0.f;
     bool ok = true;
-    for (int j = t; j < n_all; j += 2) {   // key tile jb + j, this slot's u-th
-      const uint32_t u = (uint32_t)j >> 1;
-      // waits are made warp-uniform: a lane that gave up must not leave its
-      // warp's collective TMEM accesses
-      if (!__all_sync(0xffffffffu, mbar_wait(&s_full[t], u & 1u, abort_flag))) { ok = false; break; }
-      tc_fence_after_sync();
-      const int kbase = (jb + j) * kChunkKeys;
-      const bool masked = kbase + kChunkKeys - 1 > min_pos || kbase < tile_lo;
-      const int lim = pos - kbase;   // keys 0..lim of this tile are visible
-      const int lo_lim = win_lo == INT_MIN ? INT_MIN : win_lo - kbase;   // .. and lo_lim..
-      uint32_t sr[kChunkKeys];
+    // the loop once per way of writing P (write_p32), so that the
+    // common one keeps its own register allocation
+    auto slot_loop = [&](auto split_c) {
+      constexpr bool kSplit = decltype(split_c)::value;
+      for (int j = t; j < n_all; j += 2) {   // key tile jb + j, this slot's u-th
+        const uint32_t u = (uint32_t)j >> 1;
+        // waits are made warp-uniform: a lane that gave up must not leave its
+        // warp's collective TMEM accesses
+        if (!__all_sync(0xffffffffu, mbar_wait(&s_full[t], u & 1u, abort_flag))) { ok = false; break; }
+        tc_fence_after_sync();
+        const int kbase = (jb + j) * kChunkKeys;
+        const bool masked = kbase + kChunkKeys - 1 > min_pos || kbase < tile_lo;
+        const int lim = pos - kbase;   // keys 0..lim of this tile are visible
+        const int lo_lim = win_lo == INT_MIN ? INT_MIN : win_lo - kbase;   // .. and lo_lim..
+        uint32_t sr[kChunkKeys];
 #pragma unroll
-      for (int q = 0; q < kChunkKeys / 32; ++q) tmem_ld32(s_col + q * 32, sr + q * 32);
-      tmem_ld_wait();
-      if (masked) {
+        for (int q = 0; q < kChunkKeys / 32; ++q) tmem_ld32(s_col + q * 32, sr + q * 32);
+        tmem_ld_wait();
+        if (masked) {
 #pragma unroll
-        for (int i = 0; i < kChunkKeys; ++i)
-          if (i > lim || i < lo_lim) sr[i] = __float_as_uint(-INFINITY);
-      }
-      float mxp[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) mxp[e] = -INFINITY;
-#pragma unroll
-      for (int i = 0; i < kChunkKeys; i += 16) {
-#pragma unroll
-        for (int e = 0; e < 8; ++e)
-          mxp[e] = fmax3(mxp[e], __uint_as_float(sr[i + 2 * e]), __uint_as_float(sr[i + 2 * e + 1]));
-      }
-      float alpha = 1.f;
-      bool resc = false;
-      if (valid_row) {
-        const float mx = fmaxf(fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3])),
-                               fmaxf(fmaxf(mxp[4], mxp[5]), fmaxf(mxp[6], mxp[7])));
-        const float m_new = fmaxf(m_run, mx * sl2);
-        if (m_new > m_run + kRescaleThreshold) {
-          alpha = fast_exp2(m_run - m_new);
-          m_run = m_new;
-          resc = true;
+          for (int i = 0; i < kChunkKeys; ++i)
+            if (i > lim || i < lo_lim) sr[i] = __float_as_uint(-INFINITY);
         }
-      }
-      // P = 2^(s c - m) as bf16; dead rows and rows that have seen no key
-      // yet get P = 0
-      const float neg_m = (valid_row && m_run != -INFINITY) ? -m_run : -INFINITY;
-      const uint64_t c2 = pack_f32x2(sl2, sl2);
-      const uint64_t nm2 = pack_f32x2(neg_m, neg_m);
-      uint64_t lsum2[2] = {pack_f32x2(0.f, 0.f), pack_f32x2(0.f, 0.f)};
+        float mxp[8];
 #pragma unroll
-      for (int q = 0; q < kChunkKeys / 32; ++q) {
-        uint32_t pk[16];
+        for (int e = 0; e < 8; ++e) mxp[e] = -INFINITY;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          float x0, x1;
-          unpack_f32x2(fma_f32x2(pack_f32x2(__uint_as_float(sr[q * 32 + 2 * i]),
-                                            __uint_as_float(sr[q * 32 + 2 * i + 1])),
-                                 c2, nm2), x0, x1);
-          const float e0 = fast_exp2(x0), e1 = fast_exp2(x1);
-          pk[i] = pack_bf16x2(e0, e1);
-          lsum2[i & 1] = add_f32x2(lsum2[i & 1], pack_f32x2(e0, e1));
+        for (int i = 0; i < kChunkKeys; i += 16) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            mxp[e] = fmax3(mxp[e], __uint_as_float(sr[i + 2 * e]), __uint_as_float(sr[i + 2 * e + 1]));
         }
-        tmem_st16(s_col + (q >> 1) * 64 + (q & 1) * 16, pk);
-      }
-      float lsp[4];
-      unpack_f32x2(lsum2[0], lsp[0], lsp[1]);
-      unpack_f32x2(lsum2[1], lsp[2], lsp[3]);
-      if (valid_row) l_run = l_run * alpha + ((lsp[0] + lsp[1]) + (lsp[2] + lsp[3]));
-      if (jb + j == T - 1) {
-        // the last page's slots past the context were never written (its
-        // TMA box brings them in as they are): clear those V rows before
-        // the first PV that reads this tile, so that P = 0 never meets a NaN
-        const int first_bad = ctx - kbase;
-        const int end_bad = min(kChunkKeys, ((ctx + kPageSize - 1) / kPageSize) * kPageSize - kbase);
-        if (first_bad < end_bad) {
-          const int s = j % NV;
-          if (!__all_sync(0xffffffffu, mbar_wait(&v_full[s], (uint32_t)(j / NV) & 1u, abort_flag))) { ok = false; break; }
-          uint8_t* vt = sV + s * C::kTileBytes;
-          const int n_units = (end_bad - first_bad) * CH * 8;
-          for (int e = row; e < n_units; e += kChunkRows) {
-            const int key = first_bad + e / (CH * 8);
-            const int rem = e % (CH * 8);
-            *reinterpret_cast<uint4*>(vt + (rem >> 3) * 16384 + key * 128 + (rem & 7) * 16) =
-                make_uint4(0u, 0u, 0u, 0u);
+        float alpha = 1.f;
+        bool resc = false;
+        if (valid_row) {
+          const float mx = fmaxf(fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3])),
+                                 fmaxf(fmaxf(mxp[4], mxp[5]), fmaxf(mxp[6], mxp[7])));
+          const float m_new = fmaxf(m_run, mx * sl2);
+          if (m_new > m_run + kRescaleThreshold) {
+            alpha = fast_exp2(m_run - m_new);
+            m_run = m_new;
+            resc = true;
           }
-          fence_async_shared();
         }
-      }
-      // O_t is stable here (slot t's previous PV completed before its S was
-      // ready)
-      if (u > 0 && __any_sync(0xffffffffu, resc)) {
-        const float f = resc ? alpha : 1.f;
-#pragma unroll 1
-        for (int q = 0; q < D / 32; ++q) {
-          uint32_t orow[32];
-          tmem_ld32(o_col + q * 32, orow);
-          tmem_ld_wait();
+        // P = 2^(s c - m) as bf16; dead rows and rows that have seen no key
+        // yet get P = 0
+        const float neg_m = (valid_row && m_run != -INFINITY) ? -m_run : -INFINITY;
+        const uint64_t c2 = pack_f32x2(sl2, sl2);
+        const uint64_t nm2 = pack_f32x2(neg_m, neg_m);
+        uint64_t lsum2[2] = {pack_f32x2(0.f, 0.f), pack_f32x2(0.f, 0.f)};
 #pragma unroll
-          for (int i = 0; i < 32; ++i) orow[i] = __float_as_uint(__uint_as_float(orow[i]) * f);
-          tmem_st32(o_col + q * 32, orow);
+        for (int q = 0; q < kChunkKeys / 32; ++q)
+          write_p32<kSplit>(sr + q * 32, c2, nm2, s_col + (q >> 1) * 64 + (q & 1) * 16, lsum2);
+        float lsp[4];
+        unpack_f32x2(lsum2[0], lsp[0], lsp[1]);
+        unpack_f32x2(lsum2[1], lsp[2], lsp[3]);
+        if (valid_row) l_run = l_run * alpha + ((lsp[0] + lsp[1]) + (lsp[2] + lsp[3]));
+        if (jb + j == T - 1) {
+          // the last page's slots past the context were never written (its
+          // TMA box brings them in as they are): clear those V rows before
+          // the first PV that reads this tile, so that P = 0 never meets a NaN
+          const int first_bad = ctx - kbase;
+          const int end_bad = min(kChunkKeys, ((ctx + kPageSize - 1) / kPageSize) * kPageSize - kbase);
+          if (first_bad < end_bad) {
+            const int s = j % NV;
+            if (!__all_sync(0xffffffffu, mbar_wait(&v_full[s], (uint32_t)(j / NV) & 1u, abort_flag))) { ok = false; break; }
+            uint8_t* vt = sV + s * C::kTileBytes;
+            const int n_units = (end_bad - first_bad) * CH * 8;
+            for (int e = row; e < n_units; e += kChunkRows) {
+              const int key = first_bad + e / (CH * 8);
+              const int rem = e % (CH * 8);
+              *reinterpret_cast<uint4*>(vt + (rem >> 3) * 16384 + key * 128 + (rem & 7) * 16) =
+                  make_uint4(0u, 0u, 0u, 0u);
+            }
+            fence_async_shared();
+          }
         }
+        // O_t is stable here (slot t's previous PV completed before its S was
+        // ready)
+        if (u > 0 && __any_sync(0xffffffffu, resc)) {
+          const float f = resc ? alpha : 1.f;
+#pragma unroll 1
+          for (int q = 0; q < D / 32; ++q) {
+            uint32_t orow[32];
+            tmem_ld32(o_col + q * 32, orow);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) orow[i] = __float_as_uint(__uint_as_float(orow[i]) * f);
+            tmem_st32(o_col + q * 32, orow);
+          }
+        }
+        tmem_st_wait();
+        tc_fence_before_sync();
+        // one arrival per warp: the barrier completes after the slot's 4
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&p_full[t]);
       }
-      tmem_st_wait();
-      tc_fence_before_sync();
-      // one arrival per warp: the barrier completes after the slot's 4
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&p_full[t]);
-    }
+    };
+    if (few) slot_loop(std::true_type{});
+    else slot_loop(std::false_type{});
     // ---- epilogue: every MMA is complete once both slots' last PV is (slot
     // 1 is empty with one key tile)
     bool have_o = ok && mbar_wait(&o_done[0], 0u, abort_flag);

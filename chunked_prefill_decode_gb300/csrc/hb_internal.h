@@ -24,6 +24,10 @@ constexpr int kMaxGroup = 16;          // max q heads per kv head
 constexpr uint32_t kPlanMagic = 0x31504248u;  // "HBP1"
 constexpr uint32_t kPlanVersion = 4;
 constexpr int kMaxChunkSplits = 16;    // key-range pieces of one query tile (max)
+// A chunk item whose first query row sees at most this many keys carries its
+// softmax weights P as two bf16 terms (chunk_body.cuh, write_p32), and a
+// launch holding one runs the general kernel instantiation.
+constexpr int kChunkFewKeys = 256;
 
 // One decode work item: a range of logical pages of one decode row, for one
 // block of kv heads.  Rows of the same (sequence, kv block) with n_splits > 1
@@ -90,7 +94,9 @@ struct PlanHeader {
   int32_t num_chunk_merges;    // split chunk tiles
   int32_t sliding_window;      // the batch's window (the plan depends on it)
   int32_t num_decode_dynamic;  // claimable decode intervals after the static ones
-  int32_t chunk_pairs_only;    // 1: chunk items exist and all are unsplit pairs
+  int32_t chunk_pairs_only;    // bit 0: chunk items exist and all are unsplit
+                               // pairs; bit 1: some item's first row sees at
+                               // most kChunkFewKeys keys
   uint64_t ws_decode_offsets;  // device offset of the per-CTA item offsets
   uint64_t items_bytes;     // bytes of the item arrays (host and device)
   uint64_t ws_counters;     // device offsets (bytes from workspace start)

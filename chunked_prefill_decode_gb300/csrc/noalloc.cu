@@ -35,7 +35,7 @@ cudaError_t launch_attention(const DecodeParams& dec, int decode_grid, const Chu
                              const CUtensorMap& chunk_v, const CUtensorMap& chunk_knew,
                              const CUtensorMap& chunk_vnew, const void* k_cache,
                              const void* v_cache, cudaStream_t stream, bool early,
-                             bool pairs_only);
+                             int pairs_mode);
 hb_status internal_fail(hb_status s, const char* msg);
 hb_status internal_ok();
 hb_status internal_check_batch(const hb_batch* b);
@@ -193,7 +193,7 @@ extern "C" hb_status hb_decode_attention_noalloc(const hb_batch* batch, const in
     CUtensorMap unused;
     std::memset(&unused, 0, sizeof(unused));
     e = launch_attention(p, part.grid, none, D, kmap, vmap, unused, unused, unused, unused,
-                         unused, k_cache, v_cache, st, /*early=*/false, /*pairs_only=*/false);
+                         unused, k_cache, v_cache, st, /*early=*/false, /*pairs_mode=*/0);
     if (e != cudaSuccess) return internal_fail(HB_ERR_CUDA, "decode launch failed");
     internal_note_other_launch(stream);
     internal_count_launch();

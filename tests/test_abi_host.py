@@ -230,10 +230,15 @@ def _check_plan(rows, hq, hkv, d, sms, window=0):
     assert slots == set(range(len(slots))) and merges == set(range(len(merges)))
     lengths = [c[4] - c[8] for c in chk]
     assert lengths == sorted(lengths, reverse=True)
-    # the launch takes the pairs-only kernel when every chunk item is an
-    # unsplit pair of query tiles
+    # the launch takes a pairs-only kernel when every chunk item is an unsplit
+    # pair of query tiles (bit 0), and one that writes softmax weights in two
+    # terms when some item's first row sees at most 256 keys (bit 1)
+    def first_keys(c):
+        k = int(c[7]) - int(c[6]) + int(c[2]) + 1
+        return min(window, k) if window > 0 else k
     pairs_only = len(chk) > 0 and all(int(c[3]) > tpt and int(c[10]) == 1 for c in chk)
-    assert h["chunk_pairs_only"] == int(pairs_only)
+    few = any(first_keys(c) <= 256 for c in chk)
+    assert h["chunk_pairs_only"] == (1 if pairs_only else 0) | (2 if few else 0)
     return h
 
 

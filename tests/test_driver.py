@@ -117,11 +117,13 @@ def test_driver_with_whole_blocks_on_the_gpu():
     """With whole transformer blocks per iteration (measured linear layers
     around the attention step), an iteration's time grows with its tokens, so
     admitting whole prompts stretches the worst gap between a running
-    request's tokens beyond what a 256-token budget allows."""
+    request's tokens beyond what a 256-token budget allows.  (Mistral-7B-sized
+    blocks: an 8192-token iteration then holds milliseconds of GPU work, well
+    above the host's share of an iteration, which a smaller block would not.)"""
     from chunked_prefill_decode_gb300.layer import BlockShape
     reqs = driver.poisson_requests(rate=2000.0, n=12, seed=6, prompt_median=1500,
                                    output_median=8, max_total=4096)
-    blk = BlockShape(hidden=1024, num_q_heads=32, num_kv_heads=8, head_dim=128, ffn=2048)
+    blk = BlockShape(hidden=4096, num_q_heads=32, num_kv_heads=8, head_dim=128, ffn=14336)
     step = driver.GpuStep(num_pages=6000, layers=2, seed=6, block=blk)
     worst = {}
     for bud in (256, 8192):

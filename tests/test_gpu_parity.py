@@ -137,6 +137,37 @@ def test_split_pairs(geom, rows, window):
     _full_size(None, seed=19, lay=lay, repeats=3)
 
 
+@pytest.mark.parametrize("rows", [
+    [(2, 2)], [(3, 3)], [(17, 17)], [(33, 40)], [(100, 100)], [(130, 1000)],
+    [(255, 256)], [(257, 300)], [(1, 129), (64, 4160), (1, 7)], [(600, 1200), (1, 50), (9, 9)],
+])
+@pytest.mark.parametrize("geom", [(32, 8, 128), (56, 8, 128), (8, 8, 64)])
+def test_fresh_and_short_chunks(rows, geom):
+    """Chunks of 2 .. 600 tokens at offsets 0 .. 4096: the first tokens of a
+    prompt see few keys, so their output leans on a few softmax weights (such
+    items carry P in two bf16 terms); odd key-tile counts, short or empty
+    second tiles, last pages with unwritten slots."""
+    hq, hkv, d = geom
+    _full_check(layout_from_rows(Shape(hq, hkv, d), rows, 31), seed=31)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_random_batches_with_short_windows(seed):
+    """Random hybrid batches whose windows (1 .. 300 keys) or fresh chunks
+    leave every chunk row few keys."""
+    rng = np.random.default_rng(3000 + seed)
+    hq, hkv, d = [(32, 8, 128), (56, 8, 128), (64, 16, 128), (16, 1, 128), (8, 8, 64),
+                  (56, 8, 128)][seed]
+    rows = [(1, int(rng.integers(1, 2500))) for _ in range(int(rng.integers(0, 12)))]
+    for _ in range(int(rng.integers(1, 3))):
+        q = int(rng.integers(2, 400))
+        rows.append((q, q + int(rng.integers(0, 1500))))
+    rng.shuffle(rows)
+    window = int(rng.choice([0, 0, 5, 300])) if seed < 4 else [5, 1][seed - 4]
+    _full_check(layout_from_rows(Shape(hq, hkv, d, sliding_window=window),
+                                 [tuple(r) for r in rows], 3000 + seed), seed=seed)
+
+
 WINDOW_ROWS = [(1, 1), (1, 17), (1, 700), (1, 3000), (5, 37), (130, 700), (64, 4160),
                (257, 2000), (1, 129)]
 
